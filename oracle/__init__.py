@@ -1,0 +1,183 @@
+"""CPU oracle of DSpark's serial Markov draft walk (fp64 projection).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg import this package.  It shares no code with the
+CUDA library and never imports it.  The arithmetic lives in ``oracle.c``; this
+module only marshals numpy arrays through ctypes.
+
+Source of the method: "Keeping the Draft Walk on Chip: One Launch for DSpark's
+Markov Head", sections "The serial part of a parallel drafter" (recurrence and
+the rounding of W2 @ u), "The idea: make the walk resident" (ties to the
+smallest id, Philox-keyed Gumbel-max), "B200: the bf16 table fits on chip"
+(fp32 accumulation, two bf16 roundings); vLLM pull request #64442, section
+"Details" (plain fp32 Gumbel noise; tokens follow softmax(logits / T)).
+
+Every array of bf16 values is passed as its raw bits (numpy ``uint16``).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_u16p = np.ctypeslib.ndpointer(np.uint16, flags="C_CONTIGUOUS")
+_i32p = np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")
+_f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(np.float64, flags="C_CONTIGUOUS")
+_u32p = np.ctypeslib.ndpointer(np.uint32, flags="C_CONTIGUOUS")
+
+
+class OracleError(RuntimeError):
+    """The oracle rejected its input (bad size, anchor or temperature)."""
+
+
+class Oracle:
+    """The oracle library at ``path`` (the default build unless a test asks)."""
+
+    def __init__(self, path=None):
+        path = path or _build.build()
+        L = ctypes.CDLL(path)
+        L.orc_bf16_rne_many.restype = None
+        L.orc_bf16_rne_many.argtypes = [_f64p, _u16p, ctypes.c_int64]
+        L.orc_philox_many.restype = None
+        L.orc_philox_many.argtypes = [_u32p, _u32p, _u32p, ctypes.c_int64]
+        L.orc_noise_bits.restype = ctypes.c_uint32
+        L.orc_noise_bits.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int, ctypes.c_int64]
+        L.orc_uniform.restype = ctypes.c_float
+        L.orc_uniform.argtypes = [ctypes.c_uint32]
+        L.orc_gumbel.restype = ctypes.c_float
+        L.orc_gumbel.argtypes = [ctypes.c_float]
+        L.orc_sample_score.restype = ctypes.c_float
+        L.orc_sample_score.argtypes = [ctypes.c_uint16, ctypes.c_float, ctypes.c_float]
+        L.orc_walk.restype = ctypes.c_int
+        L.orc_walk.argtypes = [
+            _u16p, _u16p, ctypes.c_int64, ctypes.c_int,
+            _u16p, _i32p, _f32p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
+            ctypes.c_void_p, _i32p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+        ]
+        self.L = L
+        self.path = path
+
+    def bf16_rne(self, x):
+        """Round float64 values to bf16 (ties to even); returns uint16 bits."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        out = np.empty(x.shape, dtype=np.uint16)
+        self.L.orc_bf16_rne_many(x.reshape(-1), out.reshape(-1), x.size)
+        return out
+
+    def philox4x32_10(self, ctr, key):
+        """Philox4x32-10 on rows of ctr [n,4] and key [n,2] (uint32)."""
+        ctr = np.ascontiguousarray(ctr, dtype=np.uint32).reshape(-1, 4)
+        key = np.ascontiguousarray(key, dtype=np.uint32).reshape(-1, 2)
+        out = np.empty_like(ctr)
+        self.L.orc_philox_many(ctr, key, out, ctr.shape[0])
+        return out
+
+    def noise_bits(self, seed, b, k, v):
+        """The 32 random bits of token v, request b, step k."""
+        return int(self.L.orc_noise_bits(seed, b, k, v))
+
+    def uniform(self, x):
+        """Random bits -> the fp32 uniform the walk uses."""
+        return float(self.L.orc_uniform(x))
+
+    def gumbel(self, U):
+        """fp32 Gumbel noise -log(-log U)."""
+        return float(self.L.orc_gumbel(U))
+
+    def sample_score(self, logit_bits, T, g):
+        """fp32 selection score fp32(logit / T) + g."""
+        return float(self.L.orc_sample_score(logit_bits, T, g))
+
+    def walk(self, W1, W2, base, anchor, temperature, seed, forced=None,
+             want_logits=True, want_scores=False, nthreads=1):
+        """Run the walk for every request.
+
+        W1, W2: uint16 [V, r]; base: uint16 [B, gamma, V]; anchor: int32 [B];
+        temperature: float32 [B]; forced: optional int32 [B, gamma] (step
+        k > 0 takes prev = forced[b, k-1]).  Returns (tokens int32 [B, gamma],
+        logits uint16 [B, gamma, V] or None, scores float32 [B, gamma, V] or
+        None).
+        """
+        W1 = np.ascontiguousarray(W1, dtype=np.uint16)
+        W2 = np.ascontiguousarray(W2, dtype=np.uint16)
+        base = np.ascontiguousarray(base, dtype=np.uint16)
+        anchor = np.ascontiguousarray(anchor, dtype=np.int32)
+        temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+        V, r = W2.shape
+        if W1.shape != (V, r):
+            raise ValueError("W1 and W2 must both be [V, r]")
+        B, gamma, Vb = base.shape
+        if Vb != V or anchor.shape != (B,) or temperature.shape != (B,):
+            raise ValueError("base must be [B, gamma, V]; anchor and temperature [B]")
+        tokens = np.zeros((B, gamma), dtype=np.int32)
+        logits = np.zeros((B, gamma, V), dtype=np.uint16) if want_logits else None
+        scores = np.zeros((B, gamma, V), dtype=np.float32) if want_scores else None
+        forced_arr = None
+        if forced is not None:
+            forced_arr = np.ascontiguousarray(forced, dtype=np.int32)
+            if forced_arr.shape != (B, gamma):
+                raise ValueError("forced must be [B, gamma]")
+        rc = self.L.orc_walk(
+            W1, W2, V, r, base, anchor, temperature, int(seed) & (2**64 - 1), B, gamma,
+            forced_arr.ctypes.data if forced_arr is not None else None,
+            tokens,
+            logits.ctypes.data if logits is not None else None,
+            scores.ctypes.data if scores is not None else None,
+            int(nthreads))
+        if rc != 0:
+            raise OracleError("oracle walk rejected its input (code %d)" % rc)
+        return tokens, logits, scores
+
+
+_default = None
+
+
+def default() -> Oracle:
+    """The oracle built from ``oracle.c`` in this directory."""
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default
+
+
+def bf16_to_f64(h):
+    """bf16 bits -> float64 values (exact)."""
+    h = np.asarray(h, dtype=np.uint16)
+    return (h.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_rne(x):
+    return default().bf16_rne(x)
+
+
+def philox4x32_10(ctr, key):
+    return default().philox4x32_10(ctr, key)
+
+
+def noise_bits(seed, b, k, v):
+    return default().noise_bits(seed, b, k, v)
+
+
+def uniform(x):
+    return default().uniform(x)
+
+
+def gumbel(U):
+    return default().gumbel(U)
+
+
+def sample_score(logit_bits, T, g):
+    return default().sample_score(logit_bits, T, g)
+
+
+def walk(*args, **kwargs):
+    return default().walk(*args, **kwargs)
+
+
+def cpu_threads(nthreads):
+    """How many threads ``walk(..., nthreads)`` will really use."""
+    if nthreads > 0:
+        return nthreads
+    return os.cpu_count() or 1

@@ -1,0 +1,263 @@
+/*
+ * oracle.c -- plain, slow CPU oracle of DSpark's serial Markov draft walk.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link,
+ * load or call this file: only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code with the CUDA library.
+ *
+ * What it computes (sources, by page title and section):
+ *
+ *  - The walk recurrence: "Keeping the Draft Walk on Chip: One Launch for
+ *    DSpark's Markov Head", section "The serial part of a parallel drafter":
+ *    prev = anchor; for each step k, u = W1[prev] (rank 256),
+ *    logit_k = bf16(base_k + W2 @ u), tok_k = argmax (or a sample of
+ *    softmax(logit_k / T)), prev = tok_k.
+ *  - The rounding points: same page, same section (the default walk also
+ *    rounds W2 @ u to bf16 before the add) and section "B200: the bf16 table
+ *    fits on chip" (fp32 accumulation, bias rounded to bf16, then the sum
+ *    rounded to bf16).  Here the projection is accumulated in fp64, which is
+ *    the exact value up to fp64 rounding, and rounded to bf16 once.
+ *  - Ties go to the smallest token id: same page, section "The idea: make
+ *    the walk resident" (the inverted row index in the 64-bit key).
+ *  - Sampling: per-row Gumbel-max with Philox noise keyed by seed, request,
+ *    step and token (same section), computed in fp32 as the plain fp32
+ *    Gumbel noise named by vLLM pull request #64442, section "Details".
+ *    Tokens then follow softmax(logit / T).
+ *
+ * Readings where the pages are silent (each one is listed in the design notes):
+ *  - bf16 rounding is IEEE round-to-nearest-even, from the exact value.
+ *  - The base + bias sum is formed exactly (fp64) and rounded once.
+ *  - Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11) with key
+ *    (lo32(seed), hi32(seed)) and counter (v >> 2, k, b, 0); token v uses
+ *    output word v & 3.
+ *  - The uniform is U = (2 * (x >> 9) + 1) * 2^-24, the midpoint of one of
+ *    2^23 equal bins of (0,1); it is exact in fp32.
+ *  - The Gumbel score is s = fp32(logit / T) + fp32(-log(fp32(-log U))),
+ *    every operation rounded to fp32 (each fp64 result below is rounded to
+ *    fp32 at the same points).  T == 0 selects greedy argmax of the bf16
+ *    logits with no noise drawn; T < 0 or a non-finite T is an error.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_EINVAL (-1)
+#define ORC_EANCHOR (-5)
+#define ORC_ETEMP (-7)
+
+/* ---------------------------------------------------------------- bf16 --- */
+
+/* bf16 bits -> the exact value it denotes (bf16 is the top half of fp32). */
+double orc_bf16_to_f64(uint16_t h)
+{
+    uint32_t bits = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Round a double to the nearest bf16, ties to even.  bf16 has 8 significant
+ * bits and fp32's exponent range: normal numbers are n * 2^(e-8) with
+ * 128 <= n < 256, subnormals are multiples of 2^-133.  The quantum q of x is
+ * therefore 2^(e-8) where 2^(e-1) <= |x| < 2^e, but never below 2^-133.
+ */
+uint16_t orc_bf16_rne(double x)
+{
+    if (isnan(x))
+        return 0x7FC0;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (isinf(a))
+        return sign | 0x7F80;
+    if (a == 0.0)
+        return sign;
+    int e;
+    (void)frexp(a, &e);                 /* a = m * 2^e, 0.5 <= m < 1 */
+    int qexp = e - 8;
+    if (qexp < -133)
+        qexp = -133;
+    double scaled = ldexp(a, -qexp);    /* exact: a power-of-two scaling */
+    double n = floor(scaled);
+    double frac = scaled - n;           /* exact */
+    if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) != 0.0))
+        n += 1.0;
+    double r = ldexp(n, qexp);          /* n <= 256: at most 9 bits, exact */
+    if (r >= 0x1p128)                   /* beyond the largest finite bf16 */
+        return sign | 0x7F80;
+    float f = (float)r;                 /* exact: 8 significant bits */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return sign | (uint16_t)(bits >> 16);
+}
+
+/* -------------------------------------------------------------- Philox --- */
+
+/*
+ * Philox4x32 with 10 rounds.  One round: the products M0*c0 and M1*c2 are
+ * split into high and low words; the new counter is
+ * (hi(M1*c2) ^ c1 ^ k0, lo(M1*c2), hi(M0*c0) ^ c3 ^ k1, lo(M0*c0)).
+ * Between rounds the key is bumped by the Weyl constants (W0, W1).
+ */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += W0;
+            k1 += W1;
+        }
+        uint64_t p0 = (uint64_t)M0 * c0;
+        uint64_t p1 = (uint64_t)M1 * c2;
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        uint32_t n1 = (uint32_t)p1;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        uint32_t n3 = (uint32_t)p0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The 32 random bits that token v of request b at step k draws. */
+uint32_t orc_noise_bits(uint64_t seed, int b, int k, int64_t v)
+{
+    uint32_t ctr[4] = {(uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, 0u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    orc_philox4x32_10(ctr, key, out);
+    return out[v & 3];
+}
+
+/* Bits -> uniform in (0,1): the midpoint of bin (x >> 9) of 2^23 bins. */
+float orc_uniform(uint32_t x)
+{
+    return (float)ldexp(2.0 * (double)(x >> 9) + 1.0, -24);
+}
+
+/* Gumbel noise g = -log(-log U), each log's result rounded to fp32. */
+float orc_gumbel(float U)
+{
+    float e = (float)(-log((double)U));
+    return (float)(-log((double)e));
+}
+
+/* Selection score of one logit at temperature T > 0, in fp32 steps. */
+float orc_sample_score(uint16_t logit, float T, float g)
+{
+    float q = (float)(orc_bf16_to_f64(logit) / (double)T); /* fp32 quotient */
+    return (float)((double)q + (double)g);                 /* fp32 sum */
+}
+
+/* ---------------------------------------------------------------- walk --- */
+
+/*
+ * One Markov walk per request.
+ *
+ *   W1, W2     bf16 bits, [V, r] row-major
+ *   base       bf16 bits, [B, gamma, V]
+ *   anchor     [B] int32, each in [0, V)
+ *   T          [B] fp32 temperatures (0 = greedy)
+ *   forced     optional [B, gamma] int32: when given, step k > 0 uses
+ *              prev = forced[b, k-1] instead of this walk's own token
+ *              (teacher forcing; lets a test check each step of another
+ *              walk on its own)
+ *   out_tokens [B, gamma] int32
+ *   out_logits optional [B, gamma, V] bf16 bits
+ *   out_scores optional [B, gamma, V] fp32 selection scores (the bf16 logit
+ *              itself when T == 0)
+ *   nthreads   OpenMP threads for the loop over tokens (<= 0: all)
+ *
+ * Returns 0, or a negative code (invalid sizes, anchor or temperature).
+ */
+int orc_walk(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
+             const uint16_t *base, const int32_t *anchor, const float *T,
+             uint64_t seed, int B, int gamma, const int32_t *forced,
+             int32_t *out_tokens, uint16_t *out_logits, float *out_scores,
+             int nthreads)
+{
+    if (V <= 0 || r <= 0 || B < 0 || gamma < 0)
+        return ORC_EINVAL;
+    for (int b = 0; b < B; ++b) {
+        if (anchor[b] < 0 || anchor[b] >= V)
+            return ORC_EANCHOR;
+        if (!(T[b] >= 0.0f) || isinf(T[b]))
+            return ORC_ETEMP;
+    }
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#else
+    (void)nthreads;
+#endif
+    /* scratch rows, one vocabulary wide */
+    uint16_t *logit = (uint16_t *)malloc((size_t)V * sizeof *logit);
+    double *score = (double *)malloc((size_t)V * sizeof *score);
+    if (!logit || !score) {
+        free(logit);
+        free(score);
+        return ORC_EINVAL;
+    }
+    for (int b = 0; b < B; ++b) {
+        int64_t prev = anchor[b];
+        for (int k = 0; k < gamma; ++k) {
+            if (forced && k > 0)
+                prev = forced[(int64_t)b * gamma + (k - 1)];
+            const uint16_t *u = W1 + prev * r;            /* u = W1[prev] */
+            const uint16_t *bk = base + ((int64_t)b * gamma + k) * V;
+            const float Tb = T[b];
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+            for (int64_t v = 0; v < V; ++v) {
+                const uint16_t *w = W2 + v * r;
+                double acc = 0.0;                          /* W2[v,:] . u */
+                for (int j = 0; j < r; ++j)
+                    acc += orc_bf16_to_f64(w[j]) * orc_bf16_to_f64(u[j]);
+                uint16_t bias = orc_bf16_rne(acc);         /* first rounding */
+                uint16_t lg = orc_bf16_rne(orc_bf16_to_f64(bk[v]) +
+                                           orc_bf16_to_f64(bias)); /* second */
+                logit[v] = lg;
+                if (Tb == 0.0f) {
+                    score[v] = orc_bf16_to_f64(lg);
+                } else {
+                    float U = orc_uniform(orc_noise_bits(seed, b, k, v));
+                    score[v] = (double)orc_sample_score(lg, Tb, orc_gumbel(U));
+                }
+            }
+            int64_t best = 0;                              /* ties: lowest v */
+            for (int64_t v = 1; v < V; ++v)
+                if (score[v] > score[best])
+                    best = v;
+            out_tokens[(int64_t)b * gamma + k] = (int32_t)best;
+            if (out_logits)
+                memcpy(out_logits + ((int64_t)b * gamma + k) * V, logit,
+                       (size_t)V * sizeof *logit);
+            if (out_scores)
+                for (int64_t v = 0; v < V; ++v)
+                    out_scores[((int64_t)b * gamma + k) * V + v] = (float)score[v];
+            prev = best;
+        }
+    }
+    free(logit);
+    free(score);
+    return ORC_OK;
+}
+
+/* Batch helpers used by the tests to pin the pieces one by one. */
+void orc_bf16_rne_many(const double *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_bf16_rne(x[i]);
+}
+
+void orc_philox_many(const uint32_t *ctr, const uint32_t *key, uint32_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        orc_philox4x32_10(ctr + 4 * i, key + 2 * i, out + 4 * i);
+}

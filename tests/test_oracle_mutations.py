@@ -1,0 +1,63 @@
+"""Plant plausible slips in copies of the oracle; the pins must catch each one.
+
+Each mutation is a textual edit of oracle.c compiled into a temporary
+library.  The real oracle is never modified.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTATIONS = {
+    # one rounding of base + acc instead of two
+    "single_rounding": ("orc_bf16_to_f64(bias)); /* second */", "acc); /* second */"),
+    "sign_of_projection": ("acc += orc_bf16_to_f64(w[j])", "acc -= orc_bf16_to_f64(w[j])"),
+    "operands_swapped": ("const uint16_t *w = W2 + v * r;", "const uint16_t *w = W1 + v * r;"),
+    "tie_to_highest": ("if (score[v] > score[best])", "if (score[v] >= score[best])"),
+    "step_index_ignored": ("bk = base + ((int64_t)b * gamma + k) * V;",
+                           "bk = base + ((int64_t)b * gamma + 0) * V;"),
+    "prev_not_advanced": ("            prev = best;\n", "            (void)best;\n"),
+    "philox_multiplier": ("M0 = 0xD2511F53u", "M0 = 0xD2511F55u"),
+    "philox_key_bump": ("k1 += W1;", "k1 += W0;"),
+    "counter_layout": ("{(uint32_t)(v >> 2), (uint32_t)k, (uint32_t)b, 0u}",
+                       "{(uint32_t)(v >> 2), (uint32_t)b, (uint32_t)k, 0u}"),
+    "noise_word": ("return out[v & 3];", "return out[(v + 1) & 3];"),
+    "uniform_bin_edge": ("2.0 * (double)(x >> 9) + 1.0", "2.0 * (double)(x >> 9)"),
+    "gumbel_sign": ("return (float)(-log((double)e));", "return (float)(log((double)e));"),
+    "temperature_multiplies": ("/ (double)T); /* fp32 quotient */",
+                               "* (double)T); /* fp32 quotient */"),
+    "ties_away_from_zero": ("(frac == 0.5 && fmod(n, 2.0) != 0.0)", "(frac == 0.5)"),
+    "truncating_round": ("if (frac > 0.5 ||", "if (0 &&"),
+}
+
+
+@pytest.fixture(scope="module")
+def philox_ref():
+    pytest.importorskip("triton")
+    return pins.philox_reference()
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutation(name, tmp_path, philox_ref):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, "mutation anchor for %s not found exactly once" % name
+    path = tmp_path / "oracle_mut.c"
+    path.write_text(src.replace(old, new))
+    lib = tmp_path / "liboracle_mut.so"
+    subprocess.run(["gcc", "-O1", "-fPIC", "-shared", "-std=c11", "-fopenmp", "-o", str(lib),
+                    str(path), "-lm"], check=True)
+    O = oracle.Oracle(str(lib))
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(O)
+        except (AssertionError, oracle.OracleError) as e:
+            caught.append((pin.__name__, str(e)[:120]))
+            break
+    assert caught, "no pin caught the planted mutation %r" % name
