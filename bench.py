@@ -1,0 +1,367 @@
+"""Benchmark of the persistent serial Markov draft walk.
+
+A step is one round: the whole gamma-step walk of one batch, one launch of
+the persistent kernel, on seeded synthetic inputs already resident in HBM.
+The default workload is the Qwen3-scale fully resident walk (V = 151,936,
+r = 256, gamma = 7, B = 1, greedy, 100 seeded rounds; each step takes the
+next round's base logits and anchor).  Between timed steps L2 is flushed by
+writing a 256 MiB buffer, so every step starts with a cold L2 (as the pages
+time the walk: CUDA-graph replay, cold L2).  Each step's kernel is timed with
+CUDA events on the stream it is launched on.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle
+instead, on a bounded sample per step, and prints the same metric.
+
+Multi-GPU (torchrun, one rank per GPU): the walk does not shard across GPUs
+on this path; every rank runs independent replicas of the workload (weak
+scaling) and the slowest rank's time is reported.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = ("µs per γ-step draft walk at B=1..128; effective W2 GB/s vs "
+          "on-chip/HBM roofline")
+# context only (another GPU, int8 weights): the pages' H100 resident walk at
+# V = 151,936, gamma = 7, bs = 1 took 37 us per call
+PAGES_US = {("qwen3_resident", 1): 37.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="qwen3_resident", choices=sorted(synth.CONFIGS))
+    p.add_argument("--batch", type=int, default=None)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--only-timed", action="store_true",
+                   help="warm-up and timed steps only (for profiler runs): no warm-L2 pass, "
+                        "no end-to-end pass, no CPU baseline")
+    return p.parse_args()
+
+
+def dist_setup(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return rank, world, dist
+    if torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return 0, 1, None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms, with timestamps."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        inside = [s for t, s in self.samples if t0 - 0.25 <= t <= t1 + 0.25]
+        if not inside:                       # timed region shorter than a sample
+            mid = (t0 + t1) / 2
+            inside = [min(self.samples, key=lambda ts: abs(ts[0] - mid))[1]]
+        sm = [float(s[1]) for s in inside if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in inside if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4)
+                          if len(s) > 5 + i and s[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def load_inputs(cfg, B, n_rounds):
+    W1, W2, _ = synth.make_weights(cfg.V, cfg.r, cfg.seed)
+    rounds = [synth.make_inputs(cfg, B=B, round_index=i, weights=(W1, W2))
+              for i in range(n_rounds)]
+    return W1, W2, rounds
+
+
+def cpu_baseline(cfg, B, rounds, seconds):
+    """The oracle, as it stands, on all host cores: full walks for ~`seconds`."""
+    import oracle
+    from oracle import cpu_threads
+    O = oracle.default()
+    W1 = synth.bits(rounds[0].W1)
+    W2 = synth.bits(rounds[0].W2)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        x = rounds[n % len(rounds)]
+        O.walk(W1, W2, synth.bits(x.base), x.anchor.numpy(), x.temperature.numpy(), x.seed,
+               want_logits=False, nthreads=0)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": dt / n * 1e6, "unit": "us", "cores": cpu_threads(0), "kind": "oracle",
+            "sample": "%d full walks (rounds 0..%d of the workload), fp64 oracle on all "
+                      "host cores" % (n, min(n, len(rounds)) - 1)}
+
+
+def run_reference(args, cfg, B, rank, world):
+    """--impl reference: the CPU oracle on this arm's workload and metric."""
+    if rank != 0:
+        return
+    import oracle
+    from oracle import cpu_threads
+    O = oracle.default()
+    n_rounds = min(cfg.rounds, 8)
+    W1t, W2t, rounds = load_inputs(cfg, B, n_rounds)
+    W1, W2 = synth.bits(W1t), synth.bits(W2t)
+
+    def one_step(i):
+        # bounded sample: the work of ONE of the gamma steps of round i (all V
+        # tokens, all B requests, started from the round's anchor), scaled by
+        # gamma to a whole walk
+        x = rounds[i % n_rounds]
+        k = i % cfg.gamma
+        anchor = x.anchor.numpy()
+        base = synth.bits(x.base)[:, k:k + 1]
+        t0 = time.perf_counter()
+        O.walk(W1, W2, np.ascontiguousarray(base), anchor, x.temperature.numpy(), x.seed,
+               want_logits=False, nthreads=0)
+        return time.perf_counter() - t0
+
+    for i in range(args.warmup):
+        one_step(i)
+    times = [one_step(args.warmup + i) for i in range(args.steps)]
+    us = statistics.mean(times) * cfg.gamma * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": "us",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": us / 1000.0, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.note, "V": cfg.V, "gamma": cfg.gamma, "B": B, "r": cfg.r},
+        "cpu_baseline": {"value": us, "unit": "us", "cores": cpu_threads(0), "kind": "oracle",
+                         "sample": "per step: the work of one of the gamma walk steps (all V "
+                                   "tokens, all B requests, from the round's anchor), x gamma"},
+        "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    cfg = synth.CONFIGS[args.workload]
+    B = args.batch or cfg.batches[0]
+    rank, world, dist = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, cfg, B, rank, world)
+        if dist:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    from serial_draft_head_gb300 import walk
+    walk.load(build_if_missing=True)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    n_rounds = min(cfg.rounds, 100)
+    W1c, W2c, rounds = load_inputs(cfg, B, n_rounds)
+    W1 = W1c.to(dev)
+    W2 = W2c.to(dev)
+    w = walk.Walk(W1, W2, B, cfg.gamma)
+    plan = w.plan()
+    del W2
+    base = torch.stack([r.base for r in rounds]).to(dev)          # [R, B, gamma, V]
+    anchor = torch.stack([r.anchor for r in rounds]).to(dev)
+    temp = torch.stack([r.temperature for r in rounds]).to(dev)
+    seed = rounds[0].seed
+    tokens = torch.empty(n_rounds, B, cfg.gamma, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def launch(i):
+        j = i % n_rounds
+        walk.dspark_walk_run(w.h, base[j], anchor[j], temp[j], seed + i, tokens[j], B,
+                             cfg.gamma, None, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            flush.fill_(i)
+            launch(i)
+    torch.cuda.synchronize()
+    st = w.status(stream)
+    if st != 0:
+        raise RuntimeError("walk status %d during warm-up" % st)
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.fill_(i)                     # cold L2: 256 MiB written between steps
+            starts[i].record(stream)
+            launch(i)
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t1 = time.time()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]        # ms
+    st = w.status(stream)
+    if st != 0:
+        raise RuntimeError("walk status %d in the timed region" % st)
+
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    warm_ms = e2e_us = None
+    e2e_n = 0
+    if not args.only_timed:
+        # warm L2 (back-to-back, no flush): W2 stays in L2 across rounds
+        ws, we = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ws.record(stream)
+            for i in range(args.steps):
+                launch(i)
+            we.record(stream)
+        torch.cuda.synchronize()
+        warm_ms = ws.elapsed_time(we) / args.steps
+
+        # end to end through the C ABI with host buffers (pinned), copies included
+        hb = [r.base.pin_memory() for r in rounds[:8]]
+        ha = [r.anchor.pin_memory() for r in rounds[:8]]
+        ht = [r.temperature.pin_memory() for r in rounds[:8]]
+        hout = torch.empty(B, cfg.gamma, dtype=torch.int32).pin_memory()
+        e2e_n = min(args.steps, 200)
+        for i in range(5):
+            walk.dspark_walk_run_host(w.h, hb[i % 8], ha[i % 8], ht[i % 8], seed, hout, B,
+                                      cfg.gamma, None, stream)
+        te0 = time.perf_counter()
+        for i in range(e2e_n):
+            rc = walk.dspark_walk_run_host(w.h, hb[i % 8], ha[i % 8], ht[i % 8], seed + i, hout,
+                                           B, cfg.gamma, None, stream)
+            if rc != 0:
+                raise RuntimeError("run_host status %d" % rc)
+        e2e_us = (time.perf_counter() - te0) / e2e_n * 1e6
+    h2d = B * cfg.gamma * cfg.V * 2 + B * 4 + B * 4
+    d2h = B * cfg.gamma * 4
+
+    mean_ms = statistics.mean(per)
+    local = torch.tensor([mean_ms, (t1 - t0)], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(local, op=dist.ReduceOp.MAX)
+    mean_ms = float(local[0])
+    us = mean_ms * 1000.0
+
+    w2_bytes = cfg.gamma * cfg.V * cfg.r * 2 * B           # effective W2 bytes per walk
+    eff_gbs = w2_bytes / (mean_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    roof = {"bound": "hbm", "achieved": eff_gbs, "peak": peak, "unit": "GB/s",
+            "frac": eff_gbs / peak, "traffic": None,
+            "peak_kind": peak_kind,
+            "note": "achieved = effective W2 bytes (gamma*V*r*2*B) per launch / mean launch "
+                    "time; >1 means W2 is served from on-chip memory or L2, not HBM"}
+    line = {
+        "metric": METRIC, "value": us, "unit": "us", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
+        "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": (us / PAGES_US[(cfg.name, B)]) if (cfg.name, B) in PAGES_US else None,
+        "vs_baseline_note": "value / the pages' 37 us (H100, int8 W2): context on other "
+                            "hardware and precision" if (cfg.name, B) in PAGES_US else None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.note, "V": cfg.V, "r": cfg.r, "gamma": cfg.gamma, "B": B,
+                   "rounds": n_rounds, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "flushed between timed steps (256 MiB write)",
+                   "kernel": plan["kernel"], "n_cta": plan["n_cta"],
+                   "threads": plan["threads"]},
+        "median_us": statistics.median(per) * 1000.0,
+        "p10_us": float(np.percentile(per, 10)) * 1000.0,
+        "p90_us": float(np.percentile(per, 90)) * 1000.0,
+        "warm_l2_us": warm_ms * 1000.0 if warm_ms is not None else None,
+        "roofline": roof,
+        "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "how": "dspark_walk_run_host: pinned host base/anchor/temperature -> device, "
+                       "the round, tokens -> host, stream sync; wall clock, mean of %d" % e2e_n},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "plan": plan,
+    }
+    if rank == 0 and not args.no_cpu_baseline and not args.only_timed:
+        line["cpu_baseline"] = cpu_baseline(cfg, B, rounds, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    w.close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

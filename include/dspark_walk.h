@@ -1,0 +1,173 @@
+/*
+ * dspark_walk.h -- C ABI of the GB300 (sm_103a) serial Markov draft walk.
+ *
+ * The operation (source: "Keeping the Draft Walk on Chip: One Launch for
+ * DSpark's Markov Head", section "The serial part of a parallel drafter"):
+ * for every request b, starting from prev = anchor[b], for k = 0 .. gamma-1
+ *
+ *     u        = W1[prev]                                  (rank r = 256)
+ *     bias[v]  = bf16_rne(fp32 sum_j W2[v,j] * u[j])        for every v < V
+ *     logit[v] = bf16_rne(fp32(base[b,k,v]) + fp32(bias[v]))
+ *     tok      = argmax_v logit[v]              (temperature[b] == 0)
+ *              = argmax_v fp32(logit[v] / T) + g(b,k,v)    (T > 0, Gumbel-max)
+ *     out_tokens[b,k] = tok;  prev = tok
+ *
+ * The rounding points are those of section "B200: the bf16 table fits on
+ * chip" (fp32 accumulation, bias rounded to bf16, then the sum rounded to
+ * bf16).  Ties go to the smallest token id (section "The idea: make the walk
+ * resident": the 64-bit key holds the order-preserving logit bits and then
+ * the inverted row index).  The Gumbel noise g = -log(-log U) draws U from
+ * Philox4x32-10 keyed by (seed, request, step, token): key = (lo32(seed),
+ * hi32(seed)), counter = (v >> 2, k, b, 0), token v reads output word v & 3,
+ * U = (2 * (x >> 9) + 1) * 2^-24.  All of it is computed in fp32.
+ *
+ * One round is ONE persistent kernel launch on the caller's stream; every
+ * step of the walk runs inside it and only token ids cross between steps
+ * (same section).  All CTAs are co-resident (cooperative launch).
+ *
+ * Conventions for every call:
+ *  - Return value 0 (DSPARK_OK) or a negative DSPARK_E* code.  Nothing traps.
+ *  - "device" pointers are CUDA device (or managed) memory of the current
+ *    device; "host" pointers are ordinary or pinned host memory.
+ *  - bf16 arrays are IEEE bfloat16 bit patterns, 2 bytes per element,
+ *    row-major and contiguous.
+ *  - `stream` is a cudaStream_t (0 = the legacy default stream).
+ *  - Calls on one handle must be ordered by the caller (one stream, or
+ *    streams joined by events), as for a CUDA graph.
+ */
+#ifndef DSPARK_WALK_H
+#define DSPARK_WALK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define DSPARK_OK 0
+#define DSPARK_EINVAL (-1)       /* bad argument, detected on the host before launch */
+#define DSPARK_ENOMEM (-2)       /* device allocation failed in create */
+#define DSPARK_ECUDA (-3)        /* a CUDA runtime call failed */
+#define DSPARK_ETIMEOUT (-4)     /* a cross-CTA rendezvous waited past its limit */
+#define DSPARK_EANCHOR (-5)      /* an anchor was outside [0, V) (device-detected) */
+#define DSPARK_EUNSUPPORTED (-6) /* r != 256, or the device is not sm_103 */
+#define DSPARK_ETEMP (-7)        /* a temperature was negative or not finite (device-detected) */
+
+/* Opaque handle: resident weight layout, rendezvous slots, status word. */
+typedef struct dspark_walk dspark_walk;
+typedef dspark_walk *dspark_walk_t;
+
+/*
+ * How create() placed W2 on the chip (see dspark_walk_get_plan).
+ * Rows of W2 are split into contiguous per-CTA shards; inside a shard each
+ * row lives in exactly one tier.
+ */
+struct dspark_walk_plan {
+    int64_t V;              /* vocabulary size */
+    int r;                  /* rank (256) */
+    int n_cta;              /* CTAs of the persistent kernel (one per SM used) */
+    int threads;            /* threads per CTA */
+    int rows_per_cta;       /* rows of the largest shard */
+    int rows_tmem;          /* per CTA: rows held in tensor memory */
+    int rows_smem;          /* per CTA: rows held in shared memory */
+    int rows_rf;            /* per CTA: rows held in registers */
+    int rows_stream;        /* per CTA: rows re-read from L2/HBM every step */
+    int64_t resident_bytes; /* W2 bytes held on chip across steps, all CTAs */
+    int64_t streamed_bytes; /* W2 bytes re-read from L2/HBM per step, all CTAs */
+    int max_B;              /* largest batch a run may pass */
+    int max_gamma;          /* longest walk a run may pass */
+    int kernel;             /* which kernel runs small batches (DSPARK_KERNEL_*) */
+    int sm_count;           /* SMs on the device */
+};
+
+#define DSPARK_KERNEL_STREAM 0   /* every row re-read from global memory each step */
+#define DSPARK_KERNEL_RESIDENT 1 /* rows held in registers / shared / tensor memory */
+
+/*
+ * dspark_walk_create -- prepare a walk over fixed weights.
+ *
+ *   W1        device, bf16 [V, r] row-major: the Markov embedding.  Referenced,
+ *             not copied: keep it alive and unchanged until destroy.
+ *   W2        device, bf16 [V, r] row-major: the vocabulary projection.
+ *             Copied and repacked into a handle-owned layout (V * r * 2
+ *             bytes); the caller may free it after create returns.
+ *   V         1 <= V < 2^31
+ *   r         must be 256 (DSPARK_EUNSUPPORTED otherwise)
+ *   max_B     1 <= max_B <= 256: largest batch any run will pass
+ *   max_gamma 1 <= max_gamma <= 64: longest walk any run will pass
+ *   out       receives the handle (set to NULL on failure)
+ *
+ * Uses the current CUDA device; synchronises it once.  Errors: DSPARK_EINVAL,
+ * DSPARK_EUNSUPPORTED, DSPARK_ENOMEM, DSPARK_ECUDA.
+ */
+int dspark_walk_create(const void *W1, const void *W2, int64_t V, int r, int max_B,
+                       int max_gamma, dspark_walk_t *out);
+
+/*
+ * dspark_walk_run -- one round: the whole gamma-step walk for B requests in
+ * one launch on `stream` (asynchronous; capturable in a CUDA graph, and needs
+ * no memset between replays: the rendezvous state alternates by round parity).
+ *
+ *   base_logits  device, bf16 [B, gamma, V]: the parallel pass's logits
+ *   anchor       device, int32 [B]: the last accepted token of each request
+ *   temperature  device, fp32 [B]: 0 = greedy, > 0 = Gumbel-max sampling
+ *   seed         Philox key of this round (change it per round for fresh noise)
+ *   out_tokens   device, int32 [B, gamma]: the drafted tokens
+ *   B, gamma     1 <= B <= max_B, 1 <= gamma <= max_gamma
+ *   out_logits   NULL, or device bf16 [B, gamma, V]: receives every logit the
+ *                tokens were chosen from (for a lossless verifier)
+ *
+ * Host-detectable errors (NULL pointers, sizes) return DSPARK_EINVAL before
+ * any launch.  Device-detected errors (anchor out of range, bad temperature,
+ * rendezvous timeout) set the handle's status word and write -1 to
+ * out_tokens; read them with dspark_walk_status.
+ */
+int dspark_walk_run(dspark_walk_t h, const void *base_logits, const int32_t *anchor,
+                    const float *temperature, uint64_t seed, int32_t *out_tokens, int B,
+                    int gamma, void *out_logits, void *stream);
+
+/*
+ * dspark_walk_run_host -- the same round with HOST buffers: copies base,
+ * anchor and temperature to handle-owned device buffers on `stream`, runs the
+ * round, copies the tokens (and logits, if out_logits_host is not NULL) back,
+ * and waits for the stream.  Pinned host memory makes the copies asynchronous
+ * with respect to other streams.  Returns the round's device status (as
+ * dspark_walk_status does) or a host-side error.
+ */
+int dspark_walk_run_host(dspark_walk_t h, const void *base_logits_host,
+                         const int32_t *anchor_host, const float *temperature_host,
+                         uint64_t seed, int32_t *out_tokens_host, int B, int gamma,
+                         void *out_logits_host, void *stream);
+
+/*
+ * dspark_walk_status -- wait for `stream`, then return and clear the status
+ * word the device wrote during earlier runs (DSPARK_OK if none failed).
+ */
+int dspark_walk_status(dspark_walk_t h, void *stream);
+
+/* dspark_walk_get_plan -- copy the placement chosen at create into *p. */
+int dspark_walk_get_plan(dspark_walk_t h, struct dspark_walk_plan *p);
+
+/*
+ * dspark_walk_set_limits -- rendezvous wait limit in nanoseconds (default
+ * 200,000,000; minimum 1,000) and a fault-injection switch: skip_cta >= 0
+ * makes that CTA skip posting its arrival, so every other CTA's wait runs
+ * out and the round ends with DSPARK_ETIMEOUT (tests use it to check that a
+ * lost arrival is reported, not hung on).  skip_cta = -1 turns it off.
+ * Takes effect from the next run.
+ */
+int dspark_walk_set_limits(dspark_walk_t h, int64_t timeout_ns, int skip_cta);
+
+/* dspark_walk_strerror -- a static description of a status code. */
+const char *dspark_walk_strerror(int code);
+
+/* dspark_walk_destroy -- free everything the handle owns (synchronises the device). */
+int dspark_walk_destroy(dspark_walk_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_WALK_H */

@@ -53,7 +53,7 @@ class Oracle:
         L.orc_walk.restype = ctypes.c_int
         L.orc_walk.argtypes = [
             _u16p, _u16p, ctypes.c_int64, ctypes.c_int,
-            _u16p, _i32p, _f32p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
+            _u16p, _i32p, _f32p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_void_p, _i32p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
         ]
         self.L = L
@@ -91,12 +91,13 @@ class Oracle:
         return float(self.L.orc_sample_score(logit_bits, T, g))
 
     def walk(self, W1, W2, base, anchor, temperature, seed, forced=None,
-             want_logits=True, want_scores=False, nthreads=1):
+             want_logits=True, want_scores=False, nthreads=1, req0=0):
         """Run the walk for every request.
 
         W1, W2: uint16 [V, r]; base: uint16 [B, gamma, V]; anchor: int32 [B];
         temperature: float32 [B]; forced: optional int32 [B, gamma] (step
-        k > 0 takes prev = forced[b, k-1]).  Returns (tokens int32 [B, gamma],
+        k > 0 takes prev = forced[b, k-1]); req0: request index of row 0 (row
+        i draws request req0 + i's noise).  Returns (tokens int32 [B, gamma],
         logits uint16 [B, gamma, V] or None, scores float32 [B, gamma, V] or
         None).
         """
@@ -121,7 +122,7 @@ class Oracle:
                 raise ValueError("forced must be [B, gamma]")
         rc = self.L.orc_walk(
             W1, W2, V, r, base, anchor, temperature, int(seed) & (2**64 - 1), B, gamma,
-            forced_arr.ctypes.data if forced_arr is not None else None,
+            int(req0), forced_arr.ctypes.data if forced_arr is not None else None,
             tokens,
             logits.ctypes.data if logits is not None else None,
             scores.ctypes.data if scores is not None else None,

@@ -165,6 +165,8 @@ float orc_sample_score(uint16_t logit, float T, float g)
  *   base       bf16 bits, [B, gamma, V]
  *   anchor     [B] int32, each in [0, V)
  *   T          [B] fp32 temperatures (0 = greedy)
+ *   req0       request index of batch row 0: row i draws the noise of request
+ *              req0 + i (so one request can be replayed on its own)
  *   forced     optional [B, gamma] int32: when given, step k > 0 uses
  *              prev = forced[b, k-1] instead of this walk's own token
  *              (teacher forcing; lets a test check each step of another
@@ -179,11 +181,11 @@ float orc_sample_score(uint16_t logit, float T, float g)
  */
 int orc_walk(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
              const uint16_t *base, const int32_t *anchor, const float *T,
-             uint64_t seed, int B, int gamma, const int32_t *forced,
+             uint64_t seed, int B, int gamma, int req0, const int32_t *forced,
              int32_t *out_tokens, uint16_t *out_logits, float *out_scores,
              int nthreads)
 {
-    if (V <= 0 || r <= 0 || B < 0 || gamma < 0)
+    if (V <= 0 || r <= 0 || B < 0 || gamma < 0 || req0 < 0)
         return ORC_EINVAL;
     for (int b = 0; b < B; ++b) {
         if (anchor[b] < 0 || anchor[b] >= V)
@@ -226,7 +228,7 @@ int orc_walk(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
                 if (Tb == 0.0f) {
                     score[v] = orc_bf16_to_f64(lg);
                 } else {
-                    float U = orc_uniform(orc_noise_bits(seed, b, k, v));
+                    float U = orc_uniform(orc_noise_bits(seed, req0 + b, k, v));
                     score[v] = (double)orc_sample_score(lg, Tb, orc_gumbel(U));
                 }
             }

@@ -1,0 +1,282 @@
+// walk_api.cu -- the C ABI of include/dspark_walk.h: argument checks, the
+// shard plan, device allocations owned by a handle, and the cooperative
+// launch of one persistent kernel per round.
+#include <cuda_runtime.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "../../include/dspark_walk.h"
+#include "walk_common.cuh"
+#include "walk_kernels.h"
+
+using namespace dspark;
+
+struct dspark_walk {
+  int device = 0;
+  int sm_count = 0;
+  int64_t V = 0;
+  int r = 0;
+  int max_B = 0;
+  int max_gamma = 0;
+  const uint16_t* W1 = nullptr;   // caller-owned
+  uint16_t* W2 = nullptr;         // handle-owned copy
+  void* sync_mem = nullptr;       // SyncHeader + counts + keys
+  SyncView sync{};
+  dspark_walk_plan plan{};
+  int64_t timeout_ns = 200000000;
+  int skip_cta = -1;
+  // staging for dspark_walk_run_host (allocated on first use)
+  void* stage = nullptr;
+  size_t stage_bytes = 0;
+};
+
+namespace {
+
+int cuda_fail(cudaError_t e) {
+  if (e == cudaErrorMemoryAllocation) return DSPARK_ENOMEM;
+  return DSPARK_ECUDA;
+}
+
+#define CUDA_TRY(expr)                                 \
+  do {                                                 \
+    cudaError_t err_ = (expr);                         \
+    if (err_ != cudaSuccess) return cuda_fail(err_);   \
+  } while (0)
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Sizes of the three parts of the rendezvous memory.
+void sync_layout(int max_gamma, int max_B, size_t* count_off, size_t* key_off, size_t* total) {
+  *count_off = round_up(sizeof(SyncHeader), 128);
+  *key_off = round_up(*count_off + (size_t)2 * max_gamma * kCountStride * sizeof(uint32_t), 128);
+  *total = round_up(*key_off + (size_t)2 * max_gamma * max_B * sizeof(unsigned long long), 128);
+}
+
+// Shard plan of the streamed kernel: rows split evenly over at most one CTA
+// per SM; tiny vocabularies use fewer CTAs (at least 32 rows each), since
+// the rendezvous costs more with more CTAs.
+void plan_stream(dspark_walk* h) {
+  const int64_t min_rows = 32;
+  int64_t n = (h->V + min_rows - 1) / min_rows;
+  if (n > h->sm_count) n = h->sm_count;
+  if (n < 1) n = 1;
+  int64_t rpc = (h->V + n - 1) / n;
+  n = (h->V + rpc - 1) / rpc;     // every CTA owns at least one row
+  dspark_walk_plan& p = h->plan;
+  p.V = h->V;
+  p.r = h->r;
+  p.n_cta = (int)n;
+  p.threads = stream_threads();
+  p.rows_per_cta = (int)rpc;
+  p.rows_tmem = p.rows_smem = p.rows_rf = 0;
+  p.rows_stream = (int)rpc;
+  p.resident_bytes = 0;
+  p.streamed_bytes = h->V * (int64_t)h->r * 2;
+  p.max_B = h->max_B;
+  p.max_gamma = h->max_gamma;
+  p.kernel = DSPARK_KERNEL_STREAM;
+  p.sm_count = h->sm_count;
+}
+
+int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const float* temp,
+                 uint64_t seed, int32_t* out_tokens, int B, int gamma, void* out_logits,
+                 cudaStream_t stream) {
+  WalkArgs a{};
+  a.W1 = h->W1;
+  a.W2 = h->W2;
+  a.base = static_cast<const uint16_t*>(base);
+  a.anchor = anchor;
+  a.temperature = temp;
+  a.out_tokens = out_tokens;
+  a.out_logits = static_cast<uint16_t*>(out_logits);
+  a.sync = h->sync;
+  a.V = h->V;
+  a.B = B;
+  a.gamma = gamma;
+  a.rows_per_cta = h->plan.rows_per_cta;
+  a.seed_lo = (uint32_t)seed;
+  a.seed_hi = (uint32_t)(seed >> 32);
+  a.timeout_ns = h->timeout_ns;
+  a.skip_cta = h->skip_cta;
+
+  const void* fn = stream_kernel_for(B);
+  const size_t smem = stream_smem_bytes(B);  // <= the maximum set at create
+  void* args[] = {&a};
+  CUDA_TRY(cudaLaunchCooperativeKernel(fn, dim3(h->plan.n_cta), dim3(h->plan.threads), args,
+                                       smem, stream));
+  return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max_B,
+                       int max_gamma, dspark_walk_t* out) {
+  if (out) *out = nullptr;
+  if (!W1 || !W2 || !out) return DSPARK_EINVAL;
+  if (V < 1 || V >= ((int64_t)1 << 31)) return DSPARK_EINVAL;
+  if (max_B < 1 || max_B > kMaxB || max_gamma < 1 || max_gamma > kMaxGamma) return DSPARK_EINVAL;
+  if (r != kRank) return DSPARK_EUNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(W1) & 15u) != 0 || (reinterpret_cast<uintptr_t>(W2) & 15u) != 0)
+    return DSPARK_EINVAL;
+
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  int major = 0, minor = 0, sms = 0, coop = 0;
+  CUDA_TRY(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+  CUDA_TRY(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+  CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  CUDA_TRY(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev));
+  if (major != 10 || minor != 3 || !coop) return DSPARK_EUNSUPPORTED;
+
+  dspark_walk* h = new (std::nothrow) dspark_walk();
+  if (!h) return DSPARK_ENOMEM;
+  h->device = dev;
+  h->sm_count = sms;
+  h->V = V;
+  h->r = r;
+  h->max_B = max_B;
+  h->max_gamma = max_gamma;
+  h->W1 = static_cast<const uint16_t*>(W1);
+
+  int rc = DSPARK_OK;
+  size_t count_off, key_off, total;
+  sync_layout(max_gamma, max_B, &count_off, &key_off, &total);
+  cudaError_t e = cudaMalloc(&h->W2, (size_t)V * r * 2);
+  if (e == cudaSuccess) e = cudaMemcpy(h->W2, W2, (size_t)V * r * 2, cudaMemcpyDeviceToDevice);
+  if (e == cudaSuccess) e = cudaMalloc(&h->sync_mem, total);
+  if (e == cudaSuccess) e = cudaMemset(h->sync_mem, 0, total);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) rc = cuda_fail(e);
+  if (rc == DSPARK_OK) {
+    uint8_t* base = static_cast<uint8_t*>(h->sync_mem);
+    h->sync.hdr = reinterpret_cast<SyncHeader*>(base);
+    h->sync.count = reinterpret_cast<uint32_t*>(base + count_off);
+    h->sync.key = reinterpret_cast<unsigned long long*>(base + key_off);
+    h->sync.max_gamma = max_gamma;
+    h->sync.max_B = max_B;
+    plan_stream(h);
+    // every instantiation may use the shared memory of max_B, and one CTA
+    // per SM must fit
+    const size_t smem = stream_smem_bytes(max_B);
+    for (int b = 1; b <= 8 && rc == DSPARK_OK; b *= 2) {
+      int per_sm = 0;
+      const void* fn = stream_kernel_for(b);
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, h->plan.threads, smem);
+      if (e != cudaSuccess) rc = cuda_fail(e);
+      else if (per_sm < 1) rc = DSPARK_EUNSUPPORTED;
+    }
+  }
+  if (rc != DSPARK_OK) {
+    dspark_walk_destroy(h);
+    return rc;
+  }
+  *out = h;
+  return DSPARK_OK;
+}
+
+int dspark_walk_run(dspark_walk_t h, const void* base_logits, const int32_t* anchor,
+                    const float* temperature, uint64_t seed, int32_t* out_tokens, int B,
+                    int gamma, void* out_logits, void* stream) {
+  if (!h || !base_logits || !anchor || !temperature || !out_tokens) return DSPARK_EINVAL;
+  if (B < 1 || B > h->max_B || gamma < 1 || gamma > h->max_gamma) return DSPARK_EINVAL;
+  return launch_round(h, base_logits, anchor, temperature, seed, out_tokens, B, gamma,
+                      out_logits, static_cast<cudaStream_t>(stream));
+}
+
+int dspark_walk_run_host(dspark_walk_t h, const void* base_logits_host,
+                         const int32_t* anchor_host, const float* temperature_host,
+                         uint64_t seed, int32_t* out_tokens_host, int B, int gamma,
+                         void* out_logits_host, void* stream) {
+  if (!h || !base_logits_host || !anchor_host || !temperature_host || !out_tokens_host)
+    return DSPARK_EINVAL;
+  if (B < 1 || B > h->max_B || gamma < 1 || gamma > h->max_gamma) return DSPARK_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // staging: base | logits | anchor | temperature | tokens, sized for the maxima
+  const size_t nlog = (size_t)h->max_B * h->max_gamma * (size_t)h->V;
+  const size_t off_logits = round_up(nlog * 2, 256);
+  const size_t off_anchor = off_logits + round_up(nlog * 2, 256);
+  const size_t off_temp = off_anchor + round_up((size_t)h->max_B * 4, 256);
+  const size_t off_tok = off_temp + round_up((size_t)h->max_B * 4, 256);
+  const size_t need = off_tok + round_up((size_t)h->max_B * h->max_gamma * 4, 256);
+  if (h->stage_bytes < need) {
+    if (h->stage) cudaFree(h->stage);
+    h->stage = nullptr;
+    h->stage_bytes = 0;
+    CUDA_TRY(cudaMalloc(&h->stage, need));
+    h->stage_bytes = need;
+  }
+  uint8_t* st = static_cast<uint8_t*>(h->stage);
+  const size_t nb = (size_t)B * gamma * (size_t)h->V * 2;
+  CUDA_TRY(cudaMemcpyAsync(st, base_logits_host, nb, cudaMemcpyHostToDevice, s));
+  CUDA_TRY(cudaMemcpyAsync(st + off_anchor, anchor_host, (size_t)B * 4, cudaMemcpyHostToDevice, s));
+  CUDA_TRY(cudaMemcpyAsync(st + off_temp, temperature_host, (size_t)B * 4, cudaMemcpyHostToDevice,
+                           s));
+  int rc = launch_round(h, st, reinterpret_cast<int32_t*>(st + off_anchor),
+                        reinterpret_cast<float*>(st + off_temp), seed,
+                        reinterpret_cast<int32_t*>(st + off_tok), B, gamma,
+                        out_logits_host ? st + off_logits : nullptr, s);
+  if (rc != DSPARK_OK) return rc;
+  CUDA_TRY(cudaMemcpyAsync(out_tokens_host, st + off_tok, (size_t)B * gamma * 4,
+                           cudaMemcpyDeviceToHost, s));
+  if (out_logits_host)
+    CUDA_TRY(cudaMemcpyAsync(out_logits_host, st + off_logits, nb, cudaMemcpyDeviceToHost, s));
+  return dspark_walk_status(h, stream);
+}
+
+int dspark_walk_status(dspark_walk_t h, void* stream) {
+  if (!h) return DSPARK_EINVAL;
+  CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  int32_t st = 0;
+  CUDA_TRY(cudaMemcpy(&st, &h->sync.hdr->status, sizeof st, cudaMemcpyDeviceToHost));
+  if (st != 0) {
+    const int32_t zero = 0;
+    CUDA_TRY(cudaMemcpy(&h->sync.hdr->status, &zero, sizeof zero, cudaMemcpyHostToDevice));
+  }
+  return st;
+}
+
+int dspark_walk_get_plan(dspark_walk_t h, struct dspark_walk_plan* p) {
+  if (!h || !p) return DSPARK_EINVAL;
+  *p = h->plan;
+  return DSPARK_OK;
+}
+
+int dspark_walk_set_limits(dspark_walk_t h, int64_t timeout_ns, int skip_cta) {
+  if (!h || timeout_ns < 1000 || skip_cta < -1) return DSPARK_EINVAL;
+  h->timeout_ns = timeout_ns;
+  h->skip_cta = skip_cta;
+  return DSPARK_OK;
+}
+
+const char* dspark_walk_strerror(int code) {
+  switch (code) {
+    case DSPARK_OK: return "ok";
+    case DSPARK_EINVAL: return "invalid argument";
+    case DSPARK_ENOMEM: return "out of device memory";
+    case DSPARK_ECUDA: return "CUDA runtime error";
+    case DSPARK_ETIMEOUT: return "cross-CTA rendezvous timed out";
+    case DSPARK_EANCHOR: return "anchor token outside [0, V)";
+    case DSPARK_EUNSUPPORTED: return "unsupported rank or device (needs r = 256 on sm_103)";
+    case DSPARK_ETEMP: return "temperature negative or not finite";
+    default: return "unknown status";
+  }
+}
+
+int dspark_walk_destroy(dspark_walk_t h) {
+  if (!h) return DSPARK_EINVAL;
+  int rc = DSPARK_OK;
+  if (cudaDeviceSynchronize() != cudaSuccess) rc = DSPARK_ECUDA;
+  if (h->W2) cudaFree(h->W2);
+  if (h->sync_mem) cudaFree(h->sync_mem);
+  if (h->stage) cudaFree(h->stage);
+  delete h;
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,272 @@
+// walk_common.cuh -- device pieces shared by every walk kernel: the fused
+// epilogue (two bf16 roundings), the selection score (greedy or Philox
+// Gumbel-max), the 64-bit selection key and the cross-CTA rendezvous.
+//
+// Source: "Keeping the Draft Walk on Chip: One Launch for DSpark's Markov
+// Head", sections "The serial part of a parallel drafter" (recurrence, the
+// bf16 rounding of W2 @ u before the add), "The idea: make the walk resident"
+// (64-bit {order-preserving logit bits, inverted row index} key; {key, count}
+// rendezvous with an atomic max and an atomic add; per-round state that
+// alternates by round parity; Philox-keyed Gumbel-max; per-request
+// temperatures read on the device) and "B200: the bf16 table fits on chip"
+// (fp32 accumulation, bias rounded to bf16, sum rounded to bf16).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace dspark {
+
+constexpr int kRank = 256;         // r: the Markov head's latent width
+constexpr int kMaxB = 256;         // largest batch one round may carry
+constexpr int kMaxGamma = 64;      // longest walk one round may carry
+
+// Device-side status codes (same values as the public DSPARK_E* codes).
+constexpr int kStatusOk = 0;
+constexpr int kStatusTimeout = -4;
+constexpr int kStatusAnchor = -5;
+constexpr int kStatusTemp = -7;
+
+// Rendezvous state owned by a handle, in global memory.
+//   header: round counter (selects the parity) and the sticky status word;
+//   count[p][k]: CTAs that have posted step k in a round of parity p
+//                (one 32-byte sector each);
+//   key[p][k][b]: running maximum of the posted 64-bit keys.
+// A round of parity p clears parity p^1 at entry, so no memset is needed
+// between rounds (or between CUDA-graph replays).
+struct SyncHeader {
+  uint32_t round;
+  int32_t status;
+  uint32_t pad[6];
+};
+constexpr int kCountStride = 8;  // uint32 per count slot (32 bytes)
+
+struct SyncView {
+  SyncHeader* hdr;
+  uint32_t* count;             // [2][max_gamma][kCountStride]
+  unsigned long long* key;     // [2][max_gamma][max_B]
+  int max_gamma;
+  int max_B;
+
+  __device__ __forceinline__ uint32_t* count_at(uint32_t parity, int k) const {
+    return count + ((size_t)parity * max_gamma + k) * kCountStride;
+  }
+  __device__ __forceinline__ unsigned long long* key_at(uint32_t parity, int k, int b) const {
+    return key + ((size_t)parity * max_gamma + k) * max_B + b;
+  }
+};
+
+// Everything a launch needs (passed by value).
+struct WalkArgs {
+  const uint16_t* W1;          // [V, 256] bf16
+  const uint16_t* W2;          // [V, 256] bf16, row-major (streamed kernels)
+  const uint16_t* base;        // [B, gamma, V] bf16
+  const int32_t* anchor;       // [B]
+  const float* temperature;    // [B]
+  int32_t* out_tokens;         // [B, gamma]
+  uint16_t* out_logits;        // [B, gamma, V] bf16 or null
+  SyncView sync;
+  int64_t V;
+  int B;
+  int gamma;
+  int rows_per_cta;            // shard size (last shard may be shorter)
+  uint32_t seed_lo, seed_hi;   // Philox key
+  int64_t timeout_ns;          // rendezvous wait limit
+  int skip_cta;                // fault injection: this CTA never posts (-1: off)
+};
+
+// ------------------------------------------------------------ PTX helpers --
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int32_t ld_relaxed_gpu_s32(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_relaxed_gpu_max_u64(unsigned long long* p,
+                                                        unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void set_status(SyncHeader* hdr, int code) {
+  atomicCAS(reinterpret_cast<int*>(&hdr->status), 0, code);
+}
+
+// ------------------------------------------------------------------ bf16 --
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t h) {
+  return __uint_as_float(h << 16);
+}
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits_rn(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// ------------------------------------------------------------------- key --
+
+// Order-preserving map of an fp32 value to 32 bits (larger value, larger
+// bits); -0 is folded onto +0 so that the two compare equal.
+__device__ __forceinline__ uint32_t ord32(float x) {
+  if (x == 0.0f) x = 0.0f;
+  uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// {score bits : 32, inverted token id : 32}: the maximum key is the largest
+// score, and among equal scores the smallest token id.  Key 0 is below every
+// real key (ord32 of -inf is 0x007FFFFF), so a zeroed slot means "empty".
+__device__ __forceinline__ unsigned long long make_key(float s, uint32_t v) {
+  return ((unsigned long long)ord32(s) << 32) | (unsigned long long)(0xFFFFFFFFu - v);
+}
+
+__device__ __forceinline__ int32_t key_token(unsigned long long key) {
+  return (int32_t)(0xFFFFFFFFu - (uint32_t)key);
+}
+
+// ---------------------------------------------------------------- Philox --
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
+// 32x32->64 multiplies, the key bumped by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint32_t philox_word(uint4 r, uint32_t w) {
+  return w == 0 ? r.x : (w == 1 ? r.y : (w == 2 ? r.z : r.w));
+}
+
+// Random bits -> fp32 uniform: the midpoint of bin (x >> 9) of 2^23 bins,
+// exact in fp32 and strictly inside (0, 1).
+__device__ __forceinline__ float bits_to_uniform(uint32_t x) {
+  return (float)((x >> 9) * 2u + 1u) * 0x1p-24f;
+}
+
+// Gumbel-max score fp32(logit / T) + (-log(-log U)), each step in fp32.
+__device__ __forceinline__ float gumbel_score(float logit, float T, uint32_t x) {
+  const float U = bits_to_uniform(x);
+  const float e = -logf(U);
+  const float g = -logf(e);
+  return __fadd_rn(__fdiv_rn(logit, T), g);
+}
+
+// ------------------------------------------------------------- epilogue --
+
+// The fused epilogue of one (token v, request b, step k): fp32 accumulation
+// -> bf16 bias; fp32 add of the base logit -> bf16 logit; selection score.
+// Returns the selection key; *logit_bits receives the bf16 logit.
+__device__ __forceinline__ unsigned long long epilogue_key(
+    float acc, uint32_t base_bits, float T, uint32_t seed_lo, uint32_t seed_hi, int b, int k,
+    uint32_t v, uint16_t* logit_bits) {
+  const float bias = __bfloat162float(__float2bfloat16_rn(acc));
+  const uint16_t lb = float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(base_bits), bias));
+  *logit_bits = lb;
+  const float logit = bf16_bits_to_float(lb);
+  float s = logit;
+  if (T > 0.0f) {
+    const uint4 r = philox4x32_10(make_uint4(v >> 2, (uint32_t)k, (uint32_t)b, 0u), seed_lo,
+                                  seed_hi);
+    s = gumbel_score(logit, T, philox_word(r, v & 3u));
+  }
+  return make_key(s, v);
+}
+
+// ----------------------------------------------------------- rendezvous --
+
+// Entry checks every CTA makes on its own (so all agree without talking):
+// anchors inside [0, V), temperatures finite and >= 0.  Returns the status.
+__device__ __forceinline__ int check_inputs(const WalkArgs& a, int* flag_smem) {
+  if (threadIdx.x == 0) *flag_smem = 0;
+  __syncthreads();
+  for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
+    const int32_t an = a.anchor[b];
+    const float T = a.temperature[b];
+    if (an < 0 || (int64_t)an >= a.V) atomicCAS(flag_smem, 0, kStatusAnchor);
+    if (!(T >= 0.0f) || isinf(T)) atomicCAS(flag_smem, 0, kStatusTemp);
+  }
+  __syncthreads();
+  return *flag_smem;
+}
+
+// Clear the rendezvous slots of the other parity (CTA 0 only).
+__device__ __forceinline__ void clear_other_parity(const SyncView& s, uint32_t parity) {
+  const uint32_t q = parity ^ 1u;
+  uint32_t* c = s.count_at(q, 0);
+  for (int i = threadIdx.x; i < s.max_gamma * kCountStride; i += blockDim.x) c[i] = 0u;
+  unsigned long long* kk = s.key_at(q, 0, 0);
+  for (int i = threadIdx.x; i < s.max_gamma * s.max_B; i += blockDim.x) kk[i] = 0ull;
+}
+
+// One step's cross-CTA selection.  cta_key[b] holds this CTA's best key of
+// request b; on return tok_smem[b] holds the common winner of request b.
+// Returns false if the wait ran out or another CTA reported an error; then
+// every CTA leaves the walk.
+__device__ __forceinline__ bool exchange(const WalkArgs& a, uint32_t parity, int k,
+                                         const unsigned long long* cta_key, int32_t* tok_smem,
+                                         int* flag_smem) {
+  const bool post = (int)blockIdx.x != a.skip_cta;
+  if (post) {
+    for (int b = threadIdx.x; b < a.B; b += blockDim.x)
+      red_relaxed_gpu_max_u64(a.sync.key_at(parity, k, b), cta_key[b]);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    uint32_t* cnt = a.sync.count_at(parity, k);
+    __threadfence();
+    if (post) red_release_gpu_add(cnt, 1u);
+    const uint32_t target = gridDim.x;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t spins = 0;
+    while (ld_acquire_gpu(cnt) < target) {
+      if ((++spins & 63u) == 0u) {
+        if (ld_relaxed_gpu_s32(&a.sync.hdr->status) != 0) { ok = 0; break; }
+        if ((int64_t)(globaltimer_ns() - t0) > a.timeout_ns) {
+          set_status(a.sync.hdr, kStatusTimeout);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    *flag_smem = ok;
+  }
+  __syncthreads();
+  const bool ok = *flag_smem != 0;
+  if (ok) {
+    for (int b = threadIdx.x; b < a.B; b += blockDim.x)
+      tok_smem[b] = key_token(ld_acquire_gpu_u64(a.sync.key_at(parity, k, b)));
+  }
+  __syncthreads();
+  return ok;
+}
+
+}  // namespace dspark

@@ -1,0 +1,167 @@
+"""Compare a CUDA walk with the CPU oracle, element by element.
+
+The rule (from the walk's numerics: fp32 accumulation in any order on the GPU,
+an fp64 sum in the oracle, then two bf16 roundings on both sides):
+
+* logits: a GPU logit passes if it is within 1 bf16 ulp of the oracle logit
+  (ulp taken at the larger magnitude), or if it equals bf16(base + b') where
+  b' is the other bf16 neighbour of the exact projection (an fp32
+  accumulation may legitimately round the bias to either neighbour when the
+  exact value sits near a rounding boundary);
+* tokens: step by step, with the oracle fed the GPU's previous token (teacher
+  forcing), the GPU token must be the oracle's argmax, except at a near-tie:
+  greedy, the GPU token's oracle logit is within 2 bf16 ulp of the maximum;
+  sampled, its oracle score is within the fp32 error bound of the two scores
+  (logit error / T + 2^-18 (1 + |g|) + 2 fp32 ulp, for each of the two).
+"""
+import math
+
+import numpy as np
+
+import oracle
+import synth
+
+
+def bf16_vals(h):
+    return (np.asarray(h, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(
+        np.float64)
+
+
+def bf16_ulp(x):
+    """Spacing of bf16 at |x| (normal range; 2^-133 below it)."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    ulp = np.exp2(e - 7)
+    return np.where(a >= 2.0**-126, ulp, 2.0**-133)
+
+
+def f32_ulp(x):
+    return np.spacing(np.abs(np.asarray(x, dtype=np.float32))).astype(np.float64)
+
+
+def _other_neighbour_logit(O, W1, W2, base_bits, prev, v):
+    """bf16(base + b') with b' the other bf16 neighbour of the exact W2[v].u."""
+    u = bf16_vals(W1[prev])
+    acc = float(np.dot(bf16_vals(W2[v]), u))
+    n1 = int(O.bf16_rne(np.array([acc]))[0])
+    v1 = bf16_vals([n1])[0]
+    if v1 == acc:
+        return None
+    # neighbour on the other side of acc
+    step = math.copysign(1, acc - v1)
+    if v1 == 0:
+        n2 = 0x0001 if step > 0 else 0x8001
+    else:
+        away = (acc - v1) * v1 > 0      # moving away from zero
+        n2 = n1 + 1 if away else n1 - 1
+    other = bf16_vals([n2])[0]
+    return int(O.bf16_rne(np.array([bf16_vals([base_bits])[0] + other]))[0])
+
+
+class Report:
+    def __init__(self):
+        self.logits_checked = 0
+        self.logits_exact = 0
+        self.logits_ulp = 0
+        self.logits_neighbour = 0
+        self.steps_checked = 0
+        self.steps_exact = 0
+        self.near_ties = 0
+        self.failures = []
+
+    def ok(self):
+        return not self.failures
+
+    def __repr__(self):
+        return ("Report(logits=%d exact=%d 1ulp=%d neighbour=%d steps=%d exact=%d near_ties=%d "
+                "failures=%d %s)" % (self.logits_checked, self.logits_exact, self.logits_ulp,
+                                     self.logits_neighbour, self.steps_checked, self.steps_exact,
+                                     self.near_ties, len(self.failures), self.failures[:5]))
+
+
+def check(inputs: "synth.WalkInputs", gpu_tokens, gpu_logits=None, requests=None,
+          nthreads=0, O=None, report=None):
+    """Check the GPU's tokens [B, gamma] (and logits [B, gamma, V]) for `requests`.
+
+    Returns a Report; ``report.ok()`` is the verdict.
+    """
+    O = O or oracle.default()
+    rep = report or Report()
+    B, gamma, V = inputs.base.shape
+    requests = list(range(B)) if requests is None else list(requests)
+    W1 = synth.bits(inputs.W1)
+    W2 = synth.bits(inputs.W2)
+    base_all = synth.bits(inputs.base)
+    gpu_tokens = np.asarray(gpu_tokens)
+    for b in requests:
+        T = float(inputs.temperature[b])
+        toks = gpu_tokens[b].astype(np.int32)
+        if np.any(toks < 0) or np.any(toks >= V):
+            rep.failures.append(("token out of range", b, toks.tolist()))
+            continue
+        ot, ol, osc = _oracle_request(O, W1, W2, base_all, inputs, b, toks, nthreads)
+        rep.steps_checked += gamma
+        for k in range(gamma):
+            ok_row = ol[k]
+            if gpu_logits is not None:
+                gl = np.asarray(gpu_logits[b, k])
+                _check_logits(O, rep, W1, W2, base_all[b, k], gl, ok_row,
+                              int(inputs.anchor[b]) if k == 0 else int(toks[k - 1]), b, k)
+            g = int(toks[k])
+            if g == int(ot[k]):
+                rep.steps_exact += 1
+                continue
+            if T == 0.0:
+                vals = bf16_vals(ok_row)
+                m1, lg = vals.max(), vals[g]
+                if m1 - lg <= 2 * bf16_ulp(max(abs(m1), abs(lg))):
+                    rep.near_ties += 1
+                    continue
+                rep.failures.append(("greedy token", b, k, g, int(ot[k]), float(m1), float(lg)))
+            else:
+                s = osc[k].astype(np.float64)
+                o = int(ot[k])
+                lv = bf16_vals(ok_row)
+
+                def tol(v):
+                    gv = s[v] - lv[v] / T
+                    dl = 0.0
+                    if gpu_logits is not None:
+                        dl = abs(bf16_vals([gpu_logits[b, k, v]])[0] - lv[v]) / T
+                    return dl + 2.0**-18 * (1 + abs(gv)) + 2 * f32_ulp(s[v])
+
+                if s[o] - s[g] <= tol(o) + tol(g):
+                    rep.near_ties += 1
+                    continue
+                rep.failures.append(("sampled token", b, k, g, o, float(s[o]), float(s[g])))
+    return rep
+
+
+def _oracle_request(O, W1, W2, base_all, inputs, b, toks, nthreads):
+    """Oracle walk of request b alone (at request index b), teacher-forced."""
+    T = float(inputs.temperature[b])
+    ot, ol, osc = O.walk(W1, W2, base_all[b:b + 1], np.array([inputs.anchor[b]], np.int32),
+                         np.array([T], np.float32), inputs.seed, forced=toks[None, :],
+                         want_scores=T != 0.0, nthreads=nthreads, req0=b)
+    return ot[0], ol[0], (osc[0] if osc is not None else None)
+
+
+def _check_logits(O, rep, W1, W2, base_row, gl, ol, prev, b, k):
+    gv = bf16_vals(gl)
+    ov = bf16_vals(ol)
+    n = gv.size
+    rep.logits_checked += n
+    exact = gv == ov
+    rep.logits_exact += int(exact.sum())
+    bad = np.nonzero(~exact)[0]
+    if bad.size == 0:
+        return
+    within = np.abs(gv[bad] - ov[bad]) <= bf16_ulp(np.maximum(np.abs(gv[bad]), np.abs(ov[bad])))
+    rep.logits_ulp += int(within.sum())
+    for v in bad[~within]:
+        alt = _other_neighbour_logit(O, W1, W2, int(base_row[v]), prev, int(v))
+        if alt is not None and alt == int(gl[v]):
+            rep.logits_neighbour += 1
+            continue
+        rep.failures.append(("logit", b, k, int(v), float(gv[v]), float(ov[v])))

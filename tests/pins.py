@@ -391,15 +391,16 @@ def pin_spike(O):
 
 
 def pin_batch_independence(O):
-    """Greedy: a request's tokens are the same alone and inside a batch."""
+    """A request's walk is the same alone (at its own request index) and in a batch."""
     import synth
-    x = synth.make_custom(V=777, gamma=4, B=5, seed=8)
+    x = synth.make_custom(V=777, gamma=4, B=5, seed=8, temperatures=(0.0, 1.0, 0.6))
     bits = synth.bits
     t, lg, _ = O.walk(bits(x.W1), bits(x.W2), bits(x.base), x.anchor.numpy(),
-                      x.temperature.numpy(), 0)
+                      x.temperature.numpy(), 31)
     for b in range(5):
         tb, lb, _ = O.walk(bits(x.W1), bits(x.W2), bits(x.base[b:b + 1]),
-                           x.anchor.numpy()[b:b + 1], x.temperature.numpy()[b:b + 1], 0)
+                           x.anchor.numpy()[b:b + 1], x.temperature.numpy()[b:b + 1], 31,
+                           req0=b)
         assert np.array_equal(tb[0], t[b]) and np.array_equal(lb[0], lg[b]), \
             "request %d differs alone vs in the batch" % b
 

@@ -1,0 +1,281 @@
+"""Parity of the CUDA walk with the CPU oracle, through the C ABI (GPU only).
+
+Small shapes are compared on every logit and every step; the five full-size
+workloads are compared on sampled requests (the oracle replays one request
+at its own request index), in the launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import parity
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="session")
+def walkmod():
+    if not torch.cuda.is_available():
+        pytest.fail("a GPU test ran without a CUDA device")
+    from serial_draft_head_gb300 import walk
+    walk.load(build_if_missing=True)
+    return walk
+
+
+def make_walk(walkmod, x, max_B=None, max_gamma=None):
+    return walkmod.Walk(x.W1.cuda(), x.W2.cuda(), max_B or x.B, max_gamma or x.gamma)
+
+
+def gpu_run(w, x, want_logits=True, seed=None):
+    B, gamma, V = x.base.shape
+    base = x.base.cuda()
+    anchor = x.anchor.cuda()
+    temp = x.temperature.cuda()
+    tokens = torch.full((B, gamma), -2, dtype=torch.int32, device="cuda")
+    logits = torch.empty(B, gamma, V, dtype=torch.bfloat16, device="cuda") if want_logits else None
+    w.run(base, anchor, temp, x.seed if seed is None else seed, tokens, logits)
+    st = w.status()
+    lg = logits.view(torch.int16).cpu().numpy().view(np.uint16) if want_logits else None
+    return st, tokens.cpu().numpy(), lg
+
+
+SMALL = [
+    # V, gamma, B, temperatures, seed
+    (12, 3, 1, (0.0,), 1),                 # the Fig. 2 shape of "Weights That Stay", r = 256
+    (1000, 5, 3, (0.0, 1.0, 0.6), 2),
+    (5003, 7, 8, (0.6, 0.0, 1.0), 3),      # ragged shards
+    (152 * 33 + 17, 4, 17, (0.0, 1.0), 4),  # every SM busy plus a ragged tail, B > 16
+    (20000, 3, 2, (1.0,), 5),
+    (4096, 2, 33, (0.0, 0.6, 1.0), 6),
+    (2048, 1, 256, (0.0, 0.6, 1.0), 7),    # the largest batch
+    (3000, 64, 1, (0.0,), 8),              # the longest walk
+]
+
+
+@pytest.mark.parametrize("V,gamma,B,temps,seed", SMALL)
+def test_small_every_logit(walkmod, V, gamma, B, temps, seed):
+    x = synth.make_custom(V=V, gamma=gamma, B=B, seed=seed, temperatures=temps,
+                          noise_seed=1000 + seed)
+    w = make_walk(walkmod, x)
+    st, toks, lg = gpu_run(w, x)
+    assert st == 0, walkmod.dspark_walk_strerror(st)
+    rep = parity.check(x, toks, lg)
+    assert rep.ok(), rep
+    w.close()
+
+
+def test_tiny_config(walkmod):
+    x = synth.make_inputs("tiny")
+    w = make_walk(walkmod, x)
+    st, toks, lg = gpu_run(w, x)
+    assert st == 0
+    rep = parity.check(x, toks, lg)
+    assert rep.ok(), rep
+
+
+# ------------------------------------------------------- full-size configs --
+
+_WEIGHTS = {}
+
+
+def full_inputs(name, B, round_index=0):
+    cfg = synth.CONFIGS[name]
+    if name not in _WEIGHTS:
+        _WEIGHTS.clear()
+        W1, W2, _ = synth.make_weights(cfg.V, cfg.r, cfg.seed)
+        _WEIGHTS[name] = (W1, W2)
+    return synth.make_inputs(cfg, B=B, round_index=round_index, weights=_WEIGHTS[name])
+
+
+_WALKS = {}
+
+
+def full_walk(walkmod, name, x):
+    cfg = synth.CONFIGS[name]
+    if name not in _WALKS:
+        for w in _WALKS.values():
+            w.close()
+        _WALKS.clear()
+        _WALKS[name] = walkmod.Walk(x.W1.cuda(), x.W2.cuda(), max(cfg.batches), cfg.gamma)
+    return _WALKS[name]
+
+
+def _sample_requests(B, temps):
+    pick = {0, B - 1}
+    pick.update(range(min(B, len(temps))))          # one of each temperature
+    pick.update(range(max(0, B - len(temps)), B))
+    if B > 8:
+        pick.add(B // 2)
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("round_index", [0, 1, 99])
+def test_qwen3_resident(walkmod, round_index):
+    x = full_inputs("qwen3_resident", 1, round_index)
+    w = full_walk(walkmod, "qwen3_resident", x)
+    st, toks, lg = gpu_run(w, x)
+    assert st == 0
+    rep = parity.check(x, toks, lg)
+    assert rep.ok(), rep
+
+
+@pytest.mark.parametrize("B", [1, 4, 8, 16])
+def test_long_block(walkmod, B):
+    x = full_inputs("long_block", B)
+    w = full_walk(walkmod, "long_block", x)
+    st, toks, lg = gpu_run(w, x)
+    assert st == 0
+    rep = parity.check(x, toks, lg, requests=_sample_requests(B, (0.0,)))
+    assert rep.ok(), rep
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_partial(walkmod, B):
+    x = full_inputs("partial", B)
+    w = full_walk(walkmod, "partial", x)
+    st, toks, lg = gpu_run(w, x)
+    assert st == 0
+    rep = parity.check(x, toks, lg, requests=_sample_requests(B, (0.0,)))
+    assert rep.ok(), rep
+
+
+@pytest.mark.parametrize("B", [1, 16, 64, 128, 253])
+def test_sampled(walkmod, B):
+    x = full_inputs("sampled", B)
+    w = full_walk(walkmod, "sampled", x)
+    st, toks, lg = gpu_run(w, x)
+    assert st == 0
+    rep = parity.check(x, toks, lg, requests=_sample_requests(B, (0.0, 0.6, 1.0)))
+    assert rep.ok(), rep
+
+
+def test_sampled_full_batch_zero_projection_property(walkmod):
+    """With W2 = 0 every greedy token is argmax(base): checked for all 253 requests."""
+    x = full_inputs("sampled", 253)
+    x.temperature.zero_()
+    w = walkmod.Walk(x.W1.cuda(), torch.zeros_like(x.W2).cuda(), 253, x.gamma)
+    st, toks, _ = gpu_run(w, x, want_logits=False)
+    assert st == 0
+    want = np.argmax(x.base.float().numpy(), axis=2)
+    assert np.array_equal(toks, want)
+    w.close()
+
+
+# --------------------------------------------------------- round behaviour --
+
+def test_graph_replay_and_parity_alternation(walkmod):
+    """A captured round replays correctly many times with no memset in between."""
+    x = synth.make_custom(V=7000, gamma=5, B=4, seed=40, temperatures=(0.0, 1.0))
+    w = make_walk(walkmod, x)
+    base, anchor, temp = x.base.cuda(), x.anchor.cuda(), x.temperature.cuda()
+    tokens = torch.full((4, 5), -2, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        w.run(base, anchor, temp, 77, tokens, stream=s)      # warm-up outside capture
+    s.synchronize()
+    eager = tokens.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        w.run(base, anchor, temp, 77, tokens, stream=s)
+    for _ in range(5):
+        tokens.fill_(-2)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(tokens, eager)
+    assert w.status() == 0
+    rep = parity.check(x, eager.cpu().numpy())
+    assert rep.ok(), rep
+
+
+def test_rounds_back_to_back(walkmod):
+    """Consecutive rounds with fresh inputs on one handle each match the oracle."""
+    cfg_x = synth.make_custom(V=9001, gamma=3, B=2, seed=41, temperatures=(0.0, 0.6))
+    w = make_walk(walkmod, cfg_x)
+    for i in range(4):
+        x = synth.make_custom(V=9001, gamma=3, B=2, seed=41, temperatures=(0.0, 0.6),
+                              noise_seed=i)
+        x.base = synth.make_custom(V=9001, gamma=3, B=2, seed=500 + i).base
+        st, toks, lg = gpu_run(w, x)
+        assert st == 0
+        assert parity.check(x, toks, lg).ok()
+
+
+def test_untouched_memory(walkmod):
+    """Nothing past [B, gamma] tokens or [B, gamma, V] logits is written."""
+    x = synth.make_custom(V=3333, gamma=3, B=3, seed=42, temperatures=(0.0, 1.0))
+    w = make_walk(walkmod, x, max_B=8, max_gamma=8)
+    tok = torch.full((3 * 3 + 64,), 12345, dtype=torch.int32, device="cuda")
+    lgt = torch.full((3 * 3 * 3333 + 512,), 7.0, dtype=torch.bfloat16, device="cuda")
+    w.run(x.base.cuda(), x.anchor.cuda(), x.temperature.cuda(), x.seed, tok[:9].view(3, 3),
+          lgt[:3 * 3 * 3333].view(3, 3, 3333))
+    assert w.status() == 0
+    assert torch.all(tok[9:] == 12345)
+    assert torch.all(lgt[3 * 3 * 3333:] == 7.0)
+
+
+def test_host_buffers_match_device_buffers(walkmod):
+    x = synth.make_custom(V=4321, gamma=4, B=5, seed=43, temperatures=(0.0, 0.6, 1.0))
+    w = make_walk(walkmod, x)
+    st, toks, lg = gpu_run(w, x)
+    assert st == 0
+    base = x.base.pin_memory()
+    out = torch.full((5, 4), -2, dtype=torch.int32).pin_memory()
+    outl = torch.empty(5, 4, 4321, dtype=torch.bfloat16).pin_memory()
+    st2 = walkmod.dspark_walk_run_host(w.h, base, x.anchor.pin_memory(),
+                                       x.temperature.pin_memory(), x.seed, out, 5, 4, outl)
+    assert st2 == 0
+    assert np.array_equal(out.numpy(), toks)
+    assert np.array_equal(outl.view(torch.int16).numpy().view(np.uint16), lg)
+
+
+# ------------------------------------------------------------------ errors --
+
+def test_bad_anchor_and_temperature_are_reported(walkmod):
+    x = synth.make_custom(V=2000, gamma=3, B=2, seed=44)
+    w = make_walk(walkmod, x)
+    x.anchor[1] = 2000
+    st, toks, _ = gpu_run(w, x, want_logits=False)
+    assert st == walkmod.EANCHOR and np.all(toks == -1)
+    x.anchor[1] = 5
+    x.temperature[0] = -1.0
+    st, toks, _ = gpu_run(w, x, want_logits=False)
+    assert st == walkmod.ETEMP and np.all(toks == -1)
+    x.temperature[0] = float("nan")
+    st, toks, _ = gpu_run(w, x, want_logits=False)
+    assert st == walkmod.ETEMP
+    x.temperature[0] = 0.0
+    st, toks, lg = gpu_run(w, x)          # the handle still works afterwards
+    assert st == 0 and parity.check(x, toks, lg).ok()
+
+
+def test_host_side_errors(walkmod):
+    x = synth.make_custom(V=500, gamma=2, B=2, seed=45)
+    w = make_walk(walkmod, x)
+    base, anchor, temp = x.base.cuda(), x.anchor.cuda(), x.temperature.cuda()
+    tok = torch.empty(2, 2, dtype=torch.int32, device="cuda")
+    with pytest.raises(walkmod.WalkError) as e:
+        walkmod.dspark_walk_run(w.h, base, anchor, temp, 0, tok, 3, 2)      # B > max_B
+    assert e.value.code == walkmod.EINVAL
+    with pytest.raises(walkmod.WalkError):
+        walkmod.dspark_walk_run(w.h, base, anchor, temp, 0, tok, 2, 3)      # gamma > max
+    with pytest.raises(walkmod.WalkError):
+        walkmod.dspark_walk_run(w.h, 0, anchor, temp, 0, tok, 2, 2)         # NULL base
+    with pytest.raises(walkmod.WalkError) as e:
+        walkmod.dspark_walk_create(x.W1.cuda(), x.W2.cuda(), 500, 128, 2, 2)  # r != 256
+    assert e.value.code == walkmod.EUNSUPPORTED
+
+
+def test_lost_arrival_times_out_and_recovers(walkmod):
+    """A CTA that never posts makes the round end with ETIMEOUT, not hang."""
+    x = synth.make_custom(V=8000, gamma=4, B=2, seed=46, temperatures=(0.0, 1.0))
+    w = make_walk(walkmod, x)
+    walkmod.dspark_walk_set_limits(w.h, 50_000_000, 1)      # 50 ms; CTA 1 skips
+    st, toks, _ = gpu_run(w, x, want_logits=False)
+    assert st == walkmod.ETIMEOUT
+    assert np.all(toks == -1)
+    walkmod.dspark_walk_set_limits(w.h, 200_000_000, -1)
+    for _ in range(2):                                     # both parities clean again
+        st, toks, lg = gpu_run(w, x)
+        assert st == 0
+        assert parity.check(x, toks, lg).ok()

@@ -1,0 +1,71 @@
+"""The parity checker itself, on the CPU: it accepts the oracle's own walk and
+rejects walks with planted mistakes (a wrong token, logits off by 2 ulp)."""
+import numpy as np
+
+import oracle
+import parity
+import synth
+
+
+def _walk(x, **kw):
+    return oracle.walk(synth.bits(x.W1), synth.bits(x.W2), synth.bits(x.base), x.anchor.numpy(),
+                       x.temperature.numpy(), x.seed, **kw)
+
+
+def test_accepts_the_oracle_itself():
+    x = synth.make_custom(V=600, gamma=4, B=4, seed=21, temperatures=(0.0, 1.0, 0.6, 0.0),
+                          noise_seed=5)
+    t, lg, _ = _walk(x)
+    rep = parity.check(x, t, lg)
+    assert rep.ok(), rep
+    assert rep.logits_exact == rep.logits_checked and rep.steps_exact == rep.steps_checked
+
+
+def test_rejects_a_wrong_greedy_token():
+    x = synth.make_custom(V=600, gamma=4, B=1, seed=22)
+    t, lg, _ = _walk(x)
+    vals = parity.bf16_vals(lg[0, 2])
+    wrong = int(np.argmin(vals))          # far from the maximum
+    t2 = t.copy()
+    t2[0, 2] = wrong
+    rep = parity.check(x, t2, None)
+    assert not rep.ok() and rep.failures[0][0] == "greedy token"
+
+
+def test_rejects_a_wrong_sampled_token():
+    x = synth.make_custom(V=600, gamma=3, B=2, seed=23, temperatures=(1.0,), noise_seed=9)
+    t, lg, sc = _walk(x, want_scores=True)
+    t2 = t.copy()
+    t2[1, 1] = int(np.argmin(sc[1, 1]))
+    rep = parity.check(x, t2, None)
+    assert not rep.ok() and rep.failures[0][0] == "sampled token"
+
+
+def test_logit_tolerance():
+    x = synth.make_custom(V=300, gamma=2, B=1, seed=24)
+    t, lg, _ = _walk(x)
+    one = lg.copy()
+    v = 17
+    one[0, 0, v] = one[0, 0, v] + 1     # next bf16 pattern: 1 ulp away
+    assert parity.check(x, t, one).ok()
+    two = lg.copy()
+    two[0, 1, v] = two[0, 1, v] + 2     # 2 ulp away
+    rep = parity.check(x, t, two)
+    assert not rep.ok() and rep.failures[0][0] == "logit"
+
+
+def test_near_tie_rule_accepts_the_runner_up_of_a_tie():
+    # W2 = 0 and a base with two equal maxima: either token is a near-tie;
+    # the oracle picks the smaller id, a GPU picking the other must pass.
+    V, gamma = 50, 1
+    x = synth.make_custom(V=V, gamma=gamma, B=1, seed=25)
+    import torch
+    x.W2.zero_()
+    base = torch.zeros(1, gamma, V)
+    base[0, 0, 10] = 3.0
+    base[0, 0, 20] = 3.0 + 2.0**-6       # 1 bf16 ulp above at 3.0
+    x.base = base.to(torch.bfloat16)
+    t, lg, _ = _walk(x)
+    assert int(t[0, 0]) == 20
+    rep = parity.check(x, np.array([[10]], np.int32), lg)
+    assert rep.ok() and rep.near_ties == 1
