@@ -166,18 +166,19 @@ def test_sampled_full_batch_zero_projection_property(walkmod):
 
 def test_graph_replay_and_parity_alternation(walkmod):
     """A captured round replays correctly many times with no memset in between."""
-    x = synth.make_custom(V=7000, gamma=5, B=4, seed=40, temperatures=(0.0, 1.0))
+    x = synth.make_custom(V=7000, gamma=5, B=4, seed=40, temperatures=(0.0, 1.0),
+                          noise_seed=77)
     w = make_walk(walkmod, x)
     base, anchor, temp = x.base.cuda(), x.anchor.cuda(), x.temperature.cuda()
     tokens = torch.full((4, 5), -2, dtype=torch.int32, device="cuda")
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
-        w.run(base, anchor, temp, 77, tokens, stream=s)      # warm-up outside capture
+        w.run(base, anchor, temp, x.seed, tokens, stream=s)  # warm-up outside capture
     s.synchronize()
     eager = tokens.clone()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        w.run(base, anchor, temp, 77, tokens, stream=s)
+        w.run(base, anchor, temp, x.seed, tokens, stream=s)
     for _ in range(5):
         tokens.fill_(-2)
         g.replay()
