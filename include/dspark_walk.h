@@ -54,6 +54,7 @@ extern "C" {
 #define DSPARK_EANCHOR (-5)      /* an anchor was outside [0, V) (device-detected) */
 #define DSPARK_EUNSUPPORTED (-6) /* r != 256, or the device is not sm_103 */
 #define DSPARK_ETEMP (-7)        /* a temperature was negative or not finite (device-detected) */
+#define DSPARK_ELIMIT (-8)       /* B or gamma above dspark_walk_run_noalloc's fixed maximum */
 
 /* Opaque handle: resident weight layout, rendezvous slots, status word. */
 typedef struct dspark_walk dspark_walk;
@@ -165,6 +166,34 @@ const char *dspark_walk_strerror(int code);
 
 /* dspark_walk_destroy -- free everything the handle owns (synchronises the device). */
 int dspark_walk_destroy(dspark_walk_t h);
+
+/*
+ * dspark_walk_run_noalloc -- one round of the walk that allocates no device
+ * memory at all (the pages have no counterpart; it exists for callers, not
+ * for the method).  Some callers may not call cudaMalloc: code running inside
+ * a memory allocator or its callbacks, processes whose device memory belongs
+ * to a caching pool that must not be bypassed, and latency-critical paths
+ * that must never wait on the driver's allocator.  They cannot use
+ * dspark_walk_create, which allocates.
+ *
+ *   W1, W2       device, bf16 [V, r] row-major (read in place every step:
+ *                this is the streamed kernel, no on-chip residency)
+ *   other arguments as dspark_walk_run; 1 <= B <= 64, 1 <= gamma <= 16
+ *                (DSPARK_ELIMIT above that)
+ *
+ * The rendezvous slots live in one fixed ~17.5 KB block of device memory
+ * built into the library (every GPU that loads the library keeps it until
+ * the process exits).  The first call on a device looks up that block's
+ * address, so make it before capturing a stream into a CUDA graph.  Each
+ * call clears the block on `stream` before its launch; calls that could
+ * overlap on the GPU (unordered streams) race on the block and must not be
+ * made.  Device-detected errors (bad anchor or temperature, a rendezvous
+ * timeout) are reported only as -1 in out_tokens.
+ */
+int dspark_walk_run_noalloc(const void *W1, const void *W2, int64_t V, int r,
+                            const void *base_logits, const int32_t *anchor,
+                            const float *temperature, uint64_t seed, int32_t *out_tokens, int B,
+                            int gamma, void *out_logits, void *stream);
 
 #ifdef __cplusplus
 }

@@ -264,6 +264,9 @@ const char* dspark_walk_strerror(int code) {
     case DSPARK_EANCHOR: return "anchor token outside [0, V)";
     case DSPARK_EUNSUPPORTED: return "unsupported rank or device (needs r = 256 on sm_103)";
     case DSPARK_ETEMP: return "temperature negative or not finite";
+    case DSPARK_ELIMIT:
+      return "batch or walk length above the allocation-free entry point's maximum (B <= 64, "
+             "gamma <= 16)";
     default: return "unknown status";
   }
 }

@@ -20,6 +20,7 @@ ETIMEOUT = -4
 EANCHOR = -5
 EUNSUPPORTED = -6
 ETEMP = -7
+ELIMIT = -8
 
 KERNEL_STREAM = 0
 KERNEL_RESIDENT = 1
@@ -52,7 +53,7 @@ class dspark_walk_plan(ctypes.Structure):
 EXPORTS = [
     "dspark_walk_create", "dspark_walk_run", "dspark_walk_run_host", "dspark_walk_status",
     "dspark_walk_get_plan", "dspark_walk_set_limits", "dspark_walk_strerror",
-    "dspark_walk_destroy",
+    "dspark_walk_destroy", "dspark_walk_run_noalloc",
 ]
 
 
@@ -81,6 +82,7 @@ def load(build_if_missing=True):
     L.dspark_walk_strerror.argtypes = [i32]
     L.dspark_walk_strerror.restype = ctypes.c_char_p
     L.dspark_walk_destroy.argtypes = [vp]
+    L.dspark_walk_run_noalloc.argtypes = [vp, vp, i64, i32, vp, vp, vp, u64, vp, i32, i32, vp, vp]
     for name in EXPORTS:
         if name != "dspark_walk_strerror":
             getattr(L, name).restype = ctypes.c_int
@@ -157,6 +159,20 @@ def dspark_walk_set_limits(h, timeout_ns, skip_cta=-1):
 
 def dspark_walk_destroy(h):
     return _check(load().dspark_walk_destroy(h), "dspark_walk_destroy")
+
+
+def dspark_walk_run_noalloc(W1, W2, V, r, base_logits, anchor, temperature, seed, out_tokens,
+                            B, gamma, out_logits=None, stream=None):
+    """One round without any device allocation (B <= 64, gamma <= 16).
+
+    For callers that may not allocate device memory; W2 is read in place and
+    the rendezvous slots are a fixed block inside the library.  Returns the
+    launch status; device-detected errors show up as -1 tokens.
+    """
+    return _check(load().dspark_walk_run_noalloc(
+        _ptr(W1), _ptr(W2), int(V), int(r), _ptr(base_logits), _ptr(anchor), _ptr(temperature),
+        int(seed) & (2**64 - 1), _ptr(out_tokens), int(B), int(gamma), _ptr(out_logits),
+        _stream(stream)), "dspark_walk_run_noalloc")
 
 
 class Walk:

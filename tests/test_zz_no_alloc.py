@@ -1,0 +1,59 @@
+"""The allocation-free entry point against the handle-based one (GPU only).
+
+dspark_walk_run_noalloc serves callers that may not allocate device memory;
+its rendezvous slots live in a fixed block inside the library, shared by
+every call.  Two calls in a row must each give the same tokens and logits as
+dspark_walk_run on the same inputs.  This file is collected last on purpose.
+"""
+import numpy as np
+import pytest
+import torch
+
+import parity
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _handle_run(walk, x):
+    w = walk.Walk(x.W1.cuda(), x.W2.cuda(), x.B, x.gamma)
+    tok = torch.full((x.B, x.gamma), -2, dtype=torch.int32, device="cuda")
+    lg = torch.empty(x.B, x.gamma, x.V, dtype=torch.bfloat16, device="cuda")
+    w.run(x.base.cuda(), x.anchor.cuda(), x.temperature.cuda(), x.seed, tok, lg)
+    assert w.status() == 0
+    w.close()
+    return tok.cpu().numpy(), lg.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def test_noalloc_matches_handle_path_twice_in_a_row():
+    if not torch.cuda.is_available():
+        pytest.fail("a GPU test ran without a CUDA device")
+    from serial_draft_head_gb300 import walk
+    walk.load(build_if_missing=True)
+    for i, (V, B, gamma) in enumerate([(5003, 6, 5), (20011, 3, 7)]):
+        x = synth.make_custom(V=V, gamma=gamma, B=B, seed=60 + i, temperatures=(0.0, 0.6, 1.0),
+                              noise_seed=900 + i)
+        want_tok, want_lg = _handle_run(walk, x)
+        W1, W2 = x.W1.cuda(), x.W2.cuda()
+        tok = torch.full((B, gamma), -2, dtype=torch.int32, device="cuda")
+        lg = torch.empty(B, gamma, V, dtype=torch.bfloat16, device="cuda")
+        walk.dspark_walk_run_noalloc(W1, W2, V, 256, x.base.cuda(), x.anchor.cuda(),
+                                     x.temperature.cuda(), x.seed, tok, B, gamma, lg)
+        torch.cuda.synchronize()
+        got_tok = tok.cpu().numpy()
+        got_lg = lg.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(got_tok, want_tok)
+        # the same tolerance as every parity test: against the oracle
+        rep = parity.check(x, got_tok, got_lg)
+        assert rep.ok(), rep
+        assert np.array_equal(got_lg, want_lg)
+
+
+def test_noalloc_rejects_sizes_above_its_maximum():
+    from serial_draft_head_gb300 import walk
+    with pytest.raises(walk.WalkError) as e:
+        walk.dspark_walk_run_noalloc(16, 16, 100, 256, 16, 16, 16, 0, 16, 65, 4)
+    assert e.value.code == walk.ELIMIT
+    with pytest.raises(walk.WalkError) as e:
+        walk.dspark_walk_run_noalloc(16, 16, 100, 256, 16, 16, 16, 0, 16, 4, 17)
+    assert e.value.code == walk.ELIMIT
