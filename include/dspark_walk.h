@@ -55,6 +55,7 @@ extern "C" {
 #define DSPARK_EUNSUPPORTED (-6) /* r != 256, or the device is not sm_103 */
 #define DSPARK_ETEMP (-7)        /* a temperature was negative or not finite (device-detected) */
 #define DSPARK_ELIMIT (-8)       /* B or gamma above dspark_walk_run_noalloc's fixed maximum */
+#define DSPARK_EINTERNAL (-9)    /* a device-side consistency check failed (a bug; tokens -1) */
 
 /* Opaque handle: resident weight layout, rendezvous slots, status word. */
 typedef struct dspark_walk dspark_walk;
@@ -160,6 +161,16 @@ int dspark_walk_get_plan(dspark_walk_t h, struct dspark_walk_plan *p);
  * Takes effect from the next run.
  */
 int dspark_walk_set_limits(dspark_walk_t h, int64_t timeout_ns, int skip_cta);
+
+/*
+ * dspark_walk_set_kernel -- choose the kernel of later runs with B <= the
+ * resident layout's batch limit: DSPARK_KERNEL_RESIDENT (the default when
+ * create() found an on-chip placement) or DSPARK_KERNEL_STREAM (re-read W2
+ * from L2/HBM every step: the single-launch "L2 probe" of the blog post's
+ * section "V = 151,936: the whole bf16 table on chip", kept as an ablation).
+ * Returns DSPARK_EUNSUPPORTED if RESIDENT is asked for but was not planned.
+ */
+int dspark_walk_set_kernel(dspark_walk_t h, int kernel);
 
 /* dspark_walk_strerror -- a static description of a status code. */
 const char *dspark_walk_strerror(int code);

@@ -22,8 +22,16 @@ struct dspark_walk {
   int max_gamma = 0;
   const uint16_t* W1 = nullptr;   // caller-owned
   uint16_t* W2 = nullptr;         // handle-owned copy
-  void* sync_mem = nullptr;       // SyncHeader + counts + keys
+  void* sync_mem = nullptr;       // SyncHeader + counts + keys + resident slots
   SyncView sync{};
+  // resident layout (used for runs with B <= res_max_B)
+  uint32_t* W2p = nullptr;        // tiered repack, res_wpc words per CTA
+  unsigned long long* slots = nullptr;  // [2][res_n_cta][max_B]
+  int res_max_B = 0;              // 0: no resident layout
+  bool use_resident = true;       // dspark_walk_set_kernel
+  int res_RS = 0, res_NT = 0, res_R = 0, res_S = 0, res_n_cta = 0;
+  int64_t res_wpc = 0;
+  size_t res_smem = 0;
   dspark_walk_plan plan{};
   int64_t timeout_ns = 200000000;
   int skip_cta = -1;
@@ -47,11 +55,45 @@ int cuda_fail(cudaError_t e) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Sizes of the three parts of the rendezvous memory.
-void sync_layout(int max_gamma, int max_B, size_t* count_off, size_t* key_off, size_t* total) {
+// Sizes of the parts of the rendezvous memory: header, arrival counts and
+// keys of the streamed kernel, and the per-CTA slots of the resident kernel.
+void sync_layout(int max_gamma, int max_B, int n_slot_cta, size_t* count_off, size_t* key_off,
+                 size_t* slot_off, size_t* total) {
   *count_off = round_up(sizeof(SyncHeader), 128);
   *key_off = round_up(*count_off + (size_t)2 * max_gamma * kCountStride * sizeof(uint32_t), 128);
-  *total = round_up(*key_off + (size_t)2 * max_gamma * max_B * sizeof(unsigned long long), 128);
+  *slot_off = round_up(*key_off + (size_t)2 * max_gamma * max_B * sizeof(unsigned long long), 128);
+  *total = round_up(*slot_off + (size_t)2 * n_slot_cta * max_B * sizeof(unsigned long long), 128);
+}
+
+// Shared memory a CTA may use, minus the kernels' static shared variables.
+constexpr size_t kSmemBudget = 232448 - 1024;
+
+// Resident plan: every CTA holds 3 tensor-memory tiles (384 rows), RS
+// register strips per warp (128 RS rows) and S shared-memory strips; rows
+// are spread evenly over at most one CTA per SM (R a multiple of 16).
+// Returns false when the shard does not fit on chip (or B, V are too large),
+// in which case every run uses the streamed kernel.
+bool plan_resident(dspark_walk* h) {
+  const int mb = h->max_B < 16 ? h->max_B : 16;
+  if (h->V >= (1 << 18)) return false;          // the 18-bit id field of the slot word
+  const int RS = mb <= 8 ? 3 : 2;
+  const int NT = mb <= 8 ? 1 : 2;
+  const int fixed = resident_fixed_rows(RS);
+  int64_t R = (h->V + h->sm_count - 1) / h->sm_count;
+  R = (R + 15) / 16 * 16;
+  if (R < fixed) R = fixed;
+  const int S = (int)((R - fixed) / 16);
+  const size_t smem = resident_smem_bytes(S, mb, (int)R);
+  if (smem > kSmemBudget) return false;
+  h->res_max_B = mb;
+  h->res_RS = RS;
+  h->res_NT = NT;
+  h->res_R = (int)R;
+  h->res_S = S;
+  h->res_n_cta = (int)((h->V + R - 1) / R);
+  h->res_wpc = resident_words_per_cta(RS, S);
+  h->res_smem = smem;
+  return true;
 }
 
 // Shard plan of the streamed kernel: rows split evenly over at most one CTA
@@ -78,6 +120,18 @@ void plan_stream(dspark_walk* h) {
   p.max_gamma = h->max_gamma;
   p.kernel = DSPARK_KERNEL_STREAM;
   p.sm_count = h->sm_count;
+  if (h->res_max_B > 0) {
+    p.n_cta = h->res_n_cta;
+    p.threads = resident_threads();
+    p.rows_per_cta = h->res_R;
+    p.rows_tmem = 384;
+    p.rows_rf = 128 * h->res_RS;
+    p.rows_smem = 16 * h->res_S;
+    p.rows_stream = 0;
+    p.resident_bytes = h->V * (int64_t)h->r * 2;
+    p.streamed_bytes = 0;
+    p.kernel = DSPARK_KERNEL_RESIDENT;
+  }
 }
 
 int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const float* temp,
@@ -100,6 +154,26 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
   a.seed_hi = (uint32_t)(seed >> 32);
   a.timeout_ns = h->timeout_ns;
   a.skip_cta = h->skip_cta;
+
+  if (h->res_max_B > 0 && h->use_resident && B <= h->res_max_B) {
+    ResidentArgs ra{};
+    ra.w = a;
+    ra.w.rows_per_cta = h->res_R;
+    ra.W2p = h->W2p;
+    ra.slots = h->slots;
+    ra.R = h->res_R;
+    ra.S = h->res_S;
+    ra.words_per_cta = h->res_wpc;
+    ra.max_B = h->max_B;
+    const uintptr_t bp = reinterpret_cast<uintptr_t>(base);
+    ra.base_mode = (h->V % 8 == 0 && (bp & 15u) == 0) ? 16
+                   : (h->V % 2 == 0 && (bp & 3u) == 0) ? 4 : 2;
+    const void* rfn = resident_kernel_for(h->res_RS, h->res_NT);
+    void* rargs[] = {&ra};
+    CUDA_TRY(cudaLaunchCooperativeKernel(rfn, dim3(h->res_n_cta), dim3(resident_threads()), rargs,
+                                         h->res_smem, stream));
+    return DSPARK_OK;
+  }
 
   const void* fn = stream_kernel_for(B);
   const size_t smem = stream_smem_bytes(B);  // <= the maximum set at create
@@ -143,12 +217,18 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
   h->W1 = static_cast<const uint16_t*>(W1);
 
   int rc = DSPARK_OK;
-  size_t count_off, key_off, total;
-  sync_layout(max_gamma, max_B, &count_off, &key_off, &total);
+  const bool resident = plan_resident(h);
+  size_t count_off, key_off, slot_off, total;
+  sync_layout(max_gamma, max_B, resident ? h->res_n_cta : 0, &count_off, &key_off, &slot_off,
+              &total);
   cudaError_t e = cudaMalloc(&h->W2, (size_t)V * r * 2);
   if (e == cudaSuccess) e = cudaMemcpy(h->W2, W2, (size_t)V * r * 2, cudaMemcpyDeviceToDevice);
   if (e == cudaSuccess) e = cudaMalloc(&h->sync_mem, total);
   if (e == cudaSuccess) e = cudaMemset(h->sync_mem, 0, total);
+  if (e == cudaSuccess && resident)
+    e = cudaMalloc(&h->W2p, (size_t)h->res_wpc * h->res_n_cta * sizeof(uint32_t));
+  if (e == cudaSuccess && resident)
+    e = resident_repack(W2, h->W2p, V, h->res_R, h->res_RS, h->res_S, h->res_n_cta, 0);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) rc = cuda_fail(e);
   if (rc == DSPARK_OK) {
@@ -158,6 +238,7 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
     h->sync.key = reinterpret_cast<unsigned long long*>(base + key_off);
     h->sync.max_gamma = max_gamma;
     h->sync.max_B = max_B;
+    h->slots = reinterpret_cast<unsigned long long*>(base + slot_off);
     plan_stream(h);
     // every instantiation may use the shared memory of max_B, and one CTA
     // per SM must fit
@@ -170,6 +251,22 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, h->plan.threads, smem);
       if (e != cudaSuccess) rc = cuda_fail(e);
       else if (per_sm < 1) rc = DSPARK_EUNSUPPORTED;
+    }
+    if (rc == DSPARK_OK && resident) {
+      int per_sm = 0;
+      const void* fn = resident_kernel_for(h->res_RS, h->res_NT);
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)h->res_smem);
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, resident_threads(),
+                                                          h->res_smem);
+      // exactly one CTA per SM: two would contend for the whole tensor memory
+      if (e != cudaSuccess || per_sm != 1) {
+        // the resident kernel cannot run here: every run streams instead
+        cudaGetLastError();
+        h->res_max_B = 0;
+        plan_stream(h);
+      }
     }
   }
   if (rc != DSPARK_OK) {
@@ -254,6 +351,20 @@ int dspark_walk_set_limits(dspark_walk_t h, int64_t timeout_ns, int skip_cta) {
   return DSPARK_OK;
 }
 
+int dspark_walk_set_kernel(dspark_walk_t h, int kernel) {
+  if (!h) return DSPARK_EINVAL;
+  if (kernel == DSPARK_KERNEL_STREAM) {
+    h->use_resident = false;
+    return DSPARK_OK;
+  }
+  if (kernel == DSPARK_KERNEL_RESIDENT) {
+    if (h->res_max_B == 0) return DSPARK_EUNSUPPORTED;
+    h->use_resident = true;
+    return DSPARK_OK;
+  }
+  return DSPARK_EINVAL;
+}
+
 const char* dspark_walk_strerror(int code) {
   switch (code) {
     case DSPARK_OK: return "ok";
@@ -264,6 +375,7 @@ const char* dspark_walk_strerror(int code) {
     case DSPARK_EANCHOR: return "anchor token outside [0, V)";
     case DSPARK_EUNSUPPORTED: return "unsupported rank or device (needs r = 256 on sm_103)";
     case DSPARK_ETEMP: return "temperature negative or not finite";
+    case DSPARK_EINTERNAL: return "device-side consistency check failed";
     case DSPARK_ELIMIT:
       return "batch or walk length above the allocation-free entry point's maximum (B <= 64, "
              "gamma <= 16)";
@@ -276,6 +388,7 @@ int dspark_walk_destroy(dspark_walk_t h) {
   int rc = DSPARK_OK;
   if (cudaDeviceSynchronize() != cudaSuccess) rc = DSPARK_ECUDA;
   if (h->W2) cudaFree(h->W2);
+  if (h->W2p) cudaFree(h->W2p);
   if (h->sync_mem) cudaFree(h->sync_mem);
   if (h->stage) cudaFree(h->stage);
   delete h;

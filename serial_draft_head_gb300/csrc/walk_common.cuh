@@ -26,6 +26,7 @@ constexpr int kStatusOk = 0;
 constexpr int kStatusTimeout = -4;
 constexpr int kStatusAnchor = -5;
 constexpr int kStatusTemp = -7;
+constexpr int kStatusInternal = -9;
 
 // Rendezvous state owned by a handle, in global memory.
 //   header: round counter (selects the parity) and the sticky status word;
@@ -37,7 +38,8 @@ constexpr int kStatusTemp = -7;
 struct SyncHeader {
   uint32_t round;
   int32_t status;
-  uint32_t pad[6];
+  uint32_t abort_round;  // round + 1 of the last round a CTA gave up on
+  uint32_t pad[5];
 };
 constexpr int kCountStride = 8;  // uint32 per count slot (32 bytes)
 
@@ -55,6 +57,20 @@ struct SyncView {
     return key + ((size_t)parity * max_gamma + k) * max_B + b;
   }
 };
+
+// Give up on the current round: record the status (first error wins) and
+// mark the round, so every other CTA of THIS round stops waiting.  A status
+// left over from an earlier round does not stop later rounds.
+__device__ __forceinline__ void abort_round(SyncHeader* hdr, uint32_t round, int code) {
+  atomicCAS(reinterpret_cast<int*>(&hdr->status), 0, code);
+  atomicExch(&hdr->abort_round, round + 1u);
+}
+
+__device__ __forceinline__ bool round_aborted(const SyncHeader* hdr, uint32_t round) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(&hdr->abort_round) : "memory");
+  return v == round + 1u;
+}
 
 // Everything a launch needs (passed by value).
 struct WalkArgs {
@@ -230,9 +246,10 @@ __device__ __forceinline__ void clear_other_parity(const SyncView& s, uint32_t p
 // request b; on return tok_smem[b] holds the common winner of request b.
 // Returns false if the wait ran out or another CTA reported an error; then
 // every CTA leaves the walk.
-__device__ __forceinline__ bool exchange(const WalkArgs& a, uint32_t parity, int k,
+__device__ __forceinline__ bool exchange(const WalkArgs& a, uint32_t round, int k,
                                          const unsigned long long* cta_key, int32_t* tok_smem,
                                          int* flag_smem) {
+  const uint32_t parity = round & 1u;
   const bool post = (int)blockIdx.x != a.skip_cta;
   if (post) {
     for (int b = threadIdx.x; b < a.B; b += blockDim.x)
@@ -249,9 +266,9 @@ __device__ __forceinline__ bool exchange(const WalkArgs& a, uint32_t parity, int
     uint32_t spins = 0;
     while (ld_acquire_gpu(cnt) < target) {
       if ((++spins & 63u) == 0u) {
-        if (ld_relaxed_gpu_s32(&a.sync.hdr->status) != 0) { ok = 0; break; }
+        if (round_aborted(a.sync.hdr, round)) { ok = 0; break; }
         if ((int64_t)(globaltimer_ns() - t0) > a.timeout_ns) {
-          set_status(a.sync.hdr, kStatusTimeout);
+          abort_round(a.sync.hdr, round, kStatusTimeout);
           ok = 0;
           break;
         }
@@ -268,5 +285,17 @@ __device__ __forceinline__ bool exchange(const WalkArgs& a, uint32_t parity, int
   __syncthreads();
   return ok;
 }
+
+// Arguments of the resident kernel: the common ones plus the tiered layout.
+struct ResidentArgs {
+  WalkArgs w;
+  const uint32_t* W2p;            // repacked W2, words_per_cta words per CTA
+  unsigned long long* slots;      // [2][n_cta][max_B] rendezvous words
+  int R;                          // rows per CTA (multiple of 16)
+  int S;                          // shared-memory strips per CTA
+  int64_t words_per_cta;
+  int max_B;                      // slot stride
+  int base_mode;                  // 16, 4 or 2: bytes per base-prefetch copy
+};
 
 }  // namespace dspark

@@ -1,6 +1,8 @@
 // walk_kernels.h -- what the host side needs to know about each kernel.
 #pragma once
+#include <cuda_runtime.h>
 #include <stddef.h>
+#include <stdint.h>
 
 namespace dspark {
 
@@ -8,5 +10,14 @@ namespace dspark {
 size_t stream_smem_bytes(int B);
 int stream_threads();
 const void* stream_kernel_for(int B);
+
+// Resident kernel: W2 tiered over tensor memory, registers, shared memory.
+int64_t resident_words_per_cta(int RS, int S);
+int resident_fixed_rows(int RS);
+int resident_threads();
+size_t resident_smem_bytes(int S, int max_B, int R);
+const void* resident_kernel_for(int RS, int NT);
+cudaError_t resident_repack(const void* W2, void* out, int64_t V, int R, int RS, int S, int n_cta,
+                            cudaStream_t stream);
 
 }  // namespace dspark

@@ -1,0 +1,545 @@
+// walk_resident.cu -- the persistent walk with W2 held on chip for the whole
+// round: "Keeping the Draft Walk on Chip: One Launch for DSpark's Markov
+// Head", sections "The idea: make the walk resident" (one CTA per SM, one
+// launch per round, each CTA loads its slice of rows once and runs all gamma
+// steps) and "B200: the bf16 table fits on chip" (the table split over
+// tensor memory, shared memory and registers; tcgen05 reads the tensor-memory
+// part, mma.sync the rest; request n is column n of the MMA's N operand).
+//
+// Per CTA (256 threads, 8 warps) the R rows of its shard are placed as
+//   rows [0, 384)             3 tiles of 128 rows in tensor memory, read by
+//                             tcgen05.mma (A from TMEM, B = U from shared
+//                             memory, D = 128 x 16 fp32 in TMEM);
+//   rows [384, 384 + 128 RS)  registers: each warp holds RS 16-row strips as
+//                             mma.sync A fragments;
+//   rows [384 + 128 RS, R)    shared memory, 16-row strips read by ldmatrix
+//                             and mma.sync.
+// U (the gathered W1 rows, one per request) sits in shared memory in the
+// no-swizzle K-major core-matrix layout that both the tcgen05 descriptor and
+// the mma.sync B fragments read.
+//
+// Cross-CTA selection uses a gather rendezvous: every CTA stores one 64-bit
+// word per request {tag : 14, logit order bits : 32, inverted id : 18} in its
+// own slot (two slot sets, by step parity) and reads every CTA's slot until
+// all tags match the current (round, step); the maximum of the words is the
+// common winner.  One round trip to L2 both detects the arrivals and carries
+// the keys.  The tag makes stale slots from earlier steps or rounds harmless.
+#include "tc_ptx.cuh"
+#include "walk_common.cuh"
+#include "walk_kernels.h"
+
+namespace dspark {
+
+namespace {
+
+constexpr int kResThreads = 256;
+constexpr int kResWarps = kResThreads / 32;
+constexpr int kTmemTiles = 3;
+constexpr int kTmemCols = 512;
+constexpr int kTmemRows = kTmemTiles * 128;    // rows held in tensor memory
+constexpr int kDCol0 = kTmemTiles * 128;       // first accumulator column
+constexpr int kNMma = 16;                      // tcgen05 N (requests per MMA)
+constexpr int kTmemWords = kTmemTiles * 128 * 128;
+constexpr int kRfStripWords = kResWarps * 16 * 32 * 4;  // one strip per warp, all warps
+constexpr int kSmemStripBytes = 16 * 512;
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, kNMma);
+
+__device__ __forceinline__ unsigned long long key_max(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
+}
+
+// The 64-bit word a CTA posts for one request: tag, order bits, inverted id.
+__device__ __forceinline__ unsigned long long tagged_key(unsigned long long local, uint32_t tag) {
+  unsigned long long t = (unsigned long long)tag << 50;
+  if (local == 0ull) return t;
+  const uint32_t ord = (uint32_t)(local >> 32);
+  const uint32_t v = 0xFFFFFFFFu - (uint32_t)local;
+  return t | ((unsigned long long)ord << 18) | (unsigned long long)(0x3FFFFu - v);
+}
+
+__device__ __forceinline__ bool wait_mbar(uint64_t* bar, uint32_t parity, uint64_t t0,
+                                          int64_t limit_ns) {
+  uint32_t spins = 0;
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if ((++spins & 255u) == 0u && (int64_t)(globaltimer_ns() - t0) > limit_ns) return false;
+  }
+  return true;
+}
+
+// Stage base[b, k, row0 .. row0 + nv) for every request into base_s[b][0..R).
+__device__ __forceinline__ void prefetch_base(const ResidentArgs& ra, int k, int64_t row0,
+                                              int nv, uint16_t* base_s) {
+  const WalkArgs& a = ra.w;
+  if (k >= a.gamma) return;
+  if (ra.base_mode == 16) {
+    const int per = nv >> 3;
+    for (int i = threadIdx.x; i < a.B * per; i += blockDim.x) {
+      const int b = i / per, c = i - b * per;
+      const uint16_t* src = a.base + ((size_t)b * a.gamma + k) * (size_t)a.V + row0 + 8 * c;
+      ptx::cp_async16(base_s + (size_t)b * ra.R + 8 * c, src);
+    }
+  } else if (ra.base_mode == 4) {
+    const int per = nv >> 1;
+    for (int i = threadIdx.x; i < a.B * per; i += blockDim.x) {
+      const int b = i / per, c = i - b * per;
+      const uint16_t* src = a.base + ((size_t)b * a.gamma + k) * (size_t)a.V + row0 + 2 * c;
+      ptx::cp_async4(base_s + (size_t)b * ra.R + 2 * c, src);
+    }
+  } else {
+    for (int i = threadIdx.x; i < a.B * nv; i += blockDim.x) {
+      const int b = i / nv, c = i - b * nv;
+      base_s[(size_t)b * ra.R + c] = a.base[((size_t)b * a.gamma + k) * (size_t)a.V + row0 + c];
+    }
+  }
+}
+
+// u_b = W1[tok] into U (core matrix (kc, b/8), row b%8): one 16-byte chunk per lane.
+__device__ __forceinline__ void gather_u_row(const uint16_t* W1, int32_t tok, int b, uint8_t* U,
+                                             int lane) {
+  const uint4 x = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)tok * kRank) + lane);
+  *reinterpret_cast<uint4*>(U + (lane * 2 + (b >> 3)) * 128 + (b & 7) * 16) = x;
+  ptx::fence_proxy_async_smem();
+}
+
+// One (row, request) element of the fused epilogue, folded into a running key.
+__device__ __forceinline__ void epi_one(const WalkArgs& a, float acc, const uint16_t* base_s,
+                                        int R, float T, int b, int k, int rl, int64_t row0,
+                                        unsigned long long& best) {
+  const int64_t v = row0 + rl;
+  if (v >= a.V) return;
+  uint16_t lb;
+  const unsigned long long key = epilogue_key(acc, base_s[(size_t)b * R + rl], T, a.seed_lo,
+                                              a.seed_hi, b, k, (uint32_t)v, &lb);
+  if (a.out_logits) a.out_logits[((size_t)b * a.gamma + k) * (size_t)a.V + (size_t)v] = lb;
+  best = key_max(best, key);
+}
+
+// Epilogue of one 16-row strip held as mma.sync accumulators.
+template <int NT>
+__device__ __forceinline__ void epi_strip(const WalkArgs& a, const float (&acc)[NT][4],
+                                          const uint16_t* base_s, const float* temp_s, int R,
+                                          int k, int rl0, int64_t row0, int lane,
+                                          unsigned long long (&best)[NT][2]) {
+  const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int b = 8 * nt + 2 * t4 + e;
+      if (b < a.B) {
+        epi_one(a, acc[nt][e], base_s, R, temp_s[b], b, k, rl0 + g, row0, best[nt][e]);
+        epi_one(a, acc[nt][2 + e], base_s, R, temp_s[b], b, k, rl0 + g + 8, row0, best[nt][e]);
+      }
+    }
+  }
+}
+
+template <int RS, int NT>
+__global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const ResidentArgs ra) {
+  constexpr int NCOL = 8 * NT;
+  const WalkArgs& a = ra.w;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* smem_w2 = smem;
+  uint8_t* U = smem + (size_t)ra.S * kSmemStripBytes;
+  uint16_t* base_s = reinterpret_cast<uint16_t*>(U + 16 * 512);
+  __shared__ __align__(8) uint64_t mbar[4];
+  __shared__ unsigned long long cta_best[16];
+  __shared__ float temp_s[16];
+  __shared__ int32_t tok_s[16];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int flag_s;
+  __shared__ int abort_s;
+  __shared__ uint32_t round_s;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  const int cta = blockIdx.x;
+  const int n_cta = gridDim.x;
+  const int64_t row0 = (int64_t)cta * ra.R;
+  const int nv = (int)((a.V - row0) < ra.R ? (a.V - row0) : ra.R);  // valid rows (>= 1)
+  const uint32_t* gw = ra.W2p + (size_t)cta * (size_t)ra.words_per_cta;
+
+  const int bad = check_inputs(a, &flag_s);
+  if (bad != 0) {
+    if (cta == 0) {
+      if (threadIdx.x == 0) set_status(a.sync.hdr, bad);
+      for (int i = threadIdx.x; i < a.B * a.gamma; i += blockDim.x) a.out_tokens[i] = -1;
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------- entry ----
+  if (threadIdx.x == 0) {
+    round_s = *reinterpret_cast<volatile uint32_t*>(&a.sync.hdr->round);
+    abort_s = 0;
+    for (int i = 0; i < 4; ++i) ptx::mbar_init(&mbar[i], 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(&tmem_base_s, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (threadIdx.x < 16) {
+    temp_s[threadIdx.x] = threadIdx.x < a.B ? a.temperature[threadIdx.x] : 0.0f;
+    tok_s[threadIdx.x] = threadIdx.x < a.B ? a.anchor[threadIdx.x] : 0;
+    cta_best[threadIdx.x] = 0ull;   // afterwards cleared by the warp that consumes it
+  }
+  for (int i = threadIdx.x; i < 16 * 512 / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(U)[i] = make_uint4(0u, 0u, 0u, 0u);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  const uint32_t round_tag = (round_s % 255u) << 6;
+
+  // this CTA's slots of both step parities start empty
+  if (threadIdx.x < 2 * a.B) {
+    const int par = threadIdx.x / a.B, b = threadIdx.x - par * a.B;
+    ptx::st_relaxed_u64(ra.slots + ((size_t)par * n_cta + cta) * ra.max_B + b, 0ull);
+  }
+
+  // shared-memory tier: bulk copies straight to its final place
+  const uint64_t t_entry = globaltimer_ns();
+  if (threadIdx.x == 0 && ra.S > 0) {
+    const uint32_t bytes = (uint32_t)ra.S * kSmemStripBytes;
+    ptx::mbar_expect_tx(&mbar[3], bytes);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(gw + kTmemWords + RS * kRfStripWords);
+    for (uint32_t off = 0; off < bytes; off += 32768u) {
+      const uint32_t n = bytes - off < 32768u ? bytes - off : 32768u;
+      ptx::bulk_g2s(smem_w2 + off, src + off, n, &mbar[3]);
+    }
+  }
+
+  // tensor-memory tier: global -> registers -> tcgen05.st (warp w writes lane
+  // quarter w % 4, column half w / 4 of every tile)
+  {
+    const int q = warp & 3, h = warp >> 2;
+    const uint4* src = reinterpret_cast<const uint4*>(gw);
+#pragma unroll 1
+    for (int t = 0; t < kTmemTiles; ++t) {
+#pragma unroll
+      for (int part = 0; part < 4; ++part) {
+        uint32_t v[16];
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int c = part * 4 + c4;
+          const uint4 x = __ldg(src + ((((t * 2 + h) * 16 + c) * 4 + q) * 32 + lane));
+          v[c4 * 4 + 0] = x.x;
+          v[c4 * 4 + 1] = x.y;
+          v[c4 * 4 + 2] = x.z;
+          v[c4 * 4 + 3] = x.w;
+        }
+        ptx::tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + t * 128 + 64 * h + part * 16, v);
+      }
+    }
+    ptx::tmem_wait_st();
+  }
+
+  // register tier: this warp's RS strips as mma.sync A fragments
+  uint32_t wr[RS][16][4];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(gw + kTmemWords) +
+                       (size_t)(warp * RS) * 16 * 32 + lane;
+#pragma unroll
+    for (int s = 0; s < RS; ++s)
+#pragma unroll
+      for (int kt = 0; kt < 16; ++kt) {
+        const uint4 x = __ldg(src + (s * 16 + kt) * 32);
+        wr[s][kt][0] = x.x;
+        wr[s][kt][1] = x.y;
+        wr[s][kt][2] = x.z;
+        wr[s][kt][3] = x.w;
+      }
+  }
+
+  // step 0's inputs: base rows and u = W1[anchor]
+  prefetch_base(ra, 0, row0, nv, base_s);
+  for (int b = warp; b < a.B; b += kResWarps) gather_u_row(a.W1, tok_s[b], b, U, lane);
+  if (ra.S > 0 && threadIdx.x == 0) {
+    if (!wait_mbar(&mbar[3], 0, t_entry, a.timeout_ns)) {
+      abort_round(a.sync.hdr, round_s, kStatusTimeout);
+      abort_s = 1;
+    }
+  }
+  ptx::cp_async_wait_all();
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
+  __syncthreads();
+
+  // ----------------------------------------------------------- the walk ---
+  const uint32_t u_addr = ptx::smem_u32(U);
+  const uint32_t w2_addr = ptx::smem_u32(smem_w2);
+  bool ok = abort_s == 0;
+  int k = 0;
+  for (; k < a.gamma && ok; ++k) {
+    ptx::tc_fence_after();
+    const uint64_t t_step = globaltimer_ns();
+
+    // (1) tensor-memory tiles: 3 x 16 MMAs issued by one thread
+    if (threadIdx.x == 0) {
+#pragma unroll 1
+      for (int t = 0; t < kTmemTiles; ++t) {
+#pragma unroll
+        for (int kt = 0; kt < 16; ++kt) {
+          const uint64_t bdesc = ptx::smem_desc_noswizzle(u_addr + kt * 512, 256, 128);
+          ptx::tc_mma_tmem_a(tmem + kDCol0 + 16 * t, tmem + t * 128 + kt * 8, bdesc, kIdesc,
+                             kt > 0 ? 1u : 0u);
+        }
+        ptx::tc_commit(&mbar[t]);
+      }
+    }
+
+    // (2) register strips: B fragments of U, k-tile by k-tile
+    unsigned long long bestm[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) bestm[nt][0] = bestm[nt][1] = 0ull;
+    {
+      float acc[RS][NT][4];
+#pragma unroll
+      for (int s = 0; s < RS; ++s)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[s][nt][e] = 0.0f;
+#pragma unroll
+      for (int kt = 0; kt < 16; ++kt) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          uint32_t b0 = 0u, b1 = 0u;
+          if (8 * nt + g < a.B) {
+            b0 = *reinterpret_cast<const uint32_t*>(U + (4 * kt + nt) * 128 + lane * 4);
+            b1 = *reinterpret_cast<const uint32_t*>(U + (4 * kt + 2 + nt) * 128 + lane * 4);
+          }
+#pragma unroll
+          for (int s = 0; s < RS; ++s)
+            ptx::mma_16816(acc[s][nt], wr[s][kt][0], wr[s][kt][1], wr[s][kt][2], wr[s][kt][3],
+                           b0, b1);
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < RS; ++s)
+        epi_strip<NT>(a, acc[s], base_s, temp_s, ra.R, k, kTmemRows + (warp * RS + s) * 16, row0,
+                      lane, bestm);
+    }
+
+    // (3) shared-memory strips s2 = warp, warp + 8, ...
+#pragma unroll 1
+    for (int s2 = warp; s2 < ra.S; s2 += kResWarps) {
+      float acc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+      const uint32_t blk = w2_addr + (uint32_t)s2 * kSmemStripBytes + (lane >> 3) * 128 +
+                           (lane & 7) * 16;
+#pragma unroll
+      for (int kt = 0; kt < 16; ++kt) {
+        uint32_t a0, a1, a2, a3;
+        ptx::ldmatrix_x4(blk + kt * 512, a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          uint32_t b0 = 0u, b1 = 0u;
+          if (8 * nt + g < a.B) {
+            b0 = *reinterpret_cast<const uint32_t*>(U + (4 * kt + nt) * 128 + lane * 4);
+            b1 = *reinterpret_cast<const uint32_t*>(U + (4 * kt + 2 + nt) * 128 + lane * 4);
+          }
+          ptx::mma_16816(acc[nt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+      epi_strip<NT>(a, acc, base_s, temp_s, ra.R, k, kTmemRows + 128 * RS + s2 * 16, row0, lane,
+                    bestm);
+    }
+
+    // fold the mma-layout keys: reduce over the 8 row groups, lanes 0..3 post
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        unsigned long long x = bestm[nt][e];
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) x = key_max(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+        const int b = 8 * nt + 2 * (lane & 3) + e;
+        if (lane < 4 && b < a.B && x != 0ull) atomicMax(&cta_best[b], x);
+      }
+
+    // (4) tensor-memory epilogue: warps 0-3 take tiles 0 and 2, warps 4-7 tile 1
+    {
+      const int q = warp & 3;
+      unsigned long long bestt[NCOL];
+#pragma unroll
+      for (int c = 0; c < NCOL; ++c) bestt[c] = 0ull;
+#pragma unroll 1
+      for (int t = warp >> 2; t < kTmemTiles; t += 2) {
+        if (!wait_mbar(&mbar[t], (uint32_t)(k & 1), t_step, a.timeout_ns)) {
+          abort_round(a.sync.hdr, round_s, kStatusTimeout);
+          abort_s = 1;
+        }
+        ptx::tc_fence_after();
+        uint32_t d[NCOL];
+        ptx::tmem_ld<NCOL>(tmem + ((uint32_t)(32 * q) << 16) + kDCol0 + 16 * t, d);
+        ptx::tmem_wait_ld();
+        const int rl = t * 128 + 32 * q + lane;
+#pragma unroll
+        for (int c = 0; c < NCOL; ++c)
+          if (c < a.B)
+            epi_one(a, __uint_as_float(d[c]), base_s, ra.R, temp_s[c], c, k, rl, row0, bestt[c]);
+      }
+#pragma unroll
+      for (int c = 0; c < NCOL; ++c) {
+        if (c < a.B) {
+          unsigned long long x = bestt[c];
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) x = key_max(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+          if (lane == 0 && x != 0ull) atomicMax(&cta_best[c], x);
+        }
+      }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+
+    // (5) next step's base rows (the current ones are no longer read)
+    prefetch_base(ra, k + 1, row0, nv, base_s);
+
+    // (6) the rendezvous: warp w handles requests w and w + 8
+    const uint32_t tag = (round_tag | (uint32_t)k) + 1u;
+    unsigned long long* slot_base = ra.slots + (size_t)(k & 1) * n_cta * ra.max_B;
+    for (int b = warp; b < a.B; b += kResWarps) {
+      const unsigned long long mine = cta_best[b];
+      __syncwarp();
+      if (lane == 0) cta_best[b] = 0ull;  // ready for the next step's atomics
+      if (lane < 4 && mine != 0ull) {     // the candidate's W1 row, into L2
+        const uint32_t cand = 0xFFFFFFFFu - (uint32_t)mine;
+        ptx::prefetch_l2(a.W1 + (size_t)cand * kRank + lane * 64);
+      }
+      if (lane == 0 && cta != a.skip_cta)
+        ptx::st_relaxed_u64(slot_base + (size_t)cta * ra.max_B + b, tagged_key(mine, tag));
+      unsigned long long best = 0ull;
+      uint32_t spins = 0;
+      bool done = false;
+      while (!done) {
+        bool have = true;
+        best = 0ull;
+        for (int j = lane; j < n_cta; j += 32) {
+          const unsigned long long x = ptx::ld_relaxed_u64(slot_base + (size_t)j * ra.max_B + b);
+          if ((uint32_t)(x >> 50) != tag) have = false;
+          best = key_max(best, x & ((1ull << 50) - 1ull));
+        }
+        done = __all_sync(0xFFFFFFFFu, have);
+        if (!done && (++spins & 15u) == 0u) {
+          int stop = 0;
+          if (lane == 0)
+            stop = round_aborted(a.sync.hdr, round_s) ||
+                   ((int64_t)(globaltimer_ns() - t_step) > a.timeout_ns);
+          stop = __shfl_sync(0xFFFFFFFFu, stop, 0);
+          if (stop) {
+            if (lane == 0) {
+              abort_round(a.sync.hdr, round_s, kStatusTimeout);
+              abort_s = 1;
+            }
+            break;
+          }
+        }
+      }
+      if (!done) break;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) best = key_max(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+      int32_t tok = (int32_t)(0x3FFFFu - (uint32_t)(best & 0x3FFFFu));
+      if ((int64_t)tok >= a.V) {          // cannot happen: every CTA posts a real row
+        if (lane == 0) {
+          abort_round(a.sync.hdr, round_s, kStatusInternal);
+          abort_s = 1;
+        }
+        break;
+      }
+      if (lane == 0) {
+        tok_s[b] = tok;
+        if (cta == 0) a.out_tokens[(size_t)b * a.gamma + k] = tok;
+      }
+      gather_u_row(a.W1, tok, b, U, lane);   // next step's u_b
+    }
+    ptx::cp_async_wait_all();
+    ptx::fence_proxy_async_smem();
+    __syncthreads();
+    ok = abort_s == 0;
+  }
+
+  // -------------------------------------------------------------- exit ----
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (cta == 0) {
+    if (!ok)
+      for (int i = threadIdx.x; i < a.B * a.gamma; i += blockDim.x) a.out_tokens[i] = -1;
+    if (threadIdx.x == 0) atomicAdd(&a.sync.hdr->round, 1u);
+  }
+}
+
+// Repack row-major W2 [V, 256] into the per-CTA tiered layout (32-bit words,
+// each word two consecutive K elements).  Rows past V are zero.
+__global__ void repack_resident_kernel(const uint32_t* __restrict__ W2w, uint32_t* __restrict__ out,
+                                       int64_t V, int R, int RS, int64_t words_per_cta,
+                                       int n_cta) {
+  const int64_t total = words_per_cta * n_cta;
+  const int64_t rf_words = (int64_t)RS * kRfStripWords;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t cta = i / words_per_cta;
+    const int64_t w = i - cta * words_per_cta;
+    int rl, kp;
+    if (w < kTmemWords) {  // ((((t*2 + h)*16 + c)*4 + q)*32 + l)*4 + ww
+      const int ww = (int)(w & 3), l = (int)((w >> 2) & 31), q = (int)((w >> 7) & 3);
+      const int c = (int)((w >> 9) & 15), h = (int)((w >> 13) & 1), t = (int)(w >> 14);
+      rl = t * 128 + q * 32 + l;
+      kp = h * 64 + c * 4 + ww;
+    } else if (w < kTmemWords + rf_words) {  // (((ws)*16 + kt)*32 + l)*4 + j, ws = warp*RS + s
+      const int64_t x = w - kTmemWords;
+      const int j = (int)(x & 3), l = (int)((x >> 2) & 31), kt = (int)((x >> 7) & 15);
+      const int ws = (int)(x >> 11);
+      rl = kTmemRows + ws * 16 + (l >> 2) + 8 * (j & 1);
+      kp = kt * 8 + (l & 3) + 4 * (j >> 1);
+    } else {  // ((s2*16 + kt)*4 + m)*32 + i*4 + p
+      const int64_t x = w - kTmemWords - rf_words;
+      const int p = (int)(x & 3), ii = (int)((x >> 2) & 7), m = (int)((x >> 5) & 3);
+      const int kt = (int)((x >> 7) & 15), s2 = (int)(x >> 11);
+      rl = kTmemRows + RS * 128 + s2 * 16 + 8 * (m & 1) + ii;
+      kp = kt * 8 + 4 * (m >> 1) + p;
+    }
+    const int64_t row = cta * (int64_t)R + rl;
+    out[i] = row < V ? W2w[row * (kRank / 2) + kp] : 0u;
+  }
+}
+
+}  // namespace
+
+int64_t resident_words_per_cta(int RS, int S) {
+  return (int64_t)kTmemWords + (int64_t)RS * kRfStripWords + (int64_t)S * (kSmemStripBytes / 4);
+}
+
+int resident_fixed_rows(int RS) { return kTmemRows + 128 * RS; }
+
+int resident_threads() { return kResThreads; }
+
+size_t resident_smem_bytes(int S, int max_B, int R) {
+  return (size_t)S * kSmemStripBytes + 16 * 512 + (((size_t)max_B * R * 2 + 15) & ~(size_t)15);
+}
+
+const void* resident_kernel_for(int RS, int NT) {
+  if (RS == 3 && NT == 1) return reinterpret_cast<const void*>(&walk_resident_kernel<3, 1>);
+  if (RS == 2 && NT == 2) return reinterpret_cast<const void*>(&walk_resident_kernel<2, 2>);
+  if (RS == 2 && NT == 1) return reinterpret_cast<const void*>(&walk_resident_kernel<2, 1>);
+  return nullptr;
+}
+
+cudaError_t resident_repack(const void* W2, void* out, int64_t V, int R, int RS, int S, int n_cta,
+                            cudaStream_t stream) {
+  const int64_t wpc = resident_words_per_cta(RS, S);
+  const int64_t total = wpc * n_cta;
+  int blocks = (int)((total + 255) / 256);
+  if (blocks > 65535 * 8) blocks = 65535 * 8;
+  repack_resident_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint32_t*>(W2),
+                                                     static_cast<uint32_t*>(out), V, R, RS, wpc,
+                                                     n_cta);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

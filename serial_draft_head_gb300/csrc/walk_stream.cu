@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) walk_stream_kernel(const Wa
     for (int b0 = 0; b0 < a.B; b0 += NB)
       stream_rows<NB>(a, k, b0, row0, row1, u_s, temp_s, cta_key);
     __syncthreads();
-    ok = exchange(a, parity, k, cta_key, prev_s, &flag_s);
+    ok = exchange(a, round_s, k, cta_key, prev_s, &flag_s);
     if (ok && blockIdx.x == 0)
       for (int b = threadIdx.x; b < a.B; b += blockDim.x)
         a.out_tokens[(size_t)b * a.gamma + k] = prev_s[b];

@@ -21,6 +21,7 @@ EANCHOR = -5
 EUNSUPPORTED = -6
 ETEMP = -7
 ELIMIT = -8
+EINTERNAL = -9
 
 KERNEL_STREAM = 0
 KERNEL_RESIDENT = 1
@@ -53,7 +54,7 @@ class dspark_walk_plan(ctypes.Structure):
 EXPORTS = [
     "dspark_walk_create", "dspark_walk_run", "dspark_walk_run_host", "dspark_walk_status",
     "dspark_walk_get_plan", "dspark_walk_set_limits", "dspark_walk_strerror",
-    "dspark_walk_destroy", "dspark_walk_run_noalloc",
+    "dspark_walk_destroy", "dspark_walk_run_noalloc", "dspark_walk_set_kernel",
 ]
 
 
@@ -82,6 +83,7 @@ def load(build_if_missing=True):
     L.dspark_walk_strerror.argtypes = [i32]
     L.dspark_walk_strerror.restype = ctypes.c_char_p
     L.dspark_walk_destroy.argtypes = [vp]
+    L.dspark_walk_set_kernel.argtypes = [vp, i32]
     L.dspark_walk_run_noalloc.argtypes = [vp, vp, i64, i32, vp, vp, vp, u64, vp, i32, i32, vp, vp]
     for name in EXPORTS:
         if name != "dspark_walk_strerror":
@@ -157,6 +159,10 @@ def dspark_walk_set_limits(h, timeout_ns, skip_cta=-1):
                   "dspark_walk_set_limits")
 
 
+def dspark_walk_set_kernel(h, kernel):
+    return _check(load().dspark_walk_set_kernel(h, int(kernel)), "dspark_walk_set_kernel")
+
+
 def dspark_walk_destroy(h):
     return _check(load().dspark_walk_destroy(h), "dspark_walk_destroy")
 
@@ -188,6 +194,9 @@ class Walk:
 
     def plan(self):
         return dspark_walk_get_plan(self.h)
+
+    def set_kernel(self, kernel):
+        dspark_walk_set_kernel(self.h, kernel)
 
     def run(self, base, anchor, temperature, seed, out_tokens=None, out_logits=None,
             stream=None):

@@ -23,8 +23,11 @@ def walkmod():
     return walk
 
 
-def make_walk(walkmod, x, max_B=None, max_gamma=None):
-    return walkmod.Walk(x.W1.cuda(), x.W2.cuda(), max_B or x.B, max_gamma or x.gamma)
+def make_walk(walkmod, x, max_B=None, max_gamma=None, kernel=None):
+    w = walkmod.Walk(x.W1.cuda(), x.W2.cuda(), max_B or x.B, max_gamma or x.gamma)
+    if kernel == "stream":
+        w.set_kernel(walkmod.KERNEL_STREAM)
+    return w
 
 
 def gpu_run(w, x, want_logits=True, seed=None):
@@ -50,14 +53,18 @@ SMALL = [
     (4096, 2, 33, (0.0, 0.6, 1.0), 6),
     (2048, 1, 256, (0.0, 0.6, 1.0), 7),    # the largest batch
     (3000, 64, 1, (0.0,), 8),              # the longest walk
+    (130000, 3, 1, (0.0,), 9),             # 152 CTAs, 6 shared-memory strips each
+    (90001, 2, 5, (0.0, 1.0), 10),         # odd V: plain base loads
+    (77778, 3, 12, (0.6, 0.0), 11),        # two n-tiles (8 < B <= 16)
 ]
 
 
+@pytest.mark.parametrize("kernel", ["planned", "stream"])
 @pytest.mark.parametrize("V,gamma,B,temps,seed", SMALL)
-def test_small_every_logit(walkmod, V, gamma, B, temps, seed):
+def test_small_every_logit(walkmod, V, gamma, B, temps, seed, kernel):
     x = synth.make_custom(V=V, gamma=gamma, B=B, seed=seed, temperatures=temps,
                           noise_seed=1000 + seed)
-    w = make_walk(walkmod, x)
+    w = make_walk(walkmod, x, kernel=kernel)
     st, toks, lg = gpu_run(w, x)
     assert st == 0, walkmod.dspark_walk_strerror(st)
     rep = parity.check(x, toks, lg)
@@ -68,6 +75,7 @@ def test_small_every_logit(walkmod, V, gamma, B, temps, seed):
 def test_tiny_config(walkmod):
     x = synth.make_inputs("tiny")
     w = make_walk(walkmod, x)
+    assert w.plan()["kernel"] == walkmod.KERNEL_RESIDENT
     st, toks, lg = gpu_run(w, x)
     assert st == 0
     rep = parity.check(x, toks, lg)
@@ -114,6 +122,8 @@ def _sample_requests(B, temps):
 def test_qwen3_resident(walkmod, round_index):
     x = full_inputs("qwen3_resident", 1, round_index)
     w = full_walk(walkmod, "qwen3_resident", x)
+    plan = w.plan()
+    assert plan["kernel"] == walkmod.KERNEL_RESIDENT and plan["rows_stream"] == 0
     st, toks, lg = gpu_run(w, x)
     assert st == 0
     rep = parity.check(x, toks, lg)
