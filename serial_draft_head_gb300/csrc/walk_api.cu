@@ -33,6 +33,7 @@ struct dspark_walk {
   int64_t res_wpc = 0;
   size_t res_smem = 0;
   dspark_walk_plan plan{};
+  int st_n_cta = 0, st_rpc = 0;   // streamed kernel's shard plan
   int64_t timeout_ns = 200000000;
   int skip_cta = -1;
   // staging for dspark_walk_run_host (allocated on first use)
@@ -106,6 +107,8 @@ void plan_stream(dspark_walk* h) {
   if (n < 1) n = 1;
   int64_t rpc = (h->V + n - 1) / n;
   n = (h->V + rpc - 1) / rpc;     // every CTA owns at least one row
+  h->st_n_cta = (int)n;
+  h->st_rpc = (int)rpc;
   dspark_walk_plan& p = h->plan;
   p.V = h->V;
   p.r = h->r;
@@ -149,7 +152,7 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
   a.V = h->V;
   a.B = B;
   a.gamma = gamma;
-  a.rows_per_cta = h->plan.rows_per_cta;
+  a.rows_per_cta = h->st_rpc;
   a.seed_lo = (uint32_t)seed;
   a.seed_hi = (uint32_t)(seed >> 32);
   a.timeout_ns = h->timeout_ns;
@@ -178,7 +181,7 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
   const void* fn = stream_kernel_for(B);
   const size_t smem = stream_smem_bytes(B);  // <= the maximum set at create
   void* args[] = {&a};
-  CUDA_TRY(cudaLaunchCooperativeKernel(fn, dim3(h->plan.n_cta), dim3(h->plan.threads), args,
+  CUDA_TRY(cudaLaunchCooperativeKernel(fn, dim3(h->st_n_cta), dim3(stream_threads()), args,
                                        smem, stream));
   return DSPARK_OK;
 }
@@ -248,7 +251,7 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
       const void* fn = stream_kernel_for(b);
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, h->plan.threads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, stream_threads(), smem);
       if (e != cudaSuccess) rc = cuda_fail(e);
       else if (per_sm < 1) rc = DSPARK_EUNSUPPORTED;
     }
