@@ -33,6 +33,8 @@ def test_noalloc_matches_handle_path_twice_in_a_row():
     for i, (V, B, gamma) in enumerate([(5003, 6, 5), (20011, 3, 7)]):
         x = synth.make_custom(V=V, gamma=gamma, B=B, seed=60 + i, temperatures=(0.0, 0.6, 1.0),
                               noise_seed=900 + i)
+        # the handle path may run another kernel (another fp32 summation
+        # order), so logits agree within the parity tolerance, not bit for bit
         want_tok, want_lg = _handle_run(walk, x)
         W1, W2 = x.W1.cuda(), x.W2.cuda()
         tok = torch.full((B, gamma), -2, dtype=torch.int32, device="cuda")
@@ -43,10 +45,12 @@ def test_noalloc_matches_handle_path_twice_in_a_row():
         got_tok = tok.cpu().numpy()
         got_lg = lg.view(torch.int16).cpu().numpy().view(np.uint16)
         assert np.array_equal(got_tok, want_tok)
-        # the same tolerance as every parity test: against the oracle
+        gv, wv = parity.bf16_vals(got_lg), parity.bf16_vals(want_lg)
+        ulp = parity.bf16_ulp(np.maximum(np.abs(gv), np.abs(wv)))
+        assert np.all(np.abs(gv - wv) <= ulp)
+        # and both within the parity rule against the oracle
         rep = parity.check(x, got_tok, got_lg)
         assert rep.ok(), rep
-        assert np.array_equal(got_lg, want_lg)
 
 
 def test_noalloc_rejects_sizes_above_its_maximum():
