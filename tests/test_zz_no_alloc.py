@@ -45,10 +45,10 @@ def test_noalloc_matches_handle_path_twice_in_a_row():
         got_tok = tok.cpu().numpy()
         got_lg = lg.view(torch.int16).cpu().numpy().view(np.uint16)
         assert np.array_equal(got_tok, want_tok)
+        # each side within 1 bf16 ulp of the oracle, so within 2 of each other
         gv, wv = parity.bf16_vals(got_lg), parity.bf16_vals(want_lg)
         ulp = parity.bf16_ulp(np.maximum(np.abs(gv), np.abs(wv)))
-        assert np.all(np.abs(gv - wv) <= ulp)
-        # and both within the parity rule against the oracle
+        assert np.all(np.abs(gv - wv) <= 2 * ulp)
         rep = parity.check(x, got_tok, got_lg)
         assert rep.ok(), rep
 
