@@ -45,12 +45,17 @@ def test_noalloc_matches_handle_path_twice_in_a_row():
         got_tok = tok.cpu().numpy()
         got_lg = lg.view(torch.int16).cpu().numpy().view(np.uint16)
         assert np.array_equal(got_tok, want_tok)
-        # each side within 1 bf16 ulp of the oracle, so within 2 of each other
+        # both sides pass the parity rule against the oracle; where they
+        # differ by more than 2 bf16 ulp, one side took the other bf16
+        # neighbour of the exact projection (the rule's cancellation case)
+        rep_got = parity.check(x, got_tok, got_lg)
+        rep_want = parity.check(x, want_tok, want_lg)
+        assert rep_got.ok(), rep_got
+        assert rep_want.ok(), rep_want
         gv, wv = parity.bf16_vals(got_lg), parity.bf16_vals(want_lg)
         ulp = parity.bf16_ulp(np.maximum(np.abs(gv), np.abs(wv)))
-        assert np.all(np.abs(gv - wv) <= 2 * ulp)
-        rep = parity.check(x, got_tok, got_lg)
-        assert rep.ok(), rep
+        far = int(np.sum(np.abs(gv - wv) > 2 * ulp))
+        assert far <= rep_got.logits_neighbour + rep_want.logits_neighbour
 
 
 def test_noalloc_rejects_sizes_above_its_maximum():
