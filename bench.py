@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--batch", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--trace", action="store_true",
+                   help="after timing, run traced rounds and report the per-phase breakdown")
     p.add_argument("--only-timed", action="store_true",
                    help="warm-up and timed steps only (for profiler runs): no warm-L2 pass, "
                         "no end-to-end pass, no CPU baseline")
@@ -144,6 +146,52 @@ def load_inputs(cfg, B, n_rounds):
     rounds = [synth.make_inputs(cfg, B=B, round_index=i, weights=(W1, W2))
               for i in range(n_rounds)]
     return W1, W2, rounds
+
+
+PHASES = ["register strips", "shared strips", "tensor-memory epilogue", "CTA reduction",
+          "post key", "wait for all keys", "gather next u"]
+ENTRY = ["load tensor-memory tier", "load registers + shared tier, first u"]
+
+
+def phase_breakdown(walk, w, B, cfg, launch, stream, n_rounds, clocks, rounds=20):
+    """Median per-phase time (us) of CTA thread 0 over traced rounds (warm L2).
+
+    Stamps are SM clock64() values, converted with the SM clock sampled
+    during the timed region.
+    """
+    plan = w.plan()
+    n = plan["n_cta"]
+    g = cfg.gamma
+    buf = torch.zeros(n * (g + 1) * 8, dtype=torch.int64, device="cuda")
+    walk.dspark_walk_set_trace(w.h, buf, buf.numel() * 8)
+    mhz = clocks.get("sm_mhz") or 1965.0
+    steps, entry = [], []
+    for i in range(rounds):
+        buf.zero_()
+        with torch.cuda.stream(stream):
+            launch(i)
+        torch.cuda.synchronize()
+        t = buf.view(n, g + 1, 8).cpu().numpy().astype(np.float64) / mhz   # us
+        if not t[:, :g, 0].all():
+            break                       # this kernel writes no stamps
+        steps.append(np.diff(t[:, :g, :], axis=2))       # [n, g, 7]
+        entry.append(np.diff(t[:, g, :3], axis=1))       # [n, 2]
+        step_total = t[:, 1:g, 0] - t[:, :g - 1, 0] if g > 1 else None
+        if step_total is not None:
+            steps[-1] = np.concatenate([steps[-1][:, :g - 1, :], step_total[..., None]], axis=2)
+    walk.dspark_walk_set_trace(w.h, None, 0)
+    if not steps:
+        return None
+    st = np.stack(steps)
+    en = np.stack(entry)
+    names = PHASES + ["whole step"]
+    out = {"unit": "us (median over CTAs, steps and %d rounds; warm L2)" % len(steps),
+           "sm_mhz": mhz}
+    for j, name in enumerate(names[:st.shape[-1]]):
+        out[name] = float(np.median(st[..., j]))
+    for j, name in enumerate(ENTRY):
+        out["entry: " + name] = float(np.median(en[..., j]))
+    return out
 
 
 def cpu_baseline(cfg, B, rounds, seconds):
@@ -312,6 +360,8 @@ def main():
     h2d = B * cfg.gamma * cfg.V * 2 + B * 4 + B * 4
     d2h = B * cfg.gamma * 4
 
+    trace = phase_breakdown(walk, w, B, cfg, launch, stream, n_rounds, clocks) if args.trace else None
+
     mean_ms = statistics.mean(per)
     local = torch.tensor([mean_ms, (t1 - t0)], dtype=torch.float64, device=dev)
     if dist:
@@ -350,6 +400,7 @@ def main():
                 "how": "dspark_walk_run_host: pinned host base/anchor/temperature -> device, "
                        "the round, tokens -> host, stream sync; wall clock, mean of %d" % e2e_n},
         "gpu_launches": args.steps,
+        "phases": trace,
         "clocks": clocks,
         "plan": plan,
     }

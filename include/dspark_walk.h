@@ -172,6 +172,18 @@ int dspark_walk_set_limits(dspark_walk_t h, int64_t timeout_ns, int skip_cta);
  */
 int dspark_walk_set_kernel(dspark_walk_t h, int kernel);
 
+/*
+ * dspark_walk_set_trace -- phase timing of later runs (profiling aid).  When
+ * `device_buffer` holds at least n_cta * (gamma + 1) * 8 uint64 values, each
+ * run's CTA c writes SM clock64() stamps of its thread 0 at
+ * [(c * (gamma + 1) + slot) * 8 + phase]: slot k < gamma is step k (phases:
+ * start, register strips done, shared strips done, tensor-memory epilogue
+ * done, CTA reduction done, key posted, all keys seen, next u gathered);
+ * slot gamma is the round's entry (start, tensor memory loaded, ready).
+ * Only the resident kernel writes stamps.  NULL turns tracing off.
+ */
+int dspark_walk_set_trace(dspark_walk_t h, void *device_buffer, int64_t bytes);
+
 /* dspark_walk_strerror -- a static description of a status code. */
 const char *dspark_walk_strerror(int code);
 

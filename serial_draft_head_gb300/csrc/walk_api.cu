@@ -35,6 +35,8 @@ struct dspark_walk {
   dspark_walk_plan plan{};
   int st_n_cta = 0, st_rpc = 0;   // streamed kernel's shard plan
   int64_t timeout_ns = 200000000;
+  unsigned long long* trace = nullptr;  // caller-owned, see dspark_walk_set_trace
+  int64_t trace_bytes = 0;
   int skip_cta = -1;
   // staging for dspark_walk_run_host (allocated on first use)
   void* stage = nullptr;
@@ -157,6 +159,12 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
   a.seed_hi = (uint32_t)(seed >> 32);
   a.timeout_ns = h->timeout_ns;
   a.skip_cta = h->skip_cta;
+  {
+    const int n = (h->res_max_B > 0 && h->use_resident && B <= h->res_max_B) ? h->res_n_cta
+                                                                               : h->st_n_cta;
+    const int64_t need = (int64_t)n * (gamma + 1) * 8 * 8;
+    a.trace = (h->trace && h->trace_bytes >= need) ? h->trace : nullptr;
+  }
 
   if (h->res_max_B > 0 && h->use_resident && B <= h->res_max_B) {
     ResidentArgs ra{};
@@ -351,6 +359,13 @@ int dspark_walk_set_limits(dspark_walk_t h, int64_t timeout_ns, int skip_cta) {
   if (!h || timeout_ns < 1000 || skip_cta < -1) return DSPARK_EINVAL;
   h->timeout_ns = timeout_ns;
   h->skip_cta = skip_cta;
+  return DSPARK_OK;
+}
+
+int dspark_walk_set_trace(dspark_walk_t h, void* device_buffer, int64_t bytes) {
+  if (!h || bytes < 0 || (device_buffer == nullptr && bytes != 0)) return DSPARK_EINVAL;
+  h->trace = static_cast<unsigned long long*>(device_buffer);
+  h->trace_bytes = bytes;
   return DSPARK_OK;
 }
 

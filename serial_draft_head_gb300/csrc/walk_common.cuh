@@ -89,7 +89,15 @@ struct WalkArgs {
   uint32_t seed_lo, seed_hi;   // Philox key
   int64_t timeout_ns;          // rendezvous wait limit
   int skip_cta;                // fault injection: this CTA never posts (-1: off)
+  unsigned long long* trace;   // optional [n_cta][gamma + 1][8] SM-clock stamps
 };
+
+// Phase stamp of thread 0 (SM clock cycles) into the optional trace buffer:
+// slot k < gamma is step k, slot gamma is the round's entry.
+__device__ __forceinline__ void trace_stamp(const WalkArgs& a, int slot, int phase) {
+  if (a.trace != nullptr && threadIdx.x == 0)
+    a.trace[((size_t)blockIdx.x * (a.gamma + 1) + slot) * 8 + phase] = clock64();
+}
 
 // ------------------------------------------------------------ PTX helpers --
 

@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
   }
 
   // ------------------------------------------------------------- entry ----
+  trace_stamp(a, a.gamma, 0);
   if (threadIdx.x == 0) {
     round_s = *reinterpret_cast<volatile uint32_t*>(&a.sync.hdr->round);
     abort_s = 0;
@@ -217,23 +218,23 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     const uint4* src = reinterpret_cast<const uint4*>(gw);
 #pragma unroll 1
     for (int t = 0; t < kTmemTiles; ++t) {
+      // all 16 chunks of this thread's half row in flight at once, then store
+      uint32_t v[4][16];
 #pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        uint32_t v[16];
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int c = part * 4 + c4;
-          const uint4 x = __ldg(src + ((((t * 2 + h) * 16 + c) * 4 + q) * 32 + lane));
-          v[c4 * 4 + 0] = x.x;
-          v[c4 * 4 + 1] = x.y;
-          v[c4 * 4 + 2] = x.z;
-          v[c4 * 4 + 3] = x.w;
-        }
-        ptx::tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + t * 128 + 64 * h + part * 16, v);
+      for (int c = 0; c < 16; ++c) {
+        const uint4 x = __ldg(src + ((((t * 2 + h) * 16 + c) * 4 + q) * 32 + lane));
+        v[c >> 2][(c & 3) * 4 + 0] = x.x;
+        v[c >> 2][(c & 3) * 4 + 1] = x.y;
+        v[c >> 2][(c & 3) * 4 + 2] = x.z;
+        v[c >> 2][(c & 3) * 4 + 3] = x.w;
       }
+#pragma unroll
+      for (int part = 0; part < 4; ++part)
+        ptx::tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + t * 128 + 64 * h + part * 16, v[part]);
     }
     ptx::tmem_wait_st();
   }
+  trace_stamp(a, a.gamma, 1);
 
   // register tier: this warp's RS strips as mma.sync A fragments
   uint32_t wr[RS][16][4];
@@ -265,6 +266,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
+  trace_stamp(a, a.gamma, 2);
 
   // ----------------------------------------------------------- the walk ---
   const uint32_t u_addr = ptx::smem_u32(U);
@@ -274,6 +276,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
   for (; k < a.gamma && ok; ++k) {
     ptx::tc_fence_after();
     const uint64_t t_step = globaltimer_ns();
+    trace_stamp(a, k, 0);
 
     // (1) tensor-memory tiles: 3 x 16 MMAs issued by one thread
     if (threadIdx.x == 0) {
@@ -321,6 +324,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
         epi_strip<NT>(a, acc[s], base_s, temp_s, ra.R, k, kTmemRows + (warp * RS + s) * 16, row0,
                       lane, bestm);
     }
+    trace_stamp(a, k, 1);
 
     // (3) shared-memory strips s2 = warp, warp + 8, ...
 #pragma unroll 1
@@ -350,6 +354,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
                     bestm);
     }
 
+    trace_stamp(a, k, 2);
     // fold the mma-layout keys: reduce over the 8 row groups, lanes 0..3 post
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -394,8 +399,10 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
         }
       }
     }
+    trace_stamp(a, k, 3);
     ptx::tc_fence_before();
     __syncthreads();
+    trace_stamp(a, k, 4);
 
     // (5) next step's base rows (the current ones are no longer read)
     prefetch_base(ra, k + 1, row0, nv, base_s);
@@ -413,6 +420,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
       }
       if (lane == 0 && cta != a.skip_cta)
         ptx::st_relaxed_u64(slot_base + (size_t)cta * ra.max_B + b, tagged_key(mine, tag));
+      if (b == 0) trace_stamp(a, k, 5);
       unsigned long long best = 0ull;
       uint32_t spins = 0;
       bool done = false;
@@ -441,6 +449,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
         }
       }
       if (!done) break;
+      if (b == 0) trace_stamp(a, k, 6);
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) best = key_max(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
       int32_t tok = (int32_t)(0x3FFFFu - (uint32_t)(best & 0x3FFFFu));
@@ -460,6 +469,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     ptx::cp_async_wait_all();
     ptx::fence_proxy_async_smem();
     __syncthreads();
+    trace_stamp(a, k, 7);
     ok = abort_s == 0;
   }
 

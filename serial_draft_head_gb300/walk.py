@@ -55,6 +55,7 @@ EXPORTS = [
     "dspark_walk_create", "dspark_walk_run", "dspark_walk_run_host", "dspark_walk_status",
     "dspark_walk_get_plan", "dspark_walk_set_limits", "dspark_walk_strerror",
     "dspark_walk_destroy", "dspark_walk_run_noalloc", "dspark_walk_set_kernel",
+    "dspark_walk_set_trace",
 ]
 
 
@@ -84,6 +85,7 @@ def load(build_if_missing=True):
     L.dspark_walk_strerror.restype = ctypes.c_char_p
     L.dspark_walk_destroy.argtypes = [vp]
     L.dspark_walk_set_kernel.argtypes = [vp, i32]
+    L.dspark_walk_set_trace.argtypes = [vp, vp, i64]
     L.dspark_walk_run_noalloc.argtypes = [vp, vp, i64, i32, vp, vp, vp, u64, vp, i32, i32, vp, vp]
     for name in EXPORTS:
         if name != "dspark_walk_strerror":
@@ -161,6 +163,11 @@ def dspark_walk_set_limits(h, timeout_ns, skip_cta=-1):
 
 def dspark_walk_set_kernel(h, kernel):
     return _check(load().dspark_walk_set_kernel(h, int(kernel)), "dspark_walk_set_kernel")
+
+
+def dspark_walk_set_trace(h, device_buffer, nbytes):
+    return _check(load().dspark_walk_set_trace(h, _ptr(device_buffer), int(nbytes)),
+                  "dspark_walk_set_trace")
 
 
 def dspark_walk_destroy(h):
