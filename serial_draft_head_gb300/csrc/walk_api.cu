@@ -26,7 +26,6 @@ struct dspark_walk {
   SyncView sync{};
   // resident layout (used for runs with B <= res_max_B)
   uint32_t* W2p = nullptr;        // tiered repack, res_wpc words per CTA
-  unsigned long long* slots = nullptr;  // [2][res_n_cta][max_B]
   int res_max_B = 0;              // 0: no resident layout
   bool use_resident = true;       // dspark_walk_set_kernel
   int res_RS = 0, res_NT = 0, res_R = 0, res_S = 0, res_n_cta = 0;
@@ -58,14 +57,11 @@ int cuda_fail(cudaError_t e) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Sizes of the parts of the rendezvous memory: header, arrival counts and
-// keys of the streamed kernel, and the per-CTA slots of the resident kernel.
-void sync_layout(int max_gamma, int max_B, int n_slot_cta, size_t* count_off, size_t* key_off,
-                 size_t* slot_off, size_t* total) {
+// Sizes of the parts of the rendezvous memory: header, arrival counts, keys.
+void sync_layout(int max_gamma, int max_B, size_t* count_off, size_t* key_off, size_t* total) {
   *count_off = round_up(sizeof(SyncHeader), 128);
   *key_off = round_up(*count_off + (size_t)2 * max_gamma * kCountStride * sizeof(uint32_t), 128);
-  *slot_off = round_up(*key_off + (size_t)2 * max_gamma * max_B * sizeof(unsigned long long), 128);
-  *total = round_up(*slot_off + (size_t)2 * n_slot_cta * max_B * sizeof(unsigned long long), 128);
+  *total = round_up(*key_off + (size_t)2 * max_gamma * max_B * sizeof(unsigned long long), 128);
 }
 
 // Shared memory a CTA may use, minus the kernels' static shared variables.
@@ -171,11 +167,9 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
     ra.w = a;
     ra.w.rows_per_cta = h->res_R;
     ra.W2p = h->W2p;
-    ra.slots = h->slots;
     ra.R = h->res_R;
     ra.S = h->res_S;
     ra.words_per_cta = h->res_wpc;
-    ra.max_B = h->max_B;
     const uintptr_t bp = reinterpret_cast<uintptr_t>(base);
     ra.base_mode = (h->V % 8 == 0 && (bp & 15u) == 0) ? 16
                    : (h->V % 2 == 0 && (bp & 3u) == 0) ? 4 : 2;
@@ -229,9 +223,8 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
 
   int rc = DSPARK_OK;
   const bool resident = plan_resident(h);
-  size_t count_off, key_off, slot_off, total;
-  sync_layout(max_gamma, max_B, resident ? h->res_n_cta : 0, &count_off, &key_off, &slot_off,
-              &total);
+  size_t count_off, key_off, total;
+  sync_layout(max_gamma, max_B, &count_off, &key_off, &total);
   cudaError_t e = cudaMalloc(&h->W2, (size_t)V * r * 2);
   if (e == cudaSuccess) e = cudaMemcpy(h->W2, W2, (size_t)V * r * 2, cudaMemcpyDeviceToDevice);
   if (e == cudaSuccess) e = cudaMalloc(&h->sync_mem, total);
@@ -249,7 +242,6 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
     h->sync.key = reinterpret_cast<unsigned long long*>(base + key_off);
     h->sync.max_gamma = max_gamma;
     h->sync.max_B = max_B;
-    h->slots = reinterpret_cast<unsigned long long*>(base + slot_off);
     plan_stream(h);
     // every instantiation may use the shared memory of max_B, and one CTA
     // per SM must fit

@@ -298,11 +298,9 @@ __device__ __forceinline__ bool exchange(const WalkArgs& a, uint32_t round, int 
 struct ResidentArgs {
   WalkArgs w;
   const uint32_t* W2p;            // repacked W2, words_per_cta words per CTA
-  unsigned long long* slots;      // [2][n_cta][max_B] rendezvous words
   int R;                          // rows per CTA (multiple of 16)
   int S;                          // shared-memory strips per CTA
   int64_t words_per_cta;
-  int max_B;                      // slot stride
   int base_mode;                  // 16, 4 or 2: bytes per base-prefetch copy
 };
 
