@@ -345,15 +345,16 @@ def main():
         hb = [r.base.pin_memory() for r in rounds[:8]]
         ha = [r.anchor.pin_memory() for r in rounds[:8]]
         ht = [r.temperature.pin_memory() for r in rounds[:8]]
+        nh = len(hb)
         hout = torch.empty(B, cfg.gamma, dtype=torch.int32).pin_memory()
         e2e_n = min(args.steps, 200)
         for i in range(5):
-            walk.dspark_walk_run_host(w.h, hb[i % 8], ha[i % 8], ht[i % 8], seed, hout, B,
+            walk.dspark_walk_run_host(w.h, hb[i % nh], ha[i % nh], ht[i % nh], seed, hout, B,
                                       cfg.gamma, None, stream)
         te0 = time.perf_counter()
         for i in range(e2e_n):
-            rc = walk.dspark_walk_run_host(w.h, hb[i % 8], ha[i % 8], ht[i % 8], seed + i, hout,
-                                           B, cfg.gamma, None, stream)
+            rc = walk.dspark_walk_run_host(w.h, hb[i % nh], ha[i % nh], ht[i % nh], seed + i,
+                                           hout, B, cfg.gamma, None, stream)
             if rc != 0:
                 raise RuntimeError("run_host status %d" % rc)
         e2e_us = (time.perf_counter() - te0) / e2e_n * 1e6

@@ -62,25 +62,28 @@ __device__ __forceinline__ bool wait_mbar(uint64_t* bar, uint32_t parity, uint64
 
 // Stage base[b, k, row0 .. row0 + nv) for every request into base_s[b][0..R).
 __device__ __forceinline__ void prefetch_base(const ResidentArgs& ra, int k, int64_t row0,
-                                              int nv, uint16_t* base_s) {
+                                              int nv, uint16_t* base_s, int first = 0,
+                                              int count = 0) {
   const WalkArgs& a = ra.w;
   if (k >= a.gamma) return;
+  const int tid = (int)threadIdx.x - first;      // this thread's index among `count`
+  const int nthr = count > 0 ? count : (int)blockDim.x;
   if (ra.base_mode == 16) {
     const int per = nv >> 3;
-    for (int i = threadIdx.x; i < a.B * per; i += blockDim.x) {
+    for (int i = tid; i < a.B * per; i += nthr) {
       const int b = i / per, c = i - b * per;
       const uint16_t* src = a.base + ((size_t)b * a.gamma + k) * (size_t)a.V + row0 + 8 * c;
       ptx::cp_async16(base_s + (size_t)b * ra.R + 8 * c, src);
     }
   } else if (ra.base_mode == 4) {
     const int per = nv >> 1;
-    for (int i = threadIdx.x; i < a.B * per; i += blockDim.x) {
+    for (int i = tid; i < a.B * per; i += nthr) {
       const int b = i / per, c = i - b * per;
       const uint16_t* src = a.base + ((size_t)b * a.gamma + k) * (size_t)a.V + row0 + 2 * c;
       ptx::cp_async4(base_s + (size_t)b * ra.R + 2 * c, src);
     }
   } else {
-    for (int i = threadIdx.x; i < a.B * nv; i += blockDim.x) {
+    for (int i = tid; i < a.B * nv; i += nthr) {
       const int b = i / nv, c = i - b * nv;
       base_s[(size_t)b * ra.R + c] = a.base[((size_t)b * a.gamma + k) * (size_t)a.V + row0 + c];
     }
@@ -400,8 +403,9 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     __syncthreads();
     trace_stamp(a, k, 4);
 
-    // (5) next step's base rows (the current ones are no longer read)
-    prefetch_base(ra, k + 1, row0, nv, base_s);
+    // (5) next step's base rows (the current ones are no longer read), by
+    // warps 1-7: warp 0's release below would otherwise wait for these loads
+    if (warp != 0) prefetch_base(ra, k + 1, row0, nv, base_s, 32, kResThreads - 32);
 
     // (6) the rendezvous (warp 0): per request an atomic max into the step's
     // key slot, released by an arrival count; wait until every CTA has
