@@ -205,6 +205,17 @@ __device__ __forceinline__ float gumbel_score(float logit, float T, uint32_t x) 
 
 // ------------------------------------------------------------- epilogue --
 
+// Gumbel-max score of token v (request b, step k) at temperature T > 0.  Kept
+// out of line: the walk kernels inline the epilogue at many sites, and ten
+// Philox rounds plus two logs at each of them would overflow the instruction
+// cache on the (common) greedy path.
+__device__ __noinline__ float sampled_score(float logit, float T, uint32_t seed_lo,
+                                            uint32_t seed_hi, int b, int k, uint32_t v) {
+  const uint4 r = philox4x32_10(make_uint4(v >> 2, (uint32_t)k, (uint32_t)b, 0u), seed_lo,
+                                seed_hi);
+  return gumbel_score(logit, T, philox_word(r, v & 3u));
+}
+
 // The fused epilogue of one (token v, request b, step k): fp32 accumulation
 // -> bf16 bias; fp32 add of the base logit -> bf16 logit; selection score.
 // Returns the selection key; *logit_bits receives the bf16 logit.
@@ -216,11 +227,7 @@ __device__ __forceinline__ unsigned long long epilogue_key(
   *logit_bits = lb;
   const float logit = bf16_bits_to_float(lb);
   float s = logit;
-  if (T > 0.0f) {
-    const uint4 r = philox4x32_10(make_uint4(v >> 2, (uint32_t)k, (uint32_t)b, 0u), seed_lo,
-                                  seed_hi);
-    s = gumbel_score(logit, T, philox_word(r, v & 3u));
-  }
+  if (T > 0.0f) s = sampled_score(logit, T, seed_lo, seed_hi, b, k, v);
   return make_key(s, v);
 }
 
