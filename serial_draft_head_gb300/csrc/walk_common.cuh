@@ -209,7 +209,7 @@ __device__ __forceinline__ float gumbel_score(float logit, float T, uint32_t x) 
 // out of line: the walk kernels inline the epilogue at many sites, and ten
 // Philox rounds plus two logs at each of them would overflow the instruction
 // cache on the (common) greedy path.
-__device__ __noinline__ float sampled_score(float logit, float T, uint32_t seed_lo,
+static __device__ __noinline__ float sampled_score(float logit, float T, uint32_t seed_lo,
                                             uint32_t seed_hi, int b, int k, uint32_t v) {
   const uint4 r = philox4x32_10(make_uint4(v >> 2, (uint32_t)k, (uint32_t)b, 0u), seed_lo,
                                 seed_hi);
