@@ -67,21 +67,22 @@ void sync_layout(int max_gamma, int max_B, size_t* count_off, size_t* key_off, s
 // Shared memory a CTA may use, minus the kernels' static shared variables.
 constexpr size_t kSmemBudget = 232448 - 1024;
 
-// Resident plan: every CTA holds 3 tensor-memory tiles (384 rows), RS
-// register strips per warp (128 RS rows) and S shared-memory strips; rows
+// Resident plan: every CTA holds 3 tensor-memory tiles (384 rows), 2
+// register strips per warp (256 rows) and S <= 24 shared-memory strips; rows
 // are spread evenly over at most one CTA per SM (R a multiple of 16).
 // Returns false when the shard does not fit on chip (or B, V are too large),
 // in which case every run uses the streamed kernel.
 bool plan_resident(dspark_walk* h) {
   const int mb = h->max_B < 16 ? h->max_B : 16;
   if (h->V >= (1 << 18)) return false;          // the 18-bit id field of the slot word
-  const int RS = mb <= 8 ? 3 : 2;
+  const int RS = 2;
   const int NT = mb <= 8 ? 1 : 2;
   const int fixed = resident_fixed_rows(RS);
   int64_t R = (h->V + h->sm_count - 1) / h->sm_count;
   R = (R + 15) / 16 * 16;
   if (R < fixed) R = fixed;
   const int S = (int)((R - fixed) / 16);
+  if (S > resident_max_smem_strips()) return false;
   const size_t smem = resident_smem_bytes(S, mb, (int)R);
   if (smem > kSmemBudget) return false;
   h->res_max_B = mb;

@@ -17,6 +17,7 @@ int resident_fixed_rows(int RS);
 int resident_threads();
 size_t resident_smem_bytes(int S, int max_B, int R);
 const void* resident_kernel_for(int RS, int NT);
+int resident_max_smem_strips();
 cudaError_t resident_repack(const void* W2, void* out, int64_t V, int R, int RS, int S, int n_cta,
                             cudaStream_t stream);
 

@@ -98,17 +98,19 @@ __device__ __forceinline__ void gather_u_row(const uint16_t* W1, int32_t tok, in
   ptx::fence_proxy_async_smem();
 }
 
-// One (row, request) element of the fused epilogue, folded into a running key.
+// One (row, request) element of the fused epilogue, folded into a running key
+// (rows past V -- padding of the last shard -- are computed but not kept).
 __device__ __forceinline__ void epi_one(const WalkArgs& a, float acc, const uint16_t* base_s,
                                         int R, float T, int b, int k, int rl, int64_t row0,
                                         unsigned long long& best) {
   const int64_t v = row0 + rl;
-  if (v >= a.V) return;
+  const bool valid = v < a.V;
   uint16_t lb;
   const unsigned long long key = epilogue_key(acc, base_s[(size_t)b * R + rl], T, a.seed_lo,
                                               a.seed_hi, b, k, (uint32_t)v, &lb);
-  if (a.out_logits) a.out_logits[((size_t)b * a.gamma + k) * (size_t)a.V + (size_t)v] = lb;
-  best = key_max(best, key);
+  if (valid && a.out_logits)
+    a.out_logits[((size_t)b * a.gamma + k) * (size_t)a.V + (size_t)v] = lb;
+  best = (valid && key > best) ? key : best;
 }
 
 // Epilogue of one 16-row strip held as mma.sync accumulators.
@@ -131,7 +133,7 @@ __device__ __forceinline__ void epi_strip(const WalkArgs& a, const float (&acc)[
   }
 }
 
-template <int RS, int NT>
+template <int RS, int NT, int SMAX>
 __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const ResidentArgs ra) {
   constexpr int NCOL = 8 * NT;
   const WalkArgs& a = ra.w;
@@ -287,20 +289,31 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     }
     __syncwarp();
 
-    // (2) register strips: B fragments of U, k-tile by k-tile
+    // (2) register strips and this warp's shared-memory strips (s2 = warp,
+    // warp + 8, warp + 16) in ONE k loop: up to RS + SMAX independent mma.sync
+    // accumulation chains per warp hide the HMMA latency
     unsigned long long bestm[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) bestm[nt][0] = bestm[nt][1] = 0ull;
     {
-      float acc[RS][NT][4];
+      const int nS = (ra.S - warp + kResWarps - 1) / kResWarps;   // this warp's smem strips
+      float acc[RS + SMAX][NT][4];
 #pragma unroll
-      for (int s = 0; s < RS; ++s)
+      for (int s = 0; s < RS + SMAX; ++s)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[s][nt][e] = 0.0f;
+      const uint32_t blk0 = w2_addr + (uint32_t)warp * kSmemStripBytes + (lane >> 3) * 128 +
+                            (lane & 7) * 16;
 #pragma unroll
       for (int kt = 0; kt < 16; ++kt) {
+        uint32_t af[SMAX][4];
+#pragma unroll
+        for (int j = 0; j < SMAX; ++j)
+          if (j < nS)
+            ptx::ldmatrix_x4(blk0 + (uint32_t)(j * kResWarps) * kSmemStripBytes + kt * 512,
+                             af[j][0], af[j][1], af[j][2], af[j][3]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           uint32_t b0 = 0u, b1 = 0u;
@@ -312,41 +325,22 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
           for (int s = 0; s < RS; ++s)
             ptx::mma_16816(acc[s][nt], wr[s][kt][0], wr[s][kt][1], wr[s][kt][2], wr[s][kt][3],
                            b0, b1);
+#pragma unroll
+          for (int j = 0; j < SMAX; ++j)
+            if (j < nS)
+              ptx::mma_16816(acc[RS + j][nt], af[j][0], af[j][1], af[j][2], af[j][3], b0, b1);
         }
       }
+      trace_stamp(a, k, 1);
 #pragma unroll
       for (int s = 0; s < RS; ++s)
         epi_strip<NT>(a, acc[s], base_s, temp_s, ra.R, k, kTmemRows + (warp * RS + s) * 16, row0,
                       lane, bestm);
-    }
-    trace_stamp(a, k, 1);
-
-    // (3) shared-memory strips s2 = warp, warp + 8, ...
-#pragma unroll 1
-    for (int s2 = warp; s2 < ra.S; s2 += kResWarps) {
-      float acc[NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
-      const uint32_t blk = w2_addr + (uint32_t)s2 * kSmemStripBytes + (lane >> 3) * 128 +
-                           (lane & 7) * 16;
-#pragma unroll
-      for (int kt = 0; kt < 16; ++kt) {
-        uint32_t a0, a1, a2, a3;
-        ptx::ldmatrix_x4(blk + kt * 512, a0, a1, a2, a3);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          uint32_t b0 = 0u, b1 = 0u;
-          if (8 * nt + g < a.B) {
-            b0 = *reinterpret_cast<const uint32_t*>(U + (4 * kt + nt) * 128 + lane * 4);
-            b1 = *reinterpret_cast<const uint32_t*>(U + (4 * kt + 2 + nt) * 128 + lane * 4);
-          }
-          ptx::mma_16816(acc[nt], a0, a1, a2, a3, b0, b1);
-        }
-      }
-      epi_strip<NT>(a, acc, base_s, temp_s, ra.R, k, kTmemRows + 128 * RS + s2 * 16, row0, lane,
-                    bestm);
+      for (int j = 0; j < SMAX; ++j)
+        if (j < nS)
+          epi_strip<NT>(a, acc[RS + j], base_s, temp_s, ra.R, k,
+                        kTmemRows + 128 * RS + (warp + j * kResWarps) * 16, row0, lane, bestm);
     }
 
     trace_stamp(a, k, 2);
@@ -529,11 +523,12 @@ size_t resident_smem_bytes(int S, int max_B, int R) {
 }
 
 const void* resident_kernel_for(int RS, int NT) {
-  if (RS == 3 && NT == 1) return reinterpret_cast<const void*>(&walk_resident_kernel<3, 1>);
-  if (RS == 2 && NT == 2) return reinterpret_cast<const void*>(&walk_resident_kernel<2, 2>);
-  if (RS == 2 && NT == 1) return reinterpret_cast<const void*>(&walk_resident_kernel<2, 1>);
+  if (RS == 2 && NT == 1) return reinterpret_cast<const void*>(&walk_resident_kernel<2, 1, 3>);
+  if (RS == 2 && NT == 2) return reinterpret_cast<const void*>(&walk_resident_kernel<2, 2, 3>);
   return nullptr;
 }
+
+int resident_max_smem_strips() { return 3 * kResWarps; }
 
 cudaError_t resident_repack(const void* W2, void* out, int64_t V, int R, int RS, int S, int n_cta,
                             cudaStream_t stream) {
