@@ -98,38 +98,66 @@ __device__ __forceinline__ void gather_u_row(const uint16_t* W1, int32_t tok, in
   ptx::fence_proxy_async_smem();
 }
 
-// One (row, request) element of the fused epilogue, folded into a running key
-// (rows past V -- padding of the last shard -- are computed but not kept).
-__device__ __forceinline__ void epi_one(const WalkArgs& a, float acc, const uint16_t* base_s,
-                                        int R, float T, int b, int k, int rl, int64_t row0,
-                                        unsigned long long& best) {
-  const int64_t v = row0 + rl;
-  const bool valid = v < a.V;
-  uint16_t lb;
-  const unsigned long long key = epilogue_key(acc, base_s[(size_t)b * R + rl], T, a.seed_lo,
-                                              a.seed_hi, b, k, (uint32_t)v, &lb);
-  if (valid && a.out_logits)
-    a.out_logits[((size_t)b * a.gamma + k) * (size_t)a.V + (size_t)v] = lb;
-  best = (valid && key > best) ? key : best;
+// In-place first half of the fused epilogue: base_s[b][rl] (the bf16 base
+// logit) becomes bf16(base + bf16(acc)), the logit the token is chosen from.
+__device__ __forceinline__ void logit_in_place(uint16_t* base_s, int R, int b, int rl, float acc) {
+  uint16_t* p = base_s + (size_t)b * R + rl;
+  const float bias = __bfloat162float(__float2bfloat16_rn(acc));
+  *p = float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(*p), bias));
 }
 
-// Epilogue of one 16-row strip held as mma.sync accumulators.
+// ... for one 16-row strip held as mma.sync accumulators (column n = request n).
 template <int NT>
-__device__ __forceinline__ void epi_strip(const WalkArgs& a, const float (&acc)[NT][4],
-                                          const uint16_t* base_s, const float* temp_s, int R,
-                                          int k, int rl0, int64_t row0, int lane,
-                                          unsigned long long (&best)[NT][2]) {
+__device__ __forceinline__ void logits_strip(const float (&acc)[NT][4], uint16_t* base_s, int R,
+                                             int B, int rl0, int lane) {
   const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int b = 8 * nt + 2 * t4 + e;
-      if (b < a.B) {
-        epi_one(a, acc[nt][e], base_s, R, temp_s[b], b, k, rl0 + g, row0, best[nt][e]);
-        epi_one(a, acc[nt][2 + e], base_s, R, temp_s[b], b, k, rl0 + g + 8, row0, best[nt][e]);
+      if (b < B) {
+        logit_in_place(base_s, R, b, rl0 + g, acc[nt][e]);
+        logit_in_place(base_s, R, b, rl0 + g + 8, acc[nt][2 + e]);
       }
     }
+}
+
+// Second half, over all of the CTA's rows with every thread: selection score
+// and key of each logit (greedy: the logit; sampled: Philox Gumbel-max, one
+// Philox call per 4 consecutive tokens), the CTA's best key per request, and
+// the optional copy of the logits for the verifier.
+__device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logit_s, int R,
+                                         int nv, int64_t row0, int k, const float* temp_s,
+                                         unsigned long long* cta_best) {
+  const int lane = threadIdx.x & 31;
+  for (int b = 0; b < a.B; ++b) {
+    const float T = temp_s[b];
+    unsigned long long best = 0ull;
+    for (int c = threadIdx.x; 4 * c < nv; c += blockDim.x) {
+      const int rl0 = 4 * c;
+      const uint2 w = *reinterpret_cast<const uint2*>(logit_s + (size_t)b * R + rl0);
+      const uint32_t lb[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
+      const uint32_t v0 = (uint32_t)(row0 + rl0);       // a multiple of 4
+      uint4 r = make_uint4(0u, 0u, 0u, 0u);
+      if (T > 0.0f) r = philox4x32_10(make_uint4(v0 >> 2, (uint32_t)k, (uint32_t)b, 0u),
+                                      a.seed_lo, a.seed_hi);
+      const uint32_t x[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (rl0 + e < nv) {
+          const float logit = bf16_bits_to_float(lb[e]);
+          const float sc = T > 0.0f ? gumbel_score(logit, T, x[e]) : logit;
+          const unsigned long long key = make_key(sc, v0 + e);
+          best = key > best ? key : best;
+          if (a.out_logits)
+            a.out_logits[((size_t)b * a.gamma + k) * (size_t)a.V + v0 + e] = (uint16_t)lb[e];
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) best = key_max(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+    if (lane == 0 && best != 0ull) atomicMax(&cta_best[b], best);
   }
 }
 
@@ -292,9 +320,6 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     // (2) register strips and this warp's shared-memory strips (s2 = warp,
     // warp + 8, warp + 16) in ONE k loop: up to RS + SMAX independent mma.sync
     // accumulation chains per warp hide the HMMA latency
-    unsigned long long bestm[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) bestm[nt][0] = bestm[nt][1] = 0ull;
     {
       const int nS = (ra.S - warp + kResWarps - 1) / kResWarps;   // this warp's smem strips
       float acc[RS + SMAX][NT][4];
@@ -334,34 +359,19 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
       trace_stamp(a, k, 1);
 #pragma unroll
       for (int s = 0; s < RS; ++s)
-        epi_strip<NT>(a, acc[s], base_s, temp_s, ra.R, k, kTmemRows + (warp * RS + s) * 16, row0,
-                      lane, bestm);
+        logits_strip<NT>(acc[s], base_s, ra.R, a.B, kTmemRows + (warp * RS + s) * 16, lane);
 #pragma unroll
       for (int j = 0; j < SMAX; ++j)
         if (j < nS)
-          epi_strip<NT>(a, acc[RS + j], base_s, temp_s, ra.R, k,
-                        kTmemRows + 128 * RS + (warp + j * kResWarps) * 16, row0, lane, bestm);
+          logits_strip<NT>(acc[RS + j], base_s, ra.R, a.B,
+                           kTmemRows + 128 * RS + (warp + j * kResWarps) * 16, lane);
     }
 
     trace_stamp(a, k, 2);
-    // fold the mma-layout keys: reduce over the 8 row groups, lanes 0..3 post
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        unsigned long long x = bestm[nt][e];
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) x = key_max(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
-        const int b = 8 * nt + 2 * (lane & 3) + e;
-        if (lane < 4 && b < a.B && x != 0ull) atomicMax(&cta_best[b], x);
-      }
 
-    // (4) tensor-memory epilogue: warps 0-3 take tiles 0 and 2, warps 4-7 tile 1
+    // (4) tensor-memory rows: warps 0-3 take tiles 0 and 2, warps 4-7 tile 1
     {
       const int q = warp & 3;
-      unsigned long long bestt[NCOL];
-#pragma unroll
-      for (int c = 0; c < NCOL; ++c) bestt[c] = 0ull;
 #pragma unroll 1
       for (int t = warp >> 2; t < kTmemTiles; t += 2) {
         if (!wait_mbar(&mbar[2 * t], (uint32_t)(k & 1), t_step, a.timeout_ns) ||
@@ -379,19 +389,14 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
 #pragma unroll
         for (int c = 0; c < NCOL; ++c)
           if (c < a.B)
-            epi_one(a, __uint_as_float(d0[c]) + __uint_as_float(d1[c]), base_s, ra.R, temp_s[c],
-                    c, k, rl, row0, bestt[c]);
-      }
-#pragma unroll
-      for (int c = 0; c < NCOL; ++c) {
-        if (c < a.B) {
-          unsigned long long x = bestt[c];
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) x = key_max(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
-          if (lane == 0 && x != 0ull) atomicMax(&cta_best[c], x);
-        }
+            logit_in_place(base_s, ra.R, c, rl, __uint_as_float(d0[c]) + __uint_as_float(d1[c]));
       }
     }
+    ptx::tc_fence_before();
+    __syncthreads();
+
+    // (4b) scores and keys of all rows, every thread
+    key_pass(a, base_s, ra.R, nv, row0, k, temp_s, cta_best);
     trace_stamp(a, k, 3);
     ptx::tc_fence_before();
     __syncthreads();
