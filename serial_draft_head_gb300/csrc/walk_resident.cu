@@ -51,6 +51,16 @@ __device__ __forceinline__ unsigned long long key_max(unsigned long long a, unsi
   return a > b ? a : b;
 }
 
+// Maximum of a 64-bit key over the warp with two 32-bit redux.sync reductions
+// (high word, then the low word among the lanes holding the high maximum).
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long key) {
+  const uint32_t hi = (uint32_t)(key >> 32);
+  const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, hi);
+  const uint32_t lo = hi == mhi ? (uint32_t)key : 0u;
+  const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, lo);
+  return ((unsigned long long)mhi << 32) | mlo;
+}
+
 __device__ __forceinline__ bool wait_mbar(uint64_t* bar, uint32_t parity, uint64_t t0,
                                           int64_t limit_ns) {
   uint32_t spins = 0;
@@ -106,19 +116,35 @@ __device__ __forceinline__ void logit_in_place(uint16_t* base_s, int R, int b, i
   *p = float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(*p), bias));
 }
 
-// ... for one 16-row strip held as mma.sync accumulators (column n = request n).
+// ... for one 16-row strip held as mma.sync accumulators (column n = request
+// n).  All base values are loaded before any logit is stored: the stores
+// could otherwise alias later loads and serialise the chain.
 template <int NT>
 __device__ __forceinline__ void logits_strip(const float (&acc)[NT][4], uint16_t* base_s, int R,
                                              int B, int rl0, int lane) {
   const int g = lane >> 2, t4 = lane & 3;
+  uint32_t bv[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int b = 8 * nt + 2 * t4 + e;
+      const bool on = b < B;
+      bv[nt][e] = on ? base_s[(size_t)b * R + rl0 + g] : 0u;
+      bv[nt][2 + e] = on ? base_s[(size_t)b * R + rl0 + g + 8] : 0u;
+    }
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int b = 8 * nt + 2 * t4 + e;
       if (b < B) {
-        logit_in_place(base_s, R, b, rl0 + g, acc[nt][e]);
-        logit_in_place(base_s, R, b, rl0 + g + 8, acc[nt][2 + e]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float bias = __bfloat162float(__float2bfloat16_rn(acc[nt][2 * h + e]));
+          base_s[(size_t)b * R + rl0 + g + 8 * h] =
+              float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(bv[nt][2 * h + e]), bias));
+        }
       }
     }
 }
@@ -155,8 +181,7 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
         }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) best = key_max(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+    best = warp_max_key(best);
     if (lane == 0 && best != 0ull) atomicMax(&cta_best[b], best);
   }
 }
@@ -417,14 +442,14 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
       if (lane < a.B) {
         const unsigned long long mine = cta_best[lane];
         cta_best[lane] = 0ull;                     // ready for the next step's atomics
+        if (cta != a.skip_cta) {
+          red_relaxed_gpu_max_u64(keyk + lane, mine);
+          red_release_gpu_add(cnt, 1u);            // releases this lane's max
+        }
         if (mine != 0ull) {                        // the candidate's W1 row, into L2
           const uint16_t* row = a.W1 + (size_t)(0xFFFFFFFFu - (uint32_t)mine) * kRank;
 #pragma unroll
           for (int i = 0; i < 4; ++i) ptx::prefetch_l2(row + 64 * i);
-        }
-        if (cta != a.skip_cta) {
-          red_relaxed_gpu_max_u64(keyk + lane, mine);
-          red_release_gpu_add(cnt, 1u);            // releases this lane's max
         }
       }
       trace_stamp(a, k, 5);
