@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--batch", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--sweep", action="store_true",
+                   help="also time every workload and batch size (fewer steps) into 'sweep'")
     p.add_argument("--trace", action="store_true",
                    help="after timing, run traced rounds and report the per-phase breakdown")
     p.add_argument("--only-timed", action="store_true",
@@ -192,6 +194,48 @@ def phase_breakdown(walk, w, B, cfg, launch, stream, n_rounds, clocks, rounds=20
     for j, name in enumerate(ENTRY):
         out["entry: " + name] = float(np.median(en[..., j]))
     return out
+
+
+def measure_config(walk, cfg, B, steps=50, warmup=5):
+    """Cold- and warm-L2 us per walk of one workload at batch B (sweep mode)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    W1, W2, _ = synth.make_weights(cfg.V, cfg.r, cfg.seed)
+    x = synth.make_inputs(cfg, B=B, round_index=0, weights=(W1, W2))
+    w = walk.Walk(W1.to(dev), W2.to(dev), B, cfg.gamma)
+    plan = w.plan()
+    base, anchor, temp = x.base.to(dev), x.anchor.to(dev), x.temperature.to(dev)
+    tok = torch.empty(B, cfg.gamma, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            w.run(base, anchor, temp, x.seed, tok, stream=stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(i)
+            ev[i][0].record(stream)
+            w.run(base, anchor, temp, x.seed, tok, stream=stream)
+            ev[i][1].record(stream)
+        ws, we = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ws.record(stream)
+        for i in range(steps):
+            w.run(base, anchor, temp, x.seed, tok, stream=stream)
+        we.record(stream)
+    torch.cuda.synchronize()
+    st = w.status(stream)
+    cold = statistics.mean(s.elapsed_time(e) for s, e in ev) * 1000.0
+    warm = ws.elapsed_time(we) / steps * 1000.0
+    res = {"workload": cfg.name, "V": cfg.V, "gamma": cfg.gamma, "B": B,
+           "temperatures": list(cfg.temperatures), "status": st,
+           "kernel": "resident" if (plan["kernel"] == walk.KERNEL_RESIDENT and B <= 16)
+           else "stream",
+           "us_cold_l2": cold, "us_warm_l2": warm,
+           "eff_w2_GBs_cold": cfg.gamma * cfg.V * cfg.r * 2 * B / (cold * 1e-6) / 1e9}
+    w.close()
+    del flush, base
+    torch.cuda.empty_cache()
+    return res
 
 
 def cpu_baseline(cfg, B, rounds, seconds):
@@ -405,11 +449,16 @@ def main():
         "clocks": clocks,
         "plan": plan,
     }
+    if args.sweep:
+        w.close()
+        line["sweep"] = [measure_config(walk, c, b) for c in synth.CONFIGS.values()
+                         for b in c.batches]
     if rank == 0 and not args.no_cpu_baseline and not args.only_timed:
         line["cpu_baseline"] = cpu_baseline(cfg, B, rounds, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    w.close()
+    if not args.sweep:
+        w.close()
     if dist:
         dist.barrier()
         dist.destroy_process_group()
