@@ -436,21 +436,24 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     // counted every request, read the winners, gather the next u rows
     if (warp == 0) {
       const uint32_t parity = round_s & 1u;
-      const uint32_t target = (uint32_t)n_cta * (uint32_t)a.B;
+      const uint32_t target = (uint32_t)n_cta;
       uint32_t* cnt = a.sync.count_at(parity, k);
       unsigned long long* keyk = a.sync.key_at(parity, k, 0);
+      unsigned long long cand = 0ull;
       if (lane < a.B) {
         const unsigned long long mine = cta_best[lane];
         cta_best[lane] = 0ull;                     // ready for the next step's atomics
-        if (cta != a.skip_cta) {
-          red_relaxed_gpu_max_u64(keyk + lane, mine);
-          red_release_gpu_add(cnt, 1u);            // releases this lane's max
-        }
-        if (mine != 0ull) {                        // the candidate's W1 row, into L2
-          const uint16_t* row = a.W1 + (size_t)(0xFFFFFFFFu - (uint32_t)mine) * kRank;
+        if (cta != a.skip_cta) red_relaxed_gpu_max_u64(keyk + lane, mine);
+        cand = mine;
+      }
+      __syncwarp();
+      // one arrival per CTA: lane 0's release is cumulative over the maxes the
+      // warp barrier ordered before it
+      if (lane == 0 && cta != a.skip_cta) red_release_gpu_add(cnt, 1u);
+      if (cand != 0ull) {                          // the candidate's W1 row, into L2
+        const uint16_t* row = a.W1 + (size_t)(0xFFFFFFFFu - (uint32_t)cand) * kRank;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) ptx::prefetch_l2(row + 64 * i);
-        }
+        for (int i = 0; i < 4; ++i) ptx::prefetch_l2(row + 64 * i);
       }
       trace_stamp(a, k, 5);
       int good = 1;
@@ -482,7 +485,22 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
           }
         }
         __syncwarp();
-        for (int b = 0; b < a.B; ++b) gather_u_row(a.W1, tok_s[b], b, U, lane);
+        // four rows in flight at a time, then their stores; one proxy fence
+        for (int b0 = 0; b0 < a.B; b0 += 4) {
+          uint4 ur[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (b0 + j < a.B)
+              ur[j] = __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok_s[b0 + j] * kRank) +
+                            lane);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int b = b0 + j;
+            if (b < a.B)
+              *reinterpret_cast<uint4*>(U + (lane * 2 + (b >> 3)) * 128 + (b & 7) * 16) = ur[j];
+          }
+        }
+        ptx::fence_proxy_async_smem();
       }
     }
     ptx::cp_async_wait_all();
