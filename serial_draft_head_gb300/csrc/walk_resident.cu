@@ -159,25 +159,43 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
   const int lane = threadIdx.x & 31;
   for (int b = 0; b < a.B; ++b) {
     const float T = temp_s[b];
+    const uint16_t* ls = logit_s + (size_t)b * R;
+    uint16_t* outl = a.out_logits ? a.out_logits + ((size_t)b * a.gamma + k) * (size_t)a.V : nullptr;
     unsigned long long best = 0ull;
-    for (int c = threadIdx.x; 4 * c < nv; c += blockDim.x) {
-      const int rl0 = 4 * c;
-      const uint2 w = *reinterpret_cast<const uint2*>(logit_s + (size_t)b * R + rl0);
-      const uint32_t lb[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
-      const uint32_t v0 = (uint32_t)(row0 + rl0);       // a multiple of 4
-      uint4 r = make_uint4(0u, 0u, 0u, 0u);
-      if (T > 0.0f) r = philox4x32_10(make_uint4(v0 >> 2, (uint32_t)k, (uint32_t)b, 0u),
+    // two separate loops: a single loop with a select would let the compiler
+    // evaluate the noise for greedy requests too
+    if (T > 0.0f) {
+      for (int c = threadIdx.x; 4 * c < nv; c += blockDim.x) {
+        const int rl0 = 4 * c;
+        const uint2 w = *reinterpret_cast<const uint2*>(ls + rl0);
+        const uint32_t lb[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
+        const uint32_t v0 = (uint32_t)(row0 + rl0);     // a multiple of 4
+        const uint4 r = philox4x32_10(make_uint4(v0 >> 2, (uint32_t)k, (uint32_t)b, 0u),
                                       a.seed_lo, a.seed_hi);
-      const uint32_t x[4] = {r.x, r.y, r.z, r.w};
+        const uint32_t x[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (rl0 + e < nv) {
-          const float logit = bf16_bits_to_float(lb[e]);
-          const float sc = T > 0.0f ? gumbel_score(logit, T, x[e]) : logit;
-          const unsigned long long key = make_key(sc, v0 + e);
-          best = key > best ? key : best;
-          if (a.out_logits)
-            a.out_logits[((size_t)b * a.gamma + k) * (size_t)a.V + v0 + e] = (uint16_t)lb[e];
+        for (int e = 0; e < 4; ++e) {
+          if (rl0 + e < nv) {
+            const unsigned long long key =
+                make_key(gumbel_score(bf16_bits_to_float(lb[e]), T, x[e]), v0 + e);
+            best = key > best ? key : best;
+            if (outl) outl[v0 + e] = (uint16_t)lb[e];
+          }
+        }
+      }
+    } else {
+      for (int c = threadIdx.x; 4 * c < nv; c += blockDim.x) {
+        const int rl0 = 4 * c;
+        const uint2 w = *reinterpret_cast<const uint2*>(ls + rl0);
+        const uint32_t lb[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
+        const uint32_t v0 = (uint32_t)(row0 + rl0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (rl0 + e < nv) {
+            const unsigned long long key = make_key(bf16_bits_to_float(lb[e]), v0 + e);
+            best = key > best ? key : best;
+            if (outl) outl[v0 + e] = (uint16_t)lb[e];
+          }
         }
       }
     }
