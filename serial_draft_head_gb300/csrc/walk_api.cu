@@ -65,7 +65,7 @@ void sync_layout(int max_gamma, int max_B, size_t* count_off, size_t* key_off, s
 }
 
 // Shared memory a CTA may use, minus the kernels' static shared variables.
-constexpr size_t kSmemBudget = 232448 - 1024;
+constexpr size_t kSmemBudget = 232448 - 2048;
 
 // Resident plan: every CTA holds 3 tensor-memory tiles (384 rows), 2
 // register strips per warp (256 rows) and S <= 24 shared-memory strips; rows

@@ -109,14 +109,8 @@ __device__ __forceinline__ void gather_u_row(const uint16_t* W1, int32_t tok, in
 }
 
 // In-place first half of the fused epilogue: base_s[b][rl] (the bf16 base
-// logit) becomes bf16(base + bf16(acc)), the logit the token is chosen from.
-__device__ __forceinline__ void logit_in_place(uint16_t* base_s, int R, int b, int rl, float acc) {
-  uint16_t* p = base_s + (size_t)b * R + rl;
-  const float bias = __bfloat162float(__float2bfloat16_rn(acc));
-  *p = float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(*p), bias));
-}
-
-// ... for one 16-row strip held as mma.sync accumulators (column n = request
+// logit) becomes bf16(base + bf16(acc)), the logit the token is chosen from,
+// here for one 16-row strip held as mma.sync accumulators (column n = request
 // n).  All base values are loaded before any logit is stored: the stores
 // could otherwise alias later loads and serialise the chain.
 template <int NT>
@@ -155,7 +149,7 @@ __device__ __forceinline__ void logits_strip(const float (&acc)[NT][4], uint16_t
 // the optional copy of the logits for the verifier.
 __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logit_s, int R,
                                          int nv, int64_t row0, int k, const float* temp_s,
-                                         unsigned long long* cta_best) {
+                                         unsigned long long (*warp_best)[16]) {
   const int lane = threadIdx.x & 31;
   for (int b = 0; b < a.B; ++b) {
     const float T = temp_s[b];
@@ -200,7 +194,7 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
       }
     }
     best = warp_max_key(best);
-    if (lane == 0 && best != 0ull) atomicMax(&cta_best[b], best);
+    if (lane == 0) warp_best[threadIdx.x >> 5][b] = best;
   }
 }
 
@@ -213,7 +207,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
   uint8_t* U = smem + (size_t)ra.S * kSmemStripBytes;
   uint16_t* base_s = reinterpret_cast<uint16_t*>(U + 16 * 512);
   __shared__ __align__(8) uint64_t mbar[kIssuers + 1];
-  __shared__ unsigned long long cta_best[16];
+  __shared__ unsigned long long warp_best[kResWarps][16];
   __shared__ float temp_s[16];
   __shared__ int32_t tok_s[16];
   __shared__ uint32_t tmem_base_s;
@@ -253,7 +247,6 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
   if (threadIdx.x < 16) {
     temp_s[threadIdx.x] = threadIdx.x < a.B ? a.temperature[threadIdx.x] : 0.0f;
     tok_s[threadIdx.x] = threadIdx.x < a.B ? a.anchor[threadIdx.x] : 0;
-    cta_best[threadIdx.x] = 0ull;   // afterwards cleared by the warp that consumes it
   }
   for (int i = threadIdx.x; i < 16 * 512 / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(U)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -429,17 +422,24 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
         ptx::tmem_ld<NCOL>(tmem + lane_base + kDCol0 + 32 * t + 16, d1);   // K half 1
         ptx::tmem_wait_ld();
         const int rl = t * 128 + 32 * q + lane;
+        uint32_t bvals[NCOL];
+#pragma unroll
+        for (int c = 0; c < NCOL; ++c) bvals[c] = c < a.B ? base_s[(size_t)c * ra.R + rl] : 0u;
 #pragma unroll
         for (int c = 0; c < NCOL; ++c)
-          if (c < a.B)
-            logit_in_place(base_s, ra.R, c, rl, __uint_as_float(d0[c]) + __uint_as_float(d1[c]));
+          if (c < a.B) {
+            const float bias =
+                __bfloat162float(__float2bfloat16_rn(__uint_as_float(d0[c]) + __uint_as_float(d1[c])));
+            base_s[(size_t)c * ra.R + rl] =
+                float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(bvals[c]), bias));
+          }
       }
     }
     ptx::tc_fence_before();
     __syncthreads();
 
     // (4b) scores and keys of all rows, every thread
-    key_pass(a, base_s, ra.R, nv, row0, k, temp_s, cta_best);
+    key_pass(a, base_s, ra.R, nv, row0, k, temp_s, warp_best);
     trace_stamp(a, k, 3);
     ptx::tc_fence_before();
     __syncthreads();
@@ -459,8 +459,9 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
       unsigned long long* keyk = a.sync.key_at(parity, k, 0);
       unsigned long long cand = 0ull;
       if (lane < a.B) {
-        const unsigned long long mine = cta_best[lane];
-        cta_best[lane] = 0ull;                     // ready for the next step's atomics
+        unsigned long long mine = 0ull;
+#pragma unroll
+        for (int w = 0; w < kResWarps; ++w) mine = key_max(mine, warp_best[w][lane]);
         if (cta != a.skip_cta) red_relaxed_gpu_max_u64(keyk + lane, mine);
         cand = mine;
       }
