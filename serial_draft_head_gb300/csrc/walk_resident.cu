@@ -143,23 +143,38 @@ __device__ __forceinline__ void logits_strip(const float (&acc)[NT][4], uint16_t
     }
 }
 
-// Second half, over all of the CTA's rows with every thread: selection score
-// and key of each logit (greedy: the logit; sampled: Philox Gumbel-max, one
-// Philox call per 4 consecutive tokens), the CTA's best key per request, and
-// the optional copy of the logits for the verifier.
+// Greedy key straight from bf16 bits: the order-preserving 16 bits of the
+// logit (-0 folded onto +0) above the inverted token id.  It orders exactly
+// as make_key(logit) does, without the fp32 round trip.
+__device__ __forceinline__ unsigned long long greedy_key(uint32_t h, uint32_t v) {
+  h = h == 0x8000u ? 0u : h;
+  const uint32_t ord = (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
+  return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - v);
+}
+
+// Second half, over all of the CTA's rows: selection score and key of each
+// logit (greedy: the logit; sampled: Philox Gumbel-max, one Philox call per 4
+// consecutive tokens), the best key per (request, thread group), and the
+// optional copy of the logits for the verifier.  Requests run side by side:
+// `tpr` = blockDim / (B rounded up to a power of two) threads per request.
+// group_best[b][slot] receives one key per group of 32 (or 16) threads.
 __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logit_s, int R,
                                          int nv, int64_t row0, int k, const float* temp_s,
-                                         unsigned long long (*warp_best)[16]) {
+                                         unsigned long long (*group_best)[kResWarps]) {
+  int bp = 1;
+  while (bp < a.B) bp <<= 1;
+  const int tpr = (int)blockDim.x / bp;            // 16 .. 256
+  const int b = (int)threadIdx.x / tpr, gi = (int)threadIdx.x % tpr;
   const int lane = threadIdx.x & 31;
-  for (int b = 0; b < a.B; ++b) {
+  unsigned long long best = 0ull;
+  if (b < a.B) {
     const float T = temp_s[b];
     const uint16_t* ls = logit_s + (size_t)b * R;
-    uint16_t* outl = a.out_logits ? a.out_logits + ((size_t)b * a.gamma + k) * (size_t)a.V : nullptr;
-    unsigned long long best = 0ull;
-    // two separate loops: a single loop with a select would let the compiler
-    // evaluate the noise for greedy requests too
+    uint16_t* outl =
+        a.out_logits ? a.out_logits + ((size_t)b * a.gamma + k) * (size_t)a.V : nullptr;
+    // separate loops: one loop with a select would evaluate the noise always
     if (T > 0.0f) {
-      for (int c = threadIdx.x; 4 * c < nv; c += blockDim.x) {
+      for (int c = gi; 4 * c < nv; c += tpr) {
         const int rl0 = 4 * c;
         const uint2 w = *reinterpret_cast<const uint2*>(ls + rl0);
         const uint32_t lb[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
@@ -178,7 +193,7 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
         }
       }
     } else {
-      for (int c = threadIdx.x; 4 * c < nv; c += blockDim.x) {
+      for (int c = gi; 4 * c < nv; c += tpr) {
         const int rl0 = 4 * c;
         const uint2 w = *reinterpret_cast<const uint2*>(ls + rl0);
         const uint32_t lb[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
@@ -186,15 +201,24 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           if (rl0 + e < nv) {
-            const unsigned long long key = make_key(bf16_bits_to_float(lb[e]), v0 + e);
+            const unsigned long long key = greedy_key(lb[e], v0 + e);
             best = key > best ? key : best;
             if (outl) outl[v0 + e] = (uint16_t)lb[e];
           }
         }
       }
     }
+  }
+  if (tpr >= 32) {                                 // whole warps per request
     best = warp_max_key(best);
-    if (lane == 0) warp_best[threadIdx.x >> 5][b] = best;
+    if (lane == 0 && b < a.B) group_best[b][(threadIdx.x % tpr) >> 5] = best;
+  } else {                                         // two requests per warp
+    const unsigned mask = 0xFFFFu << (lane & 16);
+    const uint32_t hi = (uint32_t)(best >> 32);
+    const uint32_t mhi = __reduce_max_sync(mask, hi);
+    const uint32_t mlo = __reduce_max_sync(mask, hi == mhi ? (uint32_t)best : 0u);
+    if ((lane & 15) == 0 && b < a.B)
+      group_best[b][0] = ((unsigned long long)mhi << 32) | mlo;
   }
 }
 
@@ -207,7 +231,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
   uint8_t* U = smem + (size_t)ra.S * kSmemStripBytes;
   uint16_t* base_s = reinterpret_cast<uint16_t*>(U + 16 * 512);
   __shared__ __align__(8) uint64_t mbar[kIssuers + 1];
-  __shared__ unsigned long long warp_best[kResWarps][16];
+  __shared__ unsigned long long group_best[16][kResWarps];
   __shared__ float temp_s[16];
   __shared__ int32_t tok_s[16];
   __shared__ uint32_t tmem_base_s;
@@ -439,7 +463,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     __syncthreads();
 
     // (4b) scores and keys of all rows, every thread
-    key_pass(a, base_s, ra.R, nv, row0, k, temp_s, warp_best);
+    key_pass(a, base_s, ra.R, nv, row0, k, temp_s, group_best);
     trace_stamp(a, k, 3);
     ptx::tc_fence_before();
     __syncthreads();
@@ -458,10 +482,12 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
       uint32_t* cnt = a.sync.count_at(parity, k);
       unsigned long long* keyk = a.sync.key_at(parity, k, 0);
       unsigned long long cand = 0ull;
+      int bp = 1;
+      while (bp < a.B) bp <<= 1;
+      const int nslots = (kResThreads / bp) >= 32 ? (kResThreads / bp) / 32 : 1;
       if (lane < a.B) {
         unsigned long long mine = 0ull;
-#pragma unroll
-        for (int w = 0; w < kResWarps; ++w) mine = key_max(mine, warp_best[w][lane]);
+        for (int sl = 0; sl < nslots; ++sl) mine = key_max(mine, group_best[lane][sl]);
         if (cta != a.skip_cta) red_relaxed_gpu_max_u64(keyk + lane, mine);
         cand = mine;
       }
