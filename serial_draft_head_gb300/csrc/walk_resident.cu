@@ -143,15 +143,6 @@ __device__ __forceinline__ void logits_strip(const float (&acc)[NT][4], uint16_t
     }
 }
 
-// Greedy key straight from bf16 bits: the order-preserving 16 bits of the
-// logit (-0 folded onto +0) above the inverted token id.  It orders exactly
-// as make_key(logit) does, without the fp32 round trip.
-__device__ __forceinline__ unsigned long long greedy_key(uint32_t h, uint32_t v) {
-  h = h == 0x8000u ? 0u : h;
-  const uint32_t ord = (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
-  return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - v);
-}
-
 // Second half, over all of the CTA's rows: selection score and key of each
 // logit (greedy: the logit; sampled: Philox Gumbel-max, one Philox call per 4
 // consecutive tokens), the best key per (request, thread group), and the
@@ -193,19 +184,31 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
         }
       }
     } else {
-      for (int c = gi; 4 * c < nv; c += tpr) {
-        const int rl0 = 4 * c;
-        const uint2 w = *reinterpret_cast<const uint2*>(ls + rl0);
-        const uint32_t lb[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
-        const uint32_t v0 = (uint32_t)(row0 + rl0);
+      // 32-bit keys {order bits of the bf16 logit : 16, inverted local row :
+      // 16}, two independent maxima per thread, widened to the 64-bit key once
+      uint32_t m0 = 0u, m1 = 0u;
+      for (int c = gi; 4 * c < nv; c += 2 * tpr) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (rl0 + e < nv) {
-            const unsigned long long key = greedy_key(lb[e], v0 + e);
-            best = key > best ? key : best;
-            if (outl) outl[v0 + e] = (uint16_t)lb[e];
+        for (int u = 0; u < 2; ++u) {
+          const int rl0 = 4 * (c + u * tpr);
+          if (rl0 < nv) {
+            const uint2 w = *reinterpret_cast<const uint2*>(ls + rl0);
+            const uint32_t lb[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint32_t h = lb[e] == 0x8000u ? 0u : lb[e];
+              h = (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
+              const uint32_t key32 = rl0 + e < nv ? (h << 16) | (0xFFFFu - (uint32_t)(rl0 + e)) : 0u;
+              if (u == 0) m0 = max(m0, key32); else m1 = max(m1, key32);
+              if (outl && rl0 + e < nv) outl[row0 + rl0 + e] = (uint16_t)lb[e];
+            }
           }
         }
+      }
+      const uint32_t m = max(m0, m1);
+      if (m != 0u) {
+        const uint32_t v = (uint32_t)(row0 + (0xFFFFu - (m & 0xFFFFu)));
+        best = ((unsigned long long)(m >> 16) << 32) | (unsigned long long)(0xFFFFFFFFu - v);
       }
     }
   }
