@@ -86,6 +86,7 @@ struct dspark_walk_plan {
 
 #define DSPARK_KERNEL_STREAM 0   /* every row re-read from global memory each step */
 #define DSPARK_KERNEL_RESIDENT 1 /* rows held in registers / shared / tensor memory */
+#define DSPARK_KERNEL_BATCHED 2  /* rows streamed by TMA, tcgen05 with N = B (large B) */
 
 /*
  * dspark_walk_create -- prepare a walk over fixed weights.
@@ -163,12 +164,14 @@ int dspark_walk_get_plan(dspark_walk_t h, struct dspark_walk_plan *p);
 int dspark_walk_set_limits(dspark_walk_t h, int64_t timeout_ns, int skip_cta);
 
 /*
- * dspark_walk_set_kernel -- choose the kernel of later runs with B <= the
- * resident layout's batch limit: DSPARK_KERNEL_RESIDENT (the default when
- * create() found an on-chip placement) or DSPARK_KERNEL_STREAM (re-read W2
- * from L2/HBM every step: the single-launch "L2 probe" of the blog post's
- * section "V = 151,936: the whole bf16 table on chip", kept as an ablation).
- * Returns DSPARK_EUNSUPPORTED if RESIDENT is asked for but was not planned.
+ * dspark_walk_set_kernel -- choose the kernels of later runs.
+ *   DSPARK_KERNEL_RESIDENT (default): the resident kernel for batches up to
+ *     its limit (when create() found an on-chip placement), the batched
+ *     kernel above it.  DSPARK_EUNSUPPORTED if no resident placement exists.
+ *   DSPARK_KERNEL_BATCHED: the batched kernel for every batch.
+ *   DSPARK_KERNEL_STREAM: the CUDA-core kernel that re-reads W2 from L2/HBM
+ *     every step (the single-launch "L2 probe" of the blog post's section
+ *     "V = 151,936: the whole bf16 table on chip"), kept as an ablation.
  */
 int dspark_walk_set_kernel(dspark_walk_t h, int kernel);
 

@@ -33,6 +33,10 @@ struct dspark_walk {
   size_t res_smem = 0;
   dspark_walk_plan plan{};
   int st_n_cta = 0, st_rpc = 0;   // streamed kernel's shard plan
+  // batched layout (runs the resident kernel does not take)
+  uint8_t* W2b = nullptr;
+  int bat_R = 0, bat_n_cta = 0;
+  bool use_batched = true;
   int64_t timeout_ns = 200000000;
   unsigned long long* trace = nullptr;  // caller-owned, see dspark_walk_set_trace
   int64_t trace_bytes = 0;
@@ -66,6 +70,15 @@ void sync_layout(int max_gamma, int max_B, size_t* count_off, size_t* key_off, s
 
 // Shared memory a CTA may use, minus the kernels' static shared variables.
 constexpr size_t kSmemBudget = 232448 - 2048;
+
+// Batched plan: rows spread over at most one CTA per SM in whole 128-row
+// tiles; every step streams the CTA's tiles through the TMA ring.
+void plan_batched(dspark_walk* h) {
+  int64_t R = (h->V + h->sm_count - 1) / h->sm_count;
+  R = (R + 127) / 128 * 128;
+  h->bat_R = (int)R;
+  h->bat_n_cta = (int)((h->V + R - 1) / R);
+}
 
 // Resident plan: every CTA holds 3 tensor-memory tiles (384 rows), 2
 // register strips per warp (256 rows) and S <= 24 shared-memory strips; rows
@@ -163,6 +176,12 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
     a.trace = (h->trace && h->trace_bytes >= need) ? h->trace : nullptr;
   }
 
+  if (!(h->res_max_B > 0 && h->use_resident && B <= h->res_max_B) && h->W2b && h->use_batched) {
+    CUDA_TRY(batched_launch(a, h->W2b, h->bat_R, h->bat_n_cta, h->max_B, B,
+                            232448 - 1024, stream));
+    return DSPARK_OK;
+  }
+
   if (h->res_max_B > 0 && h->use_resident && B <= h->res_max_B) {
     ResidentArgs ra{};
     ra.w = a;
@@ -234,6 +253,9 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
     e = cudaMalloc(&h->W2p, (size_t)h->res_wpc * h->res_n_cta * sizeof(uint32_t));
   if (e == cudaSuccess && resident)
     e = resident_repack(W2, h->W2p, V, h->res_R, h->res_RS, h->res_S, h->res_n_cta, 0);
+  plan_batched(h);
+  if (e == cudaSuccess) e = cudaMalloc(&h->W2b, (size_t)h->bat_R * h->bat_n_cta * 512);
+  if (e == cudaSuccess) e = batched_repack(W2, h->W2b, V, h->bat_R, h->bat_n_cta, 0);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) rc = cuda_fail(e);
   if (rc == DSPARK_OK) {
@@ -255,6 +277,16 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, stream_threads(), smem);
       if (e != cudaSuccess) rc = cuda_fail(e);
       else if (per_sm < 1) rc = DSPARK_EUNSUPPORTED;
+    }
+    if (rc == DSPARK_OK) {
+      int per_sm = 0;
+      e = cudaFuncSetAttribute(batched_kernel(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               232448 - 1024);
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, batched_kernel(),
+                                                          batched_threads(), 232448 - 1024);
+      if (e != cudaSuccess) rc = cuda_fail(e);
+      else if (per_sm != 1) rc = DSPARK_EUNSUPPORTED;
     }
     if (rc == DSPARK_OK && resident) {
       int per_sm = 0;
@@ -366,11 +398,18 @@ int dspark_walk_set_kernel(dspark_walk_t h, int kernel) {
   if (!h) return DSPARK_EINVAL;
   if (kernel == DSPARK_KERNEL_STREAM) {
     h->use_resident = false;
+    h->use_batched = false;
     return DSPARK_OK;
   }
   if (kernel == DSPARK_KERNEL_RESIDENT) {
     if (h->res_max_B == 0) return DSPARK_EUNSUPPORTED;
     h->use_resident = true;
+    h->use_batched = true;
+    return DSPARK_OK;
+  }
+  if (kernel == DSPARK_KERNEL_BATCHED) {
+    h->use_resident = false;
+    h->use_batched = true;
     return DSPARK_OK;
   }
   return DSPARK_EINVAL;
@@ -400,6 +439,7 @@ int dspark_walk_destroy(dspark_walk_t h) {
   if (cudaDeviceSynchronize() != cudaSuccess) rc = DSPARK_ECUDA;
   if (h->W2) cudaFree(h->W2);
   if (h->W2p) cudaFree(h->W2p);
+  if (h->W2b) cudaFree(h->W2b);
   if (h->sync_mem) cudaFree(h->sync_mem);
   if (h->stage) cudaFree(h->stage);
   delete h;

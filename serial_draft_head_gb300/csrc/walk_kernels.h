@@ -21,4 +21,15 @@ int resident_max_smem_strips();
 cudaError_t resident_repack(const void* W2, void* out, int64_t V, int R, int RS, int S, int n_cta,
                             cudaStream_t stream);
 
+// Batched kernel: W2 streamed through a TMA ring, tcgen05 with N = B.
+struct WalkArgs;
+int batched_threads();
+size_t batched_smem_bytes(int nst, int N);
+int batched_max_stages();
+const void* batched_kernel();
+cudaError_t batched_repack(const void* W2, void* out, int64_t V, int R, int n_cta,
+                           cudaStream_t stream);
+cudaError_t batched_launch(const WalkArgs& w, const void* W2b, int R, int n_cta, int max_B, int B,
+                           size_t smem_budget, cudaStream_t stream);
+
 }  // namespace dspark

@@ -25,6 +25,7 @@ EINTERNAL = -9
 
 KERNEL_STREAM = 0
 KERNEL_RESIDENT = 1
+KERNEL_BATCHED = 2
 
 _lib = None
 

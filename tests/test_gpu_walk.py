@@ -27,6 +27,8 @@ def make_walk(walkmod, x, max_B=None, max_gamma=None, kernel=None):
     w = walkmod.Walk(x.W1.cuda(), x.W2.cuda(), max_B or x.B, max_gamma or x.gamma)
     if kernel == "stream":
         w.set_kernel(walkmod.KERNEL_STREAM)
+    elif kernel == "batched":
+        w.set_kernel(walkmod.KERNEL_BATCHED)
     return w
 
 
@@ -59,7 +61,7 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("kernel", ["planned", "stream"])
+@pytest.mark.parametrize("kernel", ["planned", "stream", "batched"])
 @pytest.mark.parametrize("V,gamma,B,temps,seed", SMALL)
 def test_small_every_logit(walkmod, V, gamma, B, temps, seed, kernel):
     x = synth.make_custom(V=V, gamma=gamma, B=B, seed=seed, temperatures=temps,
