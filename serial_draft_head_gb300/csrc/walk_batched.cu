@@ -225,11 +225,32 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
       __syncwarp();
     } else {
       // ---------------------------------------------------- epilogue warps
+      // warp w: rows 32 (w % 4) .. +31 of every tile, columns (requests)
+      // [c0, c0 + cols).  Base logits come from HBM: the loads of the next
+      // 16-column chunk are issued before the current chunk is computed.
       const int q = warp & 3, half = warp >> 2;
-      const int cols = N >> 1;                       // this warp's columns
+      const int cols = N >> 1;
       const int c0 = half * cols;
+      int act = a.B - c0;                            // this warp's live columns
+      act = act < 0 ? 0 : (act > cols ? cols : act);
+      const int cpt = (act + 15) >> 4;               // chunks per tile
+      const int nc = cpt * T;
       for (int i = lane; i < 128; i += 32) wbest[warp * 128 + i] = 0ull;
       __syncwarp();
+      uint32_t nxt[16];
+      auto prefetch = [&](int ci) {
+        const int t = ci / cpt, cb = (ci - t * cpt) * 16;
+        const int64_t v = row0 + t * 128 + 32 * q + lane;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int b = c0 + cb + j;
+          nxt[j] = (cb + j < act && v < a.V)
+                       ? (uint32_t)__ldg(a.base + ((size_t)b * a.gamma + k) * (size_t)a.V + v)
+                       : 0u;
+        }
+      };
+      if (nc > 0) prefetch(0);
+      int ci = 0;
       for (int t = 0; t < T; ++t) {
         const int Gt = G + t;
         const int d = Gt & 1;
@@ -241,24 +262,27 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
           break;
         }
         ptx::tc_fence_after();
-        const int rl = t * 128 + 32 * q + lane;
-        const int64_t v = row0 + rl;
+        const int64_t v = row0 + t * 128 + 32 * q + lane;
         const bool valid = v < a.V;
-        for (int cb = 0; cb < cols; cb += 16) {
+        for (int cc = 0; cc < cpt; ++cc, ++ci) {
+          const int cb = cc * 16;
+          uint32_t cur[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) cur[j] = nxt[j];
+          if (ci + 1 < nc) prefetch(ci + 1);
           uint32_t dv[16];
           ptx::tmem_ld<16>(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * 256 + c0 + cb), dv);
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int b = c0 + cb + j;
-            if (cb + j >= cols || b >= a.B) continue;   // uniform across the warp
+            if (cb + j >= act) continue;             // uniform across the warp
             unsigned long long key = 0ull;
             if (valid) {
-              const size_t off = ((size_t)b * a.gamma + k) * (size_t)a.V + (size_t)v;
               const float bias = __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j])));
-              const uint16_t lb = float_to_bf16_bits_rn(
-                  __fadd_rn(bf16_bits_to_float(__ldg(a.base + off)), bias));
-              if (a.out_logits) a.out_logits[off] = lb;
+              const uint16_t lb = float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(cur[j]), bias));
+              if (a.out_logits)
+                a.out_logits[((size_t)b * a.gamma + k) * (size_t)a.V + (size_t)v] = lb;
               const float T_b = temp_s[b];
               const float logit = bf16_bits_to_float(lb);
               float sc = logit;
