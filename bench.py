@@ -162,7 +162,8 @@ def phase_breakdown(walk, w, B, cfg, launch, stream, n_rounds, clocks, rounds=20
     during the timed region.
     """
     plan = w.plan()
-    n = plan["n_cta"]
+    n = plan["n_cta"] if (plan["kernel"] == walk.KERNEL_RESIDENT and B <= 16) else \
+        -(-cfg.V // (-(-(-(-cfg.V // plan["sm_count"])) // 128) * 128))
     g = cfg.gamma
     buf = torch.zeros(n * (g + 1) * 8, dtype=torch.int64, device="cuda")
     walk.dspark_walk_set_trace(w.h, buf, buf.numel() * 8)

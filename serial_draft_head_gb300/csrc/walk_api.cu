@@ -170,8 +170,8 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
   a.timeout_ns = h->timeout_ns;
   a.skip_cta = h->skip_cta;
   {
-    const int n = (h->res_max_B > 0 && h->use_resident && B <= h->res_max_B) ? h->res_n_cta
-                                                                               : h->st_n_cta;
+    const bool res = h->res_max_B > 0 && h->use_resident && B <= h->res_max_B;
+    const int n = res ? h->res_n_cta : (h->W2b && h->use_batched ? h->bat_n_cta : h->st_n_cta);
     const int64_t need = (int64_t)n * (gamma + 1) * 8 * 8;
     a.trace = (h->trace && h->trace_bytes >= need) ? h->trace : nullptr;
   }

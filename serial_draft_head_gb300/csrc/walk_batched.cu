@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
   }
 
   // ---------------------------------------------------------------- entry --
+  trace_stamp(a, a.gamma, 0);
   if (threadIdx.x == 0) {
     round_s = *reinterpret_cast<volatile uint32_t*>(&a.sync.hdr->round);
     abort_s = 0;
@@ -163,9 +164,11 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
   int consumed = 0;   // control: half-tiles whose MMAs were issued
   int G = 0;          // tiles processed so far this round (both roles track it)
 
+  trace_stamp(a, a.gamma, 2);
   for (int k = 0; k < a.gamma && ok; ++k) {
     ptx::tc_fence_after();
     const uint64_t t_step = globaltimer_ns();
+    trace_stamp(a, k, 0);
     if (warp == kEpiWarps) {
       // ------------------------------------------------------ control warp
       if (lane == 0) {
@@ -262,6 +265,7 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
           break;
         }
         ptx::tc_fence_after();
+        if (t == 0) trace_stamp(a, k, 1);
         const int64_t v = row0 + t * 128 + 32 * q + lane;
         const bool valid = v < a.V;
         for (int cc = 0; cc < cpt; ++cc, ++ci) {
@@ -305,9 +309,11 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
         __syncwarp();
         if (lane == 0) mbar_arrive(&dempty[d]);
       }
+      trace_stamp(a, k, 2);
       G += T;
     }
     __syncthreads();
+    trace_stamp(a, k, 3);
     if (abort_s) { ok = false; break; }
 
     // CTA best per request: max over the 4 lane quarters of its column half
@@ -322,7 +328,9 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
       cta_key[b] = m;
     }
     __syncthreads();
+    trace_stamp(a, k, 4);
     ok = exchange(a, round_s, k, cta_key, tok_s, &flag_s);
+    trace_stamp(a, k, 5);
     if (!ok) break;
     if (cta == 0)
       for (int b = threadIdx.x; b < a.B; b += blockDim.x)
@@ -330,6 +338,7 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
     if (k + 1 < a.gamma && warp < kEpiWarps) gather_u(a, tok_s, U, N);
     ptx::tc_fence_before();
     __syncthreads();
+    trace_stamp(a, k, 7);
   }
 
   // ----------------------------------------------------------------- exit --
