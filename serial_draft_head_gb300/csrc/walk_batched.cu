@@ -66,13 +66,29 @@ __device__ __forceinline__ unsigned long long group_max_key(unsigned mask, unsig
 }
 
 // u_b = W1[tok] into U (core matrix (kc, b / 8) at (kc * N/8 + b/8) * 128).
+// Eight rows' chunks in flight per thread before any store.
 __device__ __forceinline__ void gather_u(const WalkArgs& a, const int32_t* tok_s, uint8_t* U,
                                          int N) {
   const int epi_threads = kEpiWarps * 32;
-  for (int i = threadIdx.x; i < a.B * 32; i += epi_threads) {
-    const int b = i >> 5, c = i & 31;
-    const uint4 x = __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok_s[b] * kRank) + c);
-    *reinterpret_cast<uint4*>(U + ((size_t)c * (N >> 3) + (b >> 3)) * 128 + (b & 7) * 16) = x;
+  const int total = a.B * 32;
+  for (int i0 = threadIdx.x; i0 < total; i0 += 8 * epi_threads) {
+    uint4 x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * epi_threads;
+      if (i < total)
+        x[u] = __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok_s[i >> 5] * kRank) +
+                     (i & 31));
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * epi_threads;
+      if (i < total) {
+        const int b = i >> 5, c = i & 31;
+        *reinterpret_cast<uint4*>(U + ((size_t)c * (N >> 3) + (b >> 3)) * 128 + (b & 7) * 16) =
+            x[u];
+      }
+    }
   }
   ptx::fence_proxy_async_smem();
 }
