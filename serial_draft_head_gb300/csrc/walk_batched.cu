@@ -93,7 +93,7 @@ __device__ __forceinline__ void gather_u(const WalkArgs& a, const int32_t* tok_s
   ptx::fence_proxy_async_smem();
 }
 
-__global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const BatchedArgs ba) {
+__global__ void __maxnreg__(224) walk_batched_kernel(const BatchedArgs ba) {
   const WalkArgs& a = ba.w;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int N = ba.N;
@@ -293,12 +293,14 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
           uint32_t dv[16];
           ptx::tmem_ld<16>(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * 256 + c0 + cb), dv);
           ptx::tmem_wait_ld();
+          // all 16 keys first (independent chains the compiler can interleave),
+          // then the warp reductions
+          unsigned long long key[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int b = c0 + cb + j;
-            if (cb + j >= act) continue;             // uniform across the warp
-            unsigned long long key = 0ull;
-            if (valid) {
+            key[j] = 0ull;
+            if (cb + j < act && valid) {
               const float bias = __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j])));
               const uint16_t lb = float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(cur[j]), bias));
               if (a.out_logits)
@@ -312,12 +314,16 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
                                               a.seed_lo, a.seed_hi);
                 sc = gumbel_score(logit, T_b, philox_word(r, (uint32_t)v & 3u));
               }
-              key = make_key(sc, (uint32_t)v);
+              key[j] = make_key(sc, (uint32_t)v);
             }
-            key = group_max_key(0xFFFFFFFFu, key);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (cb + j >= act) continue;             // uniform across the warp
+            const unsigned long long m = group_max_key(0xFFFFFFFFu, key[j]);
             if (lane == 0) {
-              unsigned long long* p = &wbest[warp * 128 + (b - c0)];
-              *p = key > *p ? key : *p;
+              unsigned long long* p = &wbest[warp * 128 + (cb + j)];
+              *p = m > *p ? m : *p;
             }
           }
         }
