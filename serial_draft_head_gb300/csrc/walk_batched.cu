@@ -93,7 +93,7 @@ __device__ __forceinline__ void gather_u(const WalkArgs& a, const int32_t* tok_s
   ptx::fence_proxy_async_smem();
 }
 
-__global__ void __maxnreg__(224) walk_batched_kernel(const BatchedArgs ba) {
+__global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const BatchedArgs ba) {
   const WalkArgs& a = ba.w;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int N = ba.N;
@@ -293,37 +293,43 @@ __global__ void __maxnreg__(224) walk_batched_kernel(const BatchedArgs ba) {
           uint32_t dv[16];
           ptx::tmem_ld<16>(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * 256 + c0 + cb), dv);
           ptx::tmem_wait_ld();
-          // all 16 keys first (independent chains the compiler can interleave),
-          // then the warp reductions
-          unsigned long long key[16];
+          // 8 keys at a time first (independent chains the compiler can
+          // interleave), then their warp reductions
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int b = c0 + cb + j;
-            key[j] = 0ull;
-            if (cb + j < act && valid) {
-              const float bias = __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j])));
-              const uint16_t lb = float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(cur[j]), bias));
-              if (a.out_logits)
-                a.out_logits[((size_t)b * a.gamma + k) * (size_t)a.V + (size_t)v] = lb;
-              const float T_b = temp_s[b];
-              const float logit = bf16_bits_to_float(lb);
-              float sc = logit;
-              if (T_b > 0.0f) {
-                const uint4 r = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)k,
-                                                         (uint32_t)b, 0u),
-                                              a.seed_lo, a.seed_hi);
-                sc = gumbel_score(logit, T_b, philox_word(r, (uint32_t)v & 3u));
+          for (int j0 = 0; j0 < 16; j0 += 8) {
+            unsigned long long key[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const int j = j0 + jj;
+              const int b = c0 + cb + j;
+              key[jj] = 0ull;
+              if (cb + j < act && valid) {
+                const float bias = __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j])));
+                const uint16_t lb =
+                    float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(cur[j]), bias));
+                if (a.out_logits)
+                  a.out_logits[((size_t)b * a.gamma + k) * (size_t)a.V + (size_t)v] = lb;
+                const float T_b = temp_s[b];
+                const float logit = bf16_bits_to_float(lb);
+                float sc = logit;
+                if (T_b > 0.0f) {
+                  const uint4 r = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)k,
+                                                           (uint32_t)b, 0u),
+                                                a.seed_lo, a.seed_hi);
+                  sc = gumbel_score(logit, T_b, philox_word(r, (uint32_t)v & 3u));
+                }
+                key[jj] = make_key(sc, (uint32_t)v);
               }
-              key[j] = make_key(sc, (uint32_t)v);
             }
-          }
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (cb + j >= act) continue;             // uniform across the warp
-            const unsigned long long m = group_max_key(0xFFFFFFFFu, key[j]);
-            if (lane == 0) {
-              unsigned long long* p = &wbest[warp * 128 + (cb + j)];
-              *p = m > *p ? m : *p;
+            for (int jj = 0; jj < 8; ++jj) {
+              const int j = j0 + jj;
+              if (cb + j >= act) continue;           // uniform across the warp
+              const unsigned long long m = group_max_key(0xFFFFFFFFu, key[jj]);
+              if (lane == 0) {
+                unsigned long long* p = &wbest[warp * 128 + (cb + j)];
+                *p = m > *p ? m : *p;
+              }
             }
           }
         }
