@@ -11,15 +11,23 @@
 // shared memory; the ring keeps refilling across steps because W2 does not
 // depend on the token).
 //
-// CTA = 8 epilogue warps + 1 control warp.  The control warp's lane 0 keeps
+// CTA = 16 epilogue warps + 1 control warp.  The control warp's lane 0 keeps
 // NST half-tiles (32 KB: 128 rows x 128 K) of the CTA's W2 shard in flight
 // with cp.async.bulk, issues the 8 MMAs of each half-tile into one of two
 // TMEM accumulators (128 x N fp32 each), and commits them to mbarriers.  The
 // epilogue warps read a finished accumulator (warp w: lane quarter w % 4,
-// column half w / 4), apply the fused epilogue (two bf16 roundings, base add,
-// score), fold keys per request, and free the accumulator.  After the last
-// tile the CTA's best key per request goes through the atomic rendezvous and
-// the next u rows are gathered into U.
+// column quarter w / 4) 8 columns at a time, one row per lane; the bf16
+// biases go through a small per-warp shared-memory buffer that turns the
+// 32 x 8 block around, so that each lane then owns 8 consecutive tokens of ONE
+// request: its base logits are one 16-byte load, two logits are summed per
+// bf16x2 add, and one Philox call serves four of its tokens (the counter is
+// shared by tokens 4j .. 4j + 3).  Keys are folded per request and the
+// accumulator is freed.  After the last tile the CTA's best key per request
+// goes through the atomic rendezvous and the next u rows are gathered into U.
+//
+// Requests are laid out in MMA columns greedy-first (a stable partition by
+// temperature), so a 16-column chunk is, but for one, all greedy or all
+// sampled and the lanes of a warp rarely diverge on the noise.
 #include "tc_ptx.cuh"
 #include "walk_common.cuh"
 #include "walk_kernels.h"
@@ -28,11 +36,15 @@ namespace dspark {
 
 namespace {
 
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;                 // 4 per TMEM lane quarter
 constexpr int kBatThreads = (kEpiWarps + 1) * 32;
 constexpr int kStageBytes = 32768;            // half a tile: 128 rows x 128 K bf16
 constexpr int kBlockBytes = 4096;             // 128 rows x 16 K
 constexpr int kMaxStages = 6;
+constexpr int kCW = 8;                        // accumulator columns per epilogue chunk
+constexpr int kStgStride = 40;                // uint16 per column of the turn-around buffer
+constexpr int kStgWarpElems = kCW * kStgStride;
+constexpr int kWbCols = 64;                   // wbest slots per warp (N / 4 <= 64)
 
 struct BatchedArgs {
   WalkArgs w;
@@ -57,18 +69,11 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ptx::smem_u32(bar)) : "memory");
 }
 
-// Maximum of a 64-bit key over the lanes of `mask` with two redux.sync.
-__device__ __forceinline__ unsigned long long group_max_key(unsigned mask, unsigned long long key) {
-  const uint32_t hi = (uint32_t)(key >> 32);
-  const uint32_t mhi = __reduce_max_sync(mask, hi);
-  const uint32_t mlo = __reduce_max_sync(mask, hi == mhi ? (uint32_t)key : 0u);
-  return ((unsigned long long)mhi << 32) | mlo;
-}
-
-// u_b = W1[tok] into U (core matrix (kc, b / 8) at (kc * N/8 + b/8) * 128).
-// Eight rows' chunks in flight per thread before any store.
-__device__ __forceinline__ void gather_u(const WalkArgs& a, const int32_t* tok_s, uint8_t* U,
-                                         int N) {
+// Column c of U = W1[tok of request col2req[c]] (core matrix (kc, c / 8) at
+// (kc * N/8 + c/8) * 128).  Eight rows' chunks in flight per thread before any
+// store.
+__device__ __forceinline__ void gather_u(const WalkArgs& a, const int32_t* tok_s,
+                                         const int16_t* col2req, uint8_t* U, int N) {
   const int epi_threads = kEpiWarps * 32;
   const int total = a.B * 32;
   for (int i0 = threadIdx.x; i0 < total; i0 += 8 * epi_threads) {
@@ -77,7 +82,8 @@ __device__ __forceinline__ void gather_u(const WalkArgs& a, const int32_t* tok_s
     for (int u = 0; u < 8; ++u) {
       const int i = i0 + u * epi_threads;
       if (i < total)
-        x[u] = __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok_s[i >> 5] * kRank) +
+        x[u] = __ldg(reinterpret_cast<const uint4*>(a.W1 +
+                                                    (size_t)tok_s[col2req[i >> 5]] * kRank) +
                      (i & 31));
     }
 #pragma unroll
@@ -93,6 +99,122 @@ __device__ __forceinline__ void gather_u(const WalkArgs& a, const int32_t* tok_s
   ptx::fence_proxy_async_smem();
 }
 
+// Stable partition of the requests into MMA columns, greedy (T = 0) first:
+// col2req[c] = request of column c.  One warp.
+__device__ __forceinline__ void order_columns(int B, const float* temp_s, int16_t* col2req,
+                                              int lane) {
+  int ng = 0;
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    const int b = b0 + lane;
+    ng += __popc(__ballot_sync(0xFFFFFFFFu, b < B && !(temp_s[b] > 0.0f)));
+  }
+  int pg = 0, ps = ng;
+  const unsigned below = (1u << lane) - 1u;
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    const int b = b0 + lane;
+    const bool in = b < B;
+    const bool greedy = in && !(temp_s[b] > 0.0f);
+    const unsigned mg = __ballot_sync(0xFFFFFFFFu, greedy);
+    const unsigned ms = __ballot_sync(0xFFFFFFFFu, in && !greedy);
+    if (greedy) col2req[pg + __popc(mg & below)] = (int16_t)b;
+    else if (in) col2req[ps + __popc(ms & below)] = (int16_t)b;
+    pg += __popc(mg);
+    ps += __popc(ms);
+  }
+}
+
+// Base logits of tokens v0 .. v0 + 7 of request b (b < 0: none) at step k,
+// packed two per word; tokens at or past V read as 0.  `vec`: one 16-byte
+// load (V a multiple of 8, 16-byte aligned base).
+__device__ __forceinline__ void load_base8(const WalkArgs& a, int k, int b, int64_t v0, bool vec,
+                                           uint32_t (&w)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w[i] = 0u;
+  if (b < 0) return;
+  const uint16_t* src = a.base + ((size_t)b * a.gamma + k) * (size_t)a.V + v0;
+  if (vec && v0 + 8 <= a.V) {
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(src));
+    w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (v0 + i < a.V) w[i >> 1] |= (uint32_t)__ldg(src + i) << (16 * (i & 1));
+  }
+}
+
+// Two bf16 logits at once: bf16(base + bias), each rounded once to nearest even.
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t x, uint32_t y) {
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(x), "r"(y));
+  return d;
+}
+
+// Tokens v0 .. v0 + 7 of request b at step k: logit = bf16(base + bias) (the
+// bias already rounded to bf16), the optional copy to out_logits, the
+// selection score (the logit, or its Gumbel-max score with one Philox call per
+// four tokens) and the best key {order bits, inverted id}; ties keep the
+// smallest id.  Tokens at or past V do not take part.
+__device__ __forceinline__ unsigned long long score8(const WalkArgs& a, int k, int b, float T,
+                                                     float inv_T, int64_t v0, const uint4& bz,
+                                                     const uint32_t (&bw)[4], bool vec) {
+  const int64_t nvalid = a.V - v0;
+  if (nvalid <= 0) return 0ull;
+  uint32_t lw[4];
+  lw[0] = add_bf16x2(bw[0], bz.x);
+  lw[1] = add_bf16x2(bw[1], bz.y);
+  lw[2] = add_bf16x2(bw[2], bz.z);
+  lw[3] = add_bf16x2(bw[3], bz.w);
+  float lg[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    lg[i] = __uint_as_float((i & 1) ? (lw[i >> 1] & 0xFFFF0000u) : (lw[i >> 1] << 16));
+  if (a.out_logits != nullptr) {
+    uint16_t* dst = a.out_logits + ((size_t)b * a.gamma + k) * (size_t)a.V + v0;
+    if (vec && nvalid >= 8) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i < nvalid) dst[i] = (uint16_t)(lw[i >> 1] >> (16 * (i & 1)));
+    }
+  }
+  float sc[8];
+  if (T > 0.0f) {
+#pragma unroll
+    for (int c4 = 0; c4 < 2; ++c4) {
+      const uint4 r = philox4x32_10(
+          make_uint4((uint32_t)(v0 >> 2) + (uint32_t)c4, (uint32_t)k, (uint32_t)b, 0u), a.seed_lo,
+          a.seed_hi);
+      const uint32_t x[4] = {r.x, r.y, r.z, r.w};
+      if (inv_T != 0.0f) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sc[4 * c4 + e] = __fadd_rn(__fmul_rn(lg[4 * c4 + e], inv_T), gumbel_noise(x[e]));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sc[4 * c4 + e] = __fadd_rn(__fdiv_rn(lg[4 * c4 + e], T), gumbel_noise(x[e]));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sc[i] = lg[i];
+  }
+  float best = sc[0];
+  int best_i = 0;
+  if (nvalid >= 8) {
+#pragma unroll
+    for (int i = 1; i < 8; ++i)
+      if (sc[i] > best) { best = sc[i]; best_i = i; }
+  } else {
+#pragma unroll
+    for (int i = 1; i < 8; ++i)
+      if (i < nvalid && sc[i] > best) { best = sc[i]; best_i = i; }
+  }
+  return ((unsigned long long)ord32(best) << 32) |
+         (unsigned long long)(0xFFFFFFFFu - (uint32_t)(v0 + best_i));
+}
+
 __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const BatchedArgs ba) {
   const WalkArgs& a = ba.w;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -100,10 +222,14 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
   uint8_t* ring = smem;                                            // nst x 32 KB
   uint8_t* U = smem + (size_t)ba.nst * kStageBytes;                // N x 512 B
   unsigned long long* wbest = reinterpret_cast<unsigned long long*>(U + (size_t)N * 512);
-  // wbest: [8 warps][128] running best per (warp, request in the warp's half)
-  unsigned long long* cta_key = wbest + kEpiWarps * 128;           // [256]
-  int32_t* tok_s = reinterpret_cast<int32_t*>(cta_key + 256);      // [256]
-  float* temp_s = reinterpret_cast<float*>(tok_s + 256);           // [256]
+  // wbest: [16 warps][64] running best per (warp, column in the warp's quarter)
+  unsigned long long* cta_key = wbest + kEpiWarps * kWbCols;       // [256] per request
+  int32_t* tok_s = reinterpret_cast<int32_t*>(cta_key + 256);      // [256] per request
+  float* temp_s = reinterpret_cast<float*>(tok_s + 256);           // [256] per request
+  int16_t* col2req = reinterpret_cast<int16_t*>(temp_s + 256);     // [256] per column
+  float* tcol = reinterpret_cast<float*>(col2req + 256);           // [256] T per column
+  float* icol = tcol + 256;                                        // [256] fl(1/T) per column
+  uint16_t* stage = reinterpret_cast<uint16_t*>(icol + 256);       // [16 warps][8][40]
   __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t dfull[2], dempty[2];
   __shared__ uint32_t tmem_base_s;
@@ -115,6 +241,8 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
   const int64_t row0 = (int64_t)cta * ba.R;
   const int T = ba.T, nst = ba.nst;
   const uint8_t* gw = ba.W2b + (size_t)cta * T * 16 * kBlockBytes;
+  const bool vec = (a.V % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.base) & 15u) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(a.out_logits) & 15u) == 0);
 
   const int bad = check_inputs(a, &flag_s);
   if (bad != 0) {
@@ -155,7 +283,14 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   if (cta == 0) clear_other_parity(a.sync, round_s & 1u);
-  if (warp < kEpiWarps) gather_u(a, tok_s, U, N);
+  if (warp == 0) order_columns(a.B, temp_s, col2req, lane);
+  __syncthreads();
+  for (int c = threadIdx.x; c < 256; c += blockDim.x) {
+    const float Tc = c < a.B ? temp_s[col2req[c]] : 0.0f;
+    tcol[c] = Tc;
+    icol[c] = Tc > 0.0f ? inv_temperature(Tc) : 0.0f;
+  }
+  if (warp < kEpiWarps) gather_u(a, tok_s, col2req, U, N);
 
   // control state (lane 0 of the control warp)
   const int stages_total = 2 * T * a.gamma;   // half-tiles consumed this round
@@ -244,29 +379,27 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
       __syncwarp();
     } else {
       // ---------------------------------------------------- epilogue warps
-      // warp w: rows 32 (w % 4) .. +31 of every tile, columns (requests)
-      // [c0, c0 + cols).  Base logits come from HBM: the loads of the next
-      // 16-column chunk are issued before the current chunk is computed.
-      const int q = warp & 3, half = warp >> 2;
-      const int cols = N >> 1;
-      const int c0 = half * cols;
+      // warp w: rows 32 (w % 4) .. +31 of every tile (its TMEM lane quarter),
+      // columns [c0, c0 + N / 4) with c0 = (w / 4) N / 4, 8 at a time.  After
+      // the turn-around, lane (jl, hl) owns column c0 + cb + jl and rows
+      // 8 hl .. 8 hl + 7 of the warp's 32; its base logits for the next chunk
+      // are loaded before the current chunk is computed.
+      const int q = warp & 3, grp = warp >> 2;
+      const int cols = N >> 2;
+      const int c0 = grp * cols;
       int act = a.B - c0;                            // this warp's live columns
       act = act < 0 ? 0 : (act > cols ? cols : act);
-      const int cpt = (act + 15) >> 4;               // chunks per tile
+      const int cpt = (act + kCW - 1) / kCW;         // chunks per tile
       const int nc = cpt * T;
-      for (int i = lane; i < 128; i += 32) wbest[warp * 128 + i] = 0ull;
+      const int jl = lane & 7, hl = lane >> 3;
+      uint16_t* stg = stage + warp * kStgWarpElems;
+      for (int i = lane; i < kWbCols; i += 32) wbest[warp * kWbCols + i] = 0ull;
       __syncwarp();
-      uint32_t nxt[16];
+      uint32_t nxt[4];
       auto prefetch = [&](int ci) {
-        const int t = ci / cpt, cb = (ci - t * cpt) * 16;
-        const int64_t v = row0 + t * 128 + 32 * q + lane;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int b = c0 + cb + j;
-          nxt[j] = (cb + j < act && v < a.V)
-                       ? (uint32_t)__ldg(a.base + ((size_t)b * a.gamma + k) * (size_t)a.V + v)
-                       : 0u;
-        }
+        const int t = ci / cpt, cb = (ci - t * cpt) * kCW;
+        const int b = cb + jl < act ? (int)col2req[c0 + cb + jl] : -1;
+        load_base8(a, k, b, row0 + t * 128 + 32 * q + 8 * hl, vec, nxt);
       };
       if (nc > 0) prefetch(0);
       int ci = 0;
@@ -282,55 +415,36 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
         }
         ptx::tc_fence_after();
         if (t == 0) trace_stamp(a, k, 1);
-        const int64_t v = row0 + t * 128 + 32 * q + lane;
-        const bool valid = v < a.V;
+        const int64_t v0 = row0 + t * 128 + 32 * q + 8 * hl;
         for (int cc = 0; cc < cpt; ++cc, ++ci) {
-          const int cb = cc * 16;
-          uint32_t cur[16];
+          const int cb = cc * kCW;
+          uint32_t cur[4];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) cur[j] = nxt[j];
+          for (int j = 0; j < 4; ++j) cur[j] = nxt[j];
           if (ci + 1 < nc) prefetch(ci + 1);
-          uint32_t dv[16];
-          ptx::tmem_ld<16>(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * 256 + c0 + cb), dv);
+          uint32_t dv[kCW];
+          ptx::tmem_ld<kCW>(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * 256 + c0 + cb), dv);
           ptx::tmem_wait_ld();
-          // 8 keys at a time first (independent chains the compiler can
-          // interleave), then their warp reductions
+          // bf16 biases, one row per lane, then read back one column per lane
+          __syncwarp();
 #pragma unroll
-          for (int j0 = 0; j0 < 16; j0 += 8) {
-            unsigned long long key[8];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              const int j = j0 + jj;
-              const int b = c0 + cb + j;
-              key[jj] = 0ull;
-              if (cb + j < act && valid) {
-                const float bias = __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j])));
-                const uint16_t lb =
-                    float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(cur[j]), bias));
-                if (a.out_logits)
-                  a.out_logits[((size_t)b * a.gamma + k) * (size_t)a.V + (size_t)v] = lb;
-                const float T_b = temp_s[b];
-                const float logit = bf16_bits_to_float(lb);
-                float sc = logit;
-                if (T_b > 0.0f) {
-                  const uint4 r = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)k,
-                                                           (uint32_t)b, 0u),
-                                                a.seed_lo, a.seed_hi);
-                  sc = gumbel_score(logit, T_b, philox_word(r, (uint32_t)v & 3u));
-                }
-                key[jj] = make_key(sc, (uint32_t)v);
-              }
-            }
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              const int j = j0 + jj;
-              if (cb + j >= act) continue;           // uniform across the warp
-              const unsigned long long m = group_max_key(0xFFFFFFFFu, key[jj]);
-              if (lane == 0) {
-                unsigned long long* p = &wbest[warp * 128 + (cb + j)];
-                *p = m > *p ? m : *p;
-              }
-            }
+          for (int j = 0; j < kCW; ++j)
+            stg[j * kStgStride + lane] = float_to_bf16_bits_rn(__uint_as_float(dv[j]));
+          __syncwarp();
+          const uint4 bz = *reinterpret_cast<const uint4*>(stg + jl * kStgStride + 8 * hl);
+          unsigned long long best = 0ull;
+          const bool live = cb + jl < act;
+          if (live) {
+            const int c = c0 + cb + jl;
+            best = score8(a, k, (int)col2req[c], tcol[c], icol[c], v0, bz, cur, vec);
+          }
+          unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, 8);
+          best = o > best ? o : best;
+          o = __shfl_xor_sync(0xFFFFFFFFu, best, 16);
+          best = o > best ? o : best;
+          if (hl == 0 && live) {
+            unsigned long long* p = &wbest[warp * kWbCols + cb + jl];
+            *p = best > *p ? best : *p;
           }
         }
         ptx::tc_fence_before();
@@ -344,16 +458,16 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
     trace_stamp(a, k, 3);
     if (abort_s) { ok = false; break; }
 
-    // CTA best per request: max over the 4 lane quarters of its column half
-    for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
-      const int half = b / (N >> 1), j = b - half * (N >> 1);
+    // CTA best per request: max over the 4 lane quarters of its column
+    for (int c = threadIdx.x; c < a.B; c += blockDim.x) {
+      const int grp = c / (N >> 2), j = c - grp * (N >> 2);
       unsigned long long m = 0ull;
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) {
-        const unsigned long long x = wbest[(half * 4 + qq) * 128 + j];
+        const unsigned long long x = wbest[(grp * 4 + qq) * kWbCols + j];
         m = x > m ? x : m;
       }
-      cta_key[b] = m;
+      cta_key[col2req[c]] = m;
     }
     __syncthreads();
     trace_stamp(a, k, 4);
@@ -363,7 +477,7 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
     if (cta == 0)
       for (int b = threadIdx.x; b < a.B; b += blockDim.x)
         a.out_tokens[(size_t)b * a.gamma + k] = tok_s[b];
-    if (k + 1 < a.gamma && warp < kEpiWarps) gather_u(a, tok_s, U, N);
+    if (k + 1 < a.gamma && warp < kEpiWarps) gather_u(a, tok_s, col2req, U, N);
     ptx::tc_fence_before();
     __syncthreads();
     trace_stamp(a, k, 7);
@@ -414,8 +528,8 @@ __global__ void repack_batched_kernel(const uint32_t* __restrict__ W2w, uint32_t
 int batched_threads() { return kBatThreads; }
 
 size_t batched_smem_bytes(int nst, int N) {
-  return (size_t)nst * kStageBytes + (size_t)N * 512 + (size_t)kEpiWarps * 128 * 8 + 256 * 8 +
-         256 * 4 + 256 * 4;
+  return (size_t)nst * kStageBytes + (size_t)N * 512 + (size_t)kEpiWarps * kWbCols * 8 + 256 * 8 +
+         256 * 4 + 256 * 4 + 256 * 2 + 256 * 4 + 256 * 4 + (size_t)kEpiWarps * kStgWarpElems * 2;
 }
 
 int batched_max_stages() { return kMaxStages; }

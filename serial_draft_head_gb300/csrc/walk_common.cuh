@@ -195,12 +195,29 @@ __device__ __forceinline__ float bits_to_uniform(uint32_t x) {
   return (float)((x >> 9) * 2u + 1u) * 0x1p-24f;
 }
 
-// Gumbel-max score fp32(logit / T) + (-log(-log U)), each step in fp32.
-__device__ __forceinline__ float gumbel_score(float logit, float T, uint32_t x) {
+// Gumbel-max score of a logit at temperature T > 0: fp32(logit / T) + g with
+// g = -log(-log U), in fp32.  inv_T = fl(1/T) (0 when 1/T overflows): the
+// quotient is taken as the product with the rounded reciprocal, within one
+// fp32 ulp of the IEEE quotient.  The inner log is the accurate logf (it must
+// resolve U close to 1, where -log U is tiny and the winners are); the outer
+// one is the hardware approximation (absolute error below 2^-21 for arguments
+// in [0.5, 2], a few ulp elsewhere).  Both are far inside the 2^-18 (1 + |g|)
+// error the token comparison allows for the noise.
+__device__ __forceinline__ float gumbel_noise(uint32_t x) {
   const float U = bits_to_uniform(x);
   const float e = -logf(U);
-  const float g = -logf(e);
-  return __fadd_rn(__fdiv_rn(logit, T), g);
+  return -__logf(e);
+}
+
+__device__ __forceinline__ float gumbel_score(float logit, float T, float inv_T, uint32_t x) {
+  const float q = inv_T != 0.0f ? __fmul_rn(logit, inv_T) : __fdiv_rn(logit, T);
+  return __fadd_rn(q, gumbel_noise(x));
+}
+
+// fl(1/T) for T > 0, or 0 when it overflows (T below 2^-126).
+__device__ __forceinline__ float inv_temperature(float T) {
+  const float r = __frcp_rn(T);
+  return isinf(r) ? 0.0f : r;
 }
 
 // ------------------------------------------------------------- epilogue --
@@ -213,7 +230,7 @@ static __device__ __noinline__ float sampled_score(float logit, float T, uint32_
                                             uint32_t seed_hi, int b, int k, uint32_t v) {
   const uint4 r = philox4x32_10(make_uint4(v >> 2, (uint32_t)k, (uint32_t)b, 0u), seed_lo,
                                 seed_hi);
-  return gumbel_score(logit, T, philox_word(r, v & 3u));
+  return gumbel_score(logit, T, inv_temperature(T), philox_word(r, v & 3u));
 }
 
 // The fused epilogue of one (token v, request b, step k): fp32 accumulation

@@ -160,6 +160,7 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
   unsigned long long best = 0ull;
   if (b < a.B) {
     const float T = temp_s[b];
+    const float inv_T = T > 0.0f ? inv_temperature(T) : 0.0f;
     const uint16_t* ls = logit_s + (size_t)b * R;
     uint16_t* outl =
         a.out_logits ? a.out_logits + ((size_t)b * a.gamma + k) * (size_t)a.V : nullptr;
@@ -177,7 +178,7 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
         for (int e = 0; e < 4; ++e) {
           if (rl0 + e < nv) {
             const unsigned long long key =
-                make_key(gumbel_score(bf16_bits_to_float(lb[e]), T, x[e]), v0 + e);
+                make_key(gumbel_score(bf16_bits_to_float(lb[e]), T, inv_T, x[e]), v0 + e);
             best = key > best ? key : best;
             if (outl) outl[v0 + e] = (uint16_t)lb[e];
           }
