@@ -70,26 +70,25 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 // Column c of U = W1[tok of request col2req[c]] (core matrix (kc, c / 8) at
-// (kc * N/8 + c/8) * 128).  Eight rows' chunks in flight per thread before any
-// store.
+// (kc * N/8 + c/8) * 128); columns without a request keep their zeros.
+// Eight rows' chunks in flight per thread before any store.
 __device__ __forceinline__ void gather_u(const WalkArgs& a, const int32_t* tok_s,
                                          const int16_t* col2req, uint8_t* U, int N) {
   const int epi_threads = kEpiWarps * 32;
-  const int total = a.B * 32;
+  const int total = N * 32;
   for (int i0 = threadIdx.x; i0 < total; i0 += 8 * epi_threads) {
     uint4 x[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int i = i0 + u * epi_threads;
-      if (i < total)
-        x[u] = __ldg(reinterpret_cast<const uint4*>(a.W1 +
-                                                    (size_t)tok_s[col2req[i >> 5]] * kRank) +
-                     (i & 31));
+      const int r = i < total ? (int)col2req[i >> 5] : -1;
+      if (r >= 0)
+        x[u] = __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok_s[r] * kRank) + (i & 31));
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int i = i0 + u * epi_threads;
-      if (i < total) {
+      if (i < total && col2req[i >> 5] >= 0) {
         const int b = i >> 5, c = i & 31;
         *reinterpret_cast<uint4*>(U + ((size_t)c * (N >> 3) + (b >> 3)) * 128 + (b & 7) * 16) =
             x[u];
@@ -99,10 +98,38 @@ __device__ __forceinline__ void gather_u(const WalkArgs& a, const int32_t* tok_s
   ptx::fence_proxy_async_smem();
 }
 
-// Stable partition of the requests into MMA columns, greedy (T = 0) first:
-// col2req[c] = request of column c.  One warp.
-__device__ __forceinline__ void order_columns(int B, const float* temp_s, int16_t* col2req,
-                                              int lane) {
+// Width of the column slots: 8 (one epilogue chunk) when a column quarter
+// holds a multiple of 8 columns, else 4.
+__device__ __forceinline__ int slot_width(int N) { return ((N >> 2) & 7) == 0 ? 8 : 4; }
+
+// MMA column of the request with rank r (ranks: greedy requests first, each
+// kind in request order).  Ranks fill slots of slot_width columns taken
+// round-robin over the four column quarters (slot s: quarter s % 4, position
+// s / 4 in it), so every quarter -- and thus every epilogue warp -- gets an
+// even share of the sampled requests, while epilogue chunks stay of one kind
+// but for at most one.  Each quarter's live columns are a prefix of it.
+__device__ __forceinline__ int rank_column(int r, int N) {
+  const int W = slot_width(N);
+  const int s = r / W;
+  return (s & 3) * (N >> 2) + (s >> 2) * W + (r - s * W);
+}
+
+// Live columns of column quarter g (a prefix of its N / 4 columns).
+__device__ __forceinline__ int quarter_live(int g, int B, int N) {
+  const int W = slot_width(N);
+  int n = 0;
+  for (int p = 0; p < (N >> 2) / W; ++p) {
+    const int m = B - (p * 4 + g) * W;
+    n += m <= 0 ? 0 : (m > W ? W : m);
+  }
+  return n;
+}
+
+// col2req[c] = request of MMA column c (-1: none).  One warp.
+__device__ __forceinline__ void order_columns(int B, int N, const float* temp_s,
+                                              int16_t* col2req, int lane) {
+  for (int c = lane; c < 256; c += 32) col2req[c] = -1;
+  __syncwarp();
   int ng = 0;
   for (int b0 = 0; b0 < B; b0 += 32) {
     const int b = b0 + lane;
@@ -116,11 +143,12 @@ __device__ __forceinline__ void order_columns(int B, const float* temp_s, int16_
     const bool greedy = in && !(temp_s[b] > 0.0f);
     const unsigned mg = __ballot_sync(0xFFFFFFFFu, greedy);
     const unsigned ms = __ballot_sync(0xFFFFFFFFu, in && !greedy);
-    if (greedy) col2req[pg + __popc(mg & below)] = (int16_t)b;
-    else if (in) col2req[ps + __popc(ms & below)] = (int16_t)b;
+    if (greedy) col2req[rank_column(pg + __popc(mg & below), N)] = (int16_t)b;
+    else if (in) col2req[rank_column(ps + __popc(ms & below), N)] = (int16_t)b;
     pg += __popc(mg);
     ps += __popc(ms);
   }
+  __syncwarp();
 }
 
 // Base logits of tokens v0 .. v0 + 7 of request b (b < 0: none) at step k,
@@ -151,12 +179,16 @@ __device__ __forceinline__ uint32_t add_bf16x2(uint32_t x, uint32_t y) {
 
 // Tokens v0 .. v0 + 7 of request b at step k: logit = bf16(base + bias) (the
 // bias already rounded to bf16), the optional copy to out_logits, the
-// selection score (the logit, or its Gumbel-max score with one Philox call per
-// four tokens) and the best key {order bits, inverted id}; ties keep the
-// smallest id.  Tokens at or past V do not take part.
-__device__ __forceinline__ unsigned long long score8(const WalkArgs& a, int k, int b, float T,
-                                                     float inv_T, int64_t v0, const uint4& bz,
-                                                     const uint32_t (&bw)[4], bool vec) {
+// selection score and the best key {order bits, inverted id}; ties keep the
+// smallest id.  Tokens at or past V do not take part.  `kind` is the same for
+// the whole warp: 0 = every live lane greedy (score = logit); 1 = noise drawn
+// for every lane (one Philox call per four tokens) and used where T > 0;
+// 2 = as 1, with the IEEE quotient where 1/T overflows.
+__device__ __forceinline__ unsigned long long score8(const WalkArgs& a, const PhiloxKeys& pk,
+                                                     int k, int b, float T, float inv_T,
+                                                     int64_t v0, const uint4& bz,
+                                                     const uint32_t (&bw)[4], bool vec,
+                                                     int kind) {
   const int64_t nvalid = a.V - v0;
   if (nvalid <= 0) return 0ull;
   uint32_t lw[4];
@@ -179,26 +211,24 @@ __device__ __forceinline__ unsigned long long score8(const WalkArgs& a, int k, i
     }
   }
   float sc[8];
-  if (T > 0.0f) {
+  if (kind == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sc[i] = lg[i];
+  } else {
+    const bool sampled = T > 0.0f;
 #pragma unroll
     for (int c4 = 0; c4 < 2; ++c4) {
       const uint4 r = philox4x32_10(
-          make_uint4((uint32_t)(v0 >> 2) + (uint32_t)c4, (uint32_t)k, (uint32_t)b, 0u), a.seed_lo,
-          a.seed_hi);
+          make_uint4((uint32_t)(v0 >> 2) + (uint32_t)c4, (uint32_t)k, (uint32_t)b, 0u), pk);
       const uint32_t x[4] = {r.x, r.y, r.z, r.w};
-      if (inv_T != 0.0f) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sc[4 * c4 + e] = __fadd_rn(__fmul_rn(lg[4 * c4 + e], inv_T), gumbel_noise(x[e]));
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sc[4 * c4 + e] = __fadd_rn(__fdiv_rn(lg[4 * c4 + e], T), gumbel_noise(x[e]));
+      for (int e = 0; e < 4; ++e) {
+        const float l = lg[4 * c4 + e];
+        float q = __fmul_rn(l, inv_T);
+        if (kind == 2 && inv_T == 0.0f) q = __fdiv_rn(l, T);
+        sc[4 * c4 + e] = sampled ? __fadd_rn(q, gumbel_noise(x[e])) : l;
       }
     }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sc[i] = lg[i];
   }
   float best = sc[0];
   int best_i = 0;
@@ -283,10 +313,10 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   if (cta == 0) clear_other_parity(a.sync, round_s & 1u);
-  if (warp == 0) order_columns(a.B, temp_s, col2req, lane);
+  if (warp == 0) order_columns(a.B, N, temp_s, col2req, lane);
   __syncthreads();
   for (int c = threadIdx.x; c < 256; c += blockDim.x) {
-    const float Tc = c < a.B ? temp_s[col2req[c]] : 0.0f;
+    const float Tc = col2req[c] >= 0 ? temp_s[col2req[c]] : 0.0f;
     tcol[c] = Tc;
     icol[c] = Tc > 0.0f ? inv_temperature(Tc) : 0.0f;
   }
@@ -387,21 +417,23 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
       const int q = warp & 3, grp = warp >> 2;
       const int cols = N >> 2;
       const int c0 = grp * cols;
-      int act = a.B - c0;                            // this warp's live columns
-      act = act < 0 ? 0 : (act > cols ? cols : act);
+      const int act = quarter_live(grp, a.B, N);     // this warp's live columns
       const int cpt = (act + kCW - 1) / kCW;         // chunks per tile
       const int nc = cpt * T;
       const int jl = lane & 7, hl = lane >> 3;
       uint16_t* stg = stage + warp * kStgWarpElems;
       for (int i = lane; i < kWbCols; i += 32) wbest[warp * kWbCols + i] = 0ull;
       __syncwarp();
+      const PhiloxKeys pk = philox_keys(a.seed_lo, a.seed_hi);
       uint32_t nxt[4];
-      auto prefetch = [&](int ci) {
-        const int t = ci / cpt, cb = (ci - t * cpt) * kCW;
-        const int b = cb + jl < act ? (int)col2req[c0 + cb + jl] : -1;
-        load_base8(a, k, b, row0 + t * 128 + 32 * q + 8 * hl, vec, nxt);
+      int pt = 0, pcb = 0;                           // tile and column of the next prefetch
+      auto prefetch = [&]() {
+        const int b = pcb + jl < act ? (int)col2req[c0 + pcb + jl] : -1;
+        load_base8(a, k, b, row0 + pt * 128 + 32 * q + 8 * hl, vec, nxt);
+        pcb += kCW;
+        if (pcb >= cpt * kCW) { pcb = 0; ++pt; }
       };
-      if (nc > 0) prefetch(0);
+      if (nc > 0) prefetch();
       int ci = 0;
       for (int t = 0; t < T; ++t) {
         const int Gt = G + t;
@@ -415,13 +447,23 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
         }
         ptx::tc_fence_after();
         if (t == 0) trace_stamp(a, k, 1);
+        // the next tile's base rows (or step k + 1's first tile) into L2: 64
+        // bytes per request, one prefetch per live column
+        {
+          const int tn = t + 1 < T ? t + 1 : 0;
+          const int kn = t + 1 < T ? k : k + 1;
+          const int64_t rs = row0 + tn * 128 + 32 * q;
+          if (kn < a.gamma && rs < a.V)
+            for (int j = lane; j < act; j += 32)
+              ptx::prefetch_l2(a.base + ((size_t)col2req[c0 + j] * a.gamma + kn) * (size_t)a.V + rs);
+        }
         const int64_t v0 = row0 + t * 128 + 32 * q + 8 * hl;
         for (int cc = 0; cc < cpt; ++cc, ++ci) {
           const int cb = cc * kCW;
           uint32_t cur[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) cur[j] = nxt[j];
-          if (ci + 1 < nc) prefetch(ci + 1);
+          if (ci + 1 < nc) prefetch();
           uint32_t dv[kCW];
           ptx::tmem_ld<kCW>(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * 256 + c0 + cb), dv);
           ptx::tmem_wait_ld();
@@ -434,10 +476,12 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
           const uint4 bz = *reinterpret_cast<const uint4*>(stg + jl * kStgStride + 8 * hl);
           unsigned long long best = 0ull;
           const bool live = cb + jl < act;
-          if (live) {
-            const int c = c0 + cb + jl;
-            best = score8(a, k, (int)col2req[c], tcol[c], icol[c], v0, bz, cur, vec);
-          }
+          const int c = c0 + cb + jl;
+          const float Tc = live ? tcol[c] : 0.0f, iTc = live ? icol[c] : 1.0f;
+          const int kind = __any_sync(0xFFFFFFFFu, Tc > 0.0f)
+                               ? (__any_sync(0xFFFFFFFFu, Tc > 0.0f && iTc == 0.0f) ? 2 : 1)
+                               : 0;
+          if (live) best = score8(a, pk, k, (int)col2req[c], Tc, iTc, v0, bz, cur, vec, kind);
           unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, 8);
           best = o > best ? o : best;
           o = __shfl_xor_sync(0xFFFFFFFFu, best, 16);
@@ -459,7 +503,8 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
     if (abort_s) { ok = false; break; }
 
     // CTA best per request: max over the 4 lane quarters of its column
-    for (int c = threadIdx.x; c < a.B; c += blockDim.x) {
+    for (int c = threadIdx.x; c < N; c += blockDim.x) {
+      if (col2req[c] < 0) continue;
       const int grp = c / (N >> 2), j = c - grp * (N >> 2);
       unsigned long long m = 0ull;
 #pragma unroll

@@ -172,17 +172,36 @@ __device__ __forceinline__ int32_t key_token(unsigned long long key) {
 // ---------------------------------------------------------------- Philox --
 
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
-// 32x32->64 multiplies, the key bumped by the Weyl constants between rounds.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// 32x32->64 multiplies; round i uses the key bumped i times by the Weyl
+// constants.  The round keys depend on the seed alone, so a thread that draws
+// many blocks computes them once.
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ PhiloxKeys philox_keys(uint32_t k0, uint32_t k1) {
+  PhiloxKeys p;
 #pragma unroll
   for (int i = 0; i < 10; ++i) {
-    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
+    p.k0[i] = k0 + (uint32_t)i * 0x9E3779B9u;
+    p.k1[i] = k1 + (uint32_t)i * 0xBB67AE85u;
+  }
+  return p;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& key) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ key.k0[i], (uint32_t)p1,
+                   (uint32_t)(p0 >> 32) ^ c.w ^ key.k1[i], (uint32_t)p0);
   }
   return c;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+  return philox4x32_10(c, philox_keys(k0, k1));
 }
 
 __device__ __forceinline__ uint32_t philox_word(uint4 r, uint32_t w) {
@@ -192,23 +211,48 @@ __device__ __forceinline__ uint32_t philox_word(uint4 r, uint32_t w) {
 // Random bits -> fp32 uniform: the midpoint of bin (x >> 9) of 2^23 bins,
 // exact in fp32 and strictly inside (0, 1).
 __device__ __forceinline__ float bits_to_uniform(uint32_t x) {
-  return (float)((x >> 9) * 2u + 1u) * 0x1p-24f;
+  return (float)((x >> 8) | 1u) * 0x1p-24f;
 }
 
-// Gumbel-max score of a logit at temperature T > 0: fp32(logit / T) + g with
-// g = -log(-log U), in fp32.  inv_T = fl(1/T) (0 when 1/T overflows): the
-// quotient is taken as the product with the rounded reciprocal, within one
-// fp32 ulp of the IEEE quotient.  The inner log is the accurate logf (it must
-// resolve U close to 1, where -log U is tiny and the winners are); the outer
-// one is the hardware approximation (absolute error below 2^-21 for arguments
-// in [0.5, 2], a few ulp elsewhere).  Both are far inside the 2^-18 (1 + |g|)
+// log2 by the hardware approximation, subnormal inputs flushed (the noise
+// never feeds it one: U >= 2^-24 and -log U >= 2^-24).
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// -log U for the uniform of bits x.  For U <= 15/16 the hardware log2
+// approximation times ln 2: its absolute error (about 2^-22 in log2 near 1,
+// relative elsewhere) is then below 2^-18 of -log U >= 0.0645.  For U > 15/16,
+// t = 1 - U is exact and -log(1 - t) = t + t^2/2 + ... + t^6/6 (the Mercator
+// series, remainder below t^7 / 7 < 2^-28 t), so the tokens whose U is close
+// to 1 -- the large-noise ones that tend to win -- keep full precision.
+__device__ __forceinline__ float neg_log_uniform(uint32_t x) {
+  const float U = bits_to_uniform(x);
+  const float t = 1.0f - U;
+  float p = fmaf(t, 1.0f / 6.0f, 0.2f);
+  p = fmaf(t, p, 0.25f);
+  p = fmaf(t, p, 1.0f / 3.0f);
+  p = fmaf(t, p, 0.5f);
+  p = fmaf(t, p, 1.0f);
+  const float series = t * p;
+  const float hw = -0.693147180559945f * lg2_approx(U);
+  return t < 0.0625f ? series : hw;
+}
+
+// Gumbel noise g = -log(-log U): the inner log as above, the outer one the
+// hardware approximation (absolute error below 2^-21 for arguments in
+// [0.5, 2], a few ulp elsewhere).  Both stay far inside the 2^-18 (1 + |g|)
 // error the token comparison allows for the noise.
 __device__ __forceinline__ float gumbel_noise(uint32_t x) {
-  const float U = bits_to_uniform(x);
-  const float e = -logf(U);
-  return -__logf(e);
+  return -0.693147180559945f * lg2_approx(neg_log_uniform(x));
 }
 
+// Gumbel-max score of a logit at temperature T > 0: fp32(logit / T) + g, in
+// fp32.  inv_T = fl(1/T) (0 when 1/T overflows): the quotient is taken as the
+// product with the rounded reciprocal, within one fp32 ulp of the IEEE
+// quotient.
 __device__ __forceinline__ float gumbel_score(float logit, float T, float inv_T, uint32_t x) {
   const float q = inv_T != 0.0f ? __fmul_rn(logit, inv_T) : __fdiv_rn(logit, T);
   return __fadd_rn(q, gumbel_noise(x));
