@@ -28,7 +28,7 @@ struct dspark_walk {
   uint32_t* W2p = nullptr;        // tiered repack, res_wpc words per CTA
   int res_max_B = 0;              // 0: no resident layout
   bool use_resident = true;       // dspark_walk_set_kernel
-  int res_RS = 0, res_NT = 0, res_R = 0, res_S = 0, res_n_cta = 0;
+  int res_RS = 0, res_NT = 0, res_R = 0, res_S = 0, res_ST = 0, res_nslot = 0, res_n_cta = 0;
   int64_t res_wpc = 0;
   size_t res_smem = 0;
   dspark_walk_plan plan{};
@@ -82,9 +82,12 @@ void plan_batched(dspark_walk* h) {
 
 // Resident plan: every CTA holds 3 tensor-memory tiles (384 rows), 2
 // register strips per warp (256 rows) and S <= 24 shared-memory strips; rows
-// are spread evenly over at most one CTA per SM (R a multiple of 16).
-// Returns false when the shard does not fit on chip (or B, V are too large),
-// in which case every run uses the streamed kernel.
+// are spread evenly over at most one CTA per SM (R a multiple of 16).  When
+// the shard does not fit, the rows left over are streamed: ST strips per CTA
+// go through a two-slot ring of 64 KB bulk copies every step (the slots that
+// ring needs come out of the shared-memory tier), as in "V = 248,320: 62% on
+// chip, the rest streamed".  Returns false when B or V are too large, in which
+// case every run uses the batched or streamed kernel.
 bool plan_resident(dspark_walk* h) {
   const int mb = h->max_B < 16 ? h->max_B : 16;
   if (h->V >= (1 << 18)) return false;          // the 18-bit id field of the slot word
@@ -94,18 +97,29 @@ bool plan_resident(dspark_walk* h) {
   int64_t R = (h->V + h->sm_count - 1) / h->sm_count;
   R = (R + 15) / 16 * 16;
   if (R < fixed) R = fixed;
-  const int S = (int)((R - fixed) / 16);
-  if (S > resident_max_smem_strips()) return false;
-  const size_t smem = resident_smem_bytes(S, mb, (int)R);
-  if (smem > kSmemBudget) return false;
+  const int S_all = (int)((R - fixed) / 16);
+  int S = S_all, ST = 0, nslot = 0;
+  if (S > resident_max_smem_strips() || resident_smem_bytes(S, 0, 0, mb, (int)R) > kSmemBudget) {
+    // as many ring slots as fit (more bytes in flight), then shared strips
+    for (nslot = resident_max_ring_slots(); nslot >= 2; --nslot)
+      if (resident_smem_bytes(0, 1, nslot, mb, (int)R) <= kSmemBudget) break;
+    if (nslot < 2) return false;
+    const size_t other = resident_smem_bytes(0, 1, nslot, mb, (int)R);
+    S = (int)((kSmemBudget - other) / 8192);
+    if (S > resident_max_smem_strips()) S = resident_max_smem_strips();
+    if (S > S_all) S = S_all;
+    ST = S_all - S;
+  }
   h->res_max_B = mb;
   h->res_RS = RS;
   h->res_NT = NT;
   h->res_R = (int)R;
   h->res_S = S;
+  h->res_ST = ST;
+  h->res_nslot = nslot;
   h->res_n_cta = (int)((h->V + R - 1) / R);
-  h->res_wpc = resident_words_per_cta(RS, S);
-  h->res_smem = smem;
+  h->res_wpc = resident_words_per_cta(RS, S + ST);
+  h->res_smem = resident_smem_bytes(S, ST, nslot, mb, (int)R);
   return true;
 }
 
@@ -142,9 +156,10 @@ void plan_stream(dspark_walk* h) {
     p.rows_tmem = 384;
     p.rows_rf = 128 * h->res_RS;
     p.rows_smem = 16 * h->res_S;
-    p.rows_stream = 0;
-    p.resident_bytes = h->V * (int64_t)h->r * 2;
-    p.streamed_bytes = 0;
+    p.rows_stream = 16 * h->res_ST;
+    p.streamed_bytes = (int64_t)16 * h->res_ST * h->res_n_cta * h->r * 2;
+    p.resident_bytes = h->V * (int64_t)h->r * 2 - p.streamed_bytes;
+    if (p.resident_bytes < 0) p.resident_bytes = 0;
     p.kernel = DSPARK_KERNEL_RESIDENT;
   }
 }
@@ -189,6 +204,8 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
     ra.W2p = h->W2p;
     ra.R = h->res_R;
     ra.S = h->res_S;
+    ra.ST = h->res_ST;
+    ra.nslot = h->res_nslot;
     ra.words_per_cta = h->res_wpc;
     const uintptr_t bp = reinterpret_cast<uintptr_t>(base);
     ra.base_mode = (h->V % 8 == 0 && (bp & 15u) == 0) ? 16
@@ -252,7 +269,7 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
   if (e == cudaSuccess && resident)
     e = cudaMalloc(&h->W2p, (size_t)h->res_wpc * h->res_n_cta * sizeof(uint32_t));
   if (e == cudaSuccess && resident)
-    e = resident_repack(W2, h->W2p, V, h->res_R, h->res_RS, h->res_S, h->res_n_cta, 0);
+    e = resident_repack(W2, h->W2p, V, h->res_R, h->res_RS, h->res_S + h->res_ST, h->res_n_cta, 0);
   plan_batched(h);
   if (e == cudaSuccess) e = cudaMalloc(&h->W2b, (size_t)h->bat_R * h->bat_n_cta * 512);
   if (e == cudaSuccess) e = batched_repack(W2, h->W2b, V, h->bat_R, h->bat_n_cta, 0);

@@ -368,6 +368,8 @@ struct ResidentArgs {
   const uint32_t* W2p;            // repacked W2, words_per_cta words per CTA
   int R;                          // rows per CTA (multiple of 16)
   int S;                          // shared-memory strips per CTA
+  int ST;                         // strips streamed every step (0: fully resident)
+  int nslot;                      // ring slots (64 KB each) of the streamed strips
   int64_t words_per_cta;
   int base_mode;                  // 16, 4 or 2: bytes per base-prefetch copy
 };

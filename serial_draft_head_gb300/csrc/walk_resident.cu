@@ -15,6 +15,13 @@
 //                             mma.sync A fragments;
 //   rows [384 + 128 RS, R)    shared memory, 16-row strips read by ldmatrix
 //                             and mma.sync.
+//   rows [.., R)              when the shard does not fit on chip ("V = 248,320:
+//                             62% on chip, the rest streamed"): ST strips in
+//                             the shared-strip layout, streamed every step
+//                             through a ring of two or three 64 KB slots (8
+//                             strips each) by bulk copies; the ring keeps
+//                             refilling across steps since W2 does not depend
+//                             on the token.  Warp w reads strip w of a slot.
 // U (the gathered W1 rows, one per request) sits in shared memory in the
 // no-swizzle K-major core-matrix layout that both the tcgen05 descriptor and
 // the mma.sync B fragments read.
@@ -45,6 +52,10 @@ constexpr int kNMma = 16;                      // tcgen05 N (requests per MMA)
 constexpr int kTmemWords = kTmemTiles * 128 * 128;
 constexpr int kRfStripWords = kResWarps * 16 * 32 * 4;  // one strip per warp, all warps
 constexpr int kSmemStripBytes = 16 * 512;
+constexpr int kChunkStrips = 8;                // streamed strips per ring slot
+constexpr int kChunkBytes = kChunkStrips * kSmemStripBytes;
+constexpr int kMaxRingSlots = 3;
+constexpr int kMbarRing = kMbarTma + 1;        // first of the ring slots' mbarriers
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, kNMma);
 
 __device__ __forceinline__ unsigned long long key_max(unsigned long long a, unsigned long long b) {
@@ -232,9 +243,13 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
   const WalkArgs& a = ra.w;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* smem_w2 = smem;
-  uint8_t* U = smem + (size_t)ra.S * kSmemStripBytes;
+  uint8_t* ring = smem + (size_t)ra.S * kSmemStripBytes;
+  const int nslot = ra.ST > 0 ? ra.nslot : 0;    // ring slots of kChunkBytes
+  uint8_t* U = ring + (size_t)nslot * kChunkBytes;
   uint16_t* base_s = reinterpret_cast<uint16_t*>(U + 16 * 512);
-  __shared__ __align__(8) uint64_t mbar[kIssuers + 1];
+  __shared__ __align__(8) uint64_t mbar[kMbarRing + kMaxRingSlots];
+  __shared__ int slot_done[kMaxRingSlots];
+  __shared__ int ring_issued, ring_consumed;
   __shared__ unsigned long long group_best[16][kResWarps];
   __shared__ float temp_s[16];
   __shared__ int32_t tok_s[16];
@@ -265,7 +280,9 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
   if (threadIdx.x == 0) {
     round_s = *reinterpret_cast<volatile uint32_t*>(&a.sync.hdr->round);
     abort_s = 0;
-    for (int i = 0; i <= kIssuers; ++i) ptx::mbar_init(&mbar[i], 1);
+    for (int i = 0; i < kMbarRing + kMaxRingSlots; ++i) ptx::mbar_init(&mbar[i], 1);
+    for (int i = 0; i < kMaxRingSlots; ++i) slot_done[i] = 0;
+    ring_issued = ring_consumed = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
@@ -296,6 +313,25 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
       const uint32_t n = bytes - off < 32768u ? bytes - off : 32768u;
       ptx::bulk_g2s(smem_w2 + off, src + off, n, &mbar[kMbarTma]);
     }
+  }
+
+  // streamed tier: the first two chunks of step 0 into the ring
+  const uint8_t* gstream = reinterpret_cast<const uint8_t*>(gw + kTmemWords + RS * kRfStripWords) +
+                           (size_t)ra.S * kSmemStripBytes;
+  const int n_chunks = (ra.ST + kChunkStrips - 1) / kChunkStrips;   // per step
+  auto issue_chunk = [&](int gi) {    // chunk gi of the round (step gi / n_chunks), slot gi % nslot
+    const int c = gi % n_chunks;
+    const int ns = ra.ST - c * kChunkStrips < kChunkStrips ? ra.ST - c * kChunkStrips : kChunkStrips;
+    const uint32_t bytes = (uint32_t)ns * kSmemStripBytes;
+    uint64_t* bar = &mbar[kMbarRing + gi % nslot];
+    ptx::mbar_expect_tx(bar, bytes);
+    ptx::bulk_g2s(ring + (size_t)(gi % nslot) * kChunkBytes, gstream + (size_t)c * kChunkBytes,
+                  bytes, bar);
+  };
+  if (threadIdx.x == 0 && ra.ST > 0) {
+    const int pre = a.gamma * n_chunks < nslot ? a.gamma * n_chunks : nslot;
+    for (int gi = 0; gi < pre; ++gi) issue_chunk(gi);
+    ring_issued = pre;
   }
 
   // tensor-memory tier: global -> registers -> tcgen05.st (warp w writes lane
@@ -381,6 +417,67 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     }
     __syncwarp();
 
+    // streamed strips: chunk after chunk through the ring; the last warp done
+    // with a slot refills it with the chunk nslot ahead (the next step's first
+    // chunks load while this step finishes).  The chunks already in the ring
+    // go first, so that their refills overlap the register/shared strips.
+    const uint32_t ring_addr = ptx::smem_u32(ring);
+    auto consume_chunk = [&](int c) -> bool {
+      const int gc = k * n_chunks + c, slot = gc % nslot;
+      if (!wait_mbar(&mbar[kMbarRing + slot], (uint32_t)((gc / nslot) & 1), t_step, a.timeout_ns)) {
+        if (lane == 0) {
+          abort_round(a.sync.hdr, round_s, kStatusTimeout);
+          abort_s = 1;
+        }
+        return false;
+      }
+      const int ns = ra.ST - c * kChunkStrips;
+      if (warp < ns) {
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+        const uint32_t blk = ring_addr + (uint32_t)slot * kChunkBytes +
+                             (uint32_t)warp * kSmemStripBytes + (lane >> 3) * 128 + (lane & 7) * 16;
+#pragma unroll
+        for (int kt = 0; kt < 16; ++kt) {
+          uint32_t f0, f1, f2, f3;
+          ptx::ldmatrix_x4(blk + kt * 512, f0, f1, f2, f3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            uint32_t b0 = 0u, b1 = 0u;
+            if (8 * nt + g < a.B) {
+              b0 = *reinterpret_cast<const uint32_t*>(U + (4 * kt + nt) * 128 + lane * 4);
+              b1 = *reinterpret_cast<const uint32_t*>(U + (4 * kt + 2 + nt) * 128 + lane * 4);
+            }
+            ptx::mma_16816(acc[nt], f0, f1, f2, f3, b0, b1);
+          }
+        }
+        logits_strip<NT>(acc, base_s, ra.R, a.B,
+                         kTmemRows + 128 * RS + 16 * (ra.S + c * kChunkStrips + warp), lane);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        // this warp's reads of the slot are done: order them before the refill
+        ptx::fence_proxy_async_smem();
+        __threadfence_block();
+        if (atomicAdd(&slot_done[slot], 1) == kResWarps - 1) {
+          __threadfence_block();
+          slot_done[slot] = 0;
+          ring_consumed = gc + 1;
+          if (gc + nslot < a.gamma * n_chunks) {
+            issue_chunk(gc + nslot);
+            ring_issued = gc + nslot + 1;
+          }
+        }
+      }
+      return true;
+    };
+    const int c_first = n_chunks < nslot ? n_chunks : nslot;
+    bool ring_ok = true;
+    for (int c = 0; c < c_first && ring_ok; ++c) ring_ok = consume_chunk(c);
+
     // (2) register strips and this warp's shared-memory strips (s2 = warp,
     // warp + 8, warp + 16) in ONE k loop: up to RS + SMAX independent mma.sync
     // accumulation chains per warp hide the HMMA latency
@@ -430,6 +527,8 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
           logits_strip<NT>(acc[RS + j], base_s, ra.R, a.B,
                            kTmemRows + 128 * RS + (warp + j * kResWarps) * 16, lane);
     }
+
+    for (int c = c_first; c < n_chunks && ring_ok; ++c) ring_ok = consume_chunk(c);
 
     trace_stamp(a, k, 2);
 
@@ -562,6 +661,14 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
   // -------------------------------------------------------------- exit ----
   ptx::tc_fence_before();
   __syncthreads();
+  // a walk that stopped early may leave ring copies in flight: let them land
+  // before the CTA's shared memory goes away
+  if (threadIdx.x == 0 && ra.ST > 0) {
+    const uint64_t t0 = globaltimer_ns();
+    for (int gi = ring_consumed; gi < ring_issued; ++gi)
+      (void)wait_mbar(&mbar[kMbarRing + gi % nslot], (uint32_t)((gi / nslot) & 1), t0,
+                      a.timeout_ns);
+  }
   if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
   if (cta == 0) {
     if (!ok)
@@ -615,8 +722,11 @@ int resident_fixed_rows(int RS) { return kTmemRows + 128 * RS; }
 
 int resident_threads() { return kResThreads; }
 
-size_t resident_smem_bytes(int S, int max_B, int R) {
-  return (size_t)S * kSmemStripBytes + 16 * 512 + (((size_t)max_B * R * 2 + 15) & ~(size_t)15);
+int resident_max_ring_slots() { return kMaxRingSlots; }
+
+size_t resident_smem_bytes(int S, int ST, int nslot, int max_B, int R) {
+  return (size_t)S * kSmemStripBytes + (ST > 0 ? (size_t)nslot * kChunkBytes : 0) +
+         16 * 512 + (((size_t)max_B * R * 2 + 15) & ~(size_t)15);
 }
 
 const void* resident_kernel_for(int RS, int NT) {

@@ -74,6 +74,26 @@ def test_small_every_logit(walkmod, V, gamma, B, temps, seed, kernel):
     w.close()
 
 
+@pytest.mark.parametrize("V,max_B,B,temps", [
+    (160000, 16, 16, (0.0, 1.0, 0.6)),   # 2 ring slots; chunks of 8, 8 and 3 strips
+    (160000, 16, 3, (0.6, 0.0)),
+    (200000, 1, 1, (0.6,)),              # 3 ring slots; 6 chunks, the last of 1 strip
+])
+def test_streamed_tier_every_logit(walkmod, V, max_B, B, temps):
+    """Shards larger than the chip: the rows the chip cannot hold are streamed
+    through the ring every step; every logit and token of every request
+    checked."""
+    x = synth.make_custom(V=V, gamma=3, B=B, seed=21, temperatures=temps, noise_seed=1021)
+    w = walkmod.Walk(x.W1.cuda(), x.W2.cuda(), max_B, x.gamma)
+    plan = w.plan()
+    assert plan["kernel"] == walkmod.KERNEL_RESIDENT and plan["rows_stream"] > 0, plan
+    st, toks, lg = gpu_run(w, x)
+    assert st == 0, walkmod.dspark_walk_strerror(st)
+    rep = parity.check(x, toks, lg)
+    assert rep.ok(), rep
+    w.close()
+
+
 def test_tiny_config(walkmod):
     x = synth.make_inputs("tiny")
     w = make_walk(walkmod, x)
@@ -146,6 +166,8 @@ def test_long_block(walkmod, B):
 def test_partial(walkmod, B):
     x = full_inputs("partial", B)
     w = full_walk(walkmod, "partial", x)
+    plan = w.plan()
+    assert plan["kernel"] == walkmod.KERNEL_RESIDENT and plan["rows_stream"] > 0
     st, toks, lg = gpu_run(w, x)
     assert st == 0
     rep = parity.check(x, toks, lg, requests=_sample_requests(B, (0.0,)))
