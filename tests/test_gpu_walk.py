@@ -94,6 +94,30 @@ def test_streamed_tier_every_logit(walkmod, V, max_B, B, temps):
     w.close()
 
 
+GREEDY_TOKENS_ONLY = [
+    # V, gamma, B, seed: all greedy and no logits requested, so the resident
+    # kernel takes its keys straight from the epilogues (no key pass)
+    (12, 3, 1, 31),
+    (5003, 7, 8, 32),
+    (152 * 33 + 17, 4, 16, 33),   # two accumulator n-tiles, ragged tail
+    (3000, 64, 1, 34),
+    (130000, 3, 1, 35),
+    (90001, 2, 5, 36),
+    (200000, 3, 1, 37),           # streamed tier
+]
+
+
+@pytest.mark.parametrize("V,gamma,B,seed", GREEDY_TOKENS_ONLY)
+def test_greedy_tokens_without_logits(walkmod, V, gamma, B, seed):
+    x = synth.make_custom(V=V, gamma=gamma, B=B, seed=seed, temperatures=(0.0,))
+    w = make_walk(walkmod, x)
+    st, toks, _ = gpu_run(w, x, want_logits=False)
+    assert st == 0, walkmod.dspark_walk_strerror(st)
+    rep = parity.check(x, toks)
+    assert rep.ok(), rep
+    w.close()
+
+
 def test_tiny_config(walkmod):
     x = synth.make_inputs("tiny")
     w = make_walk(walkmod, x)
@@ -140,35 +164,38 @@ def _sample_requests(B, temps):
     return sorted(pick)
 
 
-@pytest.mark.parametrize("round_index", [0, 1, 99])
-def test_qwen3_resident(walkmod, round_index):
+@pytest.mark.parametrize("round_index,want_logits", [(0, True), (1, True), (99, True),
+                                                    (2, False), (50, False)])
+def test_qwen3_resident(walkmod, round_index, want_logits):
     x = full_inputs("qwen3_resident", 1, round_index)
     w = full_walk(walkmod, "qwen3_resident", x)
     plan = w.plan()
     assert plan["kernel"] == walkmod.KERNEL_RESIDENT and plan["rows_stream"] == 0
-    st, toks, lg = gpu_run(w, x)
+    st, toks, lg = gpu_run(w, x, want_logits=want_logits)
     assert st == 0
     rep = parity.check(x, toks, lg)
     assert rep.ok(), rep
 
 
 @pytest.mark.parametrize("B", [1, 4, 8, 16])
-def test_long_block(walkmod, B):
+@pytest.mark.parametrize("want_logits", [True, False])
+def test_long_block(walkmod, B, want_logits):
     x = full_inputs("long_block", B)
     w = full_walk(walkmod, "long_block", x)
-    st, toks, lg = gpu_run(w, x)
+    st, toks, lg = gpu_run(w, x, want_logits=want_logits)
     assert st == 0
     rep = parity.check(x, toks, lg, requests=_sample_requests(B, (0.0,)))
     assert rep.ok(), rep
 
 
 @pytest.mark.parametrize("B", [1, 8])
-def test_partial(walkmod, B):
+@pytest.mark.parametrize("want_logits", [True, False])
+def test_partial(walkmod, B, want_logits):
     x = full_inputs("partial", B)
     w = full_walk(walkmod, "partial", x)
     plan = w.plan()
     assert plan["kernel"] == walkmod.KERNEL_RESIDENT and plan["rows_stream"] > 0
-    st, toks, lg = gpu_run(w, x)
+    st, toks, lg = gpu_run(w, x, want_logits=want_logits)
     assert st == 0
     rep = parity.check(x, toks, lg, requests=_sample_requests(B, (0.0,)))
     assert rep.ok(), rep
