@@ -160,18 +160,33 @@ __device__ __forceinline__ void logits_strip(const float (&acc)[NT][4], uint16_t
 // optional copy of the logits for the verifier.  Requests run side by side:
 // `tpr` = blockDim / (B rounded up to a power of two) threads per request.
 // group_best[b][slot] receives one key per group of 32 (or 16) threads.
-__device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logit_s, int R,
-                                         int nv, int64_t row0, int k, const float* temp_s,
-                                         unsigned long long (*group_best)[kResWarps]) {
+struct KeyPassMap {      // this thread's share of the key pass (fixed for a round)
+  int tpr;              // threads per request: blockDim / (B rounded up to a power of 2)
+  int b, gi;            // request, index among its tpr threads
+  float T, inv_T;       // the request's temperature and fl(1/T)
+};
+
+__device__ __forceinline__ KeyPassMap key_pass_map(int B, const float* temp_s) {
   int bp = 1;
-  while (bp < a.B) bp <<= 1;
-  const int tpr = (int)blockDim.x / bp;            // 16 .. 256
-  const int b = (int)threadIdx.x / tpr, gi = (int)threadIdx.x % tpr;
+  while (bp < B) bp <<= 1;
+  KeyPassMap m;
+  m.tpr = kResThreads / bp;                        // 16 .. 256
+  m.b = (int)threadIdx.x / m.tpr;
+  m.gi = (int)threadIdx.x % m.tpr;
+  m.T = m.b < B ? temp_s[m.b] : 0.0f;
+  m.inv_T = m.T > 0.0f ? inv_temperature(m.T) : 0.0f;
+  return m;
+}
+
+__device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logit_s, int R,
+                                         int nv, int64_t row0, int k, const KeyPassMap& m,
+                                         unsigned long long (*group_best)[kResWarps]) {
+  const int tpr = m.tpr, b = m.b, gi = m.gi;
   const int lane = threadIdx.x & 31;
   unsigned long long best = 0ull;
   if (b < a.B) {
-    const float T = temp_s[b];
-    const float inv_T = T > 0.0f ? inv_temperature(T) : 0.0f;
+    const float T = m.T;
+    const float inv_T = m.inv_T;
     const uint16_t* ls = logit_s + (size_t)b * R;
     uint16_t* outl =
         a.out_logits ? a.out_logits + ((size_t)b * a.gamma + k) * (size_t)a.V : nullptr;
@@ -391,6 +406,9 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
   __syncthreads();
   trace_stamp(a, a.gamma, 2);
 
+  const KeyPassMap kpm = key_pass_map(a.B, temp_s);
+  const int nslots = kpm.tpr >= 32 ? kpm.tpr / 32 : 1;   // group_best slots per request
+
   // ----------------------------------------------------------- the walk ---
   const uint32_t u_addr = ptx::smem_u32(U);
   const uint32_t w2_addr = ptx::smem_u32(smem_w2);
@@ -566,7 +584,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     __syncthreads();
 
     // (4b) scores and keys of all rows, every thread
-    key_pass(a, base_s, ra.R, nv, row0, k, temp_s, group_best);
+    key_pass(a, base_s, ra.R, nv, row0, k, kpm, group_best);
     trace_stamp(a, k, 3);
     ptx::tc_fence_before();
     __syncthreads();
@@ -585,9 +603,6 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
       uint32_t* cnt = a.sync.count_at(parity, k);
       unsigned long long* keyk = a.sync.key_at(parity, k, 0);
       unsigned long long cand = 0ull;
-      int bp = 1;
-      while (bp < a.B) bp <<= 1;
-      const int nslots = (kResThreads / bp) >= 32 ? (kResThreads / bp) / 32 : 1;
       if (lane < a.B) {
         unsigned long long mine = 0ull;
         for (int sl = 0; sl < nslots; ++sl) mine = key_max(mine, group_best[lane][sl]);
