@@ -39,6 +39,10 @@ METRIC = ("µs per γ-step draft walk at B=1..128; effective W2 GB/s vs "
 # V = 151,936, gamma = 7, bs = 1 took 37 us per call
 PAGES_US = {("qwen3_resident", 1): 37.0}
 L2_FLUSH_BYTES = 256 << 20
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the walk
+# kernel (ncu, --clock-control none), per (workload, B); refreshed whenever the
+# kernel changes (profiles/walk_resident_qwen3_resident.md)
+TRAFFIC = {}
 
 
 def parse():
@@ -197,6 +201,39 @@ def phase_breakdown(walk, w, B, cfg, launch, stream, n_rounds, clocks, rounds=20
     return out
 
 
+def kernel_label(walk, plan, B):
+    """Which kernel a run of B requests takes on a handle with this plan."""
+    if plan["kernel"] == walk.KERNEL_RESIDENT and B <= min(plan["max_B"], 16):
+        return "resident+streamed tier" if plan["rows_stream"] > 0 else "resident"
+    return "batched"
+
+
+# GB300 unit rates measured for the on-chip roofline (probes summarised in
+# profiles/gb300_unit_rates.md and profiles/gb300_streaming.md): a tcgen05.mma
+# M=128 N=16 K=16 with A in tensor memory holds the tensor pipe ~13.4 SM
+# cycles; an mma.sync m16n8k16 ~2.0 cycles per SM; bulk copies from L2 bring
+# ~142 GB/s per SM.
+TC_CYCLES_PER_TMEM_MMA = 13.4
+HMMA_CYCLES = 2.0
+STREAM_GBS_PER_SM = 142.0
+
+
+def onchip_roofline_us(plan, gamma, mhz):
+    """Lower bound of the walk from on-chip reads: per step and CTA, the
+    tensor-memory tiles through tcgen05 plus the register, shared and streamed
+    strips through mma.sync (the two share the tensor pipe), or the streamed
+    bytes at the L2 streaming rate if that is longer; W2 read once from HBM per
+    process (the entry load is not counted)."""
+    if plan["kernel"] != 1 or not plan["rows_per_cta"]:      # 1: the resident kernel
+        return None
+    tmem_mmas = plan["rows_tmem"] // 128 * 16
+    strips = (plan["rows_rf"] + plan["rows_smem"] + plan["rows_stream"]) // 16
+    cycles = tmem_mmas * TC_CYCLES_PER_TMEM_MMA + strips * 16 * HMMA_CYCLES
+    t_tensor = cycles / mhz                                   # us
+    t_stream = plan["rows_stream"] * 512 / (STREAM_GBS_PER_SM * 1e3)
+    return gamma * max(t_tensor, t_stream)
+
+
 def measure_config(walk, cfg, B, steps=50, warmup=5):
     """Cold- and warm-L2 us per walk of one workload at batch B (sweep mode)."""
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -229,10 +266,14 @@ def measure_config(walk, cfg, B, steps=50, warmup=5):
     warm = ws.elapsed_time(we) / steps * 1000.0
     res = {"workload": cfg.name, "V": cfg.V, "gamma": cfg.gamma, "B": B,
            "temperatures": list(cfg.temperatures), "status": st,
-           "kernel": "resident" if (plan["kernel"] == walk.KERNEL_RESIDENT and B <= 16)
-           else "stream",
+           "kernel": kernel_label(walk, plan, B),
            "us_cold_l2": cold, "us_warm_l2": warm,
            "eff_w2_GBs_cold": cfg.gamma * cfg.V * cfg.r * 2 * B / (cold * 1e-6) / 1e9}
+    if res["kernel"] != "batched":
+        onchip = onchip_roofline_us(plan, cfg.gamma, 2070.0)
+        if onchip is not None:
+            res["onchip_roofline_us"] = onchip
+            res["onchip_frac_warm_l2"] = onchip / warm
     w.close()
     del flush, base
     torch.cuda.empty_cache()
@@ -419,10 +460,18 @@ def main():
     eff_gbs = w2_bytes / (mean_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
     roof = {"bound": "hbm", "achieved": eff_gbs, "peak": peak, "unit": "GB/s",
-            "frac": eff_gbs / peak, "traffic": None,
+            "frac": eff_gbs / peak, "traffic": TRAFFIC.get((cfg.name, B)),
             "peak_kind": peak_kind,
             "note": "achieved = effective W2 bytes (gamma*V*r*2*B) per launch / mean launch "
                     "time; >1 means W2 is served from on-chip memory or L2, not HBM"}
+    onchip = onchip_roofline_us(plan, cfg.gamma, clocks.get("sm_mhz") or 2070.0)
+    if onchip is not None:
+        roof["onchip"] = {
+            "roofline_us": onchip, "unit": "us per walk",
+            "frac_cold_l2": onchip / us,
+            "frac_warm_l2": onchip / (warm_ms * 1000.0) if warm_ms else None,
+            "how": "per step: tensor-memory MMAs x 13.4 cycles + mma.sync strips x 16 x 2.0 "
+                   "cycles (shared tensor pipe), or streamed bytes at 142 GB/s per SM; x gamma"}
     line = {
         "metric": METRIC, "value": us, "unit": "us", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
