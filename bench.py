@@ -42,7 +42,9 @@ L2_FLUSH_BYTES = 256 << 20
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the walk
 # kernel (ncu, --clock-control none), per (workload, B); refreshed whenever the
 # kernel changes (profiles/walk_resident_qwen3_resident.md)
-TRAFFIC = {}
+TRAFFIC = {("qwen3_resident", 1): 81_894_656,
+           ("partial", 8): 275_697_408,
+           ("sampled", 253): 670_700_800}
 
 
 def parse():
@@ -464,7 +466,9 @@ def main():
             "peak_kind": peak_kind,
             "note": "achieved = effective W2 bytes (gamma*V*r*2*B) per launch / mean launch "
                     "time; >1 means W2 is served from on-chip memory or L2, not HBM"}
-    onchip = onchip_roofline_us(plan, cfg.gamma, clocks.get("sm_mhz") or 2070.0)
+    label = kernel_label(walk, plan, B)
+    onchip = (onchip_roofline_us(plan, cfg.gamma, clocks.get("sm_mhz") or 2070.0)
+              if label != "batched" else None)
     if onchip is not None:
         roof["onchip"] = {
             "roofline_us": onchip, "unit": "us per walk",
@@ -483,8 +487,8 @@ def main():
         "config": {"workload": cfg.note, "V": cfg.V, "r": cfg.r, "gamma": cfg.gamma, "B": B,
                    "rounds": n_rounds, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "flushed between timed steps (256 MiB write)",
-                   "kernel": plan["kernel"], "n_cta": plan["n_cta"],
-                   "threads": plan["threads"]},
+                   "kernel": label, "n_cta": plan["n_cta"] if label != "batched" else None,
+                   "threads": plan["threads"] if label != "batched" else None},
         "median_us": statistics.median(per) * 1000.0,
         "p10_us": float(np.percentile(per, 10)) * 1000.0,
         "p90_us": float(np.percentile(per, 90)) * 1000.0,
