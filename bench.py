@@ -55,6 +55,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="qwen3_resident", choices=sorted(synth.CONFIGS))
     p.add_argument("--batch", type=int, default=None)
+    p.add_argument("--kernel", default="planned", choices=["planned", "resident", "batched", "stream"],
+                   help="force a kernel (dspark_walk_set_kernel); default: the handle's plan")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--sweep", action="store_true",
@@ -366,6 +368,9 @@ def main():
     W1 = W1c.to(dev)
     W2 = W2c.to(dev)
     w = walk.Walk(W1, W2, B, cfg.gamma)
+    if args.kernel != "planned":
+        w.set_kernel({"resident": walk.KERNEL_RESIDENT, "batched": walk.KERNEL_BATCHED,
+                      "stream": walk.KERNEL_STREAM}[args.kernel])
     plan = w.plan()
     del W2
     base = torch.stack([r.base for r in rounds]).to(dev)          # [R, B, gamma, V]
@@ -466,7 +471,7 @@ def main():
             "peak_kind": peak_kind,
             "note": "achieved = effective W2 bytes (gamma*V*r*2*B) per launch / mean launch "
                     "time; >1 means W2 is served from on-chip memory or L2, not HBM"}
-    label = kernel_label(walk, plan, B)
+    label = kernel_label(walk, plan, B) if args.kernel == "planned" else args.kernel
     onchip = (onchip_roofline_us(plan, cfg.gamma, clocks.get("sm_mhz") or 2070.0)
               if label != "batched" else None)
     if onchip is not None:

@@ -192,13 +192,13 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
         a.out_logits ? a.out_logits + ((size_t)b * a.gamma + k) * (size_t)a.V : nullptr;
     // separate loops: one loop with a select would evaluate the noise always
     if (T > 0.0f) {
+      const PhiloxKeys pk = philox_keys(a.seed_lo, a.seed_hi);
       for (int c = gi; 4 * c < nv; c += tpr) {
         const int rl0 = 4 * c;
         const uint2 w = *reinterpret_cast<const uint2*>(ls + rl0);
         const uint32_t lb[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
         const uint32_t v0 = (uint32_t)(row0 + rl0);     // a multiple of 4
-        const uint4 r = philox4x32_10(make_uint4(v0 >> 2, (uint32_t)k, (uint32_t)b, 0u),
-                                      a.seed_lo, a.seed_hi);
+        const uint4 r = philox4x32_10(make_uint4(v0 >> 2, (uint32_t)k, (uint32_t)b, 0u), pk);
         const uint32_t x[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
