@@ -193,20 +193,27 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
     // separate loops: one loop with a select would evaluate the noise always
     if (T > 0.0f) {
       const PhiloxKeys pk = philox_keys(a.seed_lo, a.seed_hi);
-      for (int c = gi; 4 * c < nv; c += tpr) {
-        const int rl0 = 4 * c;
-        const uint2 w = *reinterpret_cast<const uint2*>(ls + rl0);
-        const uint32_t lb[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
-        const uint32_t v0 = (uint32_t)(row0 + rl0);     // a multiple of 4
-        const uint4 r = philox4x32_10(make_uint4(v0 >> 2, (uint32_t)k, (uint32_t)b, 0u), pk);
-        const uint32_t x[4] = {r.x, r.y, r.z, r.w};
+      // two blocks of 4 tokens per iteration: two independent Philox chains
+      for (int c = gi; 4 * c < nv; c += 2 * tpr) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (rl0 + e < nv) {
-            const unsigned long long key =
-                make_key(gumbel_score(bf16_bits_to_float(lb[e]), T, inv_T, x[e]), v0 + e);
-            best = key > best ? key : best;
-            if (outl) outl[v0 + e] = (uint16_t)lb[e];
+        for (int u = 0; u < 2; ++u) {
+          const int rl0 = 4 * (c + u * tpr);
+          if (rl0 < nv) {
+            const uint2 w = *reinterpret_cast<const uint2*>(ls + rl0);
+            const uint32_t lb[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
+            const uint32_t v0 = (uint32_t)(row0 + rl0);     // a multiple of 4
+            const uint4 r =
+                philox4x32_10(make_uint4(v0 >> 2, (uint32_t)k, (uint32_t)b, 0u), pk);
+            const uint32_t x[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (rl0 + e < nv) {
+                const unsigned long long key =
+                    make_key(gumbel_score(bf16_bits_to_float(lb[e]), T, inv_T, x[e]), v0 + e);
+                best = key > best ? key : best;
+                if (outl) outl[v0 + e] = (uint16_t)lb[e];
+              }
+            }
           }
         }
       }
@@ -648,8 +655,9 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
           }
         }
         __syncwarp();
-        // four rows in flight at a time, then their stores; one proxy fence
-        for (int b0 = 0; b0 < a.B; b0 += 4) {
+        // up to four rows: warp 0 fetches them here (larger batches are
+        // fetched by all warps after the barrier below)
+        for (int b0 = 0; b0 < (a.B <= 4 ? a.B : 0); b0 += 4) {
           uint4 ur[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -669,6 +677,16 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     ptx::cp_async_wait_all();
     ptx::fence_proxy_async_smem();
     __syncthreads();
+    if (a.B > 4 && abort_s == 0 && k + 1 < a.gamma) {
+      // the next u rows, all in flight at once: warp w fetches rows w, w + 8
+      for (int b = warp; b < a.B; b += kResWarps) {
+        const uint4 x =
+            __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok_s[b] * kRank) + lane);
+        *reinterpret_cast<uint4*>(U + (lane * 2 + (b >> 3)) * 128 + (b & 7) * 16) = x;
+      }
+      ptx::fence_proxy_async_smem();
+      __syncthreads();
+    }
     trace_stamp(a, k, 7);
     ok = abort_s == 0;
   }
