@@ -154,6 +154,42 @@ __device__ __forceinline__ void logits_strip(const float (&acc)[NT][4], uint16_t
     }
 }
 
+// Sampled keys of request b's rows handled by this thread (blocks of 4
+// tokens c = gi, gi + tpr, ...; two blocks per iteration, so two independent
+// Philox chains): the best key {ord32(score), inverted id}.  FASTQ: the
+// quotient logit / T as the product with fl(1/T) (else the IEEE quotient,
+// when 1/T overflows).
+template <bool FASTQ>
+__device__ __forceinline__ unsigned long long sampled_block_keys(
+    const WalkArgs& a, const uint16_t* ls, int nv, int64_t row0, int k, int b, int gi, int tpr,
+    float T, float inv_T, const PhiloxKeys& pk, uint16_t* outl) {
+  unsigned long long best = 0ull;
+  for (int c = gi; 4 * c < nv; c += 2 * tpr) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int rl0 = 4 * (c + u * tpr);
+      if (rl0 < nv) {
+        const uint2 w = *reinterpret_cast<const uint2*>(ls + rl0);
+        const uint32_t lb[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
+        const uint32_t v0 = (uint32_t)(row0 + rl0);     // a multiple of 4
+        const uint4 r = philox4x32_10(make_uint4(v0 >> 2, (uint32_t)k, (uint32_t)b, 0u), pk);
+        const uint32_t x[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (rl0 + e < nv) {
+            const float lgt = bf16_bits_to_float(lb[e]);
+            const float q = FASTQ ? __fmul_rn(lgt, inv_T) : __fdiv_rn(lgt, T);
+            const unsigned long long key = make_key(__fadd_rn(q, gumbel_noise(x[e])), v0 + e);
+            best = key > best ? key : best;
+            if (outl) outl[v0 + e] = (uint16_t)lb[e];
+          }
+        }
+      }
+    }
+  }
+  return best;
+}
+
 // Second half, over all of the CTA's rows: selection score and key of each
 // logit (greedy: the logit; sampled: Philox Gumbel-max, one Philox call per 4
 // consecutive tokens), the best key per (request, thread group), and the
@@ -193,30 +229,10 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
     // separate loops: one loop with a select would evaluate the noise always
     if (T > 0.0f) {
       const PhiloxKeys pk = philox_keys(a.seed_lo, a.seed_hi);
-      // two blocks of 4 tokens per iteration: two independent Philox chains
-      for (int c = gi; 4 * c < nv; c += 2 * tpr) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int rl0 = 4 * (c + u * tpr);
-          if (rl0 < nv) {
-            const uint2 w = *reinterpret_cast<const uint2*>(ls + rl0);
-            const uint32_t lb[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
-            const uint32_t v0 = (uint32_t)(row0 + rl0);     // a multiple of 4
-            const uint4 r =
-                philox4x32_10(make_uint4(v0 >> 2, (uint32_t)k, (uint32_t)b, 0u), pk);
-            const uint32_t x[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if (rl0 + e < nv) {
-                const unsigned long long key =
-                    make_key(gumbel_score(bf16_bits_to_float(lb[e]), T, inv_T, x[e]), v0 + e);
-                best = key > best ? key : best;
-                if (outl) outl[v0 + e] = (uint16_t)lb[e];
-              }
-            }
-          }
-        }
-      }
+      // the quotient by the rounded reciprocal unless 1/T overflows
+      best = inv_T != 0.0f
+                 ? sampled_block_keys<true>(a, ls, nv, row0, k, b, gi, tpr, T, inv_T, pk, outl)
+                 : sampled_block_keys<false>(a, ls, nv, row0, k, b, gi, tpr, T, inv_T, pk, outl);
     } else {
       // 32-bit keys {order bits of the bf16 logit : 16, inverted local row :
       // 16}, two independent maxima per thread, widened to the 64-bit key once
