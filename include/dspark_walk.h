@@ -176,6 +176,40 @@ int dspark_walk_set_limits(dspark_walk_t h, int64_t timeout_ns, int skip_cta);
 int dspark_walk_set_kernel(dspark_walk_t h, int kernel);
 
 /*
+ * dspark_walk_set_seed_mode -- how later runs key their Philox noise.
+ *   DSPARK_SEED_FIXED (default): the key is `seed` as passed to the run.
+ *   DSPARK_SEED_PER_ROUND: the key is seed + n (mod 2^64), n = the number of
+ *     rounds this handle has run before (0 for the first run after create;
+ *     rounds rejected by the host checks do not count; rounds the kernel ends
+ *     with an error status do).  The pages key the noise on the seed and a
+ *     round counter ("Keeping the Draft Walk on Chip...", section "The idea:
+ *     make the walk resident"); with this mode one CUDA graph captured with a
+ *     fixed seed draws fresh noise on every replay, with no host update.
+ * DSPARK_EINVAL for another mode.
+ */
+#define DSPARK_SEED_FIXED 0
+#define DSPARK_SEED_PER_ROUND 1
+int dspark_walk_set_seed_mode(dspark_walk_t h, int mode);
+
+/*
+ * dspark_walk_round -- the handle's round counter n (see set_seed_mode):
+ * synchronises `stream` (a cudaStream_t; NULL = legacy default stream), then
+ * reads it into *round.
+ */
+int dspark_walk_round(dspark_walk_t h, void *stream, uint64_t *round);
+
+/*
+ * dspark_walk_gumbel_noise -- the Gumbel noise the kernels add to logit / T:
+ * noise[i] = g(bits[i]), g = -log(-log U), U = (2 (bits >> 9) + 1) 2^-24 (the
+ * uniform of a Philox output word), in the kernels' own fp32 arithmetic.  It
+ * exists so that the noise can be checked against a float64 reference over
+ * every uniform (the pages fix the formula, not its implementation).
+ *   bits, noise  device, n uint32 / n float32
+ * Asynchronous on `stream`; DSPARK_EINVAL for n < 0 or null pointers with n > 0.
+ */
+int dspark_walk_gumbel_noise(const uint32_t *bits, float *noise, int64_t n, void *stream);
+
+/*
  * dspark_walk_set_trace -- phase timing of later runs (profiling aid).  When
  * `device_buffer` holds at least n_cta * (gamma + 1) * 8 uint64 values, each
  * run's CTA c writes SM clock64() stamps of its thread 0 at

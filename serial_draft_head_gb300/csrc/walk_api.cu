@@ -28,6 +28,7 @@ struct dspark_walk {
   uint32_t* W2p = nullptr;        // tiered repack, res_wpc words per CTA
   int res_max_B = 0;              // 0: no resident layout
   bool use_resident = true;       // dspark_walk_set_kernel
+  int seed_per_round = 0;         // dspark_walk_set_seed_mode
   int res_RS = 0, res_NT = 0, res_R = 0, res_S = 0, res_ST = 0, res_nslot = 0, res_n_cta = 0;
   int64_t res_wpc = 0;
   size_t res_smem = 0;
@@ -182,6 +183,7 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
   a.rows_per_cta = h->st_rpc;
   a.seed_lo = (uint32_t)seed;
   a.seed_hi = (uint32_t)(seed >> 32);
+  a.seed_per_round = h->seed_per_round;
   a.timeout_ns = h->timeout_ns;
   a.skip_cta = h->skip_cta;
   {
@@ -430,6 +432,29 @@ int dspark_walk_set_kernel(dspark_walk_t h, int kernel) {
     return DSPARK_OK;
   }
   return DSPARK_EINVAL;
+}
+
+int dspark_walk_set_seed_mode(dspark_walk_t h, int mode) {
+  if (!h || (mode != DSPARK_SEED_FIXED && mode != DSPARK_SEED_PER_ROUND)) return DSPARK_EINVAL;
+  h->seed_per_round = mode == DSPARK_SEED_PER_ROUND ? 1 : 0;
+  return DSPARK_OK;
+}
+
+int dspark_walk_round(dspark_walk_t h, void* stream, uint64_t* round) {
+  if (!h || !round) return DSPARK_EINVAL;
+  CUDA_TRY(cudaSetDevice(h->device));
+  CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  uint32_t r = 0;
+  CUDA_TRY(cudaMemcpy(&r, &h->sync.hdr->round, sizeof(r), cudaMemcpyDeviceToHost));
+  *round = r;
+  return DSPARK_OK;
+}
+
+int dspark_walk_gumbel_noise(const uint32_t* bits, float* noise, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!bits || !noise))) return DSPARK_EINVAL;
+  if (n == 0) return DSPARK_OK;
+  CUDA_TRY(gumbel_noise_launch(bits, noise, n, static_cast<cudaStream_t>(stream)));
+  return DSPARK_OK;
 }
 
 const char* dspark_walk_strerror(int code) {

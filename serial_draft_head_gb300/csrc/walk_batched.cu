@@ -424,7 +424,8 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
       uint16_t* stg = stage + warp * kStgWarpElems;
       for (int i = lane; i < kWbCols; i += 32) wbest[warp * kWbCols + i] = 0ull;
       __syncwarp();
-      const PhiloxKeys pk = philox_keys(a.seed_lo, a.seed_hi);
+      const uint2 eseed = round_seed(a, round_s);     // this round's Philox key
+      const PhiloxKeys pk = philox_keys(eseed.x, eseed.y);
       uint32_t nxt[4];
       int pt = 0, pcb = 0;                           // tile and column of the next prefetch
       auto prefetch = [&]() {

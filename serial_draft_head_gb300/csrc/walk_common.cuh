@@ -86,7 +86,8 @@ struct WalkArgs {
   int B;
   int gamma;
   int rows_per_cta;            // shard size (last shard may be shorter)
-  uint32_t seed_lo, seed_hi;   // Philox key
+  uint32_t seed_lo, seed_hi;   // Philox key (see round_seed)
+  int seed_per_round;          // add the handle's round counter to the key
   int64_t timeout_ns;          // rendezvous wait limit
   int skip_cta;                // fault injection: this CTA never posts (-1: off)
   unsigned long long* trace;   // optional [n_cta][gamma + 1][8] SM-clock stamps
@@ -97,6 +98,14 @@ struct WalkArgs {
 __device__ __forceinline__ void trace_stamp(const WalkArgs& a, int slot, int phase) {
   if (a.trace != nullptr && threadIdx.x == 0)
     a.trace[((size_t)blockIdx.x * (a.gamma + 1) + slot) * 8 + phase] = clock64();
+}
+
+// The Philox key of this round: the seed, plus the round counter when the
+// handle keys its noise per round (seed + n mod 2^64), as two 32-bit words.
+__device__ __forceinline__ uint2 round_seed(const WalkArgs& a, uint32_t round) {
+  uint64_t s = ((uint64_t)a.seed_hi << 32) | a.seed_lo;
+  if (a.seed_per_round) s += round;
+  return make_uint2((uint32_t)s, (uint32_t)(s >> 32));
 }
 
 // ------------------------------------------------------------ PTX helpers --

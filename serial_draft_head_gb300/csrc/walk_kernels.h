@@ -11,6 +11,10 @@ size_t stream_smem_bytes(int B);
 int stream_threads();
 const void* stream_kernel_for(int B);
 
+// The kernels' Gumbel noise of n Philox words (a check of its arithmetic).
+cudaError_t gumbel_noise_launch(const uint32_t* bits, float* noise, int64_t n,
+                                cudaStream_t stream);
+
 // Resident kernel: W2 tiered over tensor memory, registers, shared memory.
 int64_t resident_words_per_cta(int RS, int S);
 int resident_fixed_rows(int RS);

@@ -216,6 +216,7 @@ __device__ __forceinline__ KeyPassMap key_pass_map(int B, const float* temp_s) {
 
 __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logit_s, int R,
                                          int nv, int64_t row0, int k, const KeyPassMap& m,
+                                         uint2 seed,
                                          unsigned long long (*group_best)[kResWarps]) {
   const int tpr = m.tpr, b = m.b, gi = m.gi;
   const int lane = threadIdx.x & 31;
@@ -228,7 +229,7 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
         a.out_logits ? a.out_logits + ((size_t)b * a.gamma + k) * (size_t)a.V : nullptr;
     // separate loops: one loop with a select would evaluate the noise always
     if (T > 0.0f) {
-      const PhiloxKeys pk = philox_keys(a.seed_lo, a.seed_hi);
+      const PhiloxKeys pk = philox_keys(seed.x, seed.y);
       // the quotient by the rounded reciprocal unless 1/T overflows
       best = inv_T != 0.0f
                  ? sampled_block_keys<true>(a, ls, nv, row0, k, b, gi, tpr, T, inv_T, pk, outl)
@@ -430,6 +431,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
   trace_stamp(a, a.gamma, 2);
 
   const KeyPassMap kpm = key_pass_map(a.B, temp_s);
+  const uint2 eseed = round_seed(a, round_s);             // this round's Philox key
   const int nslots = kpm.tpr >= 32 ? kpm.tpr / 32 : 1;   // group_best slots per request
 
   // ----------------------------------------------------------- the walk ---
@@ -607,7 +609,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     __syncthreads();
 
     // (4b) scores and keys of all rows, every thread
-    key_pass(a, base_s, ra.R, nv, row0, k, kpm, group_best);
+    key_pass(a, base_s, ra.R, nv, row0, k, kpm, eseed, group_best);
     trace_stamp(a, k, 3);
     ptx::tc_fence_before();
     __syncthreads();

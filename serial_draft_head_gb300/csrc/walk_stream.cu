@@ -44,7 +44,7 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long x)
 template <int NB>
 __device__ __forceinline__ void stream_rows(const WalkArgs& a, int k, int b0, int64_t row0,
                                             int64_t row1, const uint4* u_s, const float* temp_s,
-                                            unsigned long long* cta_key) {
+                                            uint2 seed, unsigned long long* cta_key) {
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   unsigned long long best[NB];
@@ -78,7 +78,7 @@ __device__ __forceinline__ void stream_rows(const WalkArgs& a, int k, int b0, in
           const size_t off = ((size_t)b * a.gamma + k) * (size_t)a.V + (size_t)row;
           uint16_t lb;
           const unsigned long long key =
-              epilogue_key(acc[j], a.base[off], temp_s[b], a.seed_lo, a.seed_hi, b, k,
+              epilogue_key(acc[j], a.base[off], temp_s[b], seed.x, seed.y, b, k,
                            (uint32_t)row, &lb);
           if (a.out_logits) a.out_logits[off] = lb;
           best[j] = key > best[j] ? key : best[j];
@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) walk_stream_kernel(const Wa
   }
   __syncthreads();
   const uint32_t parity = round_s & 1u;
+  const uint2 eseed = round_seed(a, round_s);             // this round's Philox key
   if (blockIdx.x == 0) clear_other_parity(a.sync, parity);
 
   const int64_t row0 = (int64_t)blockIdx.x * a.rows_per_cta;
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) walk_stream_kernel(const Wa
     for (int b = threadIdx.x; b < a.B; b += blockDim.x) cta_key[b] = 0ull;
     __syncthreads();
     for (int b0 = 0; b0 < a.B; b0 += NB)
-      stream_rows<NB>(a, k, b0, row0, row1, u_s, temp_s, cta_key);
+      stream_rows<NB>(a, k, b0, row0, row1, u_s, temp_s, eseed, cta_key);
     __syncthreads();
     ok = exchange(a, round_s, k, cta_key, prev_s, &flag_s);
     if (ok && blockIdx.x == 0)
@@ -166,6 +167,25 @@ const void* stream_kernel_for(int B) {
   if (B >= 4) return reinterpret_cast<const void*>(&walk_stream_kernel<4>);
   if (B >= 2) return reinterpret_cast<const void*>(&walk_stream_kernel<2>);
   return reinterpret_cast<const void*>(&walk_stream_kernel<1>);
+}
+
+namespace {
+
+__global__ void gumbel_noise_kernel(const uint32_t* __restrict__ bits, float* __restrict__ noise,
+                                    int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    noise[i] = gumbel_noise(bits[i]);
+}
+
+}  // namespace
+
+cudaError_t gumbel_noise_launch(const uint32_t* bits, float* noise, int64_t n,
+                                cudaStream_t stream) {
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  gumbel_noise_kernel<<<(unsigned)blocks, 256, 0, stream>>>(bits, noise, n);
+  return cudaGetLastError();
 }
 
 }  // namespace dspark

@@ -27,6 +27,9 @@ KERNEL_STREAM = 0
 KERNEL_RESIDENT = 1
 KERNEL_BATCHED = 2
 
+SEED_FIXED = 0
+SEED_PER_ROUND = 1
+
 _lib = None
 
 
@@ -56,7 +59,8 @@ EXPORTS = [
     "dspark_walk_create", "dspark_walk_run", "dspark_walk_run_host", "dspark_walk_status",
     "dspark_walk_get_plan", "dspark_walk_set_limits", "dspark_walk_strerror",
     "dspark_walk_destroy", "dspark_walk_run_noalloc", "dspark_walk_set_kernel",
-    "dspark_walk_set_trace",
+    "dspark_walk_set_trace", "dspark_walk_set_seed_mode", "dspark_walk_round",
+    "dspark_walk_gumbel_noise",
 ]
 
 
@@ -88,6 +92,9 @@ def load(build_if_missing=True):
     L.dspark_walk_set_kernel.argtypes = [vp, i32]
     L.dspark_walk_set_trace.argtypes = [vp, vp, i64]
     L.dspark_walk_run_noalloc.argtypes = [vp, vp, i64, i32, vp, vp, vp, u64, vp, i32, i32, vp, vp]
+    L.dspark_walk_set_seed_mode.argtypes = [vp, i32]
+    L.dspark_walk_round.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint64)]
+    L.dspark_walk_gumbel_noise.argtypes = [vp, vp, i64, vp]
     for name in EXPORTS:
         if name != "dspark_walk_strerror":
             getattr(L, name).restype = ctypes.c_int
@@ -166,6 +173,24 @@ def dspark_walk_set_kernel(h, kernel):
     return _check(load().dspark_walk_set_kernel(h, int(kernel)), "dspark_walk_set_kernel")
 
 
+def dspark_walk_set_seed_mode(h, mode):
+    return _check(load().dspark_walk_set_seed_mode(h, int(mode)), "dspark_walk_set_seed_mode")
+
+
+def dspark_walk_round(h, stream=None):
+    r = ctypes.c_uint64(0)
+    _check(load().dspark_walk_round(h, _stream(stream), ctypes.byref(r)), "dspark_walk_round")
+    return r.value
+
+
+def dspark_walk_gumbel_noise(bits, noise, stream=None):
+    """noise[i] = the kernels' Gumbel noise of Philox word bits[i] (device tensors)."""
+    assert bits.is_cuda and noise.is_cuda and bits.numel() == noise.numel()
+    assert bits.dtype in (torch.int32, torch.uint32) and noise.dtype == torch.float32
+    return _check(load().dspark_walk_gumbel_noise(_ptr(bits), _ptr(noise), bits.numel(),
+                                                  _stream(stream)), "dspark_walk_gumbel_noise")
+
+
 def dspark_walk_set_trace(h, device_buffer, nbytes):
     return _check(load().dspark_walk_set_trace(h, _ptr(device_buffer), int(nbytes)),
                   "dspark_walk_set_trace")
@@ -205,6 +230,12 @@ class Walk:
 
     def set_kernel(self, kernel):
         dspark_walk_set_kernel(self.h, kernel)
+
+    def set_seed_mode(self, mode):
+        dspark_walk_set_seed_mode(self.h, mode)
+
+    def round(self, stream=None):
+        return dspark_walk_round(self.h, stream)
 
     def run(self, base, anchor, temperature, seed, out_tokens=None, out_logits=None,
             stream=None):

@@ -4,6 +4,7 @@ Small shapes are compared on every logit and every step; the five full-size
 workloads are compared on sampled requests (the oracle replays one request
 at its own request index), in the launch configuration the benchmark times.
 """
+import dataclasses
 import numpy as np
 import pytest
 import torch
@@ -248,6 +249,57 @@ def test_graph_replay_and_parity_alternation(walkmod):
     assert w.status() == 0
     rep = parity.check(x, eager.cpu().numpy())
     assert rep.ok(), rep
+
+
+def test_seed_per_round_graph_replays_draw_fresh_noise(walkmod):
+    """With the per-round seed mode, one captured graph replayed with a fixed
+    seed keys round n's noise on seed + n; each replay matches the oracle at
+    that key, and the sampled tokens change from replay to replay."""
+    x = synth.make_custom(V=6007, gamma=4, B=3, seed=42, temperatures=(0.6, 1.0, 0.0),
+                          noise_seed=5)
+    w = make_walk(walkmod, x)
+    w.set_seed_mode(walkmod.SEED_PER_ROUND)
+    base, anchor, temp = x.base.cuda(), x.anchor.cuda(), x.temperature.cuda()
+    tokens = torch.full((3, 4), -2, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    r0 = w.round(s)
+    with torch.cuda.stream(s):
+        w.run(base, anchor, temp, x.seed, tokens, stream=s)      # round r0, eager
+    s.synchronize()
+    first = tokens.cpu().numpy()
+    assert parity.check(dataclasses.replace(x, seed=x.seed + r0), first).ok()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        w.run(base, anchor, temp, x.seed, tokens, stream=s)
+    seen = [first]
+    for _ in range(3):
+        r = w.round(s)
+        tokens.fill_(-2)
+        g.replay()
+        torch.cuda.synchronize()
+        got = tokens.cpu().numpy()
+        rep = parity.check(dataclasses.replace(x, seed=x.seed + r), got)
+        assert rep.ok(), (r, rep)
+        seen.append(got)
+    assert w.round(s) == r0 + 4 and w.status() == 0
+    assert any(not np.array_equal(seen[0][:2], t[:2]) for t in seen[1:])
+
+
+def test_gumbel_noise_every_uniform(walkmod):
+    """The kernels' Gumbel noise against float64 -log(-log U) for all 2^23
+    uniforms: within a quarter of the 2^-18 (1 + |g|) error the token
+    comparison allows."""
+    m = torch.arange(1 << 23, dtype=torch.int64)
+    bits = ((m << 9) | 0x155).to(torch.int32).cuda()       # the low 9 bits are unused
+    noise = torch.empty(1 << 23, dtype=torch.float32, device="cuda")
+    walkmod.dspark_walk_gumbel_noise(bits, noise)
+    g = noise.cpu().numpy().astype(np.float64)
+    mm = m.numpy().astype(np.float64)
+    t = (16777216.0 - 2.0 * mm - 1.0) / 16777216.0           # 1 - U, exact
+    ref = -np.log(-np.log1p(-t))
+    err = np.abs(g - ref) / (2.0**-18 * (1.0 + np.abs(ref)))
+    assert np.all(np.isfinite(g))
+    assert err.max() <= 0.25, (err.max(), int(np.argmax(err)))
 
 
 def test_rounds_back_to_back(walkmod):
