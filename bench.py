@@ -61,6 +61,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--sweep", action="store_true",
                    help="also time every workload and batch size (fewer steps) into 'sweep'")
+    p.add_argument("--gamma-fit", action="store_true",
+                   help="also time the V=151,936 B=1 walk at gamma in {1,4,7,16} and fit "
+                        "us = entry + gamma * per-step into 'gamma_fit'")
     p.add_argument("--trace", action="store_true",
                    help="after timing, run traced rounds and report the per-phase breakdown")
     p.add_argument("--only-timed", action="store_true",
@@ -236,6 +239,50 @@ def onchip_roofline_us(plan, gamma, mhz):
     t_tensor = cycles / mhz                                   # us
     t_stream = plan["rows_stream"] * 512 / (STREAM_GBS_PER_SM * 1e3)
     return gamma * max(t_tensor, t_stream)
+
+
+def gamma_fit(walk, gammas=(1, 4, 7, 16), steps=100, warmup=5):
+    """Warm- and cold-L2 us per walk of the long-block vocabulary at B=1 for
+    several walk lengths, and the least-squares line us = entry + gamma x step."""
+    cfg = synth.CONFIGS["long_block"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    W1, W2, _ = synth.make_weights(cfg.V, cfg.r, cfg.seed)
+    x = synth.make_inputs(cfg, B=1, round_index=0, weights=(W1, W2))
+    w = walk.Walk(W1.to(dev), W2.to(dev), 1, max(gammas))
+    anchor, temp = x.anchor.to(dev), x.temperature.to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    rows = []
+    for g in gammas:
+        base = x.base[:, :g].contiguous().to(dev)
+        tok = torch.empty(1, g, dtype=torch.int32, device=dev)
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                w.run(base, anchor, temp, x.seed, tok, stream=stream)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(steps)]
+            for i in range(steps):
+                flush.fill_(i)
+                ev[i][0].record(stream)
+                w.run(base, anchor, temp, x.seed, tok, stream=stream)
+                ev[i][1].record(stream)
+            ws, we = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ws.record(stream)
+            for _ in range(steps):
+                w.run(base, anchor, temp, x.seed, tok, stream=stream)
+            we.record(stream)
+        torch.cuda.synchronize()
+        cold = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1000.0
+        warm = ws.elapsed_time(we) / steps * 1000.0
+        rows.append({"gamma": g, "us_cold_l2": cold, "us_warm_l2": warm})
+    w.close()
+    out = {"workload": "V=151,936, B=1, greedy", "points": rows}
+    gs = np.array([r["gamma"] for r in rows], dtype=np.float64)
+    for key in ("us_cold_l2", "us_warm_l2"):
+        ys = np.array([r[key] for r in rows])
+        slope, icpt = np.polyfit(gs, ys, 1)
+        out[key.replace("us_", "fit_")] = {"us_per_step": float(slope), "entry_us": float(icpt)}
+    return out
 
 
 def measure_config(walk, cfg, B, steps=50, warmup=5):
@@ -508,15 +555,18 @@ def main():
         "clocks": clocks,
         "plan": plan,
     }
-    if args.sweep:
+    if args.sweep or args.gamma_fit:
         w.close()
+    if args.sweep:
         line["sweep"] = [measure_config(walk, c, b) for c in synth.CONFIGS.values()
                          for b in c.batches]
+    if args.gamma_fit:
+        line["gamma_fit"] = gamma_fit(walk)
     if rank == 0 and not args.no_cpu_baseline and not args.only_timed:
         line["cpu_baseline"] = cpu_baseline(cfg, B, rounds, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if not args.sweep:
+    if not (args.sweep or args.gamma_fit):
         w.close()
     if dist:
         dist.barrier()
