@@ -373,34 +373,40 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     ring_issued = pre;
   }
 
-  // tensor-memory tier: global -> registers -> tcgen05.st (warp w writes lane
-  // quarter w % 4, column half w / 4 of every tile)
-  {
-    const int q = warp & 3, h = warp >> 2;
-    const uint4* src = reinterpret_cast<const uint4*>(gw);
-#pragma unroll 1
-    for (int t = 0; t < kTmemTiles; ++t) {
-      // all 16 chunks of this thread's half row in flight at once, then store
-      uint32_t v[4][16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 x = __ldg(src + ((((t * 2 + h) * 16 + c) * 4 + q) * 32 + lane));
-        v[c >> 2][(c & 3) * 4 + 0] = x.x;
-        v[c >> 2][(c & 3) * 4 + 1] = x.y;
-        v[c >> 2][(c & 3) * 4 + 2] = x.z;
-        v[c >> 2][(c & 3) * 4 + 3] = x.w;
-      }
-#pragma unroll
-      for (int part = 0; part < 4; ++part)
-        ptx::tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + t * 128 + 64 * h + part * 16, v[part]);
-    }
-    ptx::tmem_wait_st();
-  }
-  trace_stamp(a, a.gamma, 1);
+  // step 0's base rows: asynchronous copies, in flight during the loads below
+  prefetch_base(ra, 0, row0, nv, base_s);
 
-  // register tier: this warp's RS strips as mma.sync A fragments
-  uint32_t wr[RS][16][4];
+  // tensor-memory tier: global -> registers -> tcgen05.st (warp w writes lane
+  // quarter w % 4, column half w / 4 of every tile).  Tiles 0 and 1 are in
+  // flight together; tile 2 shares its round trip with the register tier.
+  const int tq = warp & 3, th = warp >> 2;
+  const uint4* tsrc = reinterpret_cast<const uint4*>(gw);
+  auto load_tile = [&](int t, uint32_t (&v)[4][16]) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 x = __ldg(tsrc + ((((t * 2 + th) * 16 + c) * 4 + tq) * 32 + lane));
+      v[c >> 2][(c & 3) * 4 + 0] = x.x;
+      v[c >> 2][(c & 3) * 4 + 1] = x.y;
+      v[c >> 2][(c & 3) * 4 + 2] = x.z;
+      v[c >> 2][(c & 3) * 4 + 3] = x.w;
+    }
+  };
+  auto store_tile = [&](int t, uint32_t (&v)[4][16]) {
+#pragma unroll
+    for (int part = 0; part < 4; ++part)
+      ptx::tmem_st16(tmem + ((uint32_t)(32 * tq) << 16) + t * 128 + 64 * th + part * 16, v[part]);
+  };
   {
+    uint32_t v0[4][16], v1[4][16];
+    load_tile(0, v0);
+    load_tile(1, v1);
+    store_tile(0, v0);
+    store_tile(1, v1);
+  }
+  uint32_t wr[RS][16][4];              // register tier: this warp's RS strips as A fragments
+  {
+    uint32_t v2[4][16];
+    load_tile(2, v2);
     const uint4* src = reinterpret_cast<const uint4*>(gw + kTmemWords) +
                        (size_t)(warp * RS) * 16 * 32 + lane;
 #pragma unroll
@@ -413,10 +419,12 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
         wr[s][kt][2] = x.z;
         wr[s][kt][3] = x.w;
       }
+    store_tile(2, v2);
   }
+  ptx::tmem_wait_st();
+  trace_stamp(a, a.gamma, 1);
 
-  // step 0's inputs: base rows and u = W1[anchor]
-  prefetch_base(ra, 0, row0, nv, base_s);
+  // step 0's u = W1[anchor]
   for (int b = warp; b < a.B; b += kResWarps) gather_u_row(a.W1, tok_s[b], b, U, lane);
   if (ra.S > 0 && threadIdx.x == 0) {
     if (!wait_mbar(&mbar[kMbarTma], 0, t_entry, a.timeout_ns)) {
