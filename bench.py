@@ -468,7 +468,7 @@ def main():
 
     sampler.stop()
     clocks = sampler.summary(t0, t1)
-    warm_ms = e2e_us = None
+    warm_ms = e2e_us = graph_warm_ms = None
     e2e_n = 0
     if not args.only_timed:
         # warm L2 (back-to-back, no flush): W2 stays in L2 across rounds
@@ -480,6 +480,23 @@ def main():
             we.record(stream)
         torch.cuda.synchronize()
         warm_ms = ws.elapsed_time(we) / args.steps
+
+        # warm L2 through a CUDA graph of back-to-back rounds (how a serving
+        # loop replays the walk): no per-launch host overhead
+        n_graph = min(args.steps, 50)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n_graph):
+                launch(i)
+        g.replay()
+        torch.cuda.synchronize()
+        gs, ge = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gs.record()
+        g.replay()
+        ge.record()
+        torch.cuda.synchronize()
+        graph_warm_ms = gs.elapsed_time(ge) / n_graph
+        del g
 
         # end to end through the C ABI with host buffers (pinned), copies included
         hb = [r.base.pin_memory() for r in rounds[:8]]
@@ -545,6 +562,7 @@ def main():
         "p10_us": float(np.percentile(per, 10)) * 1000.0,
         "p90_us": float(np.percentile(per, 90)) * 1000.0,
         "warm_l2_us": warm_ms * 1000.0 if warm_ms is not None else None,
+        "graph_warm_l2_us": graph_warm_ms * 1000.0 if graph_warm_ms is not None else None,
         "roofline": roof,
         "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
