@@ -56,6 +56,17 @@ class Oracle:
             _u16p, _i32p, _f32p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_void_p, _i32p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
         ]
+        L.orc_walk2.restype = ctypes.c_int
+        L.orc_walk2.argtypes = [
+            _u16p, _u16p, ctypes.c_int64, ctypes.c_int,
+            _u16p, _i32p, _f32p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_int, _i32p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+        ]
+        L.orc_group_uniforms.restype = None
+        L.orc_group_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int64, ctypes.POINTER(ctypes.c_float),
+                                         ctypes.POINTER(ctypes.c_float)]
         self.L = L
         self.path = path
 
@@ -91,15 +102,18 @@ class Oracle:
         return float(self.L.orc_sample_score(logit_bits, T, g))
 
     def walk(self, W1, W2, base, anchor, temperature, seed, forced=None,
-             want_logits=True, want_scores=False, nthreads=1, req0=0):
+             want_logits=True, want_scores=False, nthreads=1, req0=0, sampler=0,
+             want_groups=False):
         """Run the walk for every request.
 
         W1, W2: uint16 [V, r]; base: uint16 [B, gamma, V]; anchor: int32 [B];
         temperature: float32 [B]; forced: optional int32 [B, gamma] (step
         k > 0 takes prev = forced[b, k-1]); req0: request index of row 0 (row
-        i draws request req0 + i's noise).  Returns (tokens int32 [B, gamma],
-        logits uint16 [B, gamma, V] or None, scores float32 [B, gamma, V] or
-        None).
+        i draws request req0 + i's noise); sampler: 0 per-token Gumbel-max, 1
+        group inverse-CDF.  Returns (tokens int32 [B, gamma], logits uint16
+        [B, gamma, V] or None, scores float32 [B, gamma, V] or None), and with
+        want_groups a 4th item (group scores float32, in-group picks int32,
+        pick margins float32, each [B, gamma, ceil(V / 8)]).
         """
         W1 = np.ascontiguousarray(W1, dtype=np.uint16)
         W2 = np.ascontiguousarray(W2, dtype=np.uint16)
@@ -115,21 +129,39 @@ class Oracle:
         tokens = np.zeros((B, gamma), dtype=np.int32)
         logits = np.zeros((B, gamma, V), dtype=np.uint16) if want_logits else None
         scores = np.zeros((B, gamma, V), dtype=np.float32) if want_scores else None
+        ng = (V + 7) // 8
+        groups = None
+        if want_groups:
+            groups = (np.zeros((B, gamma, ng), dtype=np.float32),
+                      np.zeros((B, gamma, ng), dtype=np.int32),
+                      np.zeros((B, gamma, ng), dtype=np.float32))
         forced_arr = None
         if forced is not None:
             forced_arr = np.ascontiguousarray(forced, dtype=np.int32)
             if forced_arr.shape != (B, gamma):
                 raise ValueError("forced must be [B, gamma]")
-        rc = self.L.orc_walk(
+        rc = self.L.orc_walk2(
             W1, W2, V, r, base, anchor, temperature, int(seed) & (2**64 - 1), B, gamma,
             int(req0), forced_arr.ctypes.data if forced_arr is not None else None,
-            tokens,
+            int(sampler), tokens,
             logits.ctypes.data if logits is not None else None,
             scores.ctypes.data if scores is not None else None,
+            groups[0].ctypes.data if groups is not None else None,
+            groups[1].ctypes.data if groups is not None else None,
+            groups[2].ctypes.data if groups is not None else None,
             int(nthreads))
         if rc != 0:
             raise OracleError("oracle walk rejected its input (code %d)" % rc)
+        if want_groups:
+            return tokens, logits, scores, groups
         return tokens, logits, scores
+
+    def group_uniforms(self, seed, b, k, j):
+        """The two uniforms (U1, U2) of group j of request b at step k (sampler 1)."""
+        u1, u2 = ctypes.c_float(), ctypes.c_float()
+        self.L.orc_group_uniforms(int(seed) & (2**64 - 1), int(b), int(k), int(j),
+                                  ctypes.byref(u1), ctypes.byref(u2))
+        return u1.value, u2.value
 
 
 _default = None

@@ -36,6 +36,20 @@
  *    every operation rounded to fp32 (each fp64 result below is rounded to
  *    fp32 at the same points).  T == 0 selects greedy argmax of the bf16
  *    logits with no noise drawn; T < 0 or a non-finite T is an error.
+ *
+ * A second sampler (orc_walk2, sampler = 1) follows the large-batch scheme of
+ * the same blog post, section "The idea: make the walk resident" (an inverse
+ * CDF inside 8-row groups, Gumbel-max across the groups) with the in-group
+ * step of vLLM pull request #64442, section "Details" (a uniform times the
+ * group's mass, the first token whose running sum of fp32 weights passes it).
+ * Readings: groups are the 8 consecutive tokens 8j .. 8j + 7 (the last group
+ * stops at V); z_v = logit_v / T; m_j = the group's largest z; weights
+ * w_v = exp(z_v - m_j) and mass S_j = their sum; group score
+ * s_j = m_j + log(S_j) - log(-log U1_j); the group with the largest score
+ * wins (ties: the smallest j) and its token is the first v whose running sum
+ * of weights exceeds U2_j * S_j; the two uniforms of group j are the Philox
+ * words 2 (j & 1) and 2 (j & 1) + 1 of counter (j >> 1, k, b, 1).  All of it
+ * in fp64.  Tokens then follow softmax(logit / T) as well.
  */
 #include <math.h>
 #include <stdint.h>
@@ -156,6 +170,99 @@ float orc_sample_score(uint16_t logit, float T, float g)
     return (float)((double)q + (double)g);                 /* fp32 sum */
 }
 
+
+/* ------------------------------------------------------ group sampler --- */
+
+/* The two uniforms of group j of request b at step k (see the header). */
+void orc_group_uniforms(uint64_t seed, int b, int k, int64_t j, float *U1, float *U2)
+{
+    uint32_t ctr[4] = {(uint32_t)(j >> 1), (uint32_t)k, (uint32_t)b, 1u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    orc_philox4x32_10(ctr, key, out);
+    *U1 = orc_uniform(out[2 * (j & 1)]);
+    *U2 = orc_uniform(out[2 * (j & 1) + 1]);
+}
+
+/*
+ * Group inverse-CDF sampling of one row of bf16 logits at temperature T > 0.
+ * Returns the token; per group j (ng = ceil(V / 8) groups) it stores the
+ * group score, the in-group pick and the pick's margin: the distance of
+ * U2_j * S_j to the nearest running-sum boundary, relative to S_j.
+ */
+int64_t orc_group_sample(const uint16_t *logit, int64_t V, float T, uint64_t seed, int b,
+                         int k, float *gscore, int32_t *gpick, float *gmargin)
+{
+    const int64_t ng = (V + 7) / 8;
+    int64_t best_j = 0;
+    double best_s = -INFINITY;
+    for (int64_t j = 0; j < ng; ++j) {
+        const int64_t v0 = 8 * j;
+        const int n = (int)(V - v0 < 8 ? V - v0 : 8);
+        double z[8], w[8];
+        double m = -INFINITY;
+        for (int i = 0; i < n; ++i) {
+            z[i] = orc_bf16_to_f64(logit[v0 + i]) / (double)T;
+            if (z[i] > m)
+                m = z[i];
+        }
+        double S = 0.0;
+        for (int i = 0; i < n; ++i) {
+            w[i] = exp(z[i] - m);
+            S += w[i];
+        }
+        float U1, U2;
+        orc_group_uniforms(seed, b, k, j, &U1, &U2);
+        const double s = m + log(S) - log(-log((double)U1));
+        const double target = (double)U2 * S;
+        double run = 0.0, margin = INFINITY;
+        int pick = n - 1;
+        for (int i = 0; i < n; ++i) {
+            run += w[i];
+            const double d = fabs(run - target) / S;
+            if (d < margin)
+                margin = d;
+            if (run > target) {
+                pick = i;
+                break;
+            }
+        }
+        if (gscore)
+            gscore[j] = (float)s;
+        if (gpick)
+            gpick[j] = (int32_t)(v0 + pick);
+        if (gmargin)
+            gmargin[j] = (float)margin;
+        if (s > best_s) {
+            best_s = s;
+            best_j = j;
+        }
+    }
+    /* the winner's pick, recomputed so that the return does not depend on gpick */
+    const int64_t v0 = 8 * best_j;
+    const int n = (int)(V - v0 < 8 ? V - v0 : 8);
+    double z[8], w[8], m = -INFINITY, S = 0.0;
+    for (int i = 0; i < n; ++i) {
+        z[i] = orc_bf16_to_f64(logit[v0 + i]) / (double)T;
+        if (z[i] > m)
+            m = z[i];
+    }
+    for (int i = 0; i < n; ++i) {
+        w[i] = exp(z[i] - m);
+        S += w[i];
+    }
+    float U1, U2;
+    orc_group_uniforms(seed, b, k, best_j, &U1, &U2);
+    const double target = (double)U2 * S;
+    double run = 0.0;
+    for (int i = 0; i < n; ++i) {
+        run += w[i];
+        if (run > target)
+            return v0 + i;
+    }
+    return v0 + n - 1;
+}
+
 /* ---------------------------------------------------------------- walk --- */
 
 /*
@@ -173,18 +280,24 @@ float orc_sample_score(uint16_t logit, float T, float g)
  *              walk on its own)
  *   out_tokens [B, gamma] int32
  *   out_logits optional [B, gamma, V] bf16 bits
+ *   sampler    0: per-token Gumbel-max; 1: group inverse-CDF (see the header)
  *   out_scores optional [B, gamma, V] fp32 selection scores (the bf16 logit
- *              itself when T == 0)
+ *              itself when T == 0, and for every token under sampler 1)
+ *   out_gscore, out_gpick, out_gmargin  optional [B, gamma, ceil(V / 8)]:
+ *              under sampler 1 with T > 0, each group's score, in-group pick
+ *              and the pick's margin (see orc_group_sample)
  *   nthreads   OpenMP threads for the loop over tokens (<= 0: all)
  *
- * Returns 0, or a negative code (invalid sizes, anchor or temperature).
+ * Returns 0, or a negative code (invalid sizes, sampler, anchor or temperature).
  */
-int orc_walk(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
-             const uint16_t *base, const int32_t *anchor, const float *T,
-             uint64_t seed, int B, int gamma, int req0, const int32_t *forced,
-             int32_t *out_tokens, uint16_t *out_logits, float *out_scores,
-             int nthreads)
+int orc_walk2(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
+              const uint16_t *base, const int32_t *anchor, const float *T,
+              uint64_t seed, int B, int gamma, int req0, const int32_t *forced,
+              int sampler, int32_t *out_tokens, uint16_t *out_logits, float *out_scores,
+              float *out_gscore, int32_t *out_gpick, float *out_gmargin, int nthreads)
 {
+    if (sampler != 0 && sampler != 1)
+        return ORC_EINVAL;
     if (V <= 0 || r <= 0 || B < 0 || gamma < 0 || req0 < 0)
         return ORC_EINVAL;
     for (int b = 0; b < B; ++b) {
@@ -225,7 +338,7 @@ int orc_walk(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
                 uint16_t lg = orc_bf16_rne(orc_bf16_to_f64(bk[v]) +
                                            orc_bf16_to_f64(bias)); /* second */
                 logit[v] = lg;
-                if (Tb == 0.0f) {
+                if (Tb == 0.0f || sampler == 1) {
                     score[v] = orc_bf16_to_f64(lg);
                 } else {
                     float U = orc_uniform(orc_noise_bits(seed, req0 + b, k, v));
@@ -233,9 +346,18 @@ int orc_walk(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
                 }
             }
             int64_t best = 0;                              /* ties: lowest v */
-            for (int64_t v = 1; v < V; ++v)
-                if (score[v] > score[best])
-                    best = v;
+            if (sampler == 1 && Tb > 0.0f) {
+                const int64_t ng = (V + 7) / 8;
+                const int64_t go = ((int64_t)b * gamma + k) * ng;
+                best = orc_group_sample(logit, V, Tb, seed, req0 + b, k,
+                                        out_gscore ? out_gscore + go : NULL,
+                                        out_gpick ? out_gpick + go : NULL,
+                                        out_gmargin ? out_gmargin + go : NULL);
+            } else {
+                for (int64_t v = 1; v < V; ++v)
+                    if (score[v] > score[best])
+                        best = v;
+            }
             out_tokens[(int64_t)b * gamma + k] = (int32_t)best;
             if (out_logits)
                 memcpy(out_logits + ((int64_t)b * gamma + k) * V, logit,
@@ -262,4 +384,15 @@ void orc_philox_many(const uint32_t *ctr, const uint32_t *key, uint32_t *out, in
 {
     for (int64_t i = 0; i < n; ++i)
         orc_philox4x32_10(ctr + 4 * i, key + 2 * i, out + 4 * i);
+}
+
+/* The per-token Gumbel-max walk (sampler 0) with the original argument list. */
+int orc_walk(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
+             const uint16_t *base, const int32_t *anchor, const float *T,
+             uint64_t seed, int B, int gamma, int req0, const int32_t *forced,
+             int32_t *out_tokens, uint16_t *out_logits, float *out_scores,
+             int nthreads)
+{
+    return orc_walk2(W1, W2, V, r, base, anchor, T, seed, B, gamma, req0, forced, 0,
+                     out_tokens, out_logits, out_scores, NULL, NULL, NULL, nthreads);
 }

@@ -184,6 +184,10 @@ def philox_reference():
     ctr[:64, 1] %= 16
     ctr[:64, 2] %= 256
     ctr[:64, 3] = 0
+    # the group sampler's counters (j >> 1, k, b, 1)
+    ctr[64:96, 1] %= 16
+    ctr[64:96, 2] %= 256
+    ctr[64:96, 3] = 1
     key[:8] = [[1234, 0], [0, 0], [1, 0], [0xFFFFFFFF, 0xFFFFFFFF],
                [1234, 1], [7, 9], [2**31, 5], [42, 42]]
     env = dict(os.environ, TRITON_INTERPRET="1")
@@ -496,10 +500,78 @@ def pin_errors(O):
         raise AssertionError("anchor=%r T=%r was accepted" % (anchor, T))
 
 
+
+def pin_group_layout(O):
+    """Group j of request b at step k takes its two uniforms from words 2(j&1)
+    and 2(j&1)+1 of counter (j >> 1, k, b, 1)."""
+    ctr, key, want = philox_reference()
+    for i in range(64, 96):
+        c0, k, b, c3 = (int(x) for x in ctr[i])
+        assert c3 == 1
+        seed = int(key[i, 0]) | (int(key[i, 1]) << 32)
+        for par in range(2):
+            j = 2 * c0 + par
+            u1, u2 = O.group_uniforms(seed, b, k, j)
+            assert u1 == O.uniform(int(want[i, 2 * par])) and \
+                u2 == O.uniform(int(want[i, 2 * par + 1])), \
+                "group uniforms of (b=%d,k=%d,j=%d) wrong" % (b, k, j)
+
+
+def pin_group_sampling_law(O):
+    """Group inverse-CDF sampling: tokens follow softmax(logit / T) (chi-square,
+    120,000 draws), with full and ragged last groups."""
+    from scipy import stats
+    r, n = 4, 120000
+    for V in (12, 20):
+        base_row = torch.linspace(-1.5, 1.2, V).to(torch.bfloat16)
+        W = np.zeros((V, r), np.uint16)
+        base = np.broadcast_to(base_row.view(torch.int16).numpy().view(np.uint16),
+                               (n, 1, V)).copy()
+        anchor = np.zeros(n, np.int32)
+        for T in (0.6, 1.0):
+            t, _, _ = O.walk(W, W, base, anchor, np.full(n, T, np.float32), 2025, nthreads=0,
+                             sampler=1)
+            counts = np.bincount(t[:, 0], minlength=V)
+            p = _softmax(base_row.float().numpy().astype(np.float64) / T)
+            res = stats.chisquare(counts, p * n)
+            assert res.pvalue > 1e-3, "V=%d T=%g: group sampler off softmax (p=%g)" % (
+                V, T, res.pvalue)
+
+
+def pin_group_t_to_zero(O):
+    """Group sampler: as T -> 0+ the sample becomes the greedy argmax."""
+    import synth
+    x = synth.make_custom(V=300, gamma=3, B=4, seed=12)
+    bits = synth.bits
+    tg, lg, _ = O.walk(bits(x.W1), bits(x.W2), bits(x.base), x.anchor.numpy(),
+                       np.zeros(4, np.float32), 0)
+    vals = np.sort(_from_bits(lg), axis=2)
+    gap = (vals[:, :, -1] - vals[:, :, -2]).min()
+    assert gap > 0, "pick a tie-free seed"
+    T = float(gap / 100.0)
+    ts, _, _ = O.walk(bits(x.W1), bits(x.W2), bits(x.base), x.anchor.numpy(),
+                      np.full(4, T, np.float32), 77, sampler=1)
+    assert np.array_equal(ts, tg), "group sampler: T -> 0+ must give the greedy walk"
+
+
+def pin_group_batch_independence(O):
+    """Group sampler: a request's walk is the same alone and in a batch."""
+    import synth
+    x = synth.make_custom(V=777, gamma=4, B=5, seed=8, temperatures=(1.0, 0.6, 0.0))
+    bits = synth.bits
+    t, _, _ = O.walk(bits(x.W1), bits(x.W2), bits(x.base), x.anchor.numpy(),
+                     x.temperature.numpy(), 31, sampler=1)
+    for b in range(5):
+        tb, _, _ = O.walk(bits(x.W1), bits(x.W2), bits(x.base[b:b + 1]),
+                          x.anchor.numpy()[b:b + 1], x.temperature.numpy()[b:b + 1], 31,
+                          req0=b, sampler=1)
+        assert np.array_equal(tb[0], t[b]), "request %d differs alone vs in the batch" % b
+
 ALL_PINS = [
     pin_bf16_hand, pin_bf16_vs_torch, pin_bf16_vs_search,
     pin_philox_vs_triton, pin_noise_layout, pin_uniform, pin_gumbel,
     pin_hand_walk, pin_fig2_bruteforce, pin_w2_zero, pin_spike,
     pin_batch_independence, pin_permutation, pin_sampling_law, pin_t_to_zero,
-    pin_forced, pin_errors,
+    pin_forced, pin_errors, pin_group_layout, pin_group_sampling_law, pin_group_t_to_zero,
+    pin_group_batch_independence,
 ]

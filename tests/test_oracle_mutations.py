@@ -33,6 +33,15 @@ MUTATIONS = {
                                "* (double)T); /* fp32 quotient */"),
     "ties_away_from_zero": ("(frac == 0.5 && fmod(n, 2.0) != 0.0)", "(frac == 0.5)"),
     "truncating_round": ("if (frac > 0.5 ||", "if (0 &&"),
+    # group sampler
+    "group_mass_dropped": ("const double s = m + log(S) - log(-log((double)U1));",
+                           "const double s = m - log(-log((double)U1));"),
+    "group_max_dropped": ("const double s = m + log(S) - log(-log((double)U1));",
+                          "const double s = log(S) - log(-log((double)U1));"),
+    "group_pick_uses_U1": ("    const double target = (double)U2 * S;\n    double run = 0.0;\n",
+                           "    const double target = (double)U1 * S;\n    double run = 0.0;\n"),
+    "group_counter_word": ("{(uint32_t)(j >> 1), (uint32_t)k, (uint32_t)b, 1u}",
+                           "{(uint32_t)(j >> 1), (uint32_t)k, (uint32_t)b, 0u}"),
 }
 
 
