@@ -192,6 +192,29 @@ int dspark_walk_set_kernel(dspark_walk_t h, int kernel);
 int dspark_walk_set_seed_mode(dspark_walk_t h, int mode);
 
 /*
+ * dspark_walk_set_sampler -- how later runs sample requests with T > 0.
+ *   DSPARK_SAMPLER_GUMBEL (default): per-token Gumbel-max, every token's score
+ *     fp32(logit / T) - log(-log U) with U from Philox counter (v >> 2, k, b, 0)
+ *     word v & 3 ("Keeping the Draft Walk on Chip...", section "The idea: make
+ *     the walk resident").
+ *   DSPARK_SAMPLER_GROUP: the same page's large-batch sampler, an inverse CDF
+ *     inside groups of 8 consecutive tokens and Gumbel-max across the groups,
+ *     with vLLM pull request #64442's in-group step (section "Details"): for
+ *     group j, z = logit / T, m = max z, weights exp(z - m) of mass S; group
+ *     score m + log S - log(-log U1); inside the winning group the first token
+ *     whose running sum of weights exceeds U2 * S.  U1, U2 are words 2 (j & 1)
+ *     and 2 (j & 1) + 1 of Philox counter (j >> 1, k, b, 1).  Tokens follow
+ *     softmax(logit / T) as under Gumbel-max, but they are other draws; T = 0
+ *     requests are greedy either way.  One Philox call serves 16 tokens and each
+ *     token costs one exp instead of two logs.  Runs that would take the
+ *     streamed kernel (DSPARK_KERNEL_STREAM) return DSPARK_EUNSUPPORTED.
+ * DSPARK_EINVAL for another value.
+ */
+#define DSPARK_SAMPLER_GUMBEL 0
+#define DSPARK_SAMPLER_GROUP 1
+int dspark_walk_set_sampler(dspark_walk_t h, int sampler);
+
+/*
  * dspark_walk_round -- the handle's round counter n (see set_seed_mode):
  * synchronises `stream` (a cudaStream_t; NULL = legacy default stream), then
  * reads it into *round.

@@ -29,6 +29,7 @@ struct dspark_walk {
   int res_max_B = 0;              // 0: no resident layout
   bool use_resident = true;       // dspark_walk_set_kernel
   int seed_per_round = 0;         // dspark_walk_set_seed_mode
+  int sampler = 0;                // dspark_walk_set_sampler
   int res_RS = 0, res_NT = 0, res_R = 0, res_S = 0, res_ST = 0, res_nslot = 0, res_n_cta = 0;
   int64_t res_wpc = 0;
   size_t res_smem = 0;
@@ -184,6 +185,7 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
   a.seed_lo = (uint32_t)seed;
   a.seed_hi = (uint32_t)(seed >> 32);
   a.seed_per_round = h->seed_per_round;
+  a.sampler = h->sampler;
   a.timeout_ns = h->timeout_ns;
   a.skip_cta = h->skip_cta;
   {
@@ -219,6 +221,9 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
     return DSPARK_OK;
   }
 
+  // the streamed kernel scores one token per lane: the group sampler (8
+  // consecutive tokens per group) is not available there
+  if (h->sampler != DSPARK_SAMPLER_GUMBEL) return DSPARK_EUNSUPPORTED;
   const void* fn = stream_kernel_for(B);
   const size_t smem = stream_smem_bytes(B);  // <= the maximum set at create
   void* args[] = {&a};
@@ -286,12 +291,16 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
     h->sync.max_B = max_B;
     plan_stream(h);
     // every instantiation may use the shared memory of max_B, and one CTA
-    // per SM must fit
+    // per SM must fit.  A kernel's shared-memory limit is one setting for the
+    // whole process, shared by every handle (and the allocation-free entry):
+    // it is raised to what the largest batch needs, never lowered to this
+    // handle's need.
     const size_t smem = stream_smem_bytes(max_B);
     for (int b = 1; b <= 8 && rc == DSPARK_OK; b *= 2) {
       int per_sm = 0;
       const void* fn = stream_kernel_for(b);
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)stream_smem_bytes(kMaxB));
       if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, stream_threads(), smem);
       if (e != cudaSuccess) rc = cuda_fail(e);
@@ -311,7 +320,7 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
       int per_sm = 0;
       const void* fn = resident_kernel_for(h->res_RS, h->res_NT);
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)h->res_smem);
+                               (int)kSmemBudget);
       if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, resident_threads(),
                                                           h->res_smem);
@@ -437,6 +446,13 @@ int dspark_walk_set_kernel(dspark_walk_t h, int kernel) {
 int dspark_walk_set_seed_mode(dspark_walk_t h, int mode) {
   if (!h || (mode != DSPARK_SEED_FIXED && mode != DSPARK_SEED_PER_ROUND)) return DSPARK_EINVAL;
   h->seed_per_round = mode == DSPARK_SEED_PER_ROUND ? 1 : 0;
+  return DSPARK_OK;
+}
+
+int dspark_walk_set_sampler(dspark_walk_t h, int sampler) {
+  if (!h || (sampler != DSPARK_SAMPLER_GUMBEL && sampler != DSPARK_SAMPLER_GROUP))
+    return DSPARK_EINVAL;
+  h->sampler = sampler;
   return DSPARK_OK;
 }
 

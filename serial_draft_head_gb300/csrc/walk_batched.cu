@@ -183,7 +183,8 @@ __device__ __forceinline__ uint32_t add_bf16x2(uint32_t x, uint32_t y) {
 // smallest id.  Tokens at or past V do not take part.  `kind` is the same for
 // the whole warp: 0 = every live lane greedy (score = logit); 1 = noise drawn
 // for every lane (one Philox call per four tokens) and used where T > 0;
-// 2 = as 1, with the IEEE quotient where 1/T overflows.
+// 2 = as 1, with the IEEE quotient where 1/T overflows; 3 = the group sampler
+// (the 8 tokens are one group: group_key) where T > 0, greedy elsewhere.
 __device__ __forceinline__ unsigned long long score8(const WalkArgs& a, const PhiloxKeys& pk,
                                                      int k, int b, float T, float inv_T,
                                                      int64_t v0, const uint4& bz,
@@ -210,8 +211,10 @@ __device__ __forceinline__ unsigned long long score8(const WalkArgs& a, const Ph
         if (i < nvalid) dst[i] = (uint16_t)(lw[i >> 1] >> (16 * (i & 1)));
     }
   }
+  if (kind == 3 && T > 0.0f)
+    return group_key(lg, nvalid < 8 ? (int)nvalid : 8, T, inv_T, (uint32_t)v0, k, b, pk);
   float sc[8];
-  if (kind == 0) {
+  if (kind == 0 || kind == 3) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) sc[i] = lg[i];
   } else {
@@ -479,9 +482,11 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
           const bool live = cb + jl < act;
           const int c = c0 + cb + jl;
           const float Tc = live ? tcol[c] : 0.0f, iTc = live ? icol[c] : 1.0f;
-          const int kind = __any_sync(0xFFFFFFFFu, Tc > 0.0f)
-                               ? (__any_sync(0xFFFFFFFFu, Tc > 0.0f && iTc == 0.0f) ? 2 : 1)
-                               : 0;
+          const int kind =
+              __any_sync(0xFFFFFFFFu, Tc > 0.0f)
+                  ? (a.sampler == 1 ? 3
+                                    : (__any_sync(0xFFFFFFFFu, Tc > 0.0f && iTc == 0.0f) ? 2 : 1))
+                  : 0;
           if (live) best = score8(a, pk, k, (int)col2req[c], Tc, iTc, v0, bz, cur, vec, kind);
           unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, 8);
           best = o > best ? o : best;

@@ -88,6 +88,7 @@ struct WalkArgs {
   int rows_per_cta;            // shard size (last shard may be shorter)
   uint32_t seed_lo, seed_hi;   // Philox key (see round_seed)
   int seed_per_round;          // add the handle's round counter to the key
+  int sampler;                 // 0: per-token Gumbel-max; 1: group inverse-CDF
   int64_t timeout_ns;          // rendezvous wait limit
   int skip_cta;                // fault injection: this CTA never posts (-1: off)
   unsigned long long* trace;   // optional [n_cta][gamma + 1][8] SM-clock stamps
@@ -265,6 +266,64 @@ __device__ __forceinline__ float gumbel_noise(uint32_t x) {
 __device__ __forceinline__ float gumbel_score(float logit, float T, float inv_T, uint32_t x) {
   const float q = inv_T != 0.0f ? __fmul_rn(logit, inv_T) : __fdiv_rn(logit, T);
   return __fadd_rn(q, gumbel_noise(x));
+}
+
+// exp2 by the hardware approximation, subnormal results flushed.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Group inverse-CDF sampling ("Keeping the Draft Walk on Chip...", section
+// "The idea: make the walk resident": an inverse CDF inside 8-row groups and
+// Gumbel-max across them; vLLM pull request #64442, section "Details": a
+// uniform times the mass picks the first token whose running sum of fp32
+// weights passes it).  For the group j of tokens v0 = 8j .. v0 + n - 1 of
+// request b at step k, with fp32 logits lg: z = logit / T (product with
+// fl(1/T) unless that overflows), m = max z, weights w = exp(z - m), mass S;
+// score = m + log S - log(-log U1); pick = the first token whose running sum
+// of weights exceeds U2 * S (the last one if rounding leaves none).  U1, U2 are
+// the words 2 (j & 1) and 2 (j & 1) + 1 of Philox counter (j >> 1, k, b, 1).
+// Returns the group's selection key {ord32(score), inverted id of the pick}.
+__device__ __forceinline__ unsigned long long group_key(const float (&lg)[8], int n, float T,
+                                                        float inv_T, uint32_t v0, int k, int b,
+                                                        const PhiloxKeys& pk) {
+  float z[8];
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float q = inv_T != 0.0f ? __fmul_rn(lg[i], inv_T) : __fdiv_rn(lg[i], T);
+    z[i] = i < n ? q : -INFINITY;
+    m = fmaxf(m, z[i]);
+  }
+  float w[8];
+  float S = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    w[i] = i < n ? ex2_approx(__fmul_rn(__fsub_rn(z[i], m), 1.4426950408889634f)) : 0.0f;
+    S = __fadd_rn(S, w[i]);
+  }
+  const uint32_t j = v0 >> 3;
+  const uint4 r = philox4x32_10(make_uint4(j >> 1, (uint32_t)k, (uint32_t)b, 1u), pk);
+  const uint32_t x1 = (j & 1u) ? r.z : r.x;
+  const uint32_t x2 = (j & 1u) ? r.w : r.y;
+  const float score =
+      __fadd_rn(__fadd_rn(m, 0.693147180559945f * lg2_approx(S)), gumbel_noise(x1));
+  const float target = __fmul_rn(bits_to_uniform(x2), S);
+  float run = 0.0f;
+  int pick = n - 1;
+  float runs[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    run = __fadd_rn(run, w[i]);
+    runs[i] = run;
+  }
+#pragma unroll
+  for (int i = 7; i >= 0; --i)
+    if (i < n && runs[i] > target) pick = i;
+  return ((unsigned long long)ord32(score) << 32) |
+         (unsigned long long)(0xFFFFFFFFu - (v0 + (uint32_t)pick));
 }
 
 // fl(1/T) for T > 0, or 0 when it overflows (T below 2^-126).

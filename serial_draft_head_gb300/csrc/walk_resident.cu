@@ -228,7 +228,25 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
     uint16_t* outl =
         a.out_logits ? a.out_logits + ((size_t)b * a.gamma + k) * (size_t)a.V : nullptr;
     // separate loops: one loop with a select would evaluate the noise always
-    if (T > 0.0f) {
+    if (T > 0.0f && a.sampler == 1) {
+      // group sampler: one group of 8 rows (16 bytes of logits) per iteration
+      const PhiloxKeys pk = philox_keys(seed.x, seed.y);
+      for (int c = gi; 8 * c < nv; c += tpr) {
+        const int rl0 = 8 * c;
+        const uint4 w = *reinterpret_cast<const uint4*>(ls + rl0);
+        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+        float lg[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          lg[e] = bf16_bits_to_float((wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+        const int n = nv - rl0 < 8 ? nv - rl0 : 8;
+        const uint32_t v0 = (uint32_t)(row0 + rl0);     // a multiple of 8
+        const unsigned long long key = group_key(lg, n, T, inv_T, v0, k, b, pk);
+        best = key > best ? key : best;
+        if (outl)
+          for (int e = 0; e < n; ++e) outl[v0 + e] = (uint16_t)((wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+      }
+    } else if (T > 0.0f) {
       const PhiloxKeys pk = philox_keys(seed.x, seed.y);
       // the quotient by the rounded reciprocal unless 1/T overflows
       best = inv_T != 0.0f

@@ -30,6 +30,9 @@ KERNEL_BATCHED = 2
 SEED_FIXED = 0
 SEED_PER_ROUND = 1
 
+SAMPLER_GUMBEL = 0
+SAMPLER_GROUP = 1
+
 _lib = None
 
 
@@ -60,7 +63,7 @@ EXPORTS = [
     "dspark_walk_get_plan", "dspark_walk_set_limits", "dspark_walk_strerror",
     "dspark_walk_destroy", "dspark_walk_run_noalloc", "dspark_walk_set_kernel",
     "dspark_walk_set_trace", "dspark_walk_set_seed_mode", "dspark_walk_round",
-    "dspark_walk_gumbel_noise",
+    "dspark_walk_gumbel_noise", "dspark_walk_set_sampler",
 ]
 
 
@@ -93,6 +96,7 @@ def load(build_if_missing=True):
     L.dspark_walk_set_trace.argtypes = [vp, vp, i64]
     L.dspark_walk_run_noalloc.argtypes = [vp, vp, i64, i32, vp, vp, vp, u64, vp, i32, i32, vp, vp]
     L.dspark_walk_set_seed_mode.argtypes = [vp, i32]
+    L.dspark_walk_set_sampler.argtypes = [vp, i32]
     L.dspark_walk_round.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint64)]
     L.dspark_walk_gumbel_noise.argtypes = [vp, vp, i64, vp]
     for name in EXPORTS:
@@ -177,6 +181,10 @@ def dspark_walk_set_seed_mode(h, mode):
     return _check(load().dspark_walk_set_seed_mode(h, int(mode)), "dspark_walk_set_seed_mode")
 
 
+def dspark_walk_set_sampler(h, sampler):
+    return _check(load().dspark_walk_set_sampler(h, int(sampler)), "dspark_walk_set_sampler")
+
+
 def dspark_walk_round(h, stream=None):
     r = ctypes.c_uint64(0)
     _check(load().dspark_walk_round(h, _stream(stream), ctypes.byref(r)), "dspark_walk_round")
@@ -233,6 +241,9 @@ class Walk:
 
     def set_seed_mode(self, mode):
         dspark_walk_set_seed_mode(self.h, mode)
+
+    def set_sampler(self, sampler):
+        dspark_walk_set_sampler(self.h, sampler)
 
     def round(self, stream=None):
         return dspark_walk_round(self.h, stream)

@@ -80,10 +80,22 @@ class Report:
                                      self.near_ties, len(self.failures), self.failures[:5]))
 
 
+# Group sampler (sampler = 1): the GPU's group score carries fp32 errors of a
+# few ulp of |logit / T| plus the noise error (<= 0.08 of 2^-18 (1 + |g|),
+# measured over every uniform) and ~1e-6 from the hardware exp2 / log2; the
+# in-group pick compares running sums of fp32 weights with U2 * S, each within
+# ~2e-6 S of the fp64 values.  The bounds below are about 8x those.
+GROUP_SCORE_TOL = 2.0**-16
+GROUP_PICK_TOL = 1e-5
+
+
 def check(inputs: "synth.WalkInputs", gpu_tokens, gpu_logits=None, requests=None,
-          nthreads=0, O=None, report=None):
+          nthreads=0, O=None, report=None, sampler=0):
     """Check the GPU's tokens [B, gamma] (and logits [B, gamma, V]) for `requests`.
 
+    sampler 0: per-token Gumbel-max; 1: group inverse-CDF (a GPU token may
+    differ from the oracle's only at a group-score near-tie, then being that
+    group's pick, or next to a pick whose running sum sits at the threshold).
     Returns a Report; ``report.ok()`` is the verdict.
     """
     O = O or oracle.default()
@@ -100,7 +112,8 @@ def check(inputs: "synth.WalkInputs", gpu_tokens, gpu_logits=None, requests=None
         if np.any(toks < 0) or np.any(toks >= V):
             rep.failures.append(("token out of range", b, toks.tolist()))
             continue
-        ot, ol, osc = _oracle_request(O, W1, W2, base_all, inputs, b, toks, nthreads)
+        ot, ol, osc, grp = _oracle_request(O, W1, W2, base_all, inputs, b, toks, nthreads,
+                                           sampler)
         rep.steps_checked += gamma
         for k in range(gamma):
             ok_row = ol[k]
@@ -111,6 +124,26 @@ def check(inputs: "synth.WalkInputs", gpu_tokens, gpu_logits=None, requests=None
             g = int(toks[k])
             if g == int(ot[k]):
                 rep.steps_exact += 1
+                continue
+            if T != 0.0 and sampler == 1:
+                gs, gp, gm = grp[0][k], grp[1][k], grp[2][k]
+                o = int(ot[k])
+                jo, jg = o // 8, g // 8
+
+                def near_pick(j, tok):
+                    return tok == int(gp[j]) or (gm[j] <= GROUP_PICK_TOL and
+                                                 abs(tok - int(gp[j])) == 1)
+
+                if jg == jo:
+                    good = near_pick(jo, g)
+                else:
+                    tol = GROUP_SCORE_TOL * (2.0 + abs(float(gs[jo])) + abs(float(gs[jg])))
+                    good = float(gs[jo]) - float(gs[jg]) <= tol and near_pick(jg, g)
+                if good:
+                    rep.near_ties += 1
+                    continue
+                rep.failures.append(("group-sampled token", b, k, g, o, float(gs[jo]),
+                                     float(gs[jg])))
                 continue
             if T == 0.0:
                 vals = bf16_vals(ok_row)
@@ -138,13 +171,17 @@ def check(inputs: "synth.WalkInputs", gpu_tokens, gpu_logits=None, requests=None
     return rep
 
 
-def _oracle_request(O, W1, W2, base_all, inputs, b, toks, nthreads):
+def _oracle_request(O, W1, W2, base_all, inputs, b, toks, nthreads, sampler=0):
     """Oracle walk of request b alone (at request index b), teacher-forced."""
     T = float(inputs.temperature[b])
-    ot, ol, osc = O.walk(W1, W2, base_all[b:b + 1], np.array([inputs.anchor[b]], np.int32),
-                         np.array([T], np.float32), inputs.seed, forced=toks[None, :],
-                         want_scores=T != 0.0, nthreads=nthreads, req0=b)
-    return ot[0], ol[0], (osc[0] if osc is not None else None)
+    group = sampler == 1 and T != 0.0
+    res = O.walk(W1, W2, base_all[b:b + 1], np.array([inputs.anchor[b]], np.int32),
+                 np.array([T], np.float32), inputs.seed, forced=toks[None, :],
+                 want_scores=T != 0.0 and not group, nthreads=nthreads, req0=b,
+                 sampler=sampler, want_groups=group)
+    ot, ol, osc = res[0], res[1], res[2]
+    grp = tuple(a[0] for a in res[3]) if group else None
+    return ot[0], ol[0], (osc[0] if osc is not None else None), grp
 
 
 def _check_logits(O, rep, W1, W2, base_row, gl, ol, prev, b, k):

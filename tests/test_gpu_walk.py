@@ -302,6 +302,25 @@ def test_gumbel_noise_every_uniform(walkmod):
     assert err.max() <= 0.25, (err.max(), int(np.argmax(err)))
 
 
+def test_handles_with_different_shared_memory_needs(walkmod):
+    """A kernel's shared-memory limit is process-wide: creating a handle that
+    needs less must not break a handle (or the allocation-free entry) that
+    needs more."""
+    big = synth.make_custom(V=60000, gamma=2, B=16, seed=43, temperatures=(0.0, 1.0))
+    w_big = make_walk(walkmod, big)                  # resident, two n-tiles
+    w_big_s = make_walk(walkmod, big, kernel="stream")
+    small = synth.make_custom(V=60000, gamma=2, B=1, seed=44)
+    w_small = make_walk(walkmod, small)              # created afterwards, needs less
+    for w in (w_big, w_big_s):
+        st, toks, lg = gpu_run(w, big)
+        assert st == 0
+        assert parity.check(big, toks, lg).ok()
+    st, toks, _ = gpu_run(w_small, small, want_logits=False)
+    assert st == 0 and parity.check(small, toks).ok()
+    for w in (w_big, w_big_s, w_small):
+        w.close()
+
+
 def test_rounds_back_to_back(walkmod):
     """Consecutive rounds with fresh inputs on one handle each match the oracle."""
     cfg_x = synth.make_custom(V=9001, gamma=3, B=2, seed=41, temperatures=(0.0, 0.6))
@@ -393,3 +412,54 @@ def test_lost_arrival_times_out_and_recovers(walkmod):
         st, toks, lg = gpu_run(w, x)
         assert st == 0
         assert parity.check(x, toks, lg).ok()
+
+
+# ---------------------------------------------------- group inverse-CDF --
+
+GROUP_SHAPES = [
+    # V, gamma, B, temperatures, seed
+    (1000, 4, 3, (0.6, 1.0, 0.0), 51),
+    (5003, 5, 8, (1.0, 0.6), 52),                  # ragged last group (5003 = 8 * 625 + 3)
+    (152 * 33 + 17, 3, 17, (0.6, 0.0, 1.0), 53),   # B > 16: the batched kernel
+    (4096, 2, 64, (1.0, 0.6, 0.0), 54),
+    (130000, 2, 2, (1.0,), 55),
+    (200000, 2, 1, (0.6,), 56),                    # the streamed tier
+]
+
+
+@pytest.mark.parametrize("kernel", ["planned", "batched"])
+@pytest.mark.parametrize("V,gamma,B,temps,seed", GROUP_SHAPES)
+def test_group_sampler_every_logit(walkmod, V, gamma, B, temps, seed, kernel):
+    x = synth.make_custom(V=V, gamma=gamma, B=B, seed=seed, temperatures=temps,
+                          noise_seed=2000 + seed)
+    w = make_walk(walkmod, x, kernel=kernel)
+    w.set_sampler(walkmod.SAMPLER_GROUP)
+    st, toks, lg = gpu_run(w, x)
+    assert st == 0, walkmod.dspark_walk_strerror(st)
+    rep = parity.check(x, toks, lg, sampler=1)
+    assert rep.ok(), rep
+    w.close()
+
+
+@pytest.mark.parametrize("B", [16, 64, 253])
+def test_group_sampler_sampled_config(walkmod, B):
+    x = full_inputs("sampled", B)
+    w = full_walk(walkmod, "sampled", x)
+    w.set_sampler(walkmod.SAMPLER_GROUP)
+    try:
+        st, toks, lg = gpu_run(w, x)
+    finally:
+        w.set_sampler(walkmod.SAMPLER_GUMBEL)
+    assert st == 0
+    rep = parity.check(x, toks, lg, requests=_sample_requests(B, (0.0, 0.6, 1.0)), sampler=1)
+    assert rep.ok(), rep
+
+
+def test_group_sampler_not_on_the_streamed_kernel(walkmod):
+    x = synth.make_custom(V=1000, gamma=2, B=2, seed=57, temperatures=(1.0,))
+    w = make_walk(walkmod, x, kernel="stream")
+    w.set_sampler(walkmod.SAMPLER_GROUP)
+    with pytest.raises(walkmod.WalkError) as e:
+        gpu_run(w, x)
+    assert e.value.code == walkmod.EUNSUPPORTED
+    w.close()

@@ -69,3 +69,29 @@ def test_near_tie_rule_accepts_the_runner_up_of_a_tie():
     assert int(t[0, 0]) == 20
     rep = parity.check(x, np.array([[10]], np.int32), lg)
     assert rep.ok() and rep.near_ties == 1
+
+
+def test_group_sampler_accepts_the_oracle_itself():
+    x = synth.make_custom(V=603, gamma=4, B=4, seed=25, temperatures=(0.6, 1.0, 0.0, 1.0),
+                          noise_seed=6)
+    t, lg, _ = _walk(x, sampler=1)
+    rep = parity.check(x, t, lg, sampler=1)
+    assert rep.ok(), rep
+    assert rep.steps_exact == rep.steps_checked
+
+
+def test_group_sampler_rejects_a_token_of_another_group():
+    x = synth.make_custom(V=603, gamma=3, B=2, seed=26, temperatures=(1.0,), noise_seed=10)
+    O = oracle.default()
+    t, lg, _, grp = O.walk(synth.bits(x.W1), synth.bits(x.W2), synth.bits(x.base),
+                           x.anchor.numpy(), x.temperature.numpy(), x.seed, sampler=1,
+                           want_groups=True)
+    # the pick of the group with the lowest score: far from a near-tie
+    k = 1
+    j = int(np.argmin(grp[0][1, k]))
+    t2 = t.copy()
+    t2[1, k] = int(grp[1][1, k, j])
+    rep = parity.check(x, t2, None, sampler=1)
+    assert not rep.ok() and rep.failures[0][0] == "group-sampled token"
+    # and the Gumbel-max rule does not accept the group sampler's walk wholesale
+    assert not parity.check(x, t, None, sampler=0).ok()
