@@ -55,6 +55,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="qwen3_resident", choices=sorted(synth.CONFIGS))
     p.add_argument("--batch", type=int, default=None)
+    p.add_argument("--sampler", default="gumbel", choices=["gumbel", "group"],
+                   help="sampling of T > 0 requests: per-token Gumbel-max (the configs') or the "
+                        "group inverse-CDF sampler")
     p.add_argument("--kernel", default="planned", choices=["planned", "resident", "batched", "stream"],
                    help="force a kernel (dspark_walk_set_kernel); default: the handle's plan")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -285,12 +288,14 @@ def gamma_fit(walk, gammas=(1, 4, 7, 16), steps=100, warmup=5):
     return out
 
 
-def measure_config(walk, cfg, B, steps=50, warmup=5):
+def measure_config(walk, cfg, B, steps=50, warmup=5, sampler="gumbel"):
     """Cold- and warm-L2 us per walk of one workload at batch B (sweep mode)."""
     dev = torch.device("cuda", torch.cuda.current_device())
     W1, W2, _ = synth.make_weights(cfg.V, cfg.r, cfg.seed)
     x = synth.make_inputs(cfg, B=B, round_index=0, weights=(W1, W2))
     w = walk.Walk(W1.to(dev), W2.to(dev), B, cfg.gamma)
+    if sampler == "group":
+        w.set_sampler(walk.SAMPLER_GROUP)
     plan = w.plan()
     base, anchor, temp = x.base.to(dev), x.anchor.to(dev), x.temperature.to(dev)
     tok = torch.empty(B, cfg.gamma, dtype=torch.int32, device=dev)
@@ -316,7 +321,7 @@ def measure_config(walk, cfg, B, steps=50, warmup=5):
     cold = statistics.mean(s.elapsed_time(e) for s, e in ev) * 1000.0
     warm = ws.elapsed_time(we) / steps * 1000.0
     res = {"workload": cfg.name, "V": cfg.V, "gamma": cfg.gamma, "B": B,
-           "temperatures": list(cfg.temperatures), "status": st,
+           "temperatures": list(cfg.temperatures), "sampler": sampler, "status": st,
            "kernel": kernel_label(walk, plan, B),
            "us_cold_l2": cold, "us_warm_l2": warm,
            "eff_w2_GBs_cold": cfg.gamma * cfg.V * cfg.r * 2 * B / (cold * 1e-6) / 1e9}
@@ -415,6 +420,8 @@ def main():
     W1 = W1c.to(dev)
     W2 = W2c.to(dev)
     w = walk.Walk(W1, W2, B, cfg.gamma)
+    if args.sampler == "group":
+        w.set_sampler(walk.SAMPLER_GROUP)
     if args.kernel != "planned":
         w.set_kernel({"resident": walk.KERNEL_RESIDENT, "batched": walk.KERNEL_BATCHED,
                       "stream": walk.KERNEL_STREAM}[args.kernel])
@@ -553,7 +560,7 @@ def main():
         "vs_baseline_note": "value / the pages' 37 us (H100, int8 W2): context on other "
                             "hardware and precision" if (cfg.name, B) in PAGES_US else None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": cfg.note, "V": cfg.V, "r": cfg.r, "gamma": cfg.gamma, "B": B,
+        "config": {"workload": cfg.note, "sampler": args.sampler, "V": cfg.V, "r": cfg.r, "gamma": cfg.gamma, "B": B,
                    "rounds": n_rounds, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "flushed between timed steps (256 MiB write)",
                    "kernel": label, "n_cta": plan["n_cta"] if label != "batched" else None,
@@ -578,6 +585,9 @@ def main():
     if args.sweep:
         line["sweep"] = [measure_config(walk, c, b) for c in synth.CONFIGS.values()
                          for b in c.batches]
+        # the group inverse-CDF sampler on the sampled workload (not the configs' sampler)
+        line["sweep"] += [measure_config(walk, synth.CONFIGS["sampled"], b, sampler="group")
+                          for b in synth.CONFIGS["sampled"].batches]
     if args.gamma_fit:
         line["gamma_fit"] = gamma_fit(walk)
     if rank == 0 and not args.no_cpu_baseline and not args.only_timed:
