@@ -399,6 +399,39 @@ def test_host_side_errors(walkmod):
     assert e.value.code == walkmod.EUNSUPPORTED
 
 
+@pytest.mark.parametrize("kernel", ["planned", "stream", "batched"])
+@pytest.mark.parametrize("V", [1, 2, 7])
+def test_degenerate_vocabularies(walkmod, V, kernel):
+    """V = 1 (every token is 0), V = 2, V = 7 (one ragged group of the group
+    sampler), greedy and sampled requests, on every kernel."""
+    x = synth.make_custom(V=V, gamma=3, B=3, seed=60 + V, temperatures=(0.0, 1.0, 0.6),
+                          noise_seed=60)
+    w = make_walk(walkmod, x, kernel=kernel)
+    st, toks, lg = gpu_run(w, x)
+    assert st == 0
+    assert parity.check(x, toks, lg).ok()
+    if V == 1:
+        assert not toks.any()
+    if kernel != "stream":
+        w.set_sampler(walkmod.SAMPLER_GROUP)
+        st, toks, lg = gpu_run(w, x)
+        assert st == 0
+        assert parity.check(x, toks, lg, sampler=1).ok()
+    w.close()
+
+
+def test_empty_batch_and_walk_are_rejected(walkmod):
+    x = synth.make_custom(V=500, gamma=2, B=2, seed=46)
+    w = make_walk(walkmod, x)
+    base, anchor, temp = x.base.cuda(), x.anchor.cuda(), x.temperature.cuda()
+    tok = torch.empty(2, 2, dtype=torch.int32, device="cuda")
+    for B, gamma in ((0, 2), (2, 0), (-1, 2)):
+        with pytest.raises(walkmod.WalkError) as e:
+            walkmod.dspark_walk_run(w.h, base, anchor, temp, 0, tok, B, gamma)
+        assert e.value.code == walkmod.EINVAL
+    w.close()
+
+
 def test_lost_arrival_times_out_and_recovers(walkmod):
     """A CTA that never posts makes the round end with ETIMEOUT, not hang."""
     x = synth.make_custom(V=8000, gamma=4, B=2, seed=46, temperatures=(0.0, 1.0))
