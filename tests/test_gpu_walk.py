@@ -447,6 +447,25 @@ def test_lost_arrival_times_out_and_recovers(walkmod):
         assert parity.check(x, toks, lg).ok()
 
 
+def test_lost_arrival_with_streamed_tier(walkmod):
+    """A round aborted while streamed chunks are in flight ends with ETIMEOUT
+    (the ring's copies are waited for before the CTAs exit), and the next
+    rounds run clean."""
+    x = synth.make_custom(V=200000, gamma=3, B=1, seed=47, temperatures=(0.6,))
+    w = make_walk(walkmod, x)
+    assert w.plan()["rows_stream"] > 0
+    walkmod.dspark_walk_set_limits(w.h, 50_000_000, 5)      # 50 ms; CTA 5 skips
+    st, toks, _ = gpu_run(w, x, want_logits=False)
+    assert st == walkmod.ETIMEOUT
+    assert np.all(toks == -1)
+    walkmod.dspark_walk_set_limits(w.h, 200_000_000, -1)
+    for _ in range(2):
+        st, toks, lg = gpu_run(w, x)
+        assert st == 0
+        assert parity.check(x, toks, lg).ok()
+    w.close()
+
+
 # ---------------------------------------------------- group inverse-CDF --
 
 GROUP_SHAPES = [
