@@ -1,4 +1,5 @@
-"""CPU oracle of DSpark's serial Markov draft walk (fp64 projection).
+"""CPU oracle of DSpark's serial draft walk (fp64 projection): the Markov head and the
+gated and RNN recurrent heads.
 
 TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg import this package.  It shares no code with the
@@ -63,6 +64,18 @@ class Oracle:
             ctypes.c_void_p, ctypes.c_int, _i32p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
         ]
+        L.orc_walk3.restype = ctypes.c_int
+        L.orc_walk3.argtypes = [
+            _u16p, _u16p, ctypes.c_int64, ctypes.c_int,
+            _u16p, _i32p, _f32p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+            _i32p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+        ]
+        L.orc_cell_update.restype = None
+        L.orc_cell_update.argtypes = [ctypes.c_int, _u16p, ctypes.c_int, ctypes.c_void_p, _u16p,
+                                      _u16p, ctypes.c_void_p]
         L.orc_group_uniforms.restype = None
         L.orc_group_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int64, ctypes.POINTER(ctypes.c_float),
@@ -156,6 +169,68 @@ class Oracle:
             return tokens, logits, scores, groups
         return tokens, logits, scores
 
+    def walk_cell(self, W1, W2, base, anchor, temperature, seed, cell, M=None, forced=None,
+                  forced_state=None, want_logits=True, want_scores=False, nthreads=1, req0=0,
+                  sampler=0):
+        """A recurrent head's walk (cell 1 gated, 2 RNN; 0 is the Markov head).
+
+        M: uint16 [r, r] recurrent matrix; forced_state: optional uint16
+        [B, gamma, r] (step k updates from forced_state[b, k-1] and projects
+        forced_state[b, k]).  Returns (tokens, logits, scores, states uint16
+        [B, gamma, r], states_exact float64 [B, gamma, r]).
+        """
+        W1 = np.ascontiguousarray(W1, dtype=np.uint16)
+        W2 = np.ascontiguousarray(W2, dtype=np.uint16)
+        base = np.ascontiguousarray(base, dtype=np.uint16)
+        anchor = np.ascontiguousarray(anchor, dtype=np.int32)
+        temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+        V, r = W2.shape
+        if W1.shape != (V, r):
+            raise ValueError("W1 and W2 must both be [V, r]")
+        B, gamma, Vb = base.shape
+        if Vb != V or anchor.shape != (B,) or temperature.shape != (B,):
+            raise ValueError("base must be [B, gamma, V]; anchor and temperature [B]")
+        Mc = None
+        if M is not None:
+            Mc = np.ascontiguousarray(M, dtype=np.uint16)
+            if Mc.shape != (r, r):
+                raise ValueError("M must be [r, r]")
+        fs = None
+        if forced_state is not None:
+            fs = np.ascontiguousarray(forced_state, dtype=np.uint16)
+            if fs.shape != (B, gamma, r):
+                raise ValueError("forced_state must be [B, gamma, r]")
+        forced_arr = None
+        if forced is not None:
+            forced_arr = np.ascontiguousarray(forced, dtype=np.int32)
+            if forced_arr.shape != (B, gamma):
+                raise ValueError("forced must be [B, gamma]")
+        tokens = np.zeros((B, gamma), dtype=np.int32)
+        logits = np.zeros((B, gamma, V), dtype=np.uint16) if want_logits else None
+        scores = np.zeros((B, gamma, V), dtype=np.float32) if want_scores else None
+        states = np.zeros((B, gamma, r), dtype=np.uint16)
+        exact = np.zeros((B, gamma, r), dtype=np.float64)
+        ptr = lambda a: a.ctypes.data if a is not None else None
+        rc = self.L.orc_walk3(
+            W1, W2, V, r, base, anchor, temperature, int(seed) & (2**64 - 1), B, gamma,
+            int(req0), ptr(forced_arr), int(sampler), int(cell), ptr(Mc), ptr(fs), tokens,
+            ptr(logits), ptr(scores), None, None, None, ptr(states), ptr(exact), int(nthreads))
+        if rc != 0:
+            raise OracleError("oracle walk rejected its input (code %d)" % rc)
+        return tokens, logits, scores, states, exact
+
+    def cell_update(self, cell, M, hprev, x):
+        """One state update: (h bf16 bits [r], the fp64 values before rounding)."""
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        r = x.shape[0]
+        M = np.ascontiguousarray(M, dtype=np.uint16)
+        hp = None if hprev is None else np.ascontiguousarray(hprev, dtype=np.uint16)
+        h = np.zeros(r, np.uint16)
+        ex = np.zeros(r, np.float64)
+        self.L.orc_cell_update(int(cell), M, r, hp.ctypes.data if hp is not None else None, x, h,
+                               ex.ctypes.data)
+        return h, ex
+
     def group_uniforms(self, seed, b, k, j):
         """The two uniforms (U1, U2) of group j of request b at step k (sampler 1)."""
         u1, u2 = ctypes.c_float(), ctypes.c_float()
@@ -207,6 +282,13 @@ def sample_score(logit_bits, T, g):
 
 def walk(*args, **kwargs):
     return default().walk(*args, **kwargs)
+
+
+def walk_cell(*args, **kwargs):
+    return default().walk_cell(*args, **kwargs)
+
+
+CELL_MARKOV, CELL_GATED, CELL_RNN = 0, 1, 2
 
 
 def cpu_threads(nthreads):

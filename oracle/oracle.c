@@ -50,6 +50,18 @@
  * of weights exceeds U2_j * S_j; the two uniforms of group j are the Philox
  * words 2 (j & 1) and 2 (j & 1) + 1 of counter (j >> 1, k, b, 1).  All of it
  * in fp64.  Tokens then follow softmax(logit / T) as well.
+ *
+ * Recurrent heads (orc_walk3, cell = 1 or 2) follow "Keeping the Draft Walk on
+ * Chip", section "Beyond DSpark: other serial heads": the head keeps a small
+ * state, updates it each step, and projects the new state through the same
+ * W2 (the Markov head projects W1[prev]).  The pages name DSpark's gated and
+ * RNN heads and where their 256 x 256 recurrent matrix M lives, but print no
+ * cell equations.  Readings:
+ *   h_{-1} = 0; x_k = W1[prev_k] (prev_0 = anchor); p_k = M @ h_{k-1} (fp64);
+ *   gated: z = 1 / (1 + exp(-p_k)), h_k = bf16((1 - z) * h_{k-1} + z * x_k);
+ *   RNN:   h_k = bf16(tanh(p_k + x_k));
+ *   the projected vector is u_k = h_k; each element's value is formed in fp64
+ *   and rounded to bf16 once.
  */
 #include <math.h>
 #include <stdint.h>
@@ -263,10 +275,47 @@ int64_t orc_group_sample(const uint16_t *logit, int64_t V, float T, uint64_t see
     return v0 + n - 1;
 }
 
+/* ------------------------------------------------------ recurrent cells --- */
+
+#define ORC_CELL_MARKOV 0
+#define ORC_CELL_GATED 1
+#define ORC_CELL_RNN 2
+
+/*
+ * One state update of a recurrent head (see the header): from the previous
+ * state hprev (bf16 bits, r; NULL means h = 0) and the token's row x of W1,
+ * h[i] = bf16(value_i) with value_i formed in fp64 from p_i = M[i, :] . hprev.
+ * M is bf16 bits, [r, r] row-major.  exact (optional, r) receives value_i.
+ */
+void orc_cell_update(int cell, const uint16_t *M, int r, const uint16_t *hprev,
+                     const uint16_t *x, uint16_t *h, double *exact)
+{
+    for (int i = 0; i < r; ++i) {
+        double p = 0.0;                                  /* M[i, :] . h_{k-1} */
+        if (hprev)
+            for (int j = 0; j < r; ++j)
+                p += orc_bf16_to_f64(M[(int64_t)i * r + j]) * orc_bf16_to_f64(hprev[j]);
+        const double hp = hprev ? orc_bf16_to_f64(hprev[i]) : 0.0;
+        const double xi = orc_bf16_to_f64(x[i]);
+        double val;
+        if (cell == ORC_CELL_GATED) {
+            const double z = 1.0 / (1.0 + exp(-p));     /* update gate */
+            val = (1.0 - z) * hp + z * xi;
+        } else if (cell == ORC_CELL_RNN) {
+            val = tanh(p + xi);
+        } else {
+            val = xi;                                    /* Markov: u = W1[prev] */
+        }
+        h[i] = orc_bf16_rne(val);
+        if (exact)
+            exact[i] = val;
+    }
+}
+
 /* ---------------------------------------------------------------- walk --- */
 
 /*
- * One Markov walk per request.
+ * One walk per request (the Markov head, or a recurrent head's state walk).
  *
  *   W1, W2     bf16 bits, [V, r] row-major
  *   base       bf16 bits, [B, gamma, V]
@@ -286,17 +335,32 @@ int64_t orc_group_sample(const uint16_t *logit, int64_t V, float T, uint64_t see
  *   out_gscore, out_gpick, out_gmargin  optional [B, gamma, ceil(V / 8)]:
  *              under sampler 1 with T > 0, each group's score, in-group pick
  *              and the pick's margin (see orc_group_sample)
+ *   cell       0: Markov (u = W1[prev]); 1: gated; 2: RNN (see the header)
+ *   M          the recurrent matrix, bf16 bits [r, r] (cells 1 and 2)
+ *   forced_state  optional [B, gamma, r] bf16 bits: when given (with a
+ *              cell), step k updates the state from forced_state[b, k-1]
+ *              and projects forced_state[b, k] (teacher forcing of the
+ *              state; out_state still receives this oracle's own update)
+ *   out_state  optional [B, gamma, r] bf16 bits: each step's state h_k
+ *   out_state_exact  optional [B, gamma, r] fp64: its value before rounding
  *   nthreads   OpenMP threads for the loop over tokens (<= 0: all)
  *
- * Returns 0, or a negative code (invalid sizes, sampler, anchor or temperature).
+ * Returns 0, or a negative code (invalid sizes, sampler, cell, anchor or
+ * temperature).
  */
-int orc_walk2(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
+int orc_walk3(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
               const uint16_t *base, const int32_t *anchor, const float *T,
               uint64_t seed, int B, int gamma, int req0, const int32_t *forced,
-              int sampler, int32_t *out_tokens, uint16_t *out_logits, float *out_scores,
-              float *out_gscore, int32_t *out_gpick, float *out_gmargin, int nthreads)
+              int sampler, int cell, const uint16_t *M, const uint16_t *forced_state,
+              int32_t *out_tokens, uint16_t *out_logits, float *out_scores,
+              float *out_gscore, int32_t *out_gpick, float *out_gmargin,
+              uint16_t *out_state, double *out_state_exact, int nthreads)
 {
     if (sampler != 0 && sampler != 1)
+        return ORC_EINVAL;
+    if (cell != ORC_CELL_MARKOV && cell != ORC_CELL_GATED && cell != ORC_CELL_RNN)
+        return ORC_EINVAL;
+    if (cell != ORC_CELL_MARKOV && !M)
         return ORC_EINVAL;
     if (V <= 0 || r <= 0 || B < 0 || gamma < 0 || req0 < 0)
         return ORC_EINVAL;
@@ -315,9 +379,13 @@ int orc_walk2(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
     /* scratch rows, one vocabulary wide */
     uint16_t *logit = (uint16_t *)malloc((size_t)V * sizeof *logit);
     double *score = (double *)malloc((size_t)V * sizeof *score);
-    if (!logit || !score) {
+    uint16_t *hbuf = (uint16_t *)malloc(2 * (size_t)r * sizeof *hbuf);   /* h_{k-1}, h_k */
+    double *hex = (double *)malloc((size_t)r * sizeof *hex);
+    if (!logit || !score || !hbuf || !hex) {
         free(logit);
         free(score);
+        free(hbuf);
+        free(hex);
         return ORC_EINVAL;
     }
     for (int b = 0; b < B; ++b) {
@@ -326,6 +394,23 @@ int orc_walk2(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
             if (forced && k > 0)
                 prev = forced[(int64_t)b * gamma + (k - 1)];
             const uint16_t *u = W1 + prev * r;            /* u = W1[prev] */
+            if (cell != ORC_CELL_MARKOV) {
+                /* h_{k-1}: this walk's own, or the forced one; h_{-1} = 0 */
+                const uint16_t *hprev = NULL;
+                if (k > 0)
+                    hprev = forced_state ? forced_state + ((int64_t)b * gamma + (k - 1)) * r
+                                         : hbuf;
+                uint16_t *hk = hbuf + r;
+                orc_cell_update(cell, M, r, hprev, u, hk, hex);
+                if (out_state)
+                    memcpy(out_state + ((int64_t)b * gamma + k) * r, hk, (size_t)r * sizeof *hk);
+                if (out_state_exact)
+                    memcpy(out_state_exact + ((int64_t)b * gamma + k) * r, hex,
+                           (size_t)r * sizeof *hex);
+                memcpy(hbuf, hk, (size_t)r * sizeof *hk);  /* h_k becomes h_{k-1} */
+                /* the projected state: h_k, or the forced walk's own h_k */
+                u = forced_state ? forced_state + ((int64_t)b * gamma + k) * r : hbuf;
+            }
             const uint16_t *bk = base + ((int64_t)b * gamma + k) * V;
             const float Tb = T[b];
 #pragma omp parallel for num_threads(nthreads) schedule(static)
@@ -370,7 +455,21 @@ int orc_walk2(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
     }
     free(logit);
     free(score);
+    free(hbuf);
+    free(hex);
     return ORC_OK;
+}
+
+/* The Markov walk with either sampler (the argument list before the cells). */
+int orc_walk2(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
+              const uint16_t *base, const int32_t *anchor, const float *T,
+              uint64_t seed, int B, int gamma, int req0, const int32_t *forced,
+              int sampler, int32_t *out_tokens, uint16_t *out_logits, float *out_scores,
+              float *out_gscore, int32_t *out_gpick, float *out_gmargin, int nthreads)
+{
+    return orc_walk3(W1, W2, V, r, base, anchor, T, seed, B, gamma, req0, forced, sampler,
+                     ORC_CELL_MARKOV, NULL, NULL, out_tokens, out_logits, out_scores,
+                     out_gscore, out_gpick, out_gmargin, NULL, NULL, nthreads);
 }
 
 /* Batch helpers used by the tests to pin the pieces one by one. */

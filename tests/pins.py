@@ -567,11 +567,146 @@ def pin_group_batch_independence(O):
                           req0=b, sampler=1)
         assert np.array_equal(tb[0], t[b]), "request %d differs alone vs in the batch" % b
 
+# ------------------------------------------------------ recurrent heads ---
+# The recurrent cells of "Keeping the Draft Walk on Chip", section "Beyond
+# DSpark: other serial heads" (readings in oracle.c's header): special cases
+# where a cell walk reduces to the pinned Markov walk or to a closed form.
+
+def _cell_inputs(V, gamma, seed, spike_token=None, w1=None):
+    """W1, W2, base, anchor (bits) for one request; with spike_token, a +40
+    spike at that token in every step's base and the anchor at that token."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    r = 256
+    W1 = (torch.randn(V, r, generator=g) / 16) if w1 is None else w1
+    W2 = torch.randn(V, r, generator=g)
+    base = torch.randn(1, gamma, V, generator=g)
+    anchor = int(torch.randint(0, V, (1,), generator=g))
+    if spike_token is not None:
+        base[0, :, spike_token] += 40.0
+        anchor = spike_token
+    bits = lambda t: t.to(torch.bfloat16).contiguous().view(torch.int16).numpy().view(np.uint16)
+    return bits(W1), bits(W2), bits(base), np.array([anchor], np.int32)
+
+
+def _bits_of(t):
+    return t.to(torch.bfloat16).contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def pin_cell_rnn_zero_matrix(O):
+    """RNN head with M = 0 is the Markov walk over the table bf16(tanh(W1))."""
+    V, gamma = 500, 5
+    W1, W2, base, anchor = _cell_inputs(V, gamma, 41)
+    W1[:7] = _bits_of(torch.full((7, 256), 3.0))               # saturating rows too
+    M = np.zeros((256, 256), np.uint16)
+    T = np.zeros(1, np.float32)
+    t, lg, _, st, _ = O.walk_cell(W1, W2, base, anchor, T, 0, 2, M=M)
+    W1t = O.bf16_rne(np.tanh(_from_bits(W1)).ravel()).reshape(W1.shape)
+    tm, lm, _ = O.walk(W1t, W2, base, anchor, T, 0)
+    assert np.array_equal(t, tm) and np.array_equal(lg, lm), \
+        "RNN with M = 0 must walk like Markov over tanh(W1)"
+    prev = [int(anchor[0])] + [int(v) for v in t[0, :-1]]
+    assert np.array_equal(st[0], W1t[prev]), "RNN with M = 0: state must be tanh(W1[prev])"
+
+
+def pin_cell_gated_half(O):
+    """Gated head with M = 0 (gate 1/2) on a constant token path: the state is
+    the geometric series x (1 - 2^-(k+1)), exact in bf16 for k <= 7; each step
+    projects it like a Markov step whose W1 row is that state."""
+    V, gamma, t0 = 300, 8, 17
+    g = torch.Generator("cpu").manual_seed(42)
+    W1f = torch.randn(V, 256, generator=g) / 16
+    vals = torch.tensor([1.0, 2.0, 4.0, 8.0, -1.0, -2.0, -4.0, -8.0]) / 64
+    W1f[t0] = vals[torch.randint(0, 8, (256,), generator=g)]
+    W1, W2, base, anchor = _cell_inputs(V, gamma, 43, spike_token=t0, w1=W1f)
+    M = np.zeros((256, 256), np.uint16)
+    T = np.zeros(1, np.float32)
+    t, lg, _, st, _ = O.walk_cell(W1, W2, base, anchor, T, 0, 1, M=M)
+    assert np.all(t == t0), "the spike must hold the token path"
+    x = _from_bits(W1[t0])
+    for k in range(gamma):
+        want = x * (1.0 - 2.0 ** -(k + 1))
+        assert np.array_equal(_from_bits(st[0, k]), want), "gated M = 0: state %d" % k
+        W1k = W1.copy()
+        W1k[t0] = st[0, k]
+        _, lk, _ = O.walk(W1k, W2, base[:, k:k + 1], anchor, T, 0)
+        assert np.array_equal(lk[0, 0], lg[0, k]), "gated: step %d must project its state" % k
+
+
+def pin_cell_gated_saturation(O):
+    """Gated head, M = c * ones with W1 >= 0: from step 1 the gate is 1 (fp64:
+    1 - z < 1e-17) and the state is W1[prev], the Markov walk's latent; with
+    M = -c * ones the gate is 0 and the state stays h_0 = W1[anchor] / 2."""
+    V, gamma = 400, 6
+    g = torch.Generator("cpu").manual_seed(44)
+    W1f = torch.randn(V, 256, generator=g).abs() / 16
+    W1, W2, base, anchor = _cell_inputs(V, gamma, 45, w1=W1f)
+    T = np.zeros(1, np.float32)
+    for c in (64.0, -64.0):
+        M = _bits_of(torch.full((256, 256), c))
+        t, lg, _, st, _ = O.walk_cell(W1, W2, base, anchor, T, 0, 1, M=M)
+        h0 = _from_bits(W1[anchor[0]]) / 2
+        assert np.array_equal(_from_bits(st[0, 0]), h0), "gated: h_0 = W1[anchor] / 2"
+        if c > 0:
+            prev = [int(v) for v in t[0, :-1]]
+            assert np.array_equal(st[0, 1:], W1[prev]), "gated, open gate: state = W1[prev]"
+            _, lm, _ = O.walk(W1, W2, base, anchor, T, 0, forced=t)
+            assert np.array_equal(lm[0, 1:], lg[0, 1:]), "gated, open gate: Markov logits"
+        else:
+            for k in range(1, gamma):
+                assert np.array_equal(st[0, k], st[0, 0]), "gated, shut gate: state frozen"
+
+
+def pin_cell_rnn_permutation(O):
+    """RNN head with M = a * P (row i holds a at column pi(i)) on a constant
+    token path: element i follows the scalar map h_i <- tanh(a h_pi(i) + x_i)."""
+    V, gamma, t0 = 300, 6, 123
+    W1, W2, base, anchor = _cell_inputs(V, gamma, 46, spike_token=t0)
+    g = torch.Generator("cpu").manual_seed(47)
+    pi = torch.randperm(256, generator=g).numpy()
+    a = 0.75
+    Mf = torch.zeros(256, 256)
+    Mf[torch.arange(256), torch.from_numpy(pi)] = a
+    T = np.zeros(1, np.float32)
+    t, _, _, st, _ = O.walk_cell(W1, W2, base, anchor, T, 0, 2, M=_bits_of(Mf))
+    assert np.all(t == t0), "the spike must hold the token path"
+    x = _from_bits(W1[t0])
+    h = np.zeros(256)
+    for k in range(gamma):
+        h = _from_bits(O.bf16_rne(np.tanh(a * h[pi] + x)))
+        assert np.array_equal(_from_bits(st[0, k]), h), "RNN permutation: state %d" % k
+
+
+def pin_cell_batch_and_forcing(O):
+    """Each request keeps its own state (alone == in a batch), and forcing a
+    walk with its own tokens and states changes nothing."""
+    import synth
+    x = synth.make_custom(V=333, gamma=4, B=3, seed=48, temperatures=(0.0, 1.0, 0.6))
+    g = torch.Generator("cpu").manual_seed(49)
+    M = _bits_of(torch.randn(256, 256, generator=g) / 16)
+    bits = synth.bits
+    for cell in (1, 2):
+        args = (bits(x.W1), bits(x.W2))
+        t, lg, _, st, _ = O.walk_cell(*args, bits(x.base), x.anchor.numpy(),
+                                      x.temperature.numpy(), 77, cell, M=M)
+        for b in range(3):
+            tb, lb, _, sb, _ = O.walk_cell(*args, bits(x.base[b:b + 1]),
+                                           x.anchor.numpy()[b:b + 1],
+                                           x.temperature.numpy()[b:b + 1], 77, cell, M=M, req0=b)
+            assert np.array_equal(tb[0], t[b]) and np.array_equal(lb[0], lg[b]) and \
+                np.array_equal(sb[0], st[b]), "cell %d: request %d differs alone" % (cell, b)
+        tf, lf, _, sf, _ = O.walk_cell(*args, bits(x.base), x.anchor.numpy(),
+                                       x.temperature.numpy(), 77, cell, M=M, forced=t,
+                                       forced_state=st)
+        assert np.array_equal(tf, t) and np.array_equal(lf, lg) and np.array_equal(sf, st), \
+            "cell %d: forcing a walk with itself changed it" % cell
+
+
 ALL_PINS = [
     pin_bf16_hand, pin_bf16_vs_torch, pin_bf16_vs_search,
     pin_philox_vs_triton, pin_noise_layout, pin_uniform, pin_gumbel,
     pin_hand_walk, pin_fig2_bruteforce, pin_w2_zero, pin_spike,
     pin_batch_independence, pin_permutation, pin_sampling_law, pin_t_to_zero,
     pin_forced, pin_errors, pin_group_layout, pin_group_sampling_law, pin_group_t_to_zero,
-    pin_group_batch_independence,
+    pin_group_batch_independence, pin_cell_rnn_zero_matrix, pin_cell_gated_half,
+    pin_cell_gated_saturation, pin_cell_rnn_permutation, pin_cell_batch_and_forcing,
 ]

@@ -42,6 +42,17 @@ MUTATIONS = {
                            "    const double target = (double)U1 * S;\n    double run = 0.0;\n"),
     "group_counter_word": ("{(uint32_t)(j >> 1), (uint32_t)k, (uint32_t)b, 1u}",
                            "{(uint32_t)(j >> 1), (uint32_t)k, (uint32_t)b, 0u}"),
+    # recurrent heads
+    "cell_gate_swapped": ("val = (1.0 - z) * hp + z * xi;", "val = z * hp + (1.0 - z) * xi;"),
+    "cell_gate_sign": ("1.0 / (1.0 + exp(-p));", "1.0 / (1.0 + exp(p));"),
+    "cell_matrix_transposed": ("orc_bf16_to_f64(M[(int64_t)i * r + j])",
+                               "orc_bf16_to_f64(M[(int64_t)j * r + i])"),
+    "cell_rnn_drops_input": ("val = tanh(p + xi);", "val = tanh(p);"),
+    "cell_rnn_drops_recurrence": ("val = tanh(p + xi);", "val = tanh(xi);"),
+    "cell_state_not_carried": ("memcpy(hbuf, hk, (size_t)r * sizeof *hk);",
+                               "memset(hbuf, 0, (size_t)r * sizeof *hk);"),
+    "cell_projects_input": ("* r : hbuf;\n", "* r : u;\n"),
+    "cell_initial_state_is_input": ("const uint16_t *hprev = NULL;", "const uint16_t *hprev = u;"),
 }
 
 
