@@ -30,6 +30,10 @@ struct dspark_walk {
   bool use_resident = true;       // dspark_walk_set_kernel
   int seed_per_round = 0;         // dspark_walk_set_seed_mode
   int sampler = 0;                // dspark_walk_set_sampler
+  int cell = 0;                   // dspark_walk_set_cell
+  const uint16_t* cell_M = nullptr;   // caller-owned [256, 256]
+  float* cell_p = nullptr;        // handle-owned [max_gamma][16][256] fp32
+  uint16_t* out_state = nullptr;  // caller-owned, dspark_walk_set_state_output
   int res_RS = 0, res_NT = 0, res_R = 0, res_S = 0, res_ST = 0, res_nslot = 0, res_n_cta = 0;
   int64_t res_wpc = 0;
   size_t res_smem = 0;
@@ -195,6 +199,17 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
     a.trace = (h->trace && h->trace_bytes >= need) ? h->trace : nullptr;
   }
 
+  a.out_state = h->out_state;
+  a.cell = h->cell;
+  a.cell_M = h->cell_M;
+  a.cell_p = h->cell_p;
+  a.cell_q = 1;
+  const bool resident_run = h->res_max_B > 0 && h->use_resident && B <= h->res_max_B;
+  // recurrent heads and the state output run on the resident kernel only
+  if ((h->cell != DSPARK_CELL_MARKOV || h->out_state) && !resident_run)
+    return DSPARK_EUNSUPPORTED;
+  if (resident_run) a.cell_q = (kRank + h->res_n_cta - 1) / h->res_n_cta;
+
   if (!(h->res_max_B > 0 && h->use_resident && B <= h->res_max_B) && h->W2b && h->use_batched) {
     CUDA_TRY(batched_launch(a, h->W2b, h->bat_R, h->bat_n_cta, h->max_B, B,
                             232448 - 1024, stream));
@@ -214,7 +229,8 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
     const uintptr_t bp = reinterpret_cast<uintptr_t>(base);
     ra.base_mode = (h->V % 8 == 0 && (bp & 15u) == 0) ? 16
                    : (h->V % 2 == 0 && (bp & 3u) == 0) ? 4 : 2;
-    const void* rfn = resident_kernel_for(h->res_RS, h->res_NT);
+    const void* rfn = resident_kernel_for(h->res_RS, h->res_NT,
+                                          h->cell != DSPARK_CELL_MARKOV || h->out_state);
     void* rargs[] = {&ra};
     CUDA_TRY(cudaLaunchCooperativeKernel(rfn, dim3(h->res_n_cta), dim3(resident_threads()), rargs,
                                          h->res_smem, stream));
@@ -318,9 +334,13 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
     }
     if (rc == DSPARK_OK && resident) {
       int per_sm = 0;
-      const void* fn = resident_kernel_for(h->res_RS, h->res_NT);
+      const void* fn = resident_kernel_for(h->res_RS, h->res_NT, false);
+      const void* fn_cell = resident_kernel_for(h->res_RS, h->res_NT, true);
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kSmemBudget);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn_cell, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBudget);
       if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, resident_threads(),
                                                           h->res_smem);
@@ -456,6 +476,32 @@ int dspark_walk_set_sampler(dspark_walk_t h, int sampler) {
   return DSPARK_OK;
 }
 
+int dspark_walk_set_cell(dspark_walk_t h, int cell, const void* M) {
+  if (!h) return DSPARK_EINVAL;
+  if (cell == DSPARK_CELL_MARKOV) {
+    h->cell = cell;
+    h->cell_M = nullptr;
+    return DSPARK_OK;
+  }
+  if ((cell != DSPARK_CELL_GATED && cell != DSPARK_CELL_RNN) || !M ||
+      (reinterpret_cast<uintptr_t>(M) & 15u) != 0)
+    return DSPARK_EINVAL;
+  if (h->res_max_B == 0) return DSPARK_EUNSUPPORTED;   // no resident layout to run on
+  if (!h->cell_p) {
+    CUDA_TRY(cudaSetDevice(h->device));
+    CUDA_TRY(cudaMalloc(&h->cell_p, (size_t)h->max_gamma * 16 * kRank * sizeof(float)));
+  }
+  h->cell = cell;
+  h->cell_M = static_cast<const uint16_t*>(M);
+  return DSPARK_OK;
+}
+
+int dspark_walk_set_state_output(dspark_walk_t h, void* out_state) {
+  if (!h || (reinterpret_cast<uintptr_t>(out_state) & 1u) != 0) return DSPARK_EINVAL;
+  h->out_state = static_cast<uint16_t*>(out_state);
+  return DSPARK_OK;
+}
+
 int dspark_walk_round(dspark_walk_t h, void* stream, uint64_t* round) {
   if (!h || !round) return DSPARK_EINVAL;
   CUDA_TRY(cudaSetDevice(h->device));
@@ -500,6 +546,7 @@ int dspark_walk_destroy(dspark_walk_t h) {
   if (h->W2b) cudaFree(h->W2b);
   if (h->sync_mem) cudaFree(h->sync_mem);
   if (h->stage) cudaFree(h->stage);
+  if (h->cell_p) cudaFree(h->cell_p);
   delete h;
   return rc;
 }

@@ -92,7 +92,14 @@ struct WalkArgs {
   int64_t timeout_ns;          // rendezvous wait limit
   int skip_cta;                // fault injection: this CTA never posts (-1: off)
   unsigned long long* trace;   // optional [n_cta][gamma + 1][8] SM-clock stamps
+  // recurrent heads (resident kernel only)
+  int cell;                    // 0: Markov (u = W1[prev]); 1: gated; 2: RNN
+  const uint16_t* cell_M;      // [256, 256] bf16 recurrent matrix, row-major
+  float* cell_p;               // [gamma][16][256] fp32: M @ h_k, published slice by slice
+  int cell_q;                  // rows of M per CTA: CTA c owns rows [c q, c q + q)
+  uint16_t* out_state;         // [B, gamma, 256] bf16 states u_k, or null
 };
+
 
 // Phase stamp of thread 0 (SM clock cycles) into the optional trace buffer:
 // slot k < gamma is step k, slot gamma is the round's entry.
@@ -129,6 +136,12 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned 
   return v;
 }
 
+__device__ __forceinline__ float ld_relaxed_gpu_f32(const float* p) {
+  float v;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ int32_t ld_relaxed_gpu_s32(const int32_t* p) {
   int32_t v;
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -156,6 +169,23 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t h) {
 
 __device__ __forceinline__ uint16_t float_to_bf16_bits_rn(float x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// One element of a recurrent head's state update ("Keeping the Draft Walk on
+// Chip", section "Beyond DSpark: other serial heads"; the pages print no cell
+// equations, these are the plain gated and Elman forms): from p = M[i, :] .
+// h_{k-1}, the token's W1 element x and the previous state element hp,
+//   gated: z = 1 / (1 + exp(-p)), (1 - z) hp + z x;   RNN: tanh(p + x);
+// in fp32, each operation rounded (no contraction), then rounded to bf16.
+__device__ __forceinline__ uint16_t cell_element(int cell, float p, float x, float hp) {
+  float v;
+  if (cell == 1) {
+    const float z = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-p)));
+    v = __fadd_rn(__fmul_rn(__fsub_rn(1.0f, z), hp), __fmul_rn(z, x));
+  } else {
+    v = tanhf(__fadd_rn(p, x));
+  }
+  return float_to_bf16_bits_rn(v);
 }
 
 // ------------------------------------------------------------------- key --

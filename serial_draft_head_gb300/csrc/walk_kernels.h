@@ -21,7 +21,7 @@ int resident_fixed_rows(int RS);
 int resident_threads();
 size_t resident_smem_bytes(int S, int ST, int nslot, int max_B, int R);
 int resident_max_ring_slots();
-const void* resident_kernel_for(int RS, int NT);
+const void* resident_kernel_for(int RS, int NT, bool cell);   // cell: recurrent heads / state output
 int resident_max_smem_strips();
 cudaError_t resident_repack(const void* W2, void* out, int64_t V, int R, int RS, int S, int n_cta,
                             cudaStream_t stream);

@@ -57,6 +57,7 @@ constexpr int kChunkBytes = kChunkStrips * kSmemStripBytes;
 constexpr int kMaxRingSlots = 3;
 constexpr int kMbarRing = kMbarTma + 1;        // first of the ring slots' mbarriers
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, kNMma);
+static_assert(kResThreads == kRank, "one thread per state element");
 
 __device__ __forceinline__ unsigned long long key_max(unsigned long long a, unsigned long long b) {
   return a > b ? a : b;
@@ -112,11 +113,52 @@ __device__ __forceinline__ void prefetch_base(const ResidentArgs& ra, int k, int
 }
 
 // u_b = W1[tok] into U (core matrix (kc, b/8), row b%8): one 16-byte chunk per lane.
+// A recurrent head's first state h_0 (from h_{-1} = 0: p = 0, previous state 0)
+// is formed from that row in place.
 __device__ __forceinline__ void gather_u_row(const uint16_t* W1, int32_t tok, int b, uint8_t* U,
-                                             int lane) {
-  const uint4 x = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)tok * kRank) + lane);
+                                             int lane, int cell) {
+  uint4 x = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)tok * kRank) + lane);
+  if (cell != 0) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = cell_element(cell, 0.0f, bf16_bits_to_float(w[j] & 0xFFFFu), 0.0f);
+      const uint32_t hi = cell_element(cell, 0.0f, bf16_bits_to_float(w[j] >> 16), 0.0f);
+      w[j] = lo | (hi << 16);
+    }
+  }
   *reinterpret_cast<uint4*>(U + (lane * 2 + (b >> 3)) * 128 + (b & 7) * 16) = x;
   ptx::fence_proxy_async_smem();
+}
+
+// U element (i, b): the bf16 at row i of request b's column.
+__device__ __forceinline__ uint16_t* u_elem(uint8_t* U, int i, int b) {
+  return reinterpret_cast<uint16_t*>(U + ((i >> 3) * 2 + (b >> 3)) * 128 + (b & 7) * 16) + (i & 7);
+}
+
+// A recurrent head's exchange, published with this step's arrival: this CTA's
+// rows of p = M @ h_k for every request (M rows [cta q, cta q + q)), one warp
+// per (row, request): each lane sums its 8 products in order, then a 5-level
+// butterfly adds the lanes (13 fp32 additions deep).
+__device__ __forceinline__ void publish_cell_rows(const WalkArgs& a, const uint8_t* U, int k,
+                                                  int cta, int warp, int lane) {
+  const int r0 = cta * a.cell_q;
+  const int nr = kRank - r0 < a.cell_q ? kRank - r0 : a.cell_q;
+  for (int pr = warp; pr < nr * a.B; pr += kResWarps) {
+    const int row = r0 + pr / a.B, b = pr % a.B;
+    const uint4 m = __ldg(reinterpret_cast<const uint4*>(a.cell_M + (size_t)row * kRank) + lane);
+    const uint4 h = *reinterpret_cast<const uint4*>(U + (lane * 2 + (b >> 3)) * 128 + (b & 7) * 16);
+    const uint32_t mw[4] = {m.x, m.y, m.z, m.w}, hw[4] = {h.x, h.y, h.z, h.w};
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc = __fmaf_rn(bf16_bits_to_float(mw[j] & 0xFFFFu), bf16_bits_to_float(hw[j] & 0xFFFFu), acc);
+      acc = __fmaf_rn(bf16_bits_to_float(mw[j] >> 16), bf16_bits_to_float(hw[j] >> 16), acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, o));
+    if (lane == 0) a.cell_p[((size_t)k * 16 + b) * kRank + row] = acc;
+  }
 }
 
 // In-place first half of the fused epilogue: base_s[b][rl] (the bf16 base
@@ -294,7 +336,9 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
   }
 }
 
-template <int RS, int NT, int SMAX>
+// CELL: the instantiation that also runs the recurrent heads and writes the
+// state output (the Markov-only one carries none of that code).
+template <int RS, int NT, int SMAX, bool CELL>
 __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const ResidentArgs ra) {
   constexpr int NCOL = 8 * NT;
   const WalkArgs& a = ra.w;
@@ -443,7 +487,8 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
   trace_stamp(a, a.gamma, 1);
 
   // step 0's u = W1[anchor]
-  for (int b = warp; b < a.B; b += kResWarps) gather_u_row(a.W1, tok_s[b], b, U, lane);
+  for (int b = warp; b < a.B; b += kResWarps)
+    gather_u_row(a.W1, tok_s[b], b, U, lane, CELL ? a.cell : 0);
   if (ra.S > 0 && threadIdx.x == 0) {
     if (!wait_mbar(&mbar[kMbarTma], 0, t_entry, a.timeout_ns)) {
       abort_round(a.sync.hdr, round_s, kStatusTimeout);
@@ -469,6 +514,9 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     ptx::tc_fence_after();
     const uint64_t t_step = globaltimer_ns();
     trace_stamp(a, k, 0);
+    if (CELL && a.out_state != nullptr && cta == 0)   // this step's latent (the state)
+      for (int b = 0; b < a.B; ++b)
+        a.out_state[((size_t)b * a.gamma + k) * kRank + threadIdx.x] = *u_elem(U, threadIdx.x, b);
 
     // (1) tensor-memory tiles: a single thread issues one tcgen05.mma per ~45
     // cycles, so six warps each issue one (tile, K half): 8 MMAs into their
@@ -631,6 +679,8 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
           }
       }
     }
+    // (4a) a recurrent head's rows of M @ h_k, released with this step's arrival
+    if (CELL && a.cell != 0 && k + 1 < a.gamma) publish_cell_rows(a, U, k, cta, warp, lane);
     ptx::tc_fence_before();
     __syncthreads();
 
@@ -701,7 +751,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
         __syncwarp();
         // up to four rows: warp 0 fetches them here (larger batches are
         // fetched by all warps after the barrier below)
-        for (int b0 = 0; b0 < (a.B <= 4 ? a.B : 0); b0 += 4) {
+        for (int b0 = 0; b0 < (a.B <= 4 && !(CELL && a.cell != 0) ? a.B : 0); b0 += 4) {
           uint4 ur[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -721,12 +771,26 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     ptx::cp_async_wait_all();
     ptx::fence_proxy_async_smem();
     __syncthreads();
-    if (a.B > 4 && abort_s == 0 && k + 1 < a.gamma) {
+    if (!(CELL && a.cell != 0) && a.B > 4 && abort_s == 0 && k + 1 < a.gamma) {
       // the next u rows, all in flight at once: warp w fetches rows w, w + 8
       for (int b = warp; b < a.B; b += kResWarps) {
         const uint4 x =
             __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok_s[b] * kRank) + lane);
         *reinterpret_cast<uint4*>(U + (lane * 2 + (b >> 3)) * 128 + (b & 7) * 16) = x;
+      }
+      ptx::fence_proxy_async_smem();
+      __syncthreads();
+    }
+    if (CELL && a.cell != 0 && abort_s == 0 && k + 1 < a.gamma) {
+      // a recurrent head's next state, every CTA alike: thread i updates
+      // element i of each request from p (all CTAs' rows, visible since the
+      // arrivals were acquired), the winner's W1 row and the current state
+      const int i = threadIdx.x;
+      for (int b = 0; b < a.B; ++b) {
+        const float p = ld_relaxed_gpu_f32(a.cell_p + ((size_t)k * 16 + b) * kRank + i);
+        const float x = bf16_bits_to_float(__ldg(a.W1 + (size_t)tok_s[b] * kRank + i));
+        uint16_t* hu = u_elem(U, i, b);
+        *hu = cell_element(a.cell, p, x, bf16_bits_to_float(*hu));
       }
       ptx::fence_proxy_async_smem();
       __syncthreads();
@@ -806,9 +870,15 @@ size_t resident_smem_bytes(int S, int ST, int nslot, int max_B, int R) {
          16 * 512 + (((size_t)max_B * R * 2 + 15) & ~(size_t)15);
 }
 
-const void* resident_kernel_for(int RS, int NT) {
-  if (RS == 2 && NT == 1) return reinterpret_cast<const void*>(&walk_resident_kernel<2, 1, 3>);
-  if (RS == 2 && NT == 2) return reinterpret_cast<const void*>(&walk_resident_kernel<2, 2, 3>);
+const void* resident_kernel_for(int RS, int NT, bool cell) {
+  if (RS == 2 && NT == 1 && !cell)
+    return reinterpret_cast<const void*>(&walk_resident_kernel<2, 1, 3, false>);
+  if (RS == 2 && NT == 2 && !cell)
+    return reinterpret_cast<const void*>(&walk_resident_kernel<2, 2, 3, false>);
+  if (RS == 2 && NT == 1 && cell)
+    return reinterpret_cast<const void*>(&walk_resident_kernel<2, 1, 3, true>);
+  if (RS == 2 && NT == 2 && cell)
+    return reinterpret_cast<const void*>(&walk_resident_kernel<2, 2, 3, true>);
   return nullptr;
 }
 

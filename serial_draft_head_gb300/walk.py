@@ -33,6 +33,10 @@ SEED_PER_ROUND = 1
 SAMPLER_GUMBEL = 0
 SAMPLER_GROUP = 1
 
+CELL_MARKOV = 0
+CELL_GATED = 1
+CELL_RNN = 2
+
 _lib = None
 
 
@@ -63,7 +67,8 @@ EXPORTS = [
     "dspark_walk_get_plan", "dspark_walk_set_limits", "dspark_walk_strerror",
     "dspark_walk_destroy", "dspark_walk_run_noalloc", "dspark_walk_set_kernel",
     "dspark_walk_set_trace", "dspark_walk_set_seed_mode", "dspark_walk_round",
-    "dspark_walk_gumbel_noise", "dspark_walk_set_sampler",
+    "dspark_walk_gumbel_noise", "dspark_walk_set_sampler", "dspark_walk_set_cell",
+    "dspark_walk_set_state_output",
 ]
 
 
@@ -97,6 +102,8 @@ def load(build_if_missing=True):
     L.dspark_walk_run_noalloc.argtypes = [vp, vp, i64, i32, vp, vp, vp, u64, vp, i32, i32, vp, vp]
     L.dspark_walk_set_seed_mode.argtypes = [vp, i32]
     L.dspark_walk_set_sampler.argtypes = [vp, i32]
+    L.dspark_walk_set_cell.argtypes = [vp, i32, vp]
+    L.dspark_walk_set_state_output.argtypes = [vp, vp]
     L.dspark_walk_round.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint64)]
     L.dspark_walk_gumbel_noise.argtypes = [vp, vp, i64, vp]
     for name in EXPORTS:
@@ -185,6 +192,24 @@ def dspark_walk_set_sampler(h, sampler):
     return _check(load().dspark_walk_set_sampler(h, int(sampler)), "dspark_walk_set_sampler")
 
 
+def dspark_walk_set_cell(h, cell, M=None):
+    """The serial head: CELL_MARKOV, or CELL_GATED / CELL_RNN with M a device
+    bf16 [256, 256] tensor (referenced by the handle: keep it alive)."""
+    if M is not None:
+        assert M.is_cuda and M.dtype == torch.bfloat16 and tuple(M.shape) == (256, 256)
+        assert M.is_contiguous()
+    return _check(load().dspark_walk_set_cell(h, int(cell), _ptr(M)), "dspark_walk_set_cell")
+
+
+def dspark_walk_set_state_output(h, out_state=None):
+    """Later runs write each step's latent into out_state (device bf16 [B, gamma, 256])."""
+    if out_state is not None:
+        assert out_state.is_cuda and out_state.dtype == torch.bfloat16
+        assert out_state.is_contiguous()
+    return _check(load().dspark_walk_set_state_output(h, _ptr(out_state)),
+                  "dspark_walk_set_state_output")
+
+
 def dspark_walk_round(h, stream=None):
     r = ctypes.c_uint64(0)
     _check(load().dspark_walk_round(h, _stream(stream), ctypes.byref(r)), "dspark_walk_round")
@@ -244,6 +269,13 @@ class Walk:
 
     def set_sampler(self, sampler):
         dspark_walk_set_sampler(self.h, sampler)
+
+    def set_cell(self, cell, M=None):
+        self.M = None if M is None else M.contiguous()      # referenced: keep alive
+        dspark_walk_set_cell(self.h, cell, self.M)
+
+    def set_state_output(self, out_state=None):
+        dspark_walk_set_state_output(self.h, out_state)
 
     def round(self, stream=None):
         return dspark_walk_round(self.h, stream)

@@ -11,7 +11,9 @@ of the same shapes stand in for them:
 
 * W1 [V, r] ~ N(0, 1) / 16 and W2 [V, r] ~ N(0, 1), so W2 @ W1[p] ~ N(0, 1);
 * base logits [B, gamma, V] ~ N(0, sigma^2);
-* anchors uniform in [0, V); temperatures per request.
+* anchors uniform in [0, V); temperatures per request;
+* a recurrent head's matrix M [r, r] ~ N(0, 1) / 16 (``make_cell_matrix``), so
+  M @ h is of the size of the W1 rows it is added to.
 
 Every tensor is drawn in fp32 from ``torch.Generator('cpu')`` and rounded to
 bf16 by PyTorch's cast: W1 then W2 from the config's weight seed, then base
@@ -152,3 +154,9 @@ def make_custom(V: int, gamma: int, B: int, seed: int, r: int = RANK,
                                      noise_seed)
     return WalkInputs(W1, W2, base, anchor, temps, noise_seed,
                       meta={"config": "custom", "V": V, "B": B, "seed": seed})
+
+
+def make_cell_matrix(seed: int, r: int = RANK) -> torch.Tensor:
+    """A recurrent head's bf16 matrix M [r, r] ~ N(0, 1) / 16 (synthetic weights)."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    return (torch.randn(r, r, generator=g) / 16).to(torch.bfloat16)

@@ -40,9 +40,9 @@ def f32_ulp(x):
     return np.spacing(np.abs(np.asarray(x, dtype=np.float32))).astype(np.float64)
 
 
-def _other_neighbour_logit(O, W1, W2, base_bits, prev, v):
+def _other_neighbour_logit(O, u_bits, W2, base_bits, v):
     """bf16(base + b') with b' the other bf16 neighbour of the exact W2[v].u."""
-    u = bf16_vals(W1[prev])
+    u = bf16_vals(u_bits)
     acc = float(np.dot(bf16_vals(W2[v]), u))
     n1 = int(O.bf16_rne(np.array([acc]))[0])
     v1 = bf16_vals([n1])[0]
@@ -68,6 +68,9 @@ class Report:
         self.steps_checked = 0
         self.steps_exact = 0
         self.near_ties = 0
+        self.states_checked = 0
+        self.states_exact = 0
+        self.states_flipped = 0
         self.failures = []
 
     def ok(self):
@@ -75,9 +78,11 @@ class Report:
 
     def __repr__(self):
         return ("Report(logits=%d exact=%d 1ulp=%d neighbour=%d steps=%d exact=%d near_ties=%d "
-                "failures=%d %s)" % (self.logits_checked, self.logits_exact, self.logits_ulp,
-                                     self.logits_neighbour, self.steps_checked, self.steps_exact,
-                                     self.near_ties, len(self.failures), self.failures[:5]))
+                "states=%d exact=%d flipped=%d failures=%d %s)" % (
+                    self.logits_checked, self.logits_exact, self.logits_ulp,
+                    self.logits_neighbour, self.steps_checked, self.steps_exact,
+                    self.near_ties, self.states_checked, self.states_exact,
+                    self.states_flipped, len(self.failures), self.failures[:5]))
 
 
 # Group sampler (sampler = 1): the GPU's group score carries fp32 errors of a
@@ -89,13 +94,53 @@ GROUP_SCORE_TOL = 2.0**-16
 GROUP_PICK_TOL = 1e-5
 
 
+# Recurrent heads: the GPU's p = M[i, :] . h is an fp32 sum 13 additions deep
+# (8 in order per lane, then a 5-level butterfly), so its error is below
+# 13 * 2^-24 * sum_j |M_ij h_j| < 2^-20 * sum_j |M_ij h_j|; the gate or tanh,
+# the products and the add each add a few fp32 ulps of values below
+# 1 + |p| + |x| + |h|.  A state element may take the other bf16 neighbour of
+# the exact value only when that value lies within this bound of the
+# midpoint between the two neighbours.
+CELL_TOL = 2.0**-20
+
+
+def _check_states(O, rep, cell, M, W1, gh_prev, x_tok, gh, oh, oex, b, k):
+    """GPU state gh [r] against the oracle's update oh / oex of the GPU's own
+    previous state gh_prev (None at step 0) and token row x_tok."""
+    rep.states_checked += gh.size
+    same = gh == oh
+    rep.states_exact += int(same.sum())
+    bad = np.nonzero(~same)[0]
+    if bad.size == 0:
+        return
+    Mv = bf16_vals(M)
+    hp = np.zeros(gh.size) if gh_prev is None else bf16_vals(gh_prev)
+    p = Mv @ hp
+    mass = np.abs(Mv) @ np.abs(hp)
+    x = bf16_vals(x_tok)
+    gv, ov = bf16_vals(gh), bf16_vals(oh)
+    for i in bad:
+        ex = float(oex[i])
+        mid = 0.5 * (gv[i] + ov[i])
+        neighbours = abs(gv[i] - ov[i]) <= bf16_ulp(max(abs(gv[i]), abs(ov[i])))
+        tol = CELL_TOL * (mass[i] + 1.0 + abs(p[i]) + abs(x[i]) + abs(hp[i]))
+        if neighbours and (gv[i] - ex) * (ov[i] - ex) <= 0 and abs(ex - mid) <= tol:
+            rep.states_flipped += 1
+            continue
+        rep.failures.append(("state", b, k, int(i), float(gv[i]), float(ov[i]), ex))
+
+
 def check(inputs: "synth.WalkInputs", gpu_tokens, gpu_logits=None, requests=None,
-          nthreads=0, O=None, report=None, sampler=0):
+          nthreads=0, O=None, report=None, sampler=0, cell=0, M=None, gpu_states=None):
     """Check the GPU's tokens [B, gamma] (and logits [B, gamma, V]) for `requests`.
 
     sampler 0: per-token Gumbel-max; 1: group inverse-CDF (a GPU token may
     differ from the oracle's only at a group-score near-tie, then being that
     group's pick, or next to a pick whose running sum sits at the threshold).
+    cell 1 or 2 (a recurrent head with matrix M, bits [r, r]): gpu_states
+    [B, gamma, r] are the GPU's states; each step's state is checked against
+    the oracle's update of the GPU's previous state and token (see CELL_TOL),
+    and the step's logits against the oracle's projection of the GPU state.
     Returns a Report; ``report.ok()`` is the verdict.
     """
     O = O or oracle.default()
@@ -112,15 +157,29 @@ def check(inputs: "synth.WalkInputs", gpu_tokens, gpu_logits=None, requests=None
         if np.any(toks < 0) or np.any(toks >= V):
             rep.failures.append(("token out of range", b, toks.tolist()))
             continue
-        ot, ol, osc, grp = _oracle_request(O, W1, W2, base_all, inputs, b, toks, nthreads,
-                                           sampler)
+        gs = None
+        if cell != 0:
+            gs = np.asarray(gpu_states[b]).astype(np.uint16)
+            ot, ol, osc, ost, oex = O.walk_cell(
+                W1, W2, base_all[b:b + 1], np.array([inputs.anchor[b]], np.int32),
+                np.array([T], np.float32), inputs.seed, cell, M=M, forced=toks[None, :],
+                forced_state=gs[None], want_scores=T != 0.0, nthreads=nthreads, req0=b)
+            ot, ol, osc = ot[0], ol[0], (osc[0] if osc is not None else None)
+            grp = None
+        else:
+            ot, ol, osc, grp = _oracle_request(O, W1, W2, base_all, inputs, b, toks, nthreads,
+                                               sampler)
         rep.steps_checked += gamma
         for k in range(gamma):
             ok_row = ol[k]
+            prev = int(inputs.anchor[b]) if k == 0 else int(toks[k - 1])
+            if cell != 0:
+                _check_states(O, rep, cell, M, W1, gs[k - 1] if k > 0 else None, W1[prev],
+                              gs[k], ost[0, k], oex[0, k], b, k)
             if gpu_logits is not None:
                 gl = np.asarray(gpu_logits[b, k])
-                _check_logits(O, rep, W1, W2, base_all[b, k], gl, ok_row,
-                              int(inputs.anchor[b]) if k == 0 else int(toks[k - 1]), b, k)
+                u = gs[k] if cell != 0 else W1[prev]
+                _check_logits(O, rep, u, W2, base_all[b, k], gl, ok_row, b, k)
             g = int(toks[k])
             if g == int(ot[k]):
                 rep.steps_exact += 1
@@ -184,7 +243,7 @@ def _oracle_request(O, W1, W2, base_all, inputs, b, toks, nthreads, sampler=0):
     return ot[0], ol[0], (osc[0] if osc is not None else None), grp
 
 
-def _check_logits(O, rep, W1, W2, base_row, gl, ol, prev, b, k):
+def _check_logits(O, rep, u, W2, base_row, gl, ol, b, k):
     gv = bf16_vals(gl)
     ov = bf16_vals(ol)
     n = gv.size
@@ -197,7 +256,7 @@ def _check_logits(O, rep, W1, W2, base_row, gl, ol, prev, b, k):
     within = np.abs(gv[bad] - ov[bad]) <= bf16_ulp(np.maximum(np.abs(gv[bad]), np.abs(ov[bad])))
     rep.logits_ulp += int(within.sum())
     for v in bad[~within]:
-        alt = _other_neighbour_logit(O, W1, W2, int(base_row[v]), prev, int(v))
+        alt = _other_neighbour_logit(O, u, W2, int(base_row[v]), int(v))
         if alt is not None and alt == int(gl[v]):
             rep.logits_neighbour += 1
             continue

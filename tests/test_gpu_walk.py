@@ -515,3 +515,96 @@ def test_group_sampler_not_on_the_streamed_kernel(walkmod):
         gpu_run(w, x)
     assert e.value.code == walkmod.EUNSUPPORTED
     w.close()
+
+
+# ------------------------------------------------------- recurrent heads --
+
+CELL_SHAPES = [
+    # V, gamma, B, temperatures, seed
+    (12, 3, 1, (0.0,), 61),                       # fewer CTAs than rows of M
+    (1000, 5, 3, (0.0, 1.0, 0.6), 62),
+    (5003, 7, 8, (0.6, 0.0, 1.0), 63),
+    (152 * 33 + 17, 4, 16, (0.0, 1.0), 64),       # two n-tiles, the largest resident batch
+    (130000, 6, 2, (0.0, 0.6), 65),               # 128 of the CTAs own two rows of M
+    (200000, 3, 1, (0.6,), 66),                   # the streamed tier
+]
+
+
+def cell_run(walkmod, w, x, cell, M, want_logits=True):
+    B, gamma, _ = x.base.shape
+    Md = M.cuda()
+    states = torch.empty(B, gamma, 256, dtype=torch.bfloat16, device="cuda")
+    w.set_cell(cell, Md)
+    w.set_state_output(states)
+    try:
+        st, toks, lg = gpu_run(w, x, want_logits=want_logits)
+    finally:
+        w.set_state_output(None)
+        w.set_cell(walkmod.CELL_MARKOV)
+    return st, toks, lg, synth.bits(states.cpu())
+
+
+@pytest.mark.parametrize("cell", [1, 2])
+@pytest.mark.parametrize("V,gamma,B,temps,seed", CELL_SHAPES)
+def test_cell_every_logit_and_state(walkmod, V, gamma, B, temps, seed, cell):
+    """Gated (1) and RNN (2) heads: every state element, logit and token."""
+    x = synth.make_custom(V=V, gamma=gamma, B=B, seed=seed, temperatures=temps,
+                          noise_seed=3000 + seed)
+    M = synth.make_cell_matrix(seed)
+    w = make_walk(walkmod, x)
+    st, toks, lg, states = cell_run(walkmod, w, x, cell, M)
+    assert st == 0, walkmod.dspark_walk_strerror(st)
+    rep = parity.check(x, toks, lg, cell=cell, M=synth.bits(M), gpu_states=states)
+    assert rep.ok(), rep
+    assert rep.states_checked == B * gamma * 256
+    w.close()
+
+
+@pytest.mark.parametrize("cell", [1, 2])
+def test_cell_long_block(walkmod, cell):
+    """V = 151,936, gamma = 16, B = 16 on the recurrent heads (sampled requests)."""
+    x = full_inputs("long_block", 16)
+    w = full_walk(walkmod, "long_block", x)
+    M = synth.make_cell_matrix(100 + cell)
+    st, toks, lg, states = cell_run(walkmod, w, x, cell, M)
+    assert st == 0
+    rep = parity.check(x, toks, lg, requests=_sample_requests(16, (0.0,)), cell=cell,
+                       M=synth.bits(M), gpu_states=states)
+    assert rep.ok(), rep
+
+
+def test_markov_state_output_is_the_gathered_row(walkmod):
+    """With the Markov head the state output is u_k = W1[prev_k]."""
+    x = synth.make_custom(V=3000, gamma=5, B=3, seed=67, temperatures=(0.0, 1.0))
+    w = make_walk(walkmod, x)
+    states = torch.empty(3, 5, 256, dtype=torch.bfloat16, device="cuda")
+    w.set_state_output(states)
+    st, toks, _ = gpu_run(w, x, want_logits=False)
+    assert st == 0
+    W1 = synth.bits(x.W1)
+    s = synth.bits(states.cpu())
+    for b in range(3):
+        prev = [int(x.anchor[b])] + [int(t) for t in toks[b, :-1]]
+        assert np.array_equal(s[b], W1[prev])
+    w.close()
+
+
+def test_cell_rejections(walkmod):
+    """Recurrent heads run on the resident kernel only; bad arguments are refused."""
+    x = synth.make_custom(V=4096, gamma=2, B=17, seed=68, temperatures=(0.0,))
+    w = make_walk(walkmod, x)                       # max_B 17: B = 17 takes the batched kernel
+    M = synth.make_cell_matrix(9).cuda()
+    with pytest.raises(walkmod.WalkError) as e:
+        walkmod.dspark_walk_set_cell(w.h, 7, M)
+    assert e.value.code == walkmod.EINVAL
+    with pytest.raises(walkmod.WalkError) as e:
+        walkmod.dspark_walk_set_cell(w.h, walkmod.CELL_RNN, None)
+    assert e.value.code == walkmod.EINVAL
+    w.set_cell(walkmod.CELL_RNN, M)
+    with pytest.raises(walkmod.WalkError) as e:
+        gpu_run(w, x)
+    assert e.value.code == walkmod.EUNSUPPORTED
+    w.set_cell(walkmod.CELL_MARKOV)
+    st, toks, lg = gpu_run(w, x)                    # the Markov head still runs there
+    assert st == 0 and parity.check(x, toks, lg).ok()
+    w.close()

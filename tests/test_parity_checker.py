@@ -95,3 +95,57 @@ def test_group_sampler_rejects_a_token_of_another_group():
     assert not rep.ok() and rep.failures[0][0] == "group-sampled token"
     # and the Gumbel-max rule does not accept the group sampler's walk wholesale
     assert not parity.check(x, t, None, sampler=0).ok()
+
+
+# ------------------------------------------------------- recurrent heads --
+
+def _cell_walk(x, cell, M):
+    return oracle.walk_cell(synth.bits(x.W1), synth.bits(x.W2), synth.bits(x.base),
+                            x.anchor.numpy(), x.temperature.numpy(), x.seed, cell, M=M)
+
+
+def test_cell_accepts_the_oracle_itself():
+    x = synth.make_custom(V=500, gamma=4, B=3, seed=25, temperatures=(0.0, 1.0, 0.6),
+                          noise_seed=6)
+    M = synth.bits(synth.make_cell_matrix(7))
+    for cell in (1, 2):
+        t, lg, _, st, _ = _cell_walk(x, cell, M)
+        rep = parity.check(x, t, lg, cell=cell, M=M, gpu_states=st)
+        assert rep.ok(), rep
+        assert rep.states_exact == rep.states_checked == 3 * 4 * 256
+
+
+def test_cell_rejects_a_wrong_state_element():
+    x = synth.make_custom(V=500, gamma=3, B=1, seed=26)
+    M = synth.bits(synth.make_cell_matrix(8))
+    for cell in (1, 2):
+        t, lg, _, st, ex = _cell_walk(x, cell, M)
+        st2 = st.copy()
+        i = int(np.argmax(np.abs(ex[0, 1])))   # a large element: far from any midpoint? flip it
+        st2[0, 1, i] = st2[0, 1, i] + 1        # the next bf16 pattern
+        rep = parity.check(x, t, None, cell=cell, M=M, gpu_states=st2)
+        assert not rep.ok() and any(f[0] == "state" for f in rep.failures), rep
+
+
+def test_cell_accepts_a_flip_at_a_midpoint_only():
+    # gated head, M = 0: h_0 = x / 2 exactly, so no flip is allowed at step 0;
+    # an element whose exact value is a bf16 midpoint allows either neighbour
+    x = synth.make_custom(V=300, gamma=2, B=1, seed=27)
+    M = np.zeros((256, 256), np.uint16)
+    t, lg, _, st, ex = _cell_walk(x, 1, M)
+    st2 = st.copy()
+    st2[0, 0, 5] ^= 1                          # a flip where the value is exact
+    rep = parity.check(x, t, None, cell=1, M=M, gpu_states=st2)
+    assert not rep.ok()
+    # step 1: (h_0 + x_1) / 2 is a midpoint wherever the sum needs one more bit
+    mids = [i for i in range(256)
+            if parity.bf16_vals(st[0, 1, i:i + 1])[0] != ex[0, 1, i] and ex[0, 1, i] != 0]
+    assert mids, "expected a rounded element at step 1"
+    i = mids[0]
+    lo_hi = sorted([int(st[0, 1, i]), int(st[0, 1, i]) + 1, int(st[0, 1, i]) - 1],
+                   key=lambda h: abs(parity.bf16_vals([h])[0] - ex[0, 1, i]))
+    other = lo_hi[1]                            # the other neighbour of the exact value
+    st3 = st.copy()
+    st3[0, 1, i] = other
+    rep = parity.check(x, t, None, cell=1, M=M, gpu_states=st3)
+    assert rep.ok() and rep.states_flipped == 1, rep
