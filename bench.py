@@ -58,6 +58,9 @@ def parse():
     p.add_argument("--sampler", default="gumbel", choices=["gumbel", "group"],
                    help="sampling of T > 0 requests: per-token Gumbel-max (the configs') or the "
                         "group inverse-CDF sampler")
+    p.add_argument("--cell", default="markov", choices=["markov", "gated", "rnn"],
+                   help="serial head: DSpark's Markov head (the configs') or a recurrent "
+                        "head (gated / RNN state update, synthetic recurrent matrix)")
     p.add_argument("--kernel", default="planned", choices=["planned", "resident", "batched", "stream"],
                    help="force a kernel (dspark_walk_set_kernel); default: the handle's plan")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -288,7 +291,15 @@ def gamma_fit(walk, gammas=(1, 4, 7, 16), steps=100, warmup=5):
     return out
 
 
-def measure_config(walk, cfg, B, steps=50, warmup=5, sampler="gumbel"):
+CELLS = {"markov": 0, "gated": 1, "rnn": 2}
+
+
+def cell_matrix(cfg):
+    """The recurrent heads' synthetic matrix for a workload (bf16 [256, 256])."""
+    return synth.make_cell_matrix(cfg.seed + 500)
+
+
+def measure_config(walk, cfg, B, steps=50, warmup=5, sampler="gumbel", cell="markov"):
     """Cold- and warm-L2 us per walk of one workload at batch B (sweep mode)."""
     dev = torch.device("cuda", torch.cuda.current_device())
     W1, W2, _ = synth.make_weights(cfg.V, cfg.r, cfg.seed)
@@ -296,6 +307,8 @@ def measure_config(walk, cfg, B, steps=50, warmup=5, sampler="gumbel"):
     w = walk.Walk(W1.to(dev), W2.to(dev), B, cfg.gamma)
     if sampler == "group":
         w.set_sampler(walk.SAMPLER_GROUP)
+    if cell != "markov":
+        w.set_cell(CELLS[cell], cell_matrix(cfg).to(dev))
     plan = w.plan()
     base, anchor, temp = x.base.to(dev), x.anchor.to(dev), x.temperature.to(dev)
     tok = torch.empty(B, cfg.gamma, dtype=torch.int32, device=dev)
@@ -321,7 +334,8 @@ def measure_config(walk, cfg, B, steps=50, warmup=5, sampler="gumbel"):
     cold = statistics.mean(s.elapsed_time(e) for s, e in ev) * 1000.0
     warm = ws.elapsed_time(we) / steps * 1000.0
     res = {"workload": cfg.name, "V": cfg.V, "gamma": cfg.gamma, "B": B,
-           "temperatures": list(cfg.temperatures), "sampler": sampler, "status": st,
+           "temperatures": list(cfg.temperatures), "sampler": sampler, "cell": cell,
+           "status": st,
            "kernel": kernel_label(walk, plan, B),
            "us_cold_l2": cold, "us_warm_l2": warm,
            "eff_w2_GBs_cold": cfg.gamma * cfg.V * cfg.r * 2 * B / (cold * 1e-6) / 1e9}
@@ -336,19 +350,28 @@ def measure_config(walk, cfg, B, steps=50, warmup=5, sampler="gumbel"):
     return res
 
 
-def cpu_baseline(cfg, B, rounds, seconds):
+def oracle_walk(O, cell, M, W1, W2, base, anchor, temperature, seed):
+    """One oracle walk of the bench's head (tokens only)."""
+    if cell == "markov":
+        return O.walk(W1, W2, base, anchor, temperature, seed, want_logits=False, nthreads=0)
+    return O.walk_cell(W1, W2, base, anchor, temperature, seed, CELLS[cell], M=M,
+                       want_logits=False, nthreads=0)
+
+
+def cpu_baseline(cfg, B, rounds, seconds, cell="markov"):
     """The oracle, as it stands, on all host cores: full walks for ~`seconds`."""
     import oracle
     from oracle import cpu_threads
     O = oracle.default()
     W1 = synth.bits(rounds[0].W1)
     W2 = synth.bits(rounds[0].W2)
+    M = synth.bits(cell_matrix(cfg))
     n = 0
     t0 = time.perf_counter()
     while True:
         x = rounds[n % len(rounds)]
-        O.walk(W1, W2, synth.bits(x.base), x.anchor.numpy(), x.temperature.numpy(), x.seed,
-               want_logits=False, nthreads=0)
+        oracle_walk(O, cell, M, W1, W2, synth.bits(x.base), x.anchor.numpy(),
+                    x.temperature.numpy(), x.seed)
         n += 1
         if time.perf_counter() - t0 >= seconds:
             break
@@ -368,6 +391,7 @@ def run_reference(args, cfg, B, rank, world):
     n_rounds = min(cfg.rounds, 8)
     W1t, W2t, rounds = load_inputs(cfg, B, n_rounds)
     W1, W2 = synth.bits(W1t), synth.bits(W2t)
+    M = synth.bits(cell_matrix(cfg))
 
     def one_step(i):
         # bounded sample: the work of ONE of the gamma steps of round i (all V
@@ -378,8 +402,8 @@ def run_reference(args, cfg, B, rank, world):
         anchor = x.anchor.numpy()
         base = synth.bits(x.base)[:, k:k + 1]
         t0 = time.perf_counter()
-        O.walk(W1, W2, np.ascontiguousarray(base), anchor, x.temperature.numpy(), x.seed,
-               want_logits=False, nthreads=0)
+        oracle_walk(O, args.cell, M, W1, W2, np.ascontiguousarray(base), anchor,
+                    x.temperature.numpy(), x.seed)
         return time.perf_counter() - t0
 
     for i in range(args.warmup):
@@ -391,7 +415,8 @@ def run_reference(args, cfg, B, rank, world):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": us / 1000.0, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.note, "V": cfg.V, "gamma": cfg.gamma, "B": B, "r": cfg.r},
+        "config": {"workload": cfg.note, "cell": args.cell, "V": cfg.V, "gamma": cfg.gamma,
+                   "B": B, "r": cfg.r},
         "cpu_baseline": {"value": us, "unit": "us", "cores": cpu_threads(0), "kind": "oracle",
                          "sample": "per step: the work of one of the gamma walk steps (all V "
                                    "tokens, all B requests, from the round's anchor), x gamma"},
@@ -422,6 +447,10 @@ def main():
     w = walk.Walk(W1, W2, B, cfg.gamma)
     if args.sampler == "group":
         w.set_sampler(walk.SAMPLER_GROUP)
+    M = None
+    if args.cell != "markov":
+        M = cell_matrix(cfg).to(dev)
+        w.set_cell(CELLS[args.cell], M)
     if args.kernel != "planned":
         w.set_kernel({"resident": walk.KERNEL_RESIDENT, "batched": walk.KERNEL_BATCHED,
                       "stream": walk.KERNEL_STREAM}[args.kernel])
@@ -538,7 +567,8 @@ def main():
     eff_gbs = w2_bytes / (mean_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
     roof = {"bound": "hbm", "achieved": eff_gbs, "peak": peak, "unit": "GB/s",
-            "frac": eff_gbs / peak, "traffic": TRAFFIC.get((cfg.name, B)),
+            "frac": eff_gbs / peak,
+            "traffic": TRAFFIC.get((cfg.name, B)) if args.cell == "markov" else None,
             "peak_kind": peak_kind,
             "note": "achieved = effective W2 bytes (gamma*V*r*2*B) per launch / mean launch "
                     "time; >1 means W2 is served from on-chip memory or L2, not HBM"}
@@ -560,7 +590,7 @@ def main():
         "vs_baseline_note": "value / the pages' 37 us (H100, int8 W2): context on other "
                             "hardware and precision" if (cfg.name, B) in PAGES_US else None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": cfg.note, "sampler": args.sampler, "V": cfg.V, "r": cfg.r, "gamma": cfg.gamma, "B": B,
+        "config": {"workload": cfg.note, "sampler": args.sampler, "cell": args.cell, "V": cfg.V, "r": cfg.r, "gamma": cfg.gamma, "B": B,
                    "rounds": n_rounds, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "flushed between timed steps (256 MiB write)",
                    "kernel": label, "n_cta": plan["n_cta"] if label != "batched" else None,
@@ -588,10 +618,14 @@ def main():
         # the group inverse-CDF sampler on the sampled workload (not the configs' sampler)
         line["sweep"] += [measure_config(walk, synth.CONFIGS["sampled"], b, sampler="group")
                           for b in synth.CONFIGS["sampled"].batches]
+        # the recurrent heads on the fully resident long block (B = 1 as the pages
+        # time them, and the largest resident batch)
+        line["sweep"] += [measure_config(walk, synth.CONFIGS["long_block"], b, cell=c)
+                          for c in ("gated", "rnn") for b in (1, 16)]
     if args.gamma_fit:
         line["gamma_fit"] = gamma_fit(walk)
     if rank == 0 and not args.no_cpu_baseline and not args.only_timed:
-        line["cpu_baseline"] = cpu_baseline(cfg, B, rounds, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(cfg, B, rounds, args.cpu_seconds, args.cell)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if not (args.sweep or args.gamma_fit):

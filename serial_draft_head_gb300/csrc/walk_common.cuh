@@ -180,7 +180,7 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits_rn(float x) {
 __device__ __forceinline__ uint16_t cell_element(int cell, float p, float x, float hp) {
   float v;
   if (cell == 1) {
-    const float z = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-p)));
+    const float z = __frcp_rn(__fadd_rn(1.0f, expf(-p)));
     v = __fadd_rn(__fmul_rn(__fsub_rn(1.0f, z), hp), __fmul_rn(z, x));
   } else {
     v = tanhf(__fadd_rn(p, x));

@@ -136,30 +136,77 @@ __device__ __forceinline__ uint16_t* u_elem(uint8_t* U, int i, int b) {
   return reinterpret_cast<uint16_t*>(U + ((i >> 3) * 2 + (b >> 3)) * 128 + (b & 7) * 16) + (i & 7);
 }
 
+// Lane l's share of sum_j m_j h_j over one row: elements 8l .. 8l + 7 (two
+// bf16 per word, exact products), summed in order; a 5-level butterfly over
+// the lanes then completes it (13 fp32 additions deep in all).
+__device__ __forceinline__ float lane_dot(const uint4 m, const uint4 h) {
+  const uint32_t mw[4] = {m.x, m.y, m.z, m.w}, hw[4] = {h.x, h.y, h.z, h.w};
+  float acc = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    acc = __fmaf_rn(bf16_bits_to_float(mw[e] & 0xFFFFu), bf16_bits_to_float(hw[e] & 0xFFFFu), acc);
+    acc = __fmaf_rn(bf16_bits_to_float(mw[e] >> 16), bf16_bits_to_float(hw[e] >> 16), acc);
+  }
+  return acc;
+}
+
+__device__ __forceinline__ float row_dot(const uint4 m, const uint4 h) {
+  float acc = lane_dot(m, h);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, o));
+  return acc;
+}
+
 // A recurrent head's exchange, published with this step's arrival: this CTA's
-// rows of p = M @ h_k for every request (M rows [cta q, cta q + q)), one warp
-// per (row, request): each lane sums its 8 products in order, then a 5-level
-// butterfly adds the lanes (13 fp32 additions deep).
+// rows of p = M @ h_k for every request (M rows [cta q, cta q + q)).  With
+// q <= 8 each warp keeps one row in registers for the whole walk (`mreg`,
+// row cta q + warp % q) and takes every (8 / q)-th request; otherwise (tiny
+// vocabularies on few CTAs) one warp per (row, request), rows read from L2.
 __device__ __forceinline__ void publish_cell_rows(const WalkArgs& a, const uint8_t* U, int k,
-                                                  int cta, int warp, int lane) {
-  const int r0 = cta * a.cell_q;
-  const int nr = kRank - r0 < a.cell_q ? kRank - r0 : a.cell_q;
+                                                  int cta, int warp, int lane, const uint4 mreg) {
+  const int q = a.cell_q, r0 = cta * q;
+  auto u_chunk = [&](int b) {
+    return *reinterpret_cast<const uint4*>(U + (lane * 2 + (b >> 3)) * 128 + (b & 7) * 16);
+  };
+  if (q <= kResWarps) {
+    const int j = warp % q, g = warp / q, G = kResWarps / q;
+    if (g >= G || r0 + j >= kRank) return;
+    if (a.B <= G) {                                 // one request per warp at most
+      if (g < a.B) {
+        const float acc = row_dot(mreg, u_chunk(g));
+        if (lane == 0) a.cell_p[((size_t)k * 16 + g) * kRank + r0 + j] = acc;
+      }
+      return;
+    }
+    for (int b0 = g; b0 < a.B; b0 += 4 * G) {      // four requests' butterflies interleaved
+      float acc[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int b = b0 + t * G;
+        acc[t] = b < a.B ? lane_dot(mreg, u_chunk(b)) : 0.0f;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc[t] = __fadd_rn(acc[t], __shfl_xor_sync(0xFFFFFFFFu, acc[t], o));
+      if (lane == 0)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int b = b0 + t * G;
+          if (b < a.B) a.cell_p[((size_t)k * 16 + b) * kRank + r0 + j] = acc[t];
+        }
+    }
+    return;
+  }
+  const int nr = kRank - r0 < q ? kRank - r0 : q;
   for (int pr = warp; pr < nr * a.B; pr += kResWarps) {
     const int row = r0 + pr / a.B, b = pr % a.B;
     const uint4 m = __ldg(reinterpret_cast<const uint4*>(a.cell_M + (size_t)row * kRank) + lane);
-    const uint4 h = *reinterpret_cast<const uint4*>(U + (lane * 2 + (b >> 3)) * 128 + (b & 7) * 16);
-    const uint32_t mw[4] = {m.x, m.y, m.z, m.w}, hw[4] = {h.x, h.y, h.z, h.w};
-    float acc = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      acc = __fmaf_rn(bf16_bits_to_float(mw[j] & 0xFFFFu), bf16_bits_to_float(hw[j] & 0xFFFFu), acc);
-      acc = __fmaf_rn(bf16_bits_to_float(mw[j] >> 16), bf16_bits_to_float(hw[j] >> 16), acc);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, o));
+    const float acc = row_dot(m, u_chunk(b));
     if (lane == 0) a.cell_p[((size_t)k * 16 + b) * kRank + row] = acc;
   }
 }
+
 
 // In-place first half of the fused epilogue: base_s[b][rl] (the bf16 base
 // logit) becomes bf16(base + bf16(acc)), the logit the token is chosen from,
@@ -338,6 +385,30 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
 
 // CELL: the instantiation that also runs the recurrent heads and writes the
 // state output (the Markov-only one carries none of that code).
+// A recurrent head's next state for request b, lane l's elements 8l .. 8l + 7
+// (p from L2, the winner's W1 row, the current state in U, updated in place).
+__device__ __forceinline__ void cell_update_row(const WalkArgs& a, uint8_t* U, int k, int b,
+                                                int32_t tok, int lane) {
+  const float4* pp =
+      reinterpret_cast<const float4*>(a.cell_p + ((size_t)k * 16 + b) * kRank) + 2 * lane;
+  const float4 p0 = __ldcg(pp), p1 = __ldcg(pp + 1);
+  const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok * kRank) + lane);
+  uint4* hp = reinterpret_cast<uint4*>(U + (lane * 2 + (b >> 3)) * 128 + (b & 7) * 16);
+  const uint4 hv = *hp;
+  const float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+  const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, hw[4] = {hv.x, hv.y, hv.z, hv.w};
+  uint32_t ow[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t lo = cell_element(a.cell, p[2 * e], bf16_bits_to_float(xw[e] & 0xFFFFu),
+                                     bf16_bits_to_float(hw[e] & 0xFFFFu));
+    const uint32_t hi = cell_element(a.cell, p[2 * e + 1], bf16_bits_to_float(xw[e] >> 16),
+                                     bf16_bits_to_float(hw[e] >> 16));
+    ow[e] = lo | (hi << 16);
+  }
+  *hp = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+}
+
 template <int RS, int NT, int SMAX, bool CELL>
 __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const ResidentArgs ra) {
   constexpr int NCOL = 8 * NT;
@@ -501,6 +572,13 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
   __syncthreads();
   trace_stamp(a, a.gamma, 2);
 
+  // a recurrent head's row of M for this warp (see publish_cell_rows)
+  uint4 mreg = make_uint4(0u, 0u, 0u, 0u);
+  if (CELL && a.cell != 0 && a.cell_q <= kResWarps) {
+    const int row = cta * a.cell_q + warp % a.cell_q;
+    if (row < kRank)
+      mreg = __ldg(reinterpret_cast<const uint4*>(a.cell_M + (size_t)row * kRank) + lane);
+  }
   const KeyPassMap kpm = key_pass_map(a.B, temp_s);
   const uint2 eseed = round_seed(a, round_s);             // this round's Philox key
   const int nslots = kpm.tpr >= 32 ? kpm.tpr / 32 : 1;   // group_best slots per request
@@ -680,7 +758,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
       }
     }
     // (4a) a recurrent head's rows of M @ h_k, released with this step's arrival
-    if (CELL && a.cell != 0 && k + 1 < a.gamma) publish_cell_rows(a, U, k, cta, warp, lane);
+    if (CELL && a.cell != 0 && k + 1 < a.gamma) publish_cell_rows(a, U, k, cta, warp, lane, mreg);
     ptx::tc_fence_before();
     __syncthreads();
 
@@ -749,6 +827,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
           }
         }
         __syncwarp();
+        // a recurrent head's single request: its next state, here
         // up to four rows: warp 0 fetches them here (larger batches are
         // fetched by all warps after the barrier below)
         for (int b0 = 0; b0 < (a.B <= 4 && !(CELL && a.cell != 0) ? a.B : 0); b0 += 4) {
@@ -782,15 +861,22 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
       __syncthreads();
     }
     if (CELL && a.cell != 0 && abort_s == 0 && k + 1 < a.gamma) {
-      // a recurrent head's next state, every CTA alike: thread i updates
-      // element i of each request from p (all CTAs' rows, visible since the
-      // arrivals were acquired), the winner's W1 row and the current state
-      const int i = threadIdx.x;
-      for (int b = 0; b < a.B; ++b) {
-        const float p = ld_relaxed_gpu_f32(a.cell_p + ((size_t)k * 16 + b) * kRank + i);
-        const float x = bf16_bits_to_float(__ldg(a.W1 + (size_t)tok_s[b] * kRank + i));
-        uint16_t* hu = u_elem(U, i, b);
-        *hu = cell_element(a.cell, p, x, bf16_bits_to_float(*hu));
+      // a recurrent head's next states, every CTA alike, from p (all CTAs'
+      // rows of M @ h, read from L2 where the released stores landed), the
+      // winner's W1 row and the current state.  One or two requests: thread i
+      // updates element i (the gate or tanh of 256 elements side by side);
+      // more: warp w updates requests w, w + 8, lane l elements 8l .. 8l + 7
+      // (one 16-byte chunk of each operand per lane, fewer round trips)
+      if (a.B <= 2) {
+        const int i = threadIdx.x;
+        for (int b = 0; b < a.B; ++b) {
+          const float p = ld_relaxed_gpu_f32(a.cell_p + ((size_t)k * 16 + b) * kRank + i);
+          const float x = bf16_bits_to_float(__ldg(a.W1 + (size_t)tok_s[b] * kRank + i));
+          uint16_t* hu = u_elem(U, i, b);
+          *hu = cell_element(a.cell, p, x, bf16_bits_to_float(*hu));
+        }
+      } else {
+        for (int b = warp; b < a.B; b += kResWarps) cell_update_row(a, U, k, b, tok_s[b], lane);
       }
       ptx::fence_proxy_async_smem();
       __syncthreads();
