@@ -171,13 +171,14 @@ class Oracle:
 
     def walk_cell(self, W1, W2, base, anchor, temperature, seed, cell, M=None, forced=None,
                   forced_state=None, want_logits=True, want_scores=False, nthreads=1, req0=0,
-                  sampler=0):
+                  sampler=0, want_groups=False):
         """A recurrent head's walk (cell 1 gated, 2 RNN; 0 is the Markov head).
 
         M: uint16 [r, r] recurrent matrix; forced_state: optional uint16
         [B, gamma, r] (step k updates from forced_state[b, k-1] and projects
         forced_state[b, k]).  Returns (tokens, logits, scores, states uint16
-        [B, gamma, r], states_exact float64 [B, gamma, r]).
+        [B, gamma, r], states_exact float64 [B, gamma, r]), and with want_groups a
+        6th item as ``walk``'s 4th (sampler 1's group scores, picks, margins).
         """
         W1 = np.ascontiguousarray(W1, dtype=np.uint16)
         W2 = np.ascontiguousarray(W2, dtype=np.uint16)
@@ -210,13 +211,23 @@ class Oracle:
         scores = np.zeros((B, gamma, V), dtype=np.float32) if want_scores else None
         states = np.zeros((B, gamma, r), dtype=np.uint16)
         exact = np.zeros((B, gamma, r), dtype=np.float64)
+        ng = (V + 7) // 8
+        groups = None
+        if want_groups:
+            groups = (np.zeros((B, gamma, ng), dtype=np.float32),
+                      np.zeros((B, gamma, ng), dtype=np.int32),
+                      np.zeros((B, gamma, ng), dtype=np.float32))
         ptr = lambda a: a.ctypes.data if a is not None else None
         rc = self.L.orc_walk3(
             W1, W2, V, r, base, anchor, temperature, int(seed) & (2**64 - 1), B, gamma,
             int(req0), ptr(forced_arr), int(sampler), int(cell), ptr(Mc), ptr(fs), tokens,
-            ptr(logits), ptr(scores), None, None, None, ptr(states), ptr(exact), int(nthreads))
+            ptr(logits), ptr(scores),
+            ptr(groups[0]) if groups else None, ptr(groups[1]) if groups else None,
+            ptr(groups[2]) if groups else None, ptr(states), ptr(exact), int(nthreads))
         if rc != 0:
             raise OracleError("oracle walk rejected its input (code %d)" % rc)
+        if want_groups:
+            return tokens, logits, scores, states, exact, groups
         return tokens, logits, scores, states, exact
 
     def cell_update(self, cell, M, hprev, x):

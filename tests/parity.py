@@ -160,12 +160,15 @@ def check(inputs: "synth.WalkInputs", gpu_tokens, gpu_logits=None, requests=None
         gs = None
         if cell != 0:
             gs = np.asarray(gpu_states[b]).astype(np.uint16)
-            ot, ol, osc, ost, oex = O.walk_cell(
+            group = sampler == 1 and T != 0.0
+            res = O.walk_cell(
                 W1, W2, base_all[b:b + 1], np.array([inputs.anchor[b]], np.int32),
                 np.array([T], np.float32), inputs.seed, cell, M=M, forced=toks[None, :],
-                forced_state=gs[None], want_scores=T != 0.0, nthreads=nthreads, req0=b)
+                forced_state=gs[None], want_scores=T != 0.0 and not group,
+                nthreads=nthreads, req0=b, sampler=sampler, want_groups=group)
+            ot, ol, osc, ost, oex = res[:5]
             ot, ol, osc = ot[0], ol[0], (osc[0] if osc is not None else None)
-            grp = None
+            grp = tuple(g_[0] for g_ in res[5]) if group else None
         else:
             ot, ol, osc, grp = _oracle_request(O, W1, W2, base_all, inputs, b, toks, nthreads,
                                                sampler)

@@ -608,3 +608,45 @@ def test_cell_rejections(walkmod):
     st, toks, lg = gpu_run(w, x)                    # the Markov head still runs there
     assert st == 0 and parity.check(x, toks, lg).ok()
     w.close()
+
+
+def test_cell_graph_replay_and_group_sampler(walkmod):
+    """A recurrent head inside a captured CUDA graph replays identically (the
+    exchange buffer needs no reset), and it composes with the group sampler."""
+    x = synth.make_custom(V=9000, gamma=6, B=3, seed=69, temperatures=(0.0, 1.0, 0.6),
+                          noise_seed=79)
+    M = synth.make_cell_matrix(69)
+    Md = M.cuda()
+    w = make_walk(walkmod, x)
+    states = torch.empty(3, 6, 256, dtype=torch.bfloat16, device="cuda")
+    w.set_cell(walkmod.CELL_GATED, Md)
+    w.set_state_output(states)
+    base, anchor, temp = x.base.cuda(), x.anchor.cuda(), x.temperature.cuda()
+    tokens = torch.full((3, 6), -2, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        w.run(base, anchor, temp, x.seed, tokens, stream=s)
+    s.synchronize()
+    eager, eager_states = tokens.clone(), states.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        w.run(base, anchor, temp, x.seed, tokens, stream=s)
+    for _ in range(4):
+        tokens.fill_(-2)
+        states.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(tokens, eager) and torch.equal(states, eager_states)
+    assert w.status() == 0
+    rep = parity.check(x, eager.cpu().numpy(), cell=1, M=synth.bits(M),
+                       gpu_states=synth.bits(eager_states.cpu()))
+    assert rep.ok(), rep
+    del g
+    # the same head with the group inverse-CDF sampler
+    w.set_sampler(walkmod.SAMPLER_GROUP)
+    st, toks, lg = gpu_run(w, x)
+    assert st == 0
+    rep = parity.check(x, toks, lg, cell=1, M=synth.bits(M), sampler=1,
+                       gpu_states=synth.bits(states.cpu()))
+    assert rep.ok(), rep
+    w.close()

@@ -149,3 +149,14 @@ def test_cell_accepts_a_flip_at_a_midpoint_only():
     st3[0, 1, i] = other
     rep = parity.check(x, t, None, cell=1, M=M, gpu_states=st3)
     assert rep.ok() and rep.states_flipped == 1, rep
+
+
+def test_cell_with_group_sampler_accepts_the_oracle_itself():
+    x = synth.make_custom(V=400, gamma=3, B=3, seed=28, temperatures=(0.0, 1.0, 0.6),
+                          noise_seed=8)
+    M = synth.bits(synth.make_cell_matrix(9))
+    t, lg, _, st, _ = oracle.walk_cell(synth.bits(x.W1), synth.bits(x.W2), synth.bits(x.base),
+                                       x.anchor.numpy(), x.temperature.numpy(), x.seed, 2, M=M,
+                                       sampler=1)
+    rep = parity.check(x, t, lg, cell=2, M=M, gpu_states=st, sampler=1)
+    assert rep.ok() and rep.steps_exact == rep.steps_checked, rep
