@@ -69,7 +69,7 @@ class Oracle:
             _u16p, _u16p, ctypes.c_int64, ctypes.c_int,
             _u16p, _i32p, _f32p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
-            _i32p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, _i32p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
         ]
@@ -171,10 +171,11 @@ class Oracle:
 
     def walk_cell(self, W1, W2, base, anchor, temperature, seed, cell, M=None, forced=None,
                   forced_state=None, want_logits=True, want_scores=False, nthreads=1, req0=0,
-                  sampler=0, want_groups=False):
-        """A recurrent head's walk (cell 1 gated, 2 RNN; 0 is the Markov head).
+                  sampler=0, want_groups=False, X=None):
+        """A recurrent head's walk (cell 1 gated, 2 RNN, 3 GRU; 0 is the Markov head).
 
-        M: uint16 [r, r] recurrent matrix; forced_state: optional uint16
+        M: uint16 [r, r] recurrent matrix ([3r, r] for the GRU); X: the GRU's
+        token tables, uint16 [3, V, r]; forced_state: optional uint16
         [B, gamma, r] (step k updates from forced_state[b, k-1] and projects
         forced_state[b, k]).  Returns (tokens, logits, scores, states uint16
         [B, gamma, r], states_exact float64 [B, gamma, r]), and with want_groups a
@@ -191,11 +192,15 @@ class Oracle:
         B, gamma, Vb = base.shape
         if Vb != V or anchor.shape != (B,) or temperature.shape != (B,):
             raise ValueError("base must be [B, gamma, V]; anchor and temperature [B]")
-        Mc = None
+        Mc = Xc = None
         if M is not None:
             Mc = np.ascontiguousarray(M, dtype=np.uint16)
-            if Mc.shape != (r, r):
-                raise ValueError("M must be [r, r]")
+            if Mc.shape != ((3 * r, r) if cell == 3 else (r, r)):
+                raise ValueError("M must be [r, r] ([3r, r] for the GRU)")
+        if X is not None:
+            Xc = np.ascontiguousarray(X, dtype=np.uint16)
+            if Xc.shape != (3, V, r):
+                raise ValueError("X must be [3, V, r]")
         fs = None
         if forced_state is not None:
             fs = np.ascontiguousarray(forced_state, dtype=np.uint16)
@@ -220,7 +225,7 @@ class Oracle:
         ptr = lambda a: a.ctypes.data if a is not None else None
         rc = self.L.orc_walk3(
             W1, W2, V, r, base, anchor, temperature, int(seed) & (2**64 - 1), B, gamma,
-            int(req0), ptr(forced_arr), int(sampler), int(cell), ptr(Mc), ptr(fs), tokens,
+            int(req0), ptr(forced_arr), int(sampler), int(cell), ptr(Mc), ptr(Xc), ptr(fs), tokens,
             ptr(logits), ptr(scores),
             ptr(groups[0]) if groups else None, ptr(groups[1]) if groups else None,
             ptr(groups[2]) if groups else None, ptr(states), ptr(exact), int(nthreads))
@@ -231,9 +236,10 @@ class Oracle:
         return tokens, logits, scores, states, exact
 
     def cell_update(self, cell, M, hprev, x):
-        """One state update: (h bf16 bits [r], the fp64 values before rounding)."""
+        """One state update: (h bf16 bits [r], the fp64 values before rounding);
+        for the GRU x holds the token's three table rows ([3r])."""
         x = np.ascontiguousarray(x, dtype=np.uint16)
-        r = x.shape[0]
+        r = x.shape[0] // 3 if cell == 3 else x.shape[0]
         M = np.ascontiguousarray(M, dtype=np.uint16)
         hp = None if hprev is None else np.ascontiguousarray(hprev, dtype=np.uint16)
         h = np.zeros(r, np.uint16)
@@ -299,7 +305,7 @@ def walk_cell(*args, **kwargs):
     return default().walk_cell(*args, **kwargs)
 
 
-CELL_MARKOV, CELL_GATED, CELL_RNN = 0, 1, 2
+CELL_MARKOV, CELL_GATED, CELL_RNN, CELL_GRU = 0, 1, 2, 3
 
 
 def cpu_threads(nthreads):

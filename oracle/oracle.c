@@ -60,6 +60,11 @@
  *   h_{-1} = 0; x_k = W1[prev_k] (prev_0 = anchor); p_k = M @ h_{k-1} (fp64);
  *   gated: z = 1 / (1 + exp(-p_k)), h_k = bf16((1 - z) * h_{k-1} + z * x_k);
  *   RNN:   h_k = bf16(tanh(p_k + x_k));
+ *   GRU (cell = 3; the page's GRU heads): three token tables X_r, X_z, X_n
+ *   [V, r] stand for the input projections folded into per-token rows, and
+ *   M stacks three recurrent matrices [3r, r]; with p_g = M_g @ h_{k-1},
+ *   r = sig(X_r[prev] + p_r), z = sig(X_z[prev] + p_z),
+ *   n = tanh(X_n[prev] + r * p_n), h_k = bf16((1 - z) * n + z * h_{k-1});
  *   the projected vector is u_k = h_k; each element's value is formed in fp64
  *   and rounded to bf16 once.
  */
@@ -280,31 +285,54 @@ int64_t orc_group_sample(const uint16_t *logit, int64_t V, float T, uint64_t see
 #define ORC_CELL_MARKOV 0
 #define ORC_CELL_GATED 1
 #define ORC_CELL_RNN 2
+#define ORC_CELL_GRU 3
+
+static double orc_sigmoid(double t) { return 1.0 / (1.0 + exp(-t)); }
+
+/* fp64 dot product sum_j a[j * stride] b[j] of bf16 values, in j order */
+static double orc_row_dot(const uint16_t *a, int64_t stride, const uint16_t *b, int r)
+{
+    double s = 0.0;
+    for (int j = 0; j < r; ++j)
+        s += orc_bf16_to_f64(a[j * stride]) * orc_bf16_to_f64(b[j]);
+    return s;
+}
 
 /*
  * One state update of a recurrent head (see the header): from the previous
- * state hprev (bf16 bits, r; NULL means h = 0) and the token's row x of W1,
+ * state hprev (bf16 bits, r; NULL means h = 0) and the token's input row x,
  * h[i] = bf16(value_i) with value_i formed in fp64 from p_i = M[i, :] . hprev.
- * M is bf16 bits, [r, r] row-major.  exact (optional, r) receives value_i.
+ * Gated / RNN: M is bf16 bits [r, r] and x the token's W1 row (r).  GRU: M is
+ * [3r, r] (the r-, z- and n-gate matrices) and x holds the token's rows of
+ * the three tables one after another (3r).  exact (optional, r) receives
+ * value_i.
  */
 void orc_cell_update(int cell, const uint16_t *M, int r, const uint16_t *hprev,
                      const uint16_t *x, uint16_t *h, double *exact)
 {
     for (int i = 0; i < r; ++i) {
-        double p = 0.0;                                  /* M[i, :] . h_{k-1} */
-        if (hprev)
-            for (int j = 0; j < r; ++j)
-                p += orc_bf16_to_f64(M[(int64_t)i * r + j]) * orc_bf16_to_f64(hprev[j]);
         const double hp = hprev ? orc_bf16_to_f64(hprev[i]) : 0.0;
         const double xi = orc_bf16_to_f64(x[i]);
         double val;
-        if (cell == ORC_CELL_GATED) {
-            const double z = 1.0 / (1.0 + exp(-p));     /* update gate */
-            val = (1.0 - z) * hp + z * xi;
-        } else if (cell == ORC_CELL_RNN) {
-            val = tanh(p + xi);
+        if (cell == ORC_CELL_GRU) {
+            double pg[3] = {0.0, 0.0, 0.0};              /* M_g[i, :] . h_{k-1} */
+            if (hprev)
+                for (int g = 0; g < 3; ++g)
+                    pg[g] = orc_row_dot(M + ((int64_t)g * r + i) * r, 1, hprev, r);
+            const double rg = orc_sigmoid(xi + pg[0]);                       /* reset */
+            const double zg = orc_sigmoid(orc_bf16_to_f64(x[r + i]) + pg[1]); /* update */
+            const double ng = tanh(orc_bf16_to_f64(x[2 * r + i]) + rg * pg[2]);
+            val = (1.0 - zg) * ng + zg * hp;
         } else {
-            val = xi;                                    /* Markov: u = W1[prev] */
+            const double p = hprev ? orc_row_dot(M + (int64_t)i * r, 1, hprev, r) : 0.0;
+            if (cell == ORC_CELL_GATED) {
+                const double z = 1.0 / (1.0 + exp(-p)); /* update gate */
+                val = (1.0 - z) * hp + z * xi;
+            } else if (cell == ORC_CELL_RNN) {
+                val = tanh(p + xi);
+            } else {
+                val = xi;                                /* Markov: u = W1[prev] */
+            }
         }
         h[i] = orc_bf16_rne(val);
         if (exact)
@@ -335,8 +363,9 @@ void orc_cell_update(int cell, const uint16_t *M, int r, const uint16_t *hprev,
  *   out_gscore, out_gpick, out_gmargin  optional [B, gamma, ceil(V / 8)]:
  *              under sampler 1 with T > 0, each group's score, in-group pick
  *              and the pick's margin (see orc_group_sample)
- *   cell       0: Markov (u = W1[prev]); 1: gated; 2: RNN (see the header)
- *   M          the recurrent matrix, bf16 bits [r, r] (cells 1 and 2)
+ *   cell       0: Markov (u = W1[prev]); 1: gated; 2: RNN; 3: GRU (see the header)
+ *   M          the recurrent matrix, bf16 bits [r, r] (cells 1 and 2), [3r, r] (GRU)
+ *   X          the GRU's token tables, bf16 bits [3, V, r] (cell 3 only)
  *   forced_state  optional [B, gamma, r] bf16 bits: when given (with a
  *              cell), step k updates the state from forced_state[b, k-1]
  *              and projects forced_state[b, k] (teacher forcing of the
@@ -351,16 +380,19 @@ void orc_cell_update(int cell, const uint16_t *M, int r, const uint16_t *hprev,
 int orc_walk3(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
               const uint16_t *base, const int32_t *anchor, const float *T,
               uint64_t seed, int B, int gamma, int req0, const int32_t *forced,
-              int sampler, int cell, const uint16_t *M, const uint16_t *forced_state,
+              int sampler, int cell, const uint16_t *M, const uint16_t *X,
+              const uint16_t *forced_state,
               int32_t *out_tokens, uint16_t *out_logits, float *out_scores,
               float *out_gscore, int32_t *out_gpick, float *out_gmargin,
               uint16_t *out_state, double *out_state_exact, int nthreads)
 {
     if (sampler != 0 && sampler != 1)
         return ORC_EINVAL;
-    if (cell != ORC_CELL_MARKOV && cell != ORC_CELL_GATED && cell != ORC_CELL_RNN)
+    if (cell < ORC_CELL_MARKOV || cell > ORC_CELL_GRU)
         return ORC_EINVAL;
     if (cell != ORC_CELL_MARKOV && !M)
+        return ORC_EINVAL;
+    if (cell == ORC_CELL_GRU && !X)
         return ORC_EINVAL;
     if (V <= 0 || r <= 0 || B < 0 || gamma < 0 || req0 < 0)
         return ORC_EINVAL;
@@ -381,11 +413,13 @@ int orc_walk3(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
     double *score = (double *)malloc((size_t)V * sizeof *score);
     uint16_t *hbuf = (uint16_t *)malloc(2 * (size_t)r * sizeof *hbuf);   /* h_{k-1}, h_k */
     double *hex = (double *)malloc((size_t)r * sizeof *hex);
-    if (!logit || !score || !hbuf || !hex) {
+    uint16_t *xin = (uint16_t *)malloc(3 * (size_t)r * sizeof *xin);      /* GRU rows */
+    if (!logit || !score || !hbuf || !hex || !xin) {
         free(logit);
         free(score);
         free(hbuf);
         free(hex);
+        free(xin);
         return ORC_EINVAL;
     }
     for (int b = 0; b < B; ++b) {
@@ -401,7 +435,14 @@ int orc_walk3(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
                     hprev = forced_state ? forced_state + ((int64_t)b * gamma + (k - 1)) * r
                                          : hbuf;
                 uint16_t *hk = hbuf + r;
-                orc_cell_update(cell, M, r, hprev, u, hk, hex);
+                const uint16_t *x = u;                     /* the token's input row(s) */
+                if (cell == ORC_CELL_GRU) {
+                    for (int g = 0; g < 3; ++g)
+                        memcpy(xin + (size_t)g * r, X + ((int64_t)g * V + prev) * r,
+                               (size_t)r * sizeof *xin);
+                    x = xin;
+                }
+                orc_cell_update(cell, M, r, hprev, x, hk, hex);
                 if (out_state)
                     memcpy(out_state + ((int64_t)b * gamma + k) * r, hk, (size_t)r * sizeof *hk);
                 if (out_state_exact)
@@ -457,6 +498,7 @@ int orc_walk3(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
     free(score);
     free(hbuf);
     free(hex);
+    free(xin);
     return ORC_OK;
 }
 
@@ -468,7 +510,7 @@ int orc_walk2(const uint16_t *W1, const uint16_t *W2, int64_t V, int r,
               float *out_gscore, int32_t *out_gpick, float *out_gmargin, int nthreads)
 {
     return orc_walk3(W1, W2, V, r, base, anchor, T, seed, B, gamma, req0, forced, sampler,
-                     ORC_CELL_MARKOV, NULL, NULL, out_tokens, out_logits, out_scores,
+                     ORC_CELL_MARKOV, NULL, NULL, NULL, out_tokens, out_logits, out_scores,
                      out_gscore, out_gpick, out_gmargin, NULL, NULL, nthreads);
 }
 

@@ -12,8 +12,9 @@ of the same shapes stand in for them:
 * W1 [V, r] ~ N(0, 1) / 16 and W2 [V, r] ~ N(0, 1), so W2 @ W1[p] ~ N(0, 1);
 * base logits [B, gamma, V] ~ N(0, sigma^2);
 * anchors uniform in [0, V); temperatures per request;
-* a recurrent head's matrix M [r, r] ~ N(0, 1) / 16 (``make_cell_matrix``), so
-  M @ h is of the size of the W1 rows it is added to.
+* a recurrent head's matrix M [r, r] ~ N(0, 1) / 16 (``make_cell_matrix``; [3r, r]
+  for the GRU), so M @ h is of the size of the W1 rows it is added to, and the
+  GRU's token tables [3, V, r] ~ N(0, 1) / 16 (``make_cell_tables``).
 
 Every tensor is drawn in fp32 from ``torch.Generator('cpu')`` and rounded to
 bf16 by PyTorch's cast: W1 then W2 from the config's weight seed, then base
@@ -156,7 +157,15 @@ def make_custom(V: int, gamma: int, B: int, seed: int, r: int = RANK,
                       meta={"config": "custom", "V": V, "B": B, "seed": seed})
 
 
-def make_cell_matrix(seed: int, r: int = RANK) -> torch.Tensor:
-    """A recurrent head's bf16 matrix M [r, r] ~ N(0, 1) / 16 (synthetic weights)."""
+def make_cell_matrix(seed: int, r: int = RANK, rows: Optional[int] = None) -> torch.Tensor:
+    """A recurrent head's bf16 matrix M [rows, r] ~ N(0, 1) / 16 (synthetic
+    weights); rows = r, or 3r for the GRU's three gate matrices stacked."""
     g = torch.Generator("cpu").manual_seed(seed)
-    return (torch.randn(r, r, generator=g) / 16).to(torch.bfloat16)
+    return (torch.randn(rows or r, r, generator=g) / 16).to(torch.bfloat16)
+
+
+def make_cell_tables(V: int, seed: int, r: int = RANK) -> torch.Tensor:
+    """The GRU head's three bf16 token tables [3, V, r] ~ N(0, 1) / 16 (the input
+    projections folded into per-token rows; synthetic weights)."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    return (torch.randn(3, V, r, generator=g) / 16).to(torch.bfloat16)

@@ -106,24 +106,26 @@ CELL_TOL = 2.0**-20
 
 def _check_states(O, rep, cell, M, W1, gh_prev, x_tok, gh, oh, oex, b, k):
     """GPU state gh [r] against the oracle's update oh / oex of the GPU's own
-    previous state gh_prev (None at step 0) and token row x_tok."""
+    previous state gh_prev (None at step 0) and token input rows x_tok ([r],
+    or [3, r] for the GRU)."""
     rep.states_checked += gh.size
     same = gh == oh
     rep.states_exact += int(same.sum())
     bad = np.nonzero(~same)[0]
     if bad.size == 0:
         return
-    Mv = bf16_vals(M)
-    hp = np.zeros(gh.size) if gh_prev is None else bf16_vals(gh_prev)
-    p = Mv @ hp
-    mass = np.abs(Mv) @ np.abs(hp)
-    x = bf16_vals(x_tok)
+    r = gh.size
+    Mv = bf16_vals(M).reshape(-1, r, r)                 # one or three gate matrices
+    hp = np.zeros(r) if gh_prev is None else bf16_vals(gh_prev)
+    p = np.abs(Mv @ hp).sum(axis=0)
+    mass = (np.abs(Mv) @ np.abs(hp)).sum(axis=0)
+    x = np.abs(bf16_vals(x_tok).reshape(-1, r)).sum(axis=0)
     gv, ov = bf16_vals(gh), bf16_vals(oh)
     for i in bad:
         ex = float(oex[i])
         mid = 0.5 * (gv[i] + ov[i])
         neighbours = abs(gv[i] - ov[i]) <= bf16_ulp(max(abs(gv[i]), abs(ov[i])))
-        tol = CELL_TOL * (mass[i] + 1.0 + abs(p[i]) + abs(x[i]) + abs(hp[i]))
+        tol = CELL_TOL * (mass[i] + 1.0 + p[i] + x[i] + abs(hp[i]))
         if neighbours and (gv[i] - ex) * (ov[i] - ex) <= 0 and abs(ex - mid) <= tol:
             rep.states_flipped += 1
             continue
@@ -131,13 +133,15 @@ def _check_states(O, rep, cell, M, W1, gh_prev, x_tok, gh, oh, oex, b, k):
 
 
 def check(inputs: "synth.WalkInputs", gpu_tokens, gpu_logits=None, requests=None,
-          nthreads=0, O=None, report=None, sampler=0, cell=0, M=None, gpu_states=None):
+          nthreads=0, O=None, report=None, sampler=0, cell=0, M=None, gpu_states=None,
+          X=None):
     """Check the GPU's tokens [B, gamma] (and logits [B, gamma, V]) for `requests`.
 
     sampler 0: per-token Gumbel-max; 1: group inverse-CDF (a GPU token may
     differ from the oracle's only at a group-score near-tie, then being that
     group's pick, or next to a pick whose running sum sits at the threshold).
-    cell 1 or 2 (a recurrent head with matrix M, bits [r, r]): gpu_states
+    cell 1, 2 or 3 (a recurrent head with matrix M, bits [r, r] or [3r, r],
+    and for the GRU the token tables X, bits [3, V, r]): gpu_states
     [B, gamma, r] are the GPU's states; each step's state is checked against
     the oracle's update of the GPU's previous state and token (see CELL_TOL),
     and the step's logits against the oracle's projection of the GPU state.
@@ -165,7 +169,7 @@ def check(inputs: "synth.WalkInputs", gpu_tokens, gpu_logits=None, requests=None
                 W1, W2, base_all[b:b + 1], np.array([inputs.anchor[b]], np.int32),
                 np.array([T], np.float32), inputs.seed, cell, M=M, forced=toks[None, :],
                 forced_state=gs[None], want_scores=T != 0.0 and not group,
-                nthreads=nthreads, req0=b, sampler=sampler, want_groups=group)
+                nthreads=nthreads, req0=b, sampler=sampler, want_groups=group, X=X)
             ot, ol, osc, ost, oex = res[:5]
             ot, ol, osc = ot[0], ol[0], (osc[0] if osc is not None else None)
             grp = tuple(g_[0] for g_ in res[5]) if group else None
@@ -177,7 +181,8 @@ def check(inputs: "synth.WalkInputs", gpu_tokens, gpu_logits=None, requests=None
             ok_row = ol[k]
             prev = int(inputs.anchor[b]) if k == 0 else int(toks[k - 1])
             if cell != 0:
-                _check_states(O, rep, cell, M, W1, gs[k - 1] if k > 0 else None, W1[prev],
+                xt = X[:, prev] if cell == 3 else W1[prev]
+                _check_states(O, rep, cell, M, W1, gs[k - 1] if k > 0 else None, xt,
                               gs[k], ost[0, k], oex[0, k], b, k)
             if gpu_logits is not None:
                 gl = np.asarray(gpu_logits[b, k])

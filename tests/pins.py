@@ -676,27 +676,104 @@ def pin_cell_rnn_permutation(O):
         assert np.array_equal(_from_bits(st[0, k]), h), "RNN permutation: state %d" % k
 
 
+def _gru_tables(V, seed, r_fill=None, z_fill=None):
+    """The GRU's three token tables [3, V, 256] ~ N(0,1)/16, with the r- and
+    z-tables optionally set to a constant."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    X = torch.randn(3, V, 256, generator=g) / 16
+    if r_fill is not None:
+        X[0] = r_fill
+    if z_fill is not None:
+        X[1] = z_fill
+    return _bits_of(X)
+
+
+def pin_cell_gru_reduces_to_rnn(O):
+    """GRU with M = 0 and a shut update gate (X_z = -40: z < 5e-18) is the
+    Markov walk over the table bf16(tanh(X_n)), whatever the reset gate."""
+    V, gamma = 450, 5
+    W1, W2, base, anchor = _cell_inputs(V, gamma, 50)
+    M = np.zeros((768, 256), np.uint16)
+    T = np.zeros(1, np.float32)
+    for r_fill in (None, -40.0, 40.0):
+        X = _gru_tables(V, 51, r_fill=r_fill, z_fill=-40.0)
+        t, lg, _, st, _ = O.walk_cell(W1, W2, base, anchor, T, 0, 3, M=M, X=X)
+        Xn = O.bf16_rne(np.tanh(_from_bits(X[2])).ravel()).reshape(V, 256)
+        tm, lm, _ = O.walk(Xn, W2, base, anchor, T, 0)
+        assert np.array_equal(t, tm) and np.array_equal(lg, lm), \
+            "GRU with M = 0, z = 0 must walk like Markov over tanh(X_n)"
+        prev = [int(anchor[0])] + [int(v) for v in t[0, :-1]]
+        assert np.array_equal(st[0], Xn[prev]), "GRU with M = 0, z = 0: state = tanh(X_n[prev])"
+
+
+def pin_cell_gru_hold(O):
+    """GRU with an open update gate (X_z = +40) keeps h = h_{-1} = 0: logits
+    equal base and tokens are argmax(base)."""
+    V, gamma = 300, 4
+    W1, W2, base, anchor = _cell_inputs(V, gamma, 52)
+    g = torch.Generator("cpu").manual_seed(53)
+    M = _bits_of(torch.randn(768, 256, generator=g) / 16)
+    X = _gru_tables(V, 54, z_fill=40.0)
+    T = np.zeros(1, np.float32)
+    t, lg, _, st, _ = O.walk_cell(W1, W2, base, anchor, T, 0, 3, M=M, X=X)
+    assert not np.any(_from_bits(st)), "GRU, open update gate: the state stays 0"
+    assert np.array_equal(_from_bits(lg[0]), _from_bits(base[0])), "GRU hold: logits = base"
+    assert np.array_equal(t[0], np.argmax(_from_bits(base[0]), axis=1)), "GRU hold: argmax"
+
+
+def pin_cell_gru_permutation(O):
+    """GRU with U_r = U_z = 0, U_n = a * P, a shut update gate and an open
+    reset gate on a constant token path: element i follows the scalar map
+    h_i <- tanh(x_n,i + a h_pi(i)); with the reset gate shut instead,
+    h_i = tanh(x_n,i) every step."""
+    V, gamma, t0 = 300, 6, 77
+    W1, W2, base, anchor = _cell_inputs(V, gamma, 55, spike_token=t0)
+    g = torch.Generator("cpu").manual_seed(56)
+    pi = torch.randperm(256, generator=g).numpy()
+    a = 0.75
+    Mf = torch.zeros(768, 256)
+    Mf[512 + torch.arange(256), torch.from_numpy(pi)] = a
+    M = _bits_of(Mf)
+    T = np.zeros(1, np.float32)
+    for r_fill in (40.0, -40.0):
+        X = _gru_tables(V, 57, r_fill=r_fill, z_fill=-40.0)
+        t, _, _, st, _ = O.walk_cell(W1, W2, base, anchor, T, 0, 3, M=M, X=X)
+        assert np.all(t == t0), "the spike must hold the token path"
+        xn = _from_bits(X[2, t0])
+        h = np.zeros(256)
+        for k in range(gamma):
+            pre = xn + a * h[pi] if r_fill > 0 else xn
+            h = _from_bits(O.bf16_rne(np.tanh(pre)))
+            assert np.array_equal(_from_bits(st[0, k]), h), \
+                "GRU permutation (reset %+g): state %d" % (r_fill, k)
+
+
 def pin_cell_batch_and_forcing(O):
     """Each request keeps its own state (alone == in a batch), and forcing a
     walk with its own tokens and states changes nothing."""
     import synth
     x = synth.make_custom(V=333, gamma=4, B=3, seed=48, temperatures=(0.0, 1.0, 0.6))
     g = torch.Generator("cpu").manual_seed(49)
-    M = _bits_of(torch.randn(256, 256, generator=g) / 16)
+    M1 = _bits_of(torch.randn(256, 256, generator=g) / 16)
+    M3 = _bits_of(torch.randn(768, 256, generator=g) / 16)
+    X = _gru_tables(333, 58)
     bits = synth.bits
-    for cell in (1, 2):
+    for cell in (1, 2, 3):
+        M = M3 if cell == 3 else M1
+        kw = {"M": M, "X": X if cell == 3 else None}
         args = (bits(x.W1), bits(x.W2))
         t, lg, _, st, _ = O.walk_cell(*args, bits(x.base), x.anchor.numpy(),
-                                      x.temperature.numpy(), 77, cell, M=M)
+                                      x.temperature.numpy(), 77, cell, **kw)
         for b in range(3):
             tb, lb, _, sb, _ = O.walk_cell(*args, bits(x.base[b:b + 1]),
                                            x.anchor.numpy()[b:b + 1],
-                                           x.temperature.numpy()[b:b + 1], 77, cell, M=M, req0=b)
+                                           x.temperature.numpy()[b:b + 1], 77, cell, req0=b,
+                                           **kw)
             assert np.array_equal(tb[0], t[b]) and np.array_equal(lb[0], lg[b]) and \
                 np.array_equal(sb[0], st[b]), "cell %d: request %d differs alone" % (cell, b)
         tf, lf, _, sf, _ = O.walk_cell(*args, bits(x.base), x.anchor.numpy(),
-                                       x.temperature.numpy(), 77, cell, M=M, forced=t,
-                                       forced_state=st)
+                                       x.temperature.numpy(), 77, cell, forced=t,
+                                       forced_state=st, **kw)
         assert np.array_equal(tf, t) and np.array_equal(lf, lg) and np.array_equal(sf, st), \
             "cell %d: forcing a walk with itself changed it" % cell
 
@@ -708,5 +785,6 @@ ALL_PINS = [
     pin_batch_independence, pin_permutation, pin_sampling_law, pin_t_to_zero,
     pin_forced, pin_errors, pin_group_layout, pin_group_sampling_law, pin_group_t_to_zero,
     pin_group_batch_independence, pin_cell_rnn_zero_matrix, pin_cell_gated_half,
-    pin_cell_gated_saturation, pin_cell_rnn_permutation, pin_cell_batch_and_forcing,
+    pin_cell_gated_saturation, pin_cell_rnn_permutation, pin_cell_gru_reduces_to_rnn,
+    pin_cell_gru_hold, pin_cell_gru_permutation, pin_cell_batch_and_forcing,
 ]

@@ -45,14 +45,22 @@ MUTATIONS = {
     # recurrent heads
     "cell_gate_swapped": ("val = (1.0 - z) * hp + z * xi;", "val = z * hp + (1.0 - z) * xi;"),
     "cell_gate_sign": ("1.0 / (1.0 + exp(-p));", "1.0 / (1.0 + exp(p));"),
-    "cell_matrix_transposed": ("orc_bf16_to_f64(M[(int64_t)i * r + j])",
-                               "orc_bf16_to_f64(M[(int64_t)j * r + i])"),
+    "cell_matrix_transposed": ("orc_row_dot(M + (int64_t)i * r, 1, hprev, r)",
+                               "orc_row_dot(M + i, r, hprev, r)"),
     "cell_rnn_drops_input": ("val = tanh(p + xi);", "val = tanh(p);"),
     "cell_rnn_drops_recurrence": ("val = tanh(p + xi);", "val = tanh(xi);"),
     "cell_state_not_carried": ("memcpy(hbuf, hk, (size_t)r * sizeof *hk);",
                                "memset(hbuf, 0, (size_t)r * sizeof *hk);"),
     "cell_projects_input": ("* r : hbuf;\n", "* r : u;\n"),
     "cell_initial_state_is_input": ("const uint16_t *hprev = NULL;", "const uint16_t *hprev = u;"),
+    "gru_update_gate_swapped": ("val = (1.0 - zg) * ng + zg * hp;",
+                                "val = zg * ng + (1.0 - zg) * hp;"),
+    "gru_reset_on_input": ("tanh(orc_bf16_to_f64(x[2 * r + i]) + rg * pg[2])",
+                           "tanh(rg * (orc_bf16_to_f64(x[2 * r + i]) + pg[2]))"),
+    "gru_gate_matrices_reversed": ("M + ((int64_t)g * r + i) * r, 1, hprev, r)",
+                                   "M + ((int64_t)(2 - g) * r + i) * r, 1, hprev, r)"),
+    "gru_tables_reversed": ("X + ((int64_t)g * V + prev) * r",
+                            "X + ((int64_t)(2 - g) * V + prev) * r"),
 }
 
 

@@ -160,3 +160,19 @@ def test_cell_with_group_sampler_accepts_the_oracle_itself():
                                        sampler=1)
     rep = parity.check(x, t, lg, cell=2, M=M, gpu_states=st, sampler=1)
     assert rep.ok() and rep.steps_exact == rep.steps_checked, rep
+
+
+def test_gru_accepts_the_oracle_and_rejects_a_wrong_state():
+    x = synth.make_custom(V=420, gamma=4, B=2, seed=29, temperatures=(0.0, 1.0), noise_seed=3)
+    M = synth.bits(synth.make_cell_matrix(10, rows=768))
+    X = synth.bits(synth.make_cell_tables(420, 11))
+    t, lg, _, st, ex = oracle.walk_cell(synth.bits(x.W1), synth.bits(x.W2), synth.bits(x.base),
+                                        x.anchor.numpy(), x.temperature.numpy(), x.seed, 3,
+                                        M=M, X=X)
+    rep = parity.check(x, t, lg, cell=3, M=M, X=X, gpu_states=st)
+    assert rep.ok() and rep.states_exact == rep.states_checked, rep
+    st2 = st.copy()
+    i = int(np.argmax(np.abs(ex[1, 2])))
+    st2[1, 2, i] = st2[1, 2, i] + 1
+    rep = parity.check(x, t, None, cell=3, M=M, X=X, gpu_states=st2)
+    assert not rep.ok() and any(f[0] == "state" for f in rep.failures), rep
