@@ -58,9 +58,9 @@ def parse():
     p.add_argument("--sampler", default="gumbel", choices=["gumbel", "group"],
                    help="sampling of T > 0 requests: per-token Gumbel-max (the configs') or the "
                         "group inverse-CDF sampler")
-    p.add_argument("--cell", default="markov", choices=["markov", "gated", "rnn"],
+    p.add_argument("--cell", default="markov", choices=["markov", "gated", "rnn", "gru"],
                    help="serial head: DSpark's Markov head (the configs') or a recurrent "
-                        "head (gated / RNN state update, synthetic recurrent matrix)")
+                        "head (gated / RNN / GRU state update, synthetic recurrent weights)")
     p.add_argument("--kernel", default="planned", choices=["planned", "resident", "batched", "stream"],
                    help="force a kernel (dspark_walk_set_kernel); default: the handle's plan")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -291,12 +291,16 @@ def gamma_fit(walk, gammas=(1, 4, 7, 16), steps=100, warmup=5):
     return out
 
 
-CELLS = {"markov": 0, "gated": 1, "rnn": 2}
+CELLS = {"markov": 0, "gated": 1, "rnn": 2, "gru": 3}
 
 
-def cell_matrix(cfg):
-    """The recurrent heads' synthetic matrix for a workload (bf16 [256, 256])."""
-    return synth.make_cell_matrix(cfg.seed + 500)
+def cell_weights(cfg, cell):
+    """A recurrent head's synthetic weights for a workload: M (bf16 [256, 256];
+    [768, 256] for the GRU) and the GRU's token tables X ([3, V, 256]; else None)."""
+    if cell == "gru":
+        return (synth.make_cell_matrix(cfg.seed + 500, rows=768),
+                synth.make_cell_tables(cfg.V, cfg.seed + 501))
+    return synth.make_cell_matrix(cfg.seed + 500), None
 
 
 def measure_config(walk, cfg, B, steps=50, warmup=5, sampler="gumbel", cell="markov"):
@@ -308,7 +312,8 @@ def measure_config(walk, cfg, B, steps=50, warmup=5, sampler="gumbel", cell="mar
     if sampler == "group":
         w.set_sampler(walk.SAMPLER_GROUP)
     if cell != "markov":
-        w.set_cell(CELLS[cell], cell_matrix(cfg).to(dev))
+        M, X = cell_weights(cfg, cell)
+        w.set_cell(CELLS[cell], M.to(dev), None if X is None else X.to(dev))
     plan = w.plan()
     base, anchor, temp = x.base.to(dev), x.anchor.to(dev), x.temperature.to(dev)
     tok = torch.empty(B, cfg.gamma, dtype=torch.int32, device=dev)
@@ -350,12 +355,17 @@ def measure_config(walk, cfg, B, steps=50, warmup=5, sampler="gumbel", cell="mar
     return res
 
 
-def oracle_walk(O, cell, M, W1, W2, base, anchor, temperature, seed):
-    """One oracle walk of the bench's head (tokens only)."""
+def oracle_walk(O, cell, MX, W1, W2, base, anchor, temperature, seed):
+    """One oracle walk of the bench's head (tokens only); MX = (M, X) bits."""
     if cell == "markov":
         return O.walk(W1, W2, base, anchor, temperature, seed, want_logits=False, nthreads=0)
-    return O.walk_cell(W1, W2, base, anchor, temperature, seed, CELLS[cell], M=M,
+    return O.walk_cell(W1, W2, base, anchor, temperature, seed, CELLS[cell], M=MX[0], X=MX[1],
                        want_logits=False, nthreads=0)
+
+
+def cell_bits(cfg, cell):
+    M, X = cell_weights(cfg, cell)
+    return synth.bits(M), (None if X is None else synth.bits(X))
 
 
 def cpu_baseline(cfg, B, rounds, seconds, cell="markov"):
@@ -365,12 +375,12 @@ def cpu_baseline(cfg, B, rounds, seconds, cell="markov"):
     O = oracle.default()
     W1 = synth.bits(rounds[0].W1)
     W2 = synth.bits(rounds[0].W2)
-    M = synth.bits(cell_matrix(cfg))
+    MX = cell_bits(cfg, cell)
     n = 0
     t0 = time.perf_counter()
     while True:
         x = rounds[n % len(rounds)]
-        oracle_walk(O, cell, M, W1, W2, synth.bits(x.base), x.anchor.numpy(),
+        oracle_walk(O, cell, MX, W1, W2, synth.bits(x.base), x.anchor.numpy(),
                     x.temperature.numpy(), x.seed)
         n += 1
         if time.perf_counter() - t0 >= seconds:
@@ -391,7 +401,7 @@ def run_reference(args, cfg, B, rank, world):
     n_rounds = min(cfg.rounds, 8)
     W1t, W2t, rounds = load_inputs(cfg, B, n_rounds)
     W1, W2 = synth.bits(W1t), synth.bits(W2t)
-    M = synth.bits(cell_matrix(cfg))
+    MX = cell_bits(cfg, args.cell)
 
     def one_step(i):
         # bounded sample: the work of ONE of the gamma steps of round i (all V
@@ -402,7 +412,7 @@ def run_reference(args, cfg, B, rank, world):
         anchor = x.anchor.numpy()
         base = synth.bits(x.base)[:, k:k + 1]
         t0 = time.perf_counter()
-        oracle_walk(O, args.cell, M, W1, W2, np.ascontiguousarray(base), anchor,
+        oracle_walk(O, args.cell, MX, W1, W2, np.ascontiguousarray(base), anchor,
                     x.temperature.numpy(), x.seed)
         return time.perf_counter() - t0
 
@@ -447,10 +457,11 @@ def main():
     w = walk.Walk(W1, W2, B, cfg.gamma)
     if args.sampler == "group":
         w.set_sampler(walk.SAMPLER_GROUP)
-    M = None
+    cell_dev = None
     if args.cell != "markov":
-        M = cell_matrix(cfg).to(dev)
-        w.set_cell(CELLS[args.cell], M)
+        M, X = cell_weights(cfg, args.cell)
+        cell_dev = (M.to(dev), None if X is None else X.to(dev))   # referenced by the handle
+        w.set_cell(CELLS[args.cell], *cell_dev)
     if args.kernel != "planned":
         w.set_kernel({"resident": walk.KERNEL_RESIDENT, "batched": walk.KERNEL_BATCHED,
                       "stream": walk.KERNEL_STREAM}[args.kernel])
@@ -621,7 +632,7 @@ def main():
         # the recurrent heads on the fully resident long block (B = 1 as the pages
         # time them, and the largest resident batch)
         line["sweep"] += [measure_config(walk, synth.CONFIGS["long_block"], b, cell=c)
-                          for c in ("gated", "rnn") for b in (1, 16)]
+                          for c in ("gated", "rnn", "gru") for b in (1, 16)]
     if args.gamma_fit:
         line["gamma_fit"] = gamma_fit(walk)
     if rank == 0 and not args.no_cpu_baseline and not args.only_timed:

@@ -218,30 +218,39 @@ int dspark_walk_set_sampler(dspark_walk_t h, int sampler);
  * dspark_walk_set_cell -- which serial head later runs walk ("Keeping the Draft
  * Walk on Chip", section "Beyond DSpark: other serial heads": the walk as a
  * template over the head's state update).
- *   DSPARK_CELL_MARKOV (default): u_k = W1[prev_k]; M is ignored.
+ *   DSPARK_CELL_MARKOV (default): u_k = W1[prev_k]; M and X are ignored.
  *   DSPARK_CELL_GATED, DSPARK_CELL_RNN: a recurrent head with state h (256
  *     bf16 values per request), h_{-1} = 0, x_k = W1[prev_k] (prev_0 = the
  *     anchor), p = M @ h_{k-1} accumulated in fp32, and per element
  *       gated: z = 1 / (1 + exp(-p)), h_k = bf16((1 - z) h_{k-1} + z x_k)
  *       RNN:   h_k = bf16(tanh(p + x_k))
- *     (fp32, each operation rounded); u_k = h_k is projected through W2 and
- *     selected from exactly as W1[prev] is.  The pages print no cell
- *     equations: these are the plain gated and Elman forms.
- *   M: device bf16 [256, 256] row-major, 16-byte aligned, referenced (not
- *     copied): the caller keeps it alive and unchanged while runs use it.
- *   Each CTA computes its share of M's rows for every request and publishes
- *   them with its arrival at the step's rendezvous; after the rendezvous every
- *   CTA forms the new state itself, so a recurrent step adds no exchange.
- *   Recurrent runs take the resident kernel (B <= the handle's resident batch,
- *   at most 16); other runs return DSPARK_EUNSUPPORTED, as does this call on
- *   a handle without a resident layout (V >= 2^18).  DSPARK_EINVAL for another
- *   cell, a null or misaligned M; DSPARK_ENOMEM / DSPARK_ECUDA if the 16 KB per
- *   step of exchange memory cannot be allocated (first recurrent cell only).
+ *     M: device bf16 [256, 256] row-major.
+ *   DSPARK_CELL_GRU: the page's GRU heads, with the input projections folded
+ *     into three token tables X = (X_r, X_z, X_n), device bf16 [3, V, 256], and
+ *     M = (M_r; M_z; M_n) stacked, device bf16 [768, 256]: with p_g = M_g @ h_{k-1},
+ *       r = sig(X_r[prev_k] + p_r), z = sig(X_z[prev_k] + p_z),
+ *       n = tanh(X_n[prev_k] + r p_n), h_k = bf16((1 - z) n + z h_{k-1})
+ *     (W1 is not read by this head).
+ *   All in fp32, each operation rounded; u_k = h_k is projected through W2 and
+ *   selected from exactly as W1[prev] is.  The pages print no cell equations:
+ *   these are the plain gated, Elman and GRU forms.
+ *   M and X are 16-byte aligned and referenced (not copied): the caller keeps
+ *   them alive and unchanged while runs use them.
+ *   Each CTA computes its share of the recurrent rows for every request and
+ *   publishes them with its arrival at the step's rendezvous; after the
+ *   rendezvous every CTA forms the new state itself, so a recurrent step adds
+ *   no exchange.  Recurrent runs take the resident kernel (B <= the handle's
+ *   resident batch, at most 16); other runs return DSPARK_EUNSUPPORTED, as does
+ *   this call on a handle without a resident layout (V >= 2^18).  DSPARK_EINVAL
+ *   for another cell, a null or misaligned M (or X for the GRU);
+ *   DSPARK_ENOMEM / DSPARK_ECUDA if the 48 KB per step of exchange memory
+ *   cannot be allocated (first recurrent cell only).
  */
 #define DSPARK_CELL_MARKOV 0
 #define DSPARK_CELL_GATED 1
 #define DSPARK_CELL_RNN 2
-int dspark_walk_set_cell(dspark_walk_t h, int cell, const void *M);
+#define DSPARK_CELL_GRU 3
+int dspark_walk_set_cell(dspark_walk_t h, int cell, const void *M, const void *X);
 
 /*
  * dspark_walk_set_state_output -- where later runs write each step's latent

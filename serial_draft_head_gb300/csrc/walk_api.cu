@@ -31,8 +31,9 @@ struct dspark_walk {
   int seed_per_round = 0;         // dspark_walk_set_seed_mode
   int sampler = 0;                // dspark_walk_set_sampler
   int cell = 0;                   // dspark_walk_set_cell
-  const uint16_t* cell_M = nullptr;   // caller-owned [256, 256]
-  float* cell_p = nullptr;        // handle-owned [max_gamma][16][256] fp32
+  const uint16_t* cell_M = nullptr;   // caller-owned [256, 256] ([768, 256] for the GRU)
+  const uint16_t* cell_X = nullptr;   // caller-owned GRU token tables [3, V, 256]
+  float* cell_p = nullptr;        // handle-owned [max_gamma][16][kCellP] fp32
   uint16_t* out_state = nullptr;  // caller-owned, dspark_walk_set_state_output
   int res_RS = 0, res_NT = 0, res_R = 0, res_S = 0, res_ST = 0, res_nslot = 0, res_n_cta = 0;
   int64_t res_wpc = 0;
@@ -202,13 +203,17 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
   a.out_state = h->out_state;
   a.cell = h->cell;
   a.cell_M = h->cell_M;
+  a.cell_X = h->cell_X;
   a.cell_p = h->cell_p;
   a.cell_q = 1;
   const bool resident_run = h->res_max_B > 0 && h->use_resident && B <= h->res_max_B;
   // recurrent heads and the state output run on the resident kernel only
   if ((h->cell != DSPARK_CELL_MARKOV || h->out_state) && !resident_run)
     return DSPARK_EUNSUPPORTED;
-  if (resident_run) a.cell_q = (kRank + h->res_n_cta - 1) / h->res_n_cta;
+  if (resident_run) {
+    const int P = h->cell == DSPARK_CELL_GRU ? kCellP : kRank;   // recurrent rows
+    a.cell_q = (P + h->res_n_cta - 1) / h->res_n_cta;
+  }
 
   if (!(h->res_max_B > 0 && h->use_resident && B <= h->res_max_B) && h->W2b && h->use_batched) {
     CUDA_TRY(batched_launch(a, h->W2b, h->bat_R, h->bat_n_cta, h->max_B, B,
@@ -476,23 +481,26 @@ int dspark_walk_set_sampler(dspark_walk_t h, int sampler) {
   return DSPARK_OK;
 }
 
-int dspark_walk_set_cell(dspark_walk_t h, int cell, const void* M) {
+int dspark_walk_set_cell(dspark_walk_t h, int cell, const void* M, const void* X) {
   if (!h) return DSPARK_EINVAL;
   if (cell == DSPARK_CELL_MARKOV) {
     h->cell = cell;
-    h->cell_M = nullptr;
+    h->cell_M = h->cell_X = nullptr;
     return DSPARK_OK;
   }
-  if ((cell != DSPARK_CELL_GATED && cell != DSPARK_CELL_RNN) || !M ||
+  if ((cell != DSPARK_CELL_GATED && cell != DSPARK_CELL_RNN && cell != DSPARK_CELL_GRU) || !M ||
       (reinterpret_cast<uintptr_t>(M) & 15u) != 0)
+    return DSPARK_EINVAL;
+  if (cell == DSPARK_CELL_GRU && (!X || (reinterpret_cast<uintptr_t>(X) & 15u) != 0))
     return DSPARK_EINVAL;
   if (h->res_max_B == 0) return DSPARK_EUNSUPPORTED;   // no resident layout to run on
   if (!h->cell_p) {
     CUDA_TRY(cudaSetDevice(h->device));
-    CUDA_TRY(cudaMalloc(&h->cell_p, (size_t)h->max_gamma * 16 * kRank * sizeof(float)));
+    CUDA_TRY(cudaMalloc(&h->cell_p, (size_t)h->max_gamma * 16 * kCellP * sizeof(float)));
   }
   h->cell = cell;
   h->cell_M = static_cast<const uint16_t*>(M);
+  h->cell_X = cell == DSPARK_CELL_GRU ? static_cast<const uint16_t*>(X) : nullptr;
   return DSPARK_OK;
 }
 

@@ -73,6 +73,8 @@ __device__ __forceinline__ bool round_aborted(const SyncHeader* hdr, uint32_t ro
 }
 
 // Everything a launch needs (passed by value).
+constexpr int kCellP = 3 * kRank;   // largest recurrent product per request (the GRU's)
+
 struct WalkArgs {
   const uint16_t* W1;          // [V, 256] bf16
   const uint16_t* W2;          // [V, 256] bf16, row-major (streamed kernels)
@@ -93,9 +95,10 @@ struct WalkArgs {
   int skip_cta;                // fault injection: this CTA never posts (-1: off)
   unsigned long long* trace;   // optional [n_cta][gamma + 1][8] SM-clock stamps
   // recurrent heads (resident kernel only)
-  int cell;                    // 0: Markov (u = W1[prev]); 1: gated; 2: RNN
-  const uint16_t* cell_M;      // [256, 256] bf16 recurrent matrix, row-major
-  float* cell_p;               // [gamma][16][256] fp32: M @ h_k, published slice by slice
+  int cell;                    // 0: Markov (u = W1[prev]); 1: gated; 2: RNN; 3: GRU
+  const uint16_t* cell_M;      // [P, 256] bf16 recurrent rows (P = 256; GRU: 768)
+  const uint16_t* cell_X;      // GRU: [3, V, 256] bf16 token tables (r, z, n)
+  float* cell_p;               // [gamma][16][kCellP] fp32: M @ h_k, published slice by slice
   int cell_q;                  // rows of M per CTA: CTA c owns rows [c q, c q + q)
   uint16_t* out_state;         // [B, gamma, 256] bf16 states u_k, or null
 };
@@ -186,6 +189,19 @@ __device__ __forceinline__ uint16_t cell_element(int cell, float p, float x, flo
     v = tanhf(__fadd_rn(p, x));
   }
   return float_to_bf16_bits_rn(v);
+}
+
+// One element of the GRU head's update (the same page; the usual reset /
+// update gate form, input projections folded into the token tables): from
+// the recurrent products pr, pz, pn, the token's table elements xr, xz, xn and
+// the previous state element hp, r = sig(xr + pr), z = sig(xz + pz),
+// n = tanh(xn + r pn), (1 - z) n + z hp; fp32, each operation rounded.
+__device__ __forceinline__ uint16_t gru_element(float pr, float pz, float pn, float xr, float xz,
+                                                float xn, float hp) {
+  const float r = __frcp_rn(__fadd_rn(1.0f, expf(-__fadd_rn(xr, pr))));
+  const float z = __frcp_rn(__fadd_rn(1.0f, expf(-__fadd_rn(xz, pz))));
+  const float n = tanhf(__fadd_rn(xn, __fmul_rn(r, pn)));
+  return float_to_bf16_bits_rn(__fadd_rn(__fmul_rn(__fsub_rn(1.0f, z), n), __fmul_rn(z, hp)));
 }
 
 // ------------------------------------------------------------------- key --

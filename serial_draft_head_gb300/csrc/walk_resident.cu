@@ -114,11 +114,30 @@ __device__ __forceinline__ void prefetch_base(const ResidentArgs& ra, int k, int
 
 // u_b = W1[tok] into U (core matrix (kc, b/8), row b%8): one 16-byte chunk per lane.
 // A recurrent head's first state h_0 (from h_{-1} = 0: p = 0, previous state 0)
-// is formed from that row in place.
-__device__ __forceinline__ void gather_u_row(const uint16_t* W1, int32_t tok, int b, uint8_t* U,
+// is formed from that row (the GRU: from the token's rows of its three tables)
+// in place.
+__device__ __forceinline__ void gather_u_row(const WalkArgs& a, int32_t tok, int b, uint8_t* U,
                                              int lane, int cell) {
-  uint4 x = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)tok * kRank) + lane);
-  if (cell != 0) {
+  uint4 x = __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok * kRank) + lane);
+  if (cell == 3) {
+    const uint4* X = reinterpret_cast<const uint4*>(a.cell_X);
+    const uint4 xr = __ldg(X + ((size_t)tok) * 32 + lane);
+    const uint4 xz = __ldg(X + ((size_t)a.V + tok) * 32 + lane);
+    const uint4 xn = __ldg(X + ((size_t)2 * a.V + tok) * 32 + lane);
+    const uint32_t rw[4] = {xr.x, xr.y, xr.z, xr.w}, zw[4] = {xz.x, xz.y, xz.z, xz.w};
+    const uint32_t nw[4] = {xn.x, xn.y, xn.z, xn.w};
+    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = gru_element(0.f, 0.f, 0.f, bf16_bits_to_float(rw[j] & 0xFFFFu),
+                                      bf16_bits_to_float(zw[j] & 0xFFFFu),
+                                      bf16_bits_to_float(nw[j] & 0xFFFFu), 0.f);
+      const uint32_t hi = gru_element(0.f, 0.f, 0.f, bf16_bits_to_float(rw[j] >> 16),
+                                      bf16_bits_to_float(zw[j] >> 16),
+                                      bf16_bits_to_float(nw[j] >> 16), 0.f);
+      w[j] = lo | (hi << 16);
+    }
+  } else if (cell != 0) {
     uint32_t* w = reinterpret_cast<uint32_t*>(&x);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -164,17 +183,17 @@ __device__ __forceinline__ float row_dot(const uint4 m, const uint4 h) {
 // vocabularies on few CTAs) one warp per (row, request), rows read from L2.
 __device__ __forceinline__ void publish_cell_rows(const WalkArgs& a, const uint8_t* U, int k,
                                                   int cta, int warp, int lane, const uint4 mreg) {
-  const int q = a.cell_q, r0 = cta * q;
+  const int q = a.cell_q, r0 = cta * q, P = a.cell == 3 ? kCellP : kRank;
   auto u_chunk = [&](int b) {
     return *reinterpret_cast<const uint4*>(U + (lane * 2 + (b >> 3)) * 128 + (b & 7) * 16);
   };
   if (q <= kResWarps) {
     const int j = warp % q, g = warp / q, G = kResWarps / q;
-    if (g >= G || r0 + j >= kRank) return;
+    if (g >= G || r0 + j >= P) return;
     if (a.B <= G) {                                 // one request per warp at most
       if (g < a.B) {
         const float acc = row_dot(mreg, u_chunk(g));
-        if (lane == 0) a.cell_p[((size_t)k * 16 + g) * kRank + r0 + j] = acc;
+        if (lane == 0) a.cell_p[((size_t)k * 16 + g) * kCellP + r0 + j] = acc;
       }
       return;
     }
@@ -193,17 +212,17 @@ __device__ __forceinline__ void publish_cell_rows(const WalkArgs& a, const uint8
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const int b = b0 + t * G;
-          if (b < a.B) a.cell_p[((size_t)k * 16 + b) * kRank + r0 + j] = acc[t];
+          if (b < a.B) a.cell_p[((size_t)k * 16 + b) * kCellP + r0 + j] = acc[t];
         }
     }
     return;
   }
-  const int nr = kRank - r0 < q ? kRank - r0 : q;
+  const int nr = P - r0 < q ? P - r0 : q;
   for (int pr = warp; pr < nr * a.B; pr += kResWarps) {
     const int row = r0 + pr / a.B, b = pr % a.B;
     const uint4 m = __ldg(reinterpret_cast<const uint4*>(a.cell_M + (size_t)row * kRank) + lane);
     const float acc = row_dot(m, u_chunk(b));
-    if (lane == 0) a.cell_p[((size_t)k * 16 + b) * kRank + row] = acc;
+    if (lane == 0) a.cell_p[((size_t)k * 16 + b) * kCellP + row] = acc;
   }
 }
 
@@ -390,7 +409,7 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
 __device__ __forceinline__ void cell_update_row(const WalkArgs& a, uint8_t* U, int k, int b,
                                                 int32_t tok, int lane) {
   const float4* pp =
-      reinterpret_cast<const float4*>(a.cell_p + ((size_t)k * 16 + b) * kRank) + 2 * lane;
+      reinterpret_cast<const float4*>(a.cell_p + ((size_t)k * 16 + b) * kCellP) + 2 * lane;
   const float4 p0 = __ldcg(pp), p1 = __ldcg(pp + 1);
   const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok * kRank) + lane);
   uint4* hp = reinterpret_cast<uint4*>(U + (lane * 2 + (b >> 3)) * 128 + (b & 7) * 16);
@@ -405,6 +424,47 @@ __device__ __forceinline__ void cell_update_row(const WalkArgs& a, uint8_t* U, i
     const uint32_t hi = cell_element(a.cell, p[2 * e + 1], bf16_bits_to_float(xw[e] >> 16),
                                      bf16_bits_to_float(hw[e] >> 16));
     ow[e] = lo | (hi << 16);
+  }
+  *hp = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+}
+
+// The GRU's next state for request b, lane l's elements 8l .. 8l + 7: the
+// three recurrent products and the token's three table rows, one 16-byte
+// chunk (two for the fp32 products) of each per lane.
+__device__ __forceinline__ void gru_update_row(const WalkArgs& a, uint8_t* U, int k, int b,
+                                               int32_t tok, int lane) {
+  const float4* pp =
+      reinterpret_cast<const float4*>(a.cell_p + ((size_t)k * 16 + b) * kCellP) + 2 * lane;
+  const uint4* X = reinterpret_cast<const uint4*>(a.cell_X);
+  float4 pv[6];
+#pragma unroll
+  for (int g = 0; g < 3; ++g) {
+    pv[2 * g] = __ldcg(pp + g * (kRank / 4));
+    pv[2 * g + 1] = __ldcg(pp + g * (kRank / 4) + 1);
+  }
+  uint4 xv[3];
+#pragma unroll
+  for (int g = 0; g < 3; ++g) xv[g] = __ldg(X + ((size_t)g * a.V + tok) * 32 + lane);
+  uint4* hp = reinterpret_cast<uint4*>(U + (lane * 2 + (b >> 3)) * 128 + (b & 7) * 16);
+  const uint4 hv = *hp;
+  const float* pf = reinterpret_cast<const float*>(pv);          // [gate][8]
+  const uint32_t* xw = reinterpret_cast<const uint32_t*>(xv);   // [gate][4]
+  const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+  uint32_t ow[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    uint32_t half[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int j = 2 * e + t;
+      const int sh = 16 * t;
+      half[t] = gru_element(pf[j], pf[8 + j], pf[16 + j],
+                            bf16_bits_to_float((xw[e] >> sh) & 0xFFFFu),
+                            bf16_bits_to_float((xw[4 + e] >> sh) & 0xFFFFu),
+                            bf16_bits_to_float((xw[8 + e] >> sh) & 0xFFFFu),
+                            bf16_bits_to_float((hw[e] >> sh) & 0xFFFFu));
+    }
+    ow[e] = half[0] | (half[1] << 16);
   }
   *hp = make_uint4(ow[0], ow[1], ow[2], ow[3]);
 }
@@ -559,7 +619,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
 
   // step 0's u = W1[anchor]
   for (int b = warp; b < a.B; b += kResWarps)
-    gather_u_row(a.W1, tok_s[b], b, U, lane, CELL ? a.cell : 0);
+    gather_u_row(a, tok_s[b], b, U, lane, CELL ? a.cell : 0);
   if (ra.S > 0 && threadIdx.x == 0) {
     if (!wait_mbar(&mbar[kMbarTma], 0, t_entry, a.timeout_ns)) {
       abort_round(a.sync.hdr, round_s, kStatusTimeout);
@@ -576,7 +636,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
   uint4 mreg = make_uint4(0u, 0u, 0u, 0u);
   if (CELL && a.cell != 0 && a.cell_q <= kResWarps) {
     const int row = cta * a.cell_q + warp % a.cell_q;
-    if (row < kRank)
+    if (row < (a.cell == 3 ? kCellP : kRank))
       mreg = __ldg(reinterpret_cast<const uint4*>(a.cell_M + (size_t)row * kRank) + lane);
   }
   const KeyPassMap kpm = key_pass_map(a.B, temp_s);
@@ -867,10 +927,24 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
       // updates element i (the gate or tanh of 256 elements side by side);
       // more: warp w updates requests w, w + 8, lane l elements 8l .. 8l + 7
       // (one 16-byte chunk of each operand per lane, fewer round trips)
-      if (a.B <= 2) {
+      if (a.cell == 3 && a.B > 2) {               // the GRU, larger batches: chunk per lane
+        for (int b = warp; b < a.B; b += kResWarps) gru_update_row(a, U, k, b, tok_s[b], lane);
+      } else if (a.cell == 3) {                   // the GRU: element per thread
         const int i = threadIdx.x;
         for (int b = 0; b < a.B; ++b) {
-          const float p = ld_relaxed_gpu_f32(a.cell_p + ((size_t)k * 16 + b) * kRank + i);
+          const float* pb = a.cell_p + ((size_t)k * 16 + b) * kCellP + i;
+          const float pr = __ldcg(pb), pz = __ldcg(pb + kRank), pn = __ldcg(pb + 2 * kRank);
+          const uint16_t* xb = a.cell_X + (size_t)tok_s[b] * kRank + i;
+          const float xr = bf16_bits_to_float(__ldg(xb));
+          const float xz = bf16_bits_to_float(__ldg(xb + (size_t)a.V * kRank));
+          const float xn = bf16_bits_to_float(__ldg(xb + (size_t)2 * a.V * kRank));
+          uint16_t* hu = u_elem(U, i, b);
+          *hu = gru_element(pr, pz, pn, xr, xz, xn, bf16_bits_to_float(*hu));
+        }
+      } else if (a.B <= 2) {
+        const int i = threadIdx.x;
+        for (int b = 0; b < a.B; ++b) {
+          const float p = ld_relaxed_gpu_f32(a.cell_p + ((size_t)k * 16 + b) * kCellP + i);
           const float x = bf16_bits_to_float(__ldg(a.W1 + (size_t)tok_s[b] * kRank + i));
           uint16_t* hu = u_elem(U, i, b);
           *hu = cell_element(a.cell, p, x, bf16_bits_to_float(*hu));

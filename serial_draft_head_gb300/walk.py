@@ -36,6 +36,7 @@ SAMPLER_GROUP = 1
 CELL_MARKOV = 0
 CELL_GATED = 1
 CELL_RNN = 2
+CELL_GRU = 3
 
 _lib = None
 
@@ -102,7 +103,7 @@ def load(build_if_missing=True):
     L.dspark_walk_run_noalloc.argtypes = [vp, vp, i64, i32, vp, vp, vp, u64, vp, i32, i32, vp, vp]
     L.dspark_walk_set_seed_mode.argtypes = [vp, i32]
     L.dspark_walk_set_sampler.argtypes = [vp, i32]
-    L.dspark_walk_set_cell.argtypes = [vp, i32, vp]
+    L.dspark_walk_set_cell.argtypes = [vp, i32, vp, vp]
     L.dspark_walk_set_state_output.argtypes = [vp, vp]
     L.dspark_walk_round.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint64)]
     L.dspark_walk_gumbel_noise.argtypes = [vp, vp, i64, vp]
@@ -192,13 +193,15 @@ def dspark_walk_set_sampler(h, sampler):
     return _check(load().dspark_walk_set_sampler(h, int(sampler)), "dspark_walk_set_sampler")
 
 
-def dspark_walk_set_cell(h, cell, M=None):
-    """The serial head: CELL_MARKOV, or CELL_GATED / CELL_RNN with M a device
-    bf16 [256, 256] tensor (referenced by the handle: keep it alive)."""
-    if M is not None:
-        assert M.is_cuda and M.dtype == torch.bfloat16 and tuple(M.shape) == (256, 256)
-        assert M.is_contiguous()
-    return _check(load().dspark_walk_set_cell(h, int(cell), _ptr(M)), "dspark_walk_set_cell")
+def dspark_walk_set_cell(h, cell, M=None, X=None):
+    """The serial head: CELL_MARKOV; CELL_GATED / CELL_RNN with M a device bf16
+    [256, 256] tensor; CELL_GRU with M [768, 256] and the token tables X
+    [3, V, 256] (referenced by the handle: keep them alive)."""
+    for t in (M, X):
+        if t is not None:
+            assert t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()
+    return _check(load().dspark_walk_set_cell(h, int(cell), _ptr(M), _ptr(X)),
+                  "dspark_walk_set_cell")
 
 
 def dspark_walk_set_state_output(h, out_state=None):
@@ -270,9 +273,10 @@ class Walk:
     def set_sampler(self, sampler):
         dspark_walk_set_sampler(self.h, sampler)
 
-    def set_cell(self, cell, M=None):
+    def set_cell(self, cell, M=None, X=None):
         self.M = None if M is None else M.contiguous()      # referenced: keep alive
-        dspark_walk_set_cell(self.h, cell, self.M)
+        self.X = None if X is None else X.contiguous()
+        dspark_walk_set_cell(self.h, cell, self.M, self.X)
 
     def set_state_output(self, out_state=None):
         dspark_walk_set_state_output(self.h, out_state)

@@ -530,11 +530,18 @@ CELL_SHAPES = [
 ]
 
 
-def cell_run(walkmod, w, x, cell, M, want_logits=True):
+def cell_weights(cell, V, seed):
+    """(M, X) of a recurrent head: X (the GRU's token tables) is None otherwise."""
+    if cell == 3:
+        return synth.make_cell_matrix(seed, rows=768), synth.make_cell_tables(V, seed + 1)
+    return synth.make_cell_matrix(seed), None
+
+
+def cell_run(walkmod, w, x, cell, M, want_logits=True, X=None):
     B, gamma, _ = x.base.shape
     Md = M.cuda()
     states = torch.empty(B, gamma, 256, dtype=torch.bfloat16, device="cuda")
-    w.set_cell(cell, Md)
+    w.set_cell(cell, Md, None if X is None else X.cuda())
     w.set_state_output(states)
     try:
         st, toks, lg = gpu_run(w, x, want_logits=want_logits)
@@ -544,32 +551,34 @@ def cell_run(walkmod, w, x, cell, M, want_logits=True):
     return st, toks, lg, synth.bits(states.cpu())
 
 
-@pytest.mark.parametrize("cell", [1, 2])
+@pytest.mark.parametrize("cell", [1, 2, 3])
 @pytest.mark.parametrize("V,gamma,B,temps,seed", CELL_SHAPES)
 def test_cell_every_logit_and_state(walkmod, V, gamma, B, temps, seed, cell):
-    """Gated (1) and RNN (2) heads: every state element, logit and token."""
+    """Gated (1), RNN (2) and GRU (3) heads: every state element, logit and token."""
     x = synth.make_custom(V=V, gamma=gamma, B=B, seed=seed, temperatures=temps,
                           noise_seed=3000 + seed)
-    M = synth.make_cell_matrix(seed)
+    M, X = cell_weights(cell, V, seed)
     w = make_walk(walkmod, x)
-    st, toks, lg, states = cell_run(walkmod, w, x, cell, M)
+    st, toks, lg, states = cell_run(walkmod, w, x, cell, M, X=X)
     assert st == 0, walkmod.dspark_walk_strerror(st)
-    rep = parity.check(x, toks, lg, cell=cell, M=synth.bits(M), gpu_states=states)
+    rep = parity.check(x, toks, lg, cell=cell, M=synth.bits(M), gpu_states=states,
+                       X=None if X is None else synth.bits(X))
     assert rep.ok(), rep
     assert rep.states_checked == B * gamma * 256
     w.close()
 
 
-@pytest.mark.parametrize("cell", [1, 2])
+@pytest.mark.parametrize("cell", [1, 2, 3])
 def test_cell_long_block(walkmod, cell):
     """V = 151,936, gamma = 16, B = 16 on the recurrent heads (sampled requests)."""
     x = full_inputs("long_block", 16)
     w = full_walk(walkmod, "long_block", x)
-    M = synth.make_cell_matrix(100 + cell)
-    st, toks, lg, states = cell_run(walkmod, w, x, cell, M)
+    M, X = cell_weights(cell, x.base.shape[2], 100 + cell)
+    st, toks, lg, states = cell_run(walkmod, w, x, cell, M, X=X)
     assert st == 0
     rep = parity.check(x, toks, lg, requests=_sample_requests(16, (0.0,)), cell=cell,
-                       M=synth.bits(M), gpu_states=states)
+                       M=synth.bits(M), gpu_states=states,
+                       X=None if X is None else synth.bits(X))
     assert rep.ok(), rep
 
 
@@ -599,6 +608,10 @@ def test_cell_rejections(walkmod):
     assert e.value.code == walkmod.EINVAL
     with pytest.raises(walkmod.WalkError) as e:
         walkmod.dspark_walk_set_cell(w.h, walkmod.CELL_RNN, None)
+    assert e.value.code == walkmod.EINVAL
+    with pytest.raises(walkmod.WalkError) as e:                # the GRU needs its tables
+        walkmod.dspark_walk_set_cell(w.h, walkmod.CELL_GRU,
+                                     synth.make_cell_matrix(9, rows=768).cuda(), None)
     assert e.value.code == walkmod.EINVAL
     w.set_cell(walkmod.CELL_RNN, M)
     with pytest.raises(walkmod.WalkError) as e:
