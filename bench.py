@@ -40,11 +40,14 @@ METRIC = ("µs per γ-step draft walk at B=1..128; effective W2 GB/s vs "
 PAGES_US = {("qwen3_resident", 1): 37.0}
 L2_FLUSH_BYTES = 256 << 20
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the walk
-# kernel (ncu, --clock-control none), per (workload, B); refreshed whenever the
-# kernel changes (profiles/walk_resident_qwen3_resident.md)
-TRAFFIC = {("qwen3_resident", 1): 81_894_656,
-           ("partial", 8): 275_697_408,
-           ("sampled", 253): 670_700_800}
+# kernel (ncu, --clock-control none), per (workload, B, head); refreshed
+# whenever the kernel changes (profiles/walk_resident_qwen3_resident.md,
+# walk_resident_partial_b8.md, walk_batched_sampled_b253.md,
+# walk_resident_rnn_long_block_b1.md)
+TRAFFIC = {("qwen3_resident", 1, "markov"): 81_785_856,
+           ("partial", 8, "markov"): 278_784_768,
+           ("sampled", 253, "markov"): 675_076_864,
+           ("long_block", 1, "rnn"): 86_105_344}
 
 
 def parse():
@@ -579,7 +582,7 @@ def main():
     peak, peak_kind = measured_peaks()
     roof = {"bound": "hbm", "achieved": eff_gbs, "peak": peak, "unit": "GB/s",
             "frac": eff_gbs / peak,
-            "traffic": TRAFFIC.get((cfg.name, B)) if args.cell == "markov" else None,
+            "traffic": TRAFFIC.get((cfg.name, B, args.cell)),
             "peak_kind": peak_kind,
             "note": "achieved = effective W2 bytes (gamma*V*r*2*B) per launch / mean launch "
                     "time; >1 means W2 is served from on-chip memory or L2, not HBM"}
