@@ -617,8 +617,10 @@ def main():
         "roofline": roof,
         "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "how": "dspark_walk_run_host: pinned host base/anchor/temperature -> device, "
-                       "the round, tokens -> host, stream sync; wall clock, mean of %d" % e2e_n},
+                "how": "dspark_walk_run_host on pinned host buffers: base/anchor/temperature "
+                       "cross the host link (read in place by the kernel up to 16 MiB of base, "
+                       "copied above), tokens written to host memory, status copied back, one "
+                       "stream sync; wall clock, mean of %d" % e2e_n},
         "gpu_launches": args.steps,
         "phases": trace,
         "clocks": clocks,

@@ -132,12 +132,19 @@ int dspark_walk_run(dspark_walk_t h, const void *base_logits, const int32_t *anc
                     int gamma, void *out_logits, void *stream);
 
 /*
- * dspark_walk_run_host -- the same round with HOST buffers: copies base,
- * anchor and temperature to handle-owned device buffers on `stream`, runs the
- * round, copies the tokens (and logits, if out_logits_host is not NULL) back,
- * and waits for the stream.  Pinned host memory makes the copies asynchronous
- * with respect to other streams.  Returns the round's device status (as
- * dspark_walk_status does) or a host-side error.
+ * dspark_walk_run_host -- the same round with HOST buffers, then waits for
+ * `stream`.  Anchor and temperature go through a pinned block the handle
+ * owns, which the kernel reads in place.  Base logits in pinned host memory
+ * (cudaHostAlloc / cudaHostRegister / a pinned PyTorch tensor) of at most
+ * 16 MiB are read in place by the kernel over the host link, each CTA
+ * fetching its rows one step ahead; other base buffers are first copied to
+ * a handle-owned device buffer on `stream`.  Tokens go straight into a pinned
+ * out_tokens_host, otherwise through a device buffer and a copy; logits (if
+ * out_logits_host is not NULL) always through a device buffer and a copy.
+ * The round's status comes back on the same stream, so the call synchronises
+ * once.  Returns the round's device status (as dspark_walk_status does, and
+ * clears it) or a host-side error.  Host buffers must not change until the
+ * call returns.
  */
 int dspark_walk_run_host(dspark_walk_t h, const void *base_logits_host,
                          const int32_t *anchor_host, const float *temperature_host,

@@ -48,9 +48,11 @@ struct dspark_walk {
   unsigned long long* trace = nullptr;  // caller-owned, see dspark_walk_set_trace
   int64_t trace_bytes = 0;
   int skip_cta = -1;
-  // staging for dspark_walk_run_host (allocated on first use)
+  // staging for dspark_walk_run_host (allocated on first use): device, and a
+  // pinned host block {anchor[max_B], temperature[max_B], status}
   void* stage = nullptr;
   size_t stage_bytes = 0;
+  void* hstage = nullptr;
 };
 
 namespace {
@@ -253,6 +255,22 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
   return DSPARK_OK;
 }
 
+// Device address of a host buffer the GPU can read in place (pinned memory,
+// cudaHostAlloc or cudaHostRegister), or null.
+const void* mapped_host(const void* p) {
+  cudaPointerAttributes pa;
+  if (cudaPointerGetAttributes(&pa, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return pa.type == cudaMemoryTypeHost ? pa.devicePointer : nullptr;
+}
+
+// Base logits up to this size are read by the kernel straight from pinned
+// host memory (each CTA fetches its rows one step ahead); larger ones are
+// copied to the device first, where the kernel's reads run at HBM speed.
+constexpr size_t kZeroCopyBaseMax = (size_t)16 << 20;
+
 }  // namespace
 
 extern "C" {
@@ -383,12 +401,11 @@ int dspark_walk_run_host(dspark_walk_t h, const void* base_logits_host,
     return DSPARK_EINVAL;
   if (B < 1 || B > h->max_B || gamma < 1 || gamma > h->max_gamma) return DSPARK_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // staging: base | logits | anchor | temperature | tokens, sized for the maxima
+  // device staging: base | logits | tokens (each used only when the host
+  // buffer cannot be read or written in place)
   const size_t nlog = (size_t)h->max_B * h->max_gamma * (size_t)h->V;
   const size_t off_logits = round_up(nlog * 2, 256);
-  const size_t off_anchor = off_logits + round_up(nlog * 2, 256);
-  const size_t off_temp = off_anchor + round_up((size_t)h->max_B * 4, 256);
-  const size_t off_tok = off_temp + round_up((size_t)h->max_B * 4, 256);
+  const size_t off_tok = off_logits + round_up(nlog * 2, 256);
   const size_t need = off_tok + round_up((size_t)h->max_B * h->max_gamma * 4, 256);
   if (h->stage_bytes < need) {
     if (h->stage) cudaFree(h->stage);
@@ -397,22 +414,46 @@ int dspark_walk_run_host(dspark_walk_t h, const void* base_logits_host,
     CUDA_TRY(cudaMalloc(&h->stage, need));
     h->stage_bytes = need;
   }
+  // pinned, mapped host block {anchor[max_B], temperature[max_B], status}
+  const size_t small = (size_t)h->max_B * 8;
+  if (!h->hstage) CUDA_TRY(cudaHostAlloc(&h->hstage, small + 16, cudaHostAllocMapped));
   uint8_t* st = static_cast<uint8_t*>(h->stage);
+  uint8_t* hs = static_cast<uint8_t*>(h->hstage);
+  void* hs_dev = nullptr;
+  CUDA_TRY(cudaHostGetDevicePointer(&hs_dev, h->hstage, 0));
+  // the previous call synchronised its stream, so the block is free
+  memcpy(hs, anchor_host, (size_t)B * 4);
+  memcpy(hs + (size_t)h->max_B * 4, temperature_host, (size_t)B * 4);
+  int32_t* hstatus = reinterpret_cast<int32_t*>(hs + small);
   const size_t nb = (size_t)B * gamma * (size_t)h->V * 2;
-  CUDA_TRY(cudaMemcpyAsync(st, base_logits_host, nb, cudaMemcpyHostToDevice, s));
-  CUDA_TRY(cudaMemcpyAsync(st + off_anchor, anchor_host, (size_t)B * 4, cudaMemcpyHostToDevice, s));
-  CUDA_TRY(cudaMemcpyAsync(st + off_temp, temperature_host, (size_t)B * 4, cudaMemcpyHostToDevice,
-                           s));
-  int rc = launch_round(h, st, reinterpret_cast<int32_t*>(st + off_anchor),
-                        reinterpret_cast<float*>(st + off_temp), seed,
-                        reinterpret_cast<int32_t*>(st + off_tok), B, gamma,
-                        out_logits_host ? st + off_logits : nullptr, s);
+  const void* base_dev = nb <= kZeroCopyBaseMax ? mapped_host(base_logits_host) : nullptr;
+  if (!base_dev) {
+    CUDA_TRY(cudaMemcpyAsync(st, base_logits_host, nb, cudaMemcpyHostToDevice, s));
+    base_dev = st;
+  }
+  int32_t* tok_dev = static_cast<int32_t*>(const_cast<void*>(mapped_host(out_tokens_host)));
+  const bool tok_copy = tok_dev == nullptr;
+  if (tok_copy) tok_dev = reinterpret_cast<int32_t*>(st + off_tok);
+  const uint8_t* hsd = static_cast<const uint8_t*>(hs_dev);
+  int rc = launch_round(h, base_dev, reinterpret_cast<const int32_t*>(hsd),
+                        reinterpret_cast<const float*>(hsd + (size_t)h->max_B * 4), seed, tok_dev,
+                        B, gamma, out_logits_host ? st + off_logits : nullptr, s);
   if (rc != DSPARK_OK) return rc;
-  CUDA_TRY(cudaMemcpyAsync(out_tokens_host, st + off_tok, (size_t)B * gamma * 4,
-                           cudaMemcpyDeviceToHost, s));
+  if (tok_copy)
+    CUDA_TRY(cudaMemcpyAsync(out_tokens_host, tok_dev, (size_t)B * gamma * 4,
+                             cudaMemcpyDeviceToHost, s));
   if (out_logits_host)
     CUDA_TRY(cudaMemcpyAsync(out_logits_host, st + off_logits, nb, cudaMemcpyDeviceToHost, s));
-  return dspark_walk_status(h, stream);
+  // the round's status rides on the same stream: one synchronisation in all
+  CUDA_TRY(cudaMemcpyAsync(hstatus, &h->sync.hdr->status, sizeof(int32_t),
+                           cudaMemcpyDeviceToHost, s));
+  CUDA_TRY(cudaStreamSynchronize(s));
+  const int32_t code = *hstatus;
+  if (code != 0) {                                   // clear it for the next run
+    const int32_t zero = 0;
+    CUDA_TRY(cudaMemcpy(&h->sync.hdr->status, &zero, sizeof zero, cudaMemcpyHostToDevice));
+  }
+  return code;
 }
 
 int dspark_walk_status(dspark_walk_t h, void* stream) {
@@ -554,6 +595,7 @@ int dspark_walk_destroy(dspark_walk_t h) {
   if (h->W2b) cudaFree(h->W2b);
   if (h->sync_mem) cudaFree(h->sync_mem);
   if (h->stage) cudaFree(h->stage);
+  if (h->hstage) cudaFreeHost(h->hstage);
   if (h->cell_p) cudaFree(h->cell_p);
   delete h;
   return rc;

@@ -360,6 +360,44 @@ def test_host_buffers_match_device_buffers(walkmod):
     assert st2 == 0
     assert np.array_equal(out.numpy(), toks)
     assert np.array_equal(outl.view(torch.int16).numpy().view(np.uint16), lg)
+    # pageable host buffers take the staged copies instead of in-place reads
+    out2 = torch.full((5, 4), -2, dtype=torch.int32)
+    st3 = walkmod.dspark_walk_run_host(w.h, x.base.clone(), x.anchor.clone(),
+                                       x.temperature.clone(), x.seed, out2, 5, 4, None)
+    assert st3 == 0 and np.array_equal(out2.numpy(), toks)
+    w.close()
+
+
+@pytest.mark.parametrize("kernel", ["planned", "stream", "batched"])
+def test_host_buffers_every_kernel_and_errors(walkmod, kernel):
+    """dspark_walk_run_host on pinned buffers (read and written in place) for
+    every kernel, a larger walk whose base is staged, and a bad anchor's
+    status coming back through it (then cleared)."""
+    x = synth.make_custom(V=20011, gamma=3, B=6, seed=44, temperatures=(0.0, 1.0))
+    w = make_walk(walkmod, x, kernel=kernel)
+    out = torch.full((6, 3), -2, dtype=torch.int32).pin_memory()
+    st = walkmod.dspark_walk_run_host(w.h, x.base.pin_memory(), x.anchor.pin_memory(),
+                                      x.temperature.pin_memory(), x.seed, out, 6, 3, None)
+    assert st == 0
+    assert parity.check(x, out.numpy()).ok()
+    bad = x.anchor.clone()
+    bad[2] = x.base.shape[2] + 5
+    st = walkmod.dspark_walk_run_host(w.h, x.base.pin_memory(), bad.pin_memory(),
+                                      x.temperature.pin_memory(), x.seed, out, 6, 3, None)
+    assert st == walkmod.EANCHOR and np.all(out.numpy() == -1)
+    st = walkmod.dspark_walk_run_host(w.h, x.base.pin_memory(), x.anchor.pin_memory(),
+                                      x.temperature.pin_memory(), x.seed, out, 6, 3, None)
+    assert st == 0 and parity.check(x, out.numpy()).ok()
+    w.close()
+    # 18 MB of base logits: above the in-place limit, staged through device memory
+    y = synth.make_custom(V=151936, gamma=4, B=15, seed=45, temperatures=(0.0,))
+    w = make_walk(walkmod, y)
+    out = torch.full((15, 4), -2, dtype=torch.int32).pin_memory()
+    st = walkmod.dspark_walk_run_host(w.h, y.base.pin_memory(), y.anchor.pin_memory(),
+                                      y.temperature.pin_memory(), y.seed, out, 15, 4, None)
+    assert st == 0
+    assert parity.check(y, out.numpy(), requests=[0, 7, 14]).ok()
+    w.close()
 
 
 # ------------------------------------------------------------------ errors --
