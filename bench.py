@@ -566,7 +566,7 @@ def main():
                 raise RuntimeError("run_host status %d" % rc)
         e2e_us = (time.perf_counter() - te0) / e2e_n * 1e6
     h2d = B * cfg.gamma * cfg.V * 2 + B * 4 + B * 4
-    d2h = B * cfg.gamma * 4
+    d2h = B * cfg.gamma * 4 + 4                             # tokens + the status word
 
     trace = phase_breakdown(walk, w, B, cfg, launch, stream, n_rounds, clocks) if args.trace else None
 
