@@ -788,7 +788,41 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     trace_stamp(a, k, 2);
 
     // (4) tensor-memory rows: warps 0-3 take tiles 0 and 2, warps 4-7 tile 1
-    {
+    if (a.B == 1) {
+      // one request: one column per K half, and a warp's two tiles are read
+      // out of tensor memory together (one load latency, not two)
+      const int q = warp & 3, t0 = warp >> 2;
+      const bool two = t0 == 0;
+      bool good = true;
+      for (int t = t0; t < kTmemTiles; t += 2)
+        good = good && wait_mbar(&mbar[2 * t], (uint32_t)(k & 1), t_step, a.timeout_ns) &&
+               wait_mbar(&mbar[2 * t + 1], (uint32_t)(k & 1), t_step, a.timeout_ns);
+      if (!good) {
+        abort_round(a.sync.hdr, round_s, kStatusTimeout);
+        abort_s = 1;
+      }
+      ptx::tc_fence_after();
+      const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+      uint32_t d[4][1];
+      ptx::tmem_ld<1>(tmem + lane_base + kDCol0 + 32 * t0, d[0]);
+      ptx::tmem_ld<1>(tmem + lane_base + kDCol0 + 32 * t0 + 16, d[1]);
+      if (two) {
+        ptx::tmem_ld<1>(tmem + lane_base + kDCol0 + 64, d[2]);
+        ptx::tmem_ld<1>(tmem + lane_base + kDCol0 + 64 + 16, d[3]);
+      }
+      const int rla = t0 * 128 + 32 * q + lane, rlb = 256 + 32 * q + lane;
+      const uint32_t ba = base_s[rla];
+      const uint32_t bb = two ? base_s[rlb] : 0u;
+      ptx::tmem_wait_ld();
+      const float bias_a =
+          __bfloat162float(__float2bfloat16_rn(__uint_as_float(d[0][0]) + __uint_as_float(d[1][0])));
+      base_s[rla] = float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(ba), bias_a));
+      if (two) {
+        const float bias_b = __bfloat162float(
+            __float2bfloat16_rn(__uint_as_float(d[2][0]) + __uint_as_float(d[3][0])));
+        base_s[rlb] = float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(bb), bias_b));
+      }
+    } else {
       const int q = warp & 3;
 #pragma unroll 1
       for (int t = warp >> 2; t < kTmemTiles; t += 2) {
