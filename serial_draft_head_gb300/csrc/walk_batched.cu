@@ -154,12 +154,12 @@ __device__ __forceinline__ void order_columns(int B, int N, const float* temp_s,
 // Base logits of tokens v0 .. v0 + 7 of request b (b < 0: none) at step k,
 // packed two per word; tokens at or past V read as 0.  `vec`: one 16-byte
 // load (V a multiple of 8, 16-byte aligned base).
-__device__ __forceinline__ void load_base8(const WalkArgs& a, int k, int b, int64_t v0, bool vec,
-                                           uint32_t (&w)[4]) {
+__device__ __forceinline__ void load_base8(const WalkArgs& a, const uint16_t* row, int64_t v0,
+                                           bool vec, uint32_t (&w)[4]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) w[i] = 0u;
-  if (b < 0) return;
-  const uint16_t* src = a.base + ((size_t)b * a.gamma + k) * (size_t)a.V + v0;
+  if (row == nullptr) return;
+  const uint16_t* src = row + v0;
   if (vec && v0 + 8 <= a.V) {
     const uint4 x = __ldg(reinterpret_cast<const uint4*>(src));
     w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
@@ -263,6 +263,9 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
   float* tcol = reinterpret_cast<float*>(col2req + 256);           // [256] T per column
   float* icol = tcol + 256;                                        // [256] fl(1/T) per column
   uint16_t* stage = reinterpret_cast<uint16_t*>(icol + 256);       // [16 warps][8][40]
+  // [256] per column: this step's base row of the column's request (null: none)
+  const uint16_t** colbase =
+      reinterpret_cast<const uint16_t**>(stage + (size_t)kEpiWarps * kStgWarpElems);
   __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t dfull[2], dempty[2];
   __shared__ uint32_t tmem_base_s;
@@ -322,6 +325,7 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
     const float Tc = col2req[c] >= 0 ? temp_s[col2req[c]] : 0.0f;
     tcol[c] = Tc;
     icol[c] = Tc > 0.0f ? inv_temperature(Tc) : 0.0f;
+    colbase[c] = col2req[c] >= 0 ? a.base + (size_t)col2req[c] * a.gamma * (size_t)a.V : nullptr;
   }
   if (warp < kEpiWarps) gather_u(a, tok_s, col2req, U, N);
 
@@ -432,12 +436,26 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
       uint32_t nxt[4];
       int pt = 0, pcb = 0;                           // tile and column of the next prefetch
       auto prefetch = [&]() {
-        const int b = pcb + jl < act ? (int)col2req[c0 + pcb + jl] : -1;
-        load_base8(a, k, b, row0 + pt * 128 + 32 * q + 8 * hl, vec, nxt);
+        const uint16_t* row = pcb + jl < act ? colbase[c0 + pcb + jl] : nullptr;
+        load_base8(a, row, row0 + pt * 128 + 32 * q + 8 * hl, vec, nxt);
         pcb += kCW;
         if (pcb >= cpt * kCW) { pcb = 0; ++pt; }
       };
       if (nc > 0) prefetch();
+      // each chunk's scoring kind, for the whole step (columns and their
+      // temperatures are fixed for the round): 2 bits per chunk
+      uint32_t kinds = 0u;
+      for (int cc = 0; cc < cpt; ++cc) {
+        const int cj = cc * kCW + jl;
+        const float Tj = cj < act ? tcol[c0 + cj] : 0.0f;
+        const float iTj = cj < act ? icol[c0 + cj] : 1.0f;
+        const uint32_t kd =
+            __any_sync(0xFFFFFFFFu, Tj > 0.0f)
+                ? (a.sampler == 1 ? 3u
+                                  : (__any_sync(0xFFFFFFFFu, Tj > 0.0f && iTj == 0.0f) ? 2u : 1u))
+                : 0u;
+        kinds |= kd << (2 * cc);
+      }
       int ci = 0;
       for (int t = 0; t < T; ++t) {
         const int Gt = G + t;
@@ -482,11 +500,7 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
           const bool live = cb + jl < act;
           const int c = c0 + cb + jl;
           const float Tc = live ? tcol[c] : 0.0f, iTc = live ? icol[c] : 1.0f;
-          const int kind =
-              __any_sync(0xFFFFFFFFu, Tc > 0.0f)
-                  ? (a.sampler == 1 ? 3
-                                    : (__any_sync(0xFFFFFFFFu, Tc > 0.0f && iTc == 0.0f) ? 2 : 1))
-                  : 0;
+          const int kind = (int)((kinds >> (2 * cc)) & 3u);
           if (live) best = score8(a, pk, k, (int)col2req[c], Tc, iTc, v0, bz, cur, vec, kind);
           unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, 8);
           best = o > best ? o : best;
@@ -529,6 +543,8 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
       for (int b = threadIdx.x; b < a.B; b += blockDim.x)
         a.out_tokens[(size_t)b * a.gamma + k] = tok_s[b];
     if (k + 1 < a.gamma && warp < kEpiWarps) gather_u(a, tok_s, col2req, U, N);
+    for (int c = threadIdx.x; c < 256; c += blockDim.x)     // next step's base rows
+      if (colbase[c] != nullptr) colbase[c] += a.V;
     ptx::tc_fence_before();
     __syncthreads();
     trace_stamp(a, k, 7);
@@ -580,7 +596,8 @@ int batched_threads() { return kBatThreads; }
 
 size_t batched_smem_bytes(int nst, int N) {
   return (size_t)nst * kStageBytes + (size_t)N * 512 + (size_t)kEpiWarps * kWbCols * 8 + 256 * 8 +
-         256 * 4 + 256 * 4 + 256 * 2 + 256 * 4 + 256 * 4 + (size_t)kEpiWarps * kStgWarpElems * 2;
+         256 * 4 + 256 * 4 + 256 * 2 + 256 * 4 + 256 * 4 + (size_t)kEpiWarps * kStgWarpElems * 2 +
+         256 * 8;
 }
 
 int batched_max_stages() { return kMaxStages; }
