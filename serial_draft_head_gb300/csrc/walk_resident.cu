@@ -362,27 +362,30 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
                  : sampled_block_keys<false>(a, ls, nv, row0, k, b, gi, tpr, T, inv_T, pk, outl);
     } else {
       // 32-bit keys {order bits of the bf16 logit : 16, inverted local row :
-      // 16}, two independent maxima per thread, widened to the 64-bit key once
-      uint32_t m0 = 0u, m1 = 0u;
-      for (int c = gi; 4 * c < nv; c += 2 * tpr) {
+      // 16}, 8 rows per 16-byte load, two rows per 32-bit word (the order map
+      // and -0 -> +0 on both halves at once), four independent maxima per
+      // thread, widened to the 64-bit key once
+      uint32_t mx[4] = {0u, 0u, 0u, 0u};
+      for (int c = gi; 8 * c < nv; c += tpr) {
+        const int rl0 = 8 * c;
+        const uint4 w = *reinterpret_cast<const uint4*>(ls + rl0);
+        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int rl0 = 4 * (c + u * tpr);
-          if (rl0 < nv) {
-            const uint2 w = *reinterpret_cast<const uint2*>(ls + rl0);
-            const uint32_t lb[4] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              uint32_t h = lb[e] == 0x8000u ? 0u : lb[e];
-              h = (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
-              const uint32_t key32 = rl0 + e < nv ? (h << 16) | (0xFFFFu - (uint32_t)(rl0 + e)) : 0u;
-              if (u == 0) m0 = max(m0, key32); else m1 = max(m1, key32);
-              if (outl && rl0 + e < nv) outl[row0 + rl0 + e] = (uint16_t)lb[e];
-            }
-          }
+        for (int p = 0; p < 4; ++p) {
+          uint32_t x = wd[p];
+          x &= ~(__vcmpeq2(x, 0x80008000u) & 0x80008000u);           // -0 -> +0
+          const uint32_t sg = x & 0x80008000u;
+          const uint32_t o = x ^ (sg | ((sg >> 15) * 0x7FFFu) | 0x80008000u);   // order bits
+          const uint32_t r = (uint32_t)(rl0 + 2 * p);
+          const uint32_t k0 = (int)r < nv ? (o << 16) | (0xFFFFu - r) : 0u;
+          const uint32_t k1 = (int)r + 1 < nv ? (o & 0xFFFF0000u) | (0xFFFEu - r) : 0u;
+          mx[p] = max(mx[p], max(k0, k1));
         }
+        if (outl)
+          for (int e = 0; e < 8 && rl0 + e < nv; ++e)
+            outl[row0 + rl0 + e] = (uint16_t)(wd[e >> 1] >> (16 * (e & 1)));
       }
-      const uint32_t m = max(m0, m1);
+      const uint32_t m = max(max(mx[0], mx[1]), max(mx[2], mx[3]));
       if (m != 0u) {
         const uint32_t v = (uint32_t)(row0 + (0xFFFFu - (m & 0xFFFFu)));
         best = ((unsigned long long)(m >> 16) << 32) | (unsigned long long)(0xFFFFFFFFu - v);
