@@ -358,12 +358,26 @@ def measure_config(walk, cfg, B, steps=50, warmup=5, sampler="gumbel", cell="mar
     return res
 
 
-def oracle_walk(O, cell, MX, W1, W2, base, anchor, temperature, seed):
+def oracle_walk(O, cell, MX, W1, W2, base, anchor, temperature, seed, nthreads=0):
     """One oracle walk of the bench's head (tokens only); MX = (M, X) bits."""
     if cell == "markov":
-        return O.walk(W1, W2, base, anchor, temperature, seed, want_logits=False, nthreads=0)
+        return O.walk(W1, W2, base, anchor, temperature, seed, want_logits=False,
+                      nthreads=nthreads)
     return O.walk_cell(W1, W2, base, anchor, temperature, seed, CELLS[cell], M=MX[0], X=MX[1],
-                       want_logits=False, nthreads=0)
+                       want_logits=False, nthreads=nthreads)
+
+
+def cpu_model():
+    """The host CPU's model name (from /proc/cpuinfo when there is one)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "processor name")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 def cell_bits(cfg, cell):
@@ -389,9 +403,22 @@ def cpu_baseline(cfg, B, rounds, seconds, cell="markov"):
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
+    # the same oracle on one thread, a third of the time budget
+    n1 = 0
+    t1 = time.perf_counter()
+    while True:
+        x = rounds[n1 % len(rounds)]
+        oracle_walk(O, cell, MX, W1, W2, synth.bits(x.base), x.anchor.numpy(),
+                    x.temperature.numpy(), x.seed, nthreads=1)
+        n1 += 1
+        if time.perf_counter() - t1 >= seconds / 3:
+            break
+    dt1 = time.perf_counter() - t1
     return {"value": dt / n * 1e6, "unit": "us", "cores": cpu_threads(0), "kind": "oracle",
             "sample": "%d full walks (rounds 0..%d of the workload), fp64 oracle on all "
-                      "host cores" % (n, min(n, len(rounds)) - 1)}
+                      "host cores" % (n, min(n, len(rounds)) - 1),
+            "single_thread_us": dt1 / n1 * 1e6, "single_thread_walks": n1,
+            "cpu_model": cpu_model(), "nproc": os.cpu_count()}
 
 
 def run_reference(args, cfg, B, rank, world):
