@@ -368,7 +368,14 @@ def oracle_walk(O, cell, MX, W1, W2, base, anchor, temperature, seed, nthreads=0
 
 
 def cpu_model():
-    """The host CPU's model name (from /proc/cpuinfo when there is one)."""
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
