@@ -1,8 +1,8 @@
 // tc_ptx.cuh -- thin inline-PTX wrappers for the sm_100-family features the
-// resident walk uses: tensor memory (tcgen05.alloc / ld / st), the 5th-gen
+// walk kernels use: tensor memory (tcgen05.alloc / ld / st), the 5th-gen
 // tensor-core MMA with A read from tensor memory, mbarriers, bulk async copies
-// (TMA 1-D), cp.async, the legacy warp-level mma.sync / ldmatrix, and
-// relaxed GPU-scope loads and stores.  Nothing here computes anything of the
+// (TMA 1-D), L2 eviction policies, cp.async, the legacy warp-level mma.sync /
+// ldmatrix, and relaxed GPU-scope loads and stores.  Nothing here computes anything of the
 // walk itself.
 #pragma once
 
@@ -55,6 +55,39 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
           "r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// L2 eviction policies for the cache-hinted loads below: lines fetched under
+// evict_last are the last candidates for eviction, under evict_first the first.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// bulk_g2s with an L2 eviction policy.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// 16-byte read-only global load that skips L1, with an L2 eviction policy.
+__device__ __forceinline__ uint4 ldg_nc_na_hint(const void* p, uint64_t policy) {
+  uint4 x;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+      : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+      : "l"(p), "l"(policy));
+  return x;
 }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {

@@ -155,13 +155,13 @@ __device__ __forceinline__ void order_columns(int B, int N, const float* temp_s,
 // packed two per word; tokens at or past V read as 0.  `vec`: one 16-byte
 // load (V a multiple of 8, 16-byte aligned base).
 __device__ __forceinline__ void load_base8(const WalkArgs& a, const uint16_t* row, int64_t v0,
-                                           bool vec, uint32_t (&w)[4]) {
+                                           bool vec, uint64_t policy, uint32_t (&w)[4]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) w[i] = 0u;
   if (row == nullptr) return;
   const uint16_t* src = row + v0;
   if (vec && v0 + 8 <= a.V) {
-    const uint4 x = __ldg(reinterpret_cast<const uint4*>(src));
+    const uint4 x = ptx::ldg_nc_na_hint(src, policy);
     w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
   } else {
 #pragma unroll
@@ -177,62 +177,39 @@ __device__ __forceinline__ uint32_t add_bf16x2(uint32_t x, uint32_t y) {
   return d;
 }
 
-// Tokens v0 .. v0 + 7 of request b at step k: logit = bf16(base + bias) (the
-// bias already rounded to bf16), the optional copy to out_logits, the
-// selection score and the best key {order bits, inverted id}; ties keep the
-// smallest id.  Tokens at or past V do not take part.  `kind` is the same for
-// the whole warp: 0 = every live lane greedy (score = logit); 1 = noise drawn
-// for every lane (one Philox call per four tokens) and used where T > 0;
-// 2 = as 1, with the IEEE quotient where 1/T overflows; 3 = the group sampler
-// (the 8 tokens are one group: group_key) where T > 0, greedy elsewhere.
-__device__ __forceinline__ unsigned long long score8(const WalkArgs& a, const PhiloxKeys& pk,
-                                                     int k, int b, float T, float inv_T,
-                                                     int64_t v0, const uint4& bz,
-                                                     const uint32_t (&bw)[4], bool vec,
-                                                     int kind) {
-  const int64_t nvalid = a.V - v0;
-  if (nvalid <= 0) return 0ull;
-  uint32_t lw[4];
-  lw[0] = add_bf16x2(bw[0], bz.x);
-  lw[1] = add_bf16x2(bw[1], bz.y);
-  lw[2] = add_bf16x2(bw[2], bz.z);
-  lw[3] = add_bf16x2(bw[3], bz.w);
-  float lg[8];
+// Temperatures below this take their reciprocal scaled (see gumbel8).
+constexpr float kTinyT = 0x1p-120f;
+
+// Gumbel-max scores of the 8 logits lg of tokens v0 .. v0 + 7 (request b,
+// step k): fp32(logit / T) + noise where T > 0, the logit itself where T = 0.
+// The quotient is the product with the rounded reciprocal, taken as
+// fl(fl(logit * inv_T) * qscale + g) in one fused step: qscale = 1 and
+// inv_T = fl(1/T) for T >= 2^-120; below, inv_T = fl(1/(2^64 T)) and qscale =
+// 2^64.  The scalings by 2^64 are exact, so this is the product with fl(1/T)
+// with the exponent range extended: the same bits wherever fl(1/T) is finite,
+// and a finite reciprocal where it overflows.
+__device__ __forceinline__ void gumbel8(const float (&lg)[8], float T, float inv_T, float qscale,
+                                        int64_t v0, int k, int b, const PhiloxKeys& pk,
+                                        float (&sc)[8]) {
+  const bool sampled = T > 0.0f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    lg[i] = __uint_as_float((i & 1) ? (lw[i >> 1] & 0xFFFF0000u) : (lw[i >> 1] << 16));
-  if (a.out_logits != nullptr) {
-    uint16_t* dst = a.out_logits + ((size_t)b * a.gamma + k) * (size_t)a.V + v0;
-    if (vec && nvalid >= 8) {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    } else {
+  for (int c4 = 0; c4 < 2; ++c4) {
+    const uint4 r = philox4x32_10(
+        make_uint4((uint32_t)(v0 >> 2) + (uint32_t)c4, (uint32_t)k, (uint32_t)b, 0u), pk);
+    const uint32_t x[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i < nvalid) dst[i] = (uint16_t)(lw[i >> 1] >> (16 * (i & 1)));
+    for (int e = 0; e < 4; ++e) {
+      const float l = lg[4 * c4 + e];
+      const float q = __fmul_rn(l, inv_T);
+      sc[4 * c4 + e] = sampled ? __fmaf_rn(q, qscale, gumbel_noise(x[e])) : l;
     }
   }
-  if (kind == 3 && T > 0.0f)
-    return group_key(lg, nvalid < 8 ? (int)nvalid : 8, T, inv_T, (uint32_t)v0, k, b, pk);
-  float sc[8];
-  if (kind == 0 || kind == 3) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sc[i] = lg[i];
-  } else {
-    const bool sampled = T > 0.0f;
-#pragma unroll
-    for (int c4 = 0; c4 < 2; ++c4) {
-      const uint4 r = philox4x32_10(
-          make_uint4((uint32_t)(v0 >> 2) + (uint32_t)c4, (uint32_t)k, (uint32_t)b, 0u), pk);
-      const uint32_t x[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float l = lg[4 * c4 + e];
-        float q = __fmul_rn(l, inv_T);
-        if (kind == 2 && inv_T == 0.0f) q = __fdiv_rn(l, T);
-        sc[4 * c4 + e] = sampled ? __fadd_rn(q, gumbel_noise(x[e])) : l;
-      }
-    }
-  }
+}
+
+// The selection key of 8 scores of tokens v0 .. v0 + 7, nvalid of them real:
+// {ord32(best score), inverted id}, ties to the smallest id.
+__device__ __forceinline__ unsigned long long best_key8(const float (&sc)[8], int64_t v0,
+                                                        int64_t nvalid) {
   float best = sc[0];
   int best_i = 0;
   if (nvalid >= 8) {
@@ -246,6 +223,57 @@ __device__ __forceinline__ unsigned long long score8(const WalkArgs& a, const Ph
   }
   return ((unsigned long long)ord32(best) << 32) |
          (unsigned long long)(0xFFFFFFFFu - (uint32_t)(v0 + best_i));
+}
+
+// bf16 logit i of the 8 packed two per word in lw, as fp32.
+__device__ __forceinline__ void unpack8(const uint32_t (&lw)[4], float (&lg)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    lg[i] = __uint_as_float((i & 1) ? (lw[i >> 1] & 0xFFFF0000u) : (lw[i >> 1] << 16));
+}
+
+// Tokens v0 .. v0 + 7 of request b at step k: logit = bf16(base + bias) (the
+// bias already rounded to bf16), the optional copy to out_logits, the
+// selection score and the best key {order bits, inverted id}; ties keep the
+// smallest id.  Tokens at or past V do not take part.  `kind` is the same for
+// the whole warp: 0 = every live lane greedy (score = logit); 1 = noise drawn
+// for every lane (one Philox call per four tokens) and used where T > 0;
+// 2 = the group sampler (the 8 tokens are one group: group_key) where T > 0,
+// greedy elsewhere.
+__device__ __forceinline__ unsigned long long score8(const WalkArgs& a, const PhiloxKeys& pk,
+                                                     int k, int b, float T, float inv_T,
+                                                     int64_t v0, const uint4& bz,
+                                                     const uint32_t (&bw)[4], bool vec,
+                                                     int kind) {
+  const int64_t nvalid = a.V - v0;
+  if (nvalid <= 0) return 0ull;
+  uint32_t lw[4];
+  lw[0] = add_bf16x2(bw[0], bz.x);
+  lw[1] = add_bf16x2(bw[1], bz.y);
+  lw[2] = add_bf16x2(bw[2], bz.z);
+  lw[3] = add_bf16x2(bw[3], bz.w);
+  float lg[8];
+  unpack8(lw, lg);
+  if (a.out_logits != nullptr) {
+    uint16_t* dst = a.out_logits + ((size_t)b * a.gamma + k) * (size_t)a.V + v0;
+    if (vec && nvalid >= 8) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i < nvalid) dst[i] = (uint16_t)(lw[i >> 1] >> (16 * (i & 1)));
+    }
+  }
+  if (kind == 2 && T > 0.0f)
+    return group_key(lg, nvalid < 8 ? (int)nvalid : 8, T, inv_T, (uint32_t)v0, k, b, pk);
+  float sc[8];
+  if (kind == 0 || kind == 2) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sc[i] = lg[i];
+  } else {
+    gumbel8(lg, T, inv_T, T < kTinyT ? 0x1p64f : 1.0f, v0, k, b, pk, sc);
+  }
+  return best_key8(sc, v0, nvalid);
 }
 
 __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const BatchedArgs ba) {
@@ -324,7 +352,11 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
   for (int c = threadIdx.x; c < 256; c += blockDim.x) {
     const float Tc = col2req[c] >= 0 ? temp_s[col2req[c]] : 0.0f;
     tcol[c] = Tc;
-    icol[c] = Tc > 0.0f ? inv_temperature(Tc) : 0.0f;
+    // the group sampler takes fl(1/T) (0 where it overflows); the Gumbel
+    // scores take the reciprocal of 2^64 T below 2^-120 (see gumbel8)
+    icol[c] = !(Tc > 0.0f)                    ? 0.0f
+              : a.sampler == 1 || Tc >= kTinyT ? inv_temperature(Tc)
+                                               : __frcp_rn(__fmul_rn(Tc, 0x1p64f));
     colbase[c] = col2req[c] >= 0 ? a.base + (size_t)col2req[c] * a.gamma * (size_t)a.V : nullptr;
   }
   if (warp < kEpiWarps) gather_u(a, tok_s, col2req, U, N);
@@ -332,13 +364,17 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
   // control state (lane 0 of the control warp)
   const int stages_total = 2 * T * a.gamma;   // half-tiles consumed this round
   int issued = 0;                             // half-tiles whose copy was issued
+  // W2 is re-read every step and the base logits once: W2 keeps its L2 lines
+  // ahead of the base stream, which would otherwise push it out at large B
+  const uint64_t w2_policy = ptx::policy_evict_last();
   if (warp == kEpiWarps && lane == 0) {
     const int pre = nst < stages_total ? nst : stages_total;
     for (; issued < pre; ++issued) {
       const int gl = issued % (2 * T);
       ptx::mbar_expect_tx(&full_bar[issued % nst], kStageBytes);
-      ptx::bulk_g2s(ring + (size_t)(issued % nst) * kStageBytes, gw + (size_t)gl * kStageBytes,
-                    kStageBytes, &full_bar[issued % nst]);
+      ptx::bulk_g2s_hint(ring + (size_t)(issued % nst) * kStageBytes,
+                         gw + (size_t)gl * kStageBytes, kStageBytes, &full_bar[issued % nst],
+                         w2_policy);
     }
   }
   ptx::tc_fence_before();
@@ -400,8 +436,8 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
               }
               const int gl = issued % (2 * T);
               ptx::mbar_expect_tx(&full_bar[ps], kStageBytes);
-              ptx::bulk_g2s(ring + (size_t)ps * kStageBytes, gw + (size_t)gl * kStageBytes,
-                            kStageBytes, &full_bar[ps]);
+              ptx::bulk_g2s_hint(ring + (size_t)ps * kStageBytes, gw + (size_t)gl * kStageBytes,
+                                 kStageBytes, &full_bar[ps], w2_policy);
               ++issued;
             }
           }
@@ -433,11 +469,12 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
       __syncwarp();
       const uint2 eseed = round_seed(a, round_s);     // this round's Philox key
       const PhiloxKeys pk = philox_keys(eseed.x, eseed.y);
+      const uint64_t base_policy = ptx::policy_evict_first();   // read once
       uint32_t nxt[4];
       int pt = 0, pcb = 0;                           // tile and column of the next prefetch
       auto prefetch = [&]() {
         const uint16_t* row = pcb + jl < act ? colbase[c0 + pcb + jl] : nullptr;
-        load_base8(a, row, row0 + pt * 128 + 32 * q + 8 * hl, vec, nxt);
+        load_base8(a, row, row0 + pt * 128 + 32 * q + 8 * hl, vec, base_policy, nxt);
         pcb += kCW;
         if (pcb >= cpt * kCW) { pcb = 0; ++pt; }
       };
@@ -448,12 +485,7 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
       for (int cc = 0; cc < cpt; ++cc) {
         const int cj = cc * kCW + jl;
         const float Tj = cj < act ? tcol[c0 + cj] : 0.0f;
-        const float iTj = cj < act ? icol[c0 + cj] : 1.0f;
-        const uint32_t kd =
-            __any_sync(0xFFFFFFFFu, Tj > 0.0f)
-                ? (a.sampler == 1 ? 3u
-                                  : (__any_sync(0xFFFFFFFFu, Tj > 0.0f && iTj == 0.0f) ? 2u : 1u))
-                : 0u;
+        const uint32_t kd = __any_sync(0xFFFFFFFFu, Tj > 0.0f) ? (a.sampler == 1 ? 2u : 1u) : 0u;
         kinds |= kd << (2 * cc);
       }
       int ci = 0;
@@ -469,16 +501,6 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
         }
         ptx::tc_fence_after();
         if (t == 0) trace_stamp(a, k, 1);
-        // the next tile's base rows (or step k + 1's first tile) into L2: 64
-        // bytes per request, one prefetch per live column
-        {
-          const int tn = t + 1 < T ? t + 1 : 0;
-          const int kn = t + 1 < T ? k : k + 1;
-          const int64_t rs = row0 + tn * 128 + 32 * q;
-          if (kn < a.gamma && rs < a.V)
-            for (int j = lane; j < act; j += 32)
-              ptx::prefetch_l2(a.base + ((size_t)col2req[c0 + j] * a.gamma + kn) * (size_t)a.V + rs);
-        }
         const int64_t v0 = row0 + t * 128 + 32 * q + 8 * hl;
         for (int cc = 0; cc < cpt; ++cc, ++ci) {
           const int cb = cc * kCW;

@@ -332,14 +332,19 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // of weights exceeds U2 * S (the last one if rounding leaves none).  U1, U2 are
 // the words 2 (j & 1) and 2 (j & 1) + 1 of Philox counter (j >> 1, k, b, 1).
 // Returns the group's selection key {ord32(score), inverted id of the pick}.
-__device__ __forceinline__ unsigned long long group_key(const float (&lg)[8], int n, float T,
-                                                        float inv_T, uint32_t v0, int k, int b,
-                                                        const PhiloxKeys& pk) {
+// kQ: how fp32(logit / T) is formed -- 0: the product with inv_T; 1: the IEEE
+// quotient; 2: the product, or the quotient where inv_T is 0, per element.
+template <int kQ>
+__device__ __forceinline__ unsigned long long group_key_q(const float (&lg)[8], int n, float T,
+                                                          float inv_T, uint32_t v0, int k, int b,
+                                                          const PhiloxKeys& pk) {
   float z[8];
   float m = -INFINITY;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float q = inv_T != 0.0f ? __fmul_rn(lg[i], inv_T) : __fdiv_rn(lg[i], T);
+    const float q = kQ == 0   ? __fmul_rn(lg[i], inv_T)
+                    : kQ == 1 ? __fdiv_rn(lg[i], T)
+                              : (inv_T != 0.0f ? __fmul_rn(lg[i], inv_T) : __fdiv_rn(lg[i], T));
     z[i] = i < n ? q : -INFINITY;
     m = fmaxf(m, z[i]);
   }
@@ -370,6 +375,27 @@ __device__ __forceinline__ unsigned long long group_key(const float (&lg)[8], in
     if (i < n && runs[i] > target) pick = i;
   return ((unsigned long long)ord32(score) << 32) |
          (unsigned long long)(0xFFFFFFFFu - (v0 + (uint32_t)pick));
+}
+
+// The group key with the IEEE quotient, for a temperature whose reciprocal
+// overflows (T below 2^-126).  Out of line, arguments by value: the rare form
+// costs the common one neither registers nor instructions.
+static __device__ __noinline__ unsigned long long group_key_div(
+    float l0, float l1, float l2, float l3, float l4, float l5, float l6, float l7, int n,
+    float T, uint32_t v0, int k, int b, uint32_t key0, uint32_t key1) {
+  const float lg[8] = {l0, l1, l2, l3, l4, l5, l6, l7};
+  return group_key_q<1>(lg, n, T, 0.0f, v0, k, b, philox_keys(key0, key1));
+}
+
+// The group key of tokens v0 .. v0 + n - 1 (see group_key_q); inv_T = fl(1/T),
+// 0 when that overflows.
+__device__ __forceinline__ unsigned long long group_key(const float (&lg)[8], int n, float T,
+                                                        float inv_T, uint32_t v0, int k, int b,
+                                                        const PhiloxKeys& pk) {
+  if (inv_T == 0.0f)
+    return group_key_div(lg[0], lg[1], lg[2], lg[3], lg[4], lg[5], lg[6], lg[7], n, T, v0, k, b,
+                         pk.k0[0], pk.k1[0]);
+  return group_key_q<0>(lg, n, T, inv_T, v0, k, b, pk);
 }
 
 // fl(1/T) for T > 0, or 0 when it overflows (T below 2^-126).

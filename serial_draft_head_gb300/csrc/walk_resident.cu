@@ -349,7 +349,7 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
           lg[e] = bf16_bits_to_float((wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
         const int n = nv - rl0 < 8 ? nv - rl0 : 8;
         const uint32_t v0 = (uint32_t)(row0 + rl0);     // a multiple of 8
-        const unsigned long long key = group_key(lg, n, T, inv_T, v0, k, b, pk);
+        const unsigned long long key = group_key_q<2>(lg, n, T, inv_T, v0, k, b, pk);
         best = key > best ? key : best;
         if (outl)
           for (int e = 0; e < n; ++e) outl[v0 + e] = (uint16_t)((wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);

@@ -59,6 +59,7 @@ SMALL = [
     (130000, 3, 1, (0.0,), 9),             # 152 CTAs, 6 shared-memory strips each
     (90001, 2, 5, (0.0, 1.0), 10),         # odd V: plain base loads
     (77778, 3, 12, (0.6, 0.0), 11),        # two n-tiles (8 < B <= 16)
+    (3001, 2, 130, (0.0, 0.6, 1.0), 12),   # B = 130: MMA N = 144, ragged column quarters
 ]
 
 
@@ -455,6 +456,31 @@ def test_degenerate_vocabularies(walkmod, V, kernel):
         st, toks, lg = gpu_run(w, x)
         assert st == 0
         assert parity.check(x, toks, lg, sampler=1).ok()
+    w.close()
+
+
+@pytest.mark.parametrize("kernel", ["planned", "stream", "batched"])
+@pytest.mark.parametrize("B", [6, 20])
+def test_tiny_temperatures(walkmod, B, kernel):
+    """Temperatures down to fp32 subnormals: fl(1/T) overflows below 2^-128 and
+    logit / T overflows for most logits below 2^-127, so the Gumbel scores
+    tie at +inf and the smallest such token wins; 1e-30 keeps the scores
+    finite.  The group sampler where logit / T stays finite in fp32."""
+    x = synth.make_custom(V=3001, gamma=3, B=B, seed=71, noise_seed=71,
+                          temperatures=(1e-40, 3e-39, 2.0**-127, 1e-30, 0.0, 1.0))
+    w = make_walk(walkmod, x, kernel=kernel)
+    st, toks, lg = gpu_run(w, x)
+    assert st == 0, walkmod.dspark_walk_strerror(st)
+    rep = parity.check(x, toks, lg)
+    assert rep.ok(), rep
+    if kernel != "stream":
+        y = synth.make_custom(V=3001, gamma=3, B=B, seed=71, noise_seed=72,
+                              temperatures=(1e-30, 1e-20, 0.0, 2.0**-100))
+        w.set_sampler(walkmod.SAMPLER_GROUP)
+        st, toks, lg = gpu_run(w, y)
+        assert st == 0
+        rep = parity.check(y, toks, lg, sampler=1)
+        assert rep.ok(), rep
     w.close()
 
 
