@@ -46,7 +46,7 @@ L2_FLUSH_BYTES = 256 << 20
 # walk_resident_rnn_long_block_b1.md)
 TRAFFIC = {("qwen3_resident", 1, "markov"): 81_745_664,
            ("partial", 8, "markov"): 273_919_232,
-           ("sampled", 253, "markov"): 674_138_880,
+           ("sampled", 253, "markov"): 401_235_968,
            ("long_block", 1, "rnn"): 86_085_632}
 
 
