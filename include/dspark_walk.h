@@ -115,7 +115,12 @@ int dspark_walk_create(const void *W1, const void *W2, int64_t V, int r, int max
  *
  *   base_logits  device, bf16 [B, gamma, V]: the parallel pass's logits
  *   anchor       device, int32 [B]: the last accepted token of each request
- *   temperature  device, fp32 [B]: 0 = greedy, > 0 = Gumbel-max sampling
+ *   temperature  device, fp32 [B]: 0 = greedy, > 0 = Gumbel-max sampling.
+ *                fp32(logit / T) is the product with fl(1/T), within one
+ *                fp32 ulp of the quotient, and overflows to +-inf where the
+ *                quotient does (then the smallest such token id wins).
+ *                Under the group sampler a request whose logit / T
+ *                overflows fp32 draws a valid but unspecified token.
  *   seed         Philox key of this round (change it per round for fresh noise)
  *   out_tokens   device, int32 [B, gamma]: the drafted tokens
  *   B, gamma     1 <= B <= max_B, 1 <= gamma <= max_gamma
