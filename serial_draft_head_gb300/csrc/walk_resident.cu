@@ -267,11 +267,17 @@ __device__ __forceinline__ void logits_strip(const float (&acc)[NT][4], uint16_t
 // Philox chains): the best key {ord32(score), inverted id}.  FASTQ: the
 // quotient logit / T as the product with fl(1/T) (else the IEEE quotient,
 // when 1/T overflows).
-template <bool FASTQ>
+// kTrack: keep the best score and its row in fp32 / int registers (this
+// thread's rows come in increasing order, so a strict > keeps the smallest id
+// among equal scores) and form the 64-bit key once, instead of a key and a
+// 64-bit maximum per row.
+template <bool FASTQ, bool kTrack = false>
 __device__ __forceinline__ unsigned long long sampled_block_keys(
     const WalkArgs& a, const uint16_t* ls, int nv, int64_t row0, int k, int b, int gi, int tpr,
     float T, float inv_T, const PhiloxKeys& pk, uint16_t* outl) {
   unsigned long long best = 0ull;
+  float bs = 0.0f;
+  int bv = -1;
   for (int c = gi; 4 * c < nv; c += 2 * tpr) {
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -287,14 +293,23 @@ __device__ __forceinline__ unsigned long long sampled_block_keys(
           if (rl0 + e < nv) {
             const float lgt = bf16_bits_to_float(lb[e]);
             const float q = FASTQ ? __fmul_rn(lgt, inv_T) : __fdiv_rn(lgt, T);
-            const unsigned long long key = make_key(__fadd_rn(q, gumbel_noise(x[e])), v0 + e);
-            best = key > best ? key : best;
+            const float sc = __fadd_rn(q, gumbel_noise(x[e]));
+            if (kTrack) {
+              if (bv < 0 || sc > bs) {
+                bs = sc;
+                bv = (int)(v0 + e);
+              }
+            } else {
+              const unsigned long long key = make_key(sc, v0 + e);
+              best = key > best ? key : best;
+            }
             if (outl) outl[v0 + e] = (uint16_t)lb[e];
           }
         }
       }
     }
   }
+  if (kTrack && bv >= 0) best = make_key(bs, (uint32_t)bv);
   return best;
 }
 
@@ -347,10 +362,11 @@ __device__ __forceinline__ KeyPassMap key_pass_map(int B, const float* temp_s) {
   return m;
 }
 
-// kHoistQ: the group sampler picks its quotient form once per thread instead
-// of per element (8% faster at B=16; the B <= 8 instantiations keep the
-// per-element form, whose code leaves the fully resident k loop 0.35 us
-// faster per round).
+// kHoistQ (the B > 8 instantiations): the group sampler picks its quotient
+// form once per thread instead of per element (8% faster at B=16), and the
+// Gumbel rows track their best in fp32 (sampled_block_keys' kTrack).  The
+// B <= 8 instantiations keep the older code, with which the fully resident k
+// loop runs 0.35 us faster per round.
 template <bool kHoistQ>
 __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logit_s, int R,
                                          int nv, int64_t row0, int k, const KeyPassMap& m,
@@ -379,9 +395,10 @@ __device__ __forceinline__ void key_pass(const WalkArgs& a, const uint16_t* logi
     } else if (T > 0.0f) {
       const PhiloxKeys pk = philox_keys(seed.x, seed.y);
       // the quotient by the rounded reciprocal unless 1/T overflows
-      best = inv_T != 0.0f
-                 ? sampled_block_keys<true>(a, ls, nv, row0, k, b, gi, tpr, T, inv_T, pk, outl)
-                 : sampled_block_keys<false>(a, ls, nv, row0, k, b, gi, tpr, T, inv_T, pk, outl);
+      best = inv_T != 0.0f ? sampled_block_keys<true, kHoistQ>(a, ls, nv, row0, k, b, gi, tpr, T,
+                                                                inv_T, pk, outl)
+                           : sampled_block_keys<false, kHoistQ>(a, ls, nv, row0, k, b, gi, tpr, T,
+                                                                 inv_T, pk, outl);
     } else {
       // 32-bit keys {order bits of the bf16 logit : 16, inverted local row :
       // 16}, 8 rows per 16-byte load, two rows per 32-bit word (the order map
