@@ -460,7 +460,7 @@ def test_degenerate_vocabularies(walkmod, V, kernel):
 
 
 @pytest.mark.parametrize("kernel", ["planned", "stream", "batched"])
-@pytest.mark.parametrize("B", [6, 20])
+@pytest.mark.parametrize("B", [6, 12, 20])
 def test_tiny_temperatures(walkmod, B, kernel):
     """Temperatures down to fp32 subnormals: fl(1/T) overflows below 2^-128 and
     logit / T overflows for most logits below 2^-127, so the Gumbel scores
