@@ -473,6 +473,40 @@ def pin_t_to_zero(O):
     assert np.array_equal(ts, tg), "T -> 0+ must give the greedy walk"
 
 
+def pin_overflowing_quotient(O):
+    """Temperatures so small that fp32(logit / T) overflows for the larger
+    logits.  The Gumbel score is that fp32 quotient plus noise, so every logit
+    whose quotient overflows scores +inf and the finite ones cannot reach it:
+    the smallest such id wins, whatever the noise.  The group sampler forms z
+    in fp64, where the quotients stay finite and ordered: it takes the argmax."""
+    V, r, gamma, B = 96, 256, 3, 4
+    g = torch.Generator("cpu").manual_seed(31)
+    W1 = (torch.randn(V, r, generator=g) / 16).to(torch.bfloat16)
+    W2 = torch.zeros(V, r, dtype=torch.bfloat16)          # logits = base exactly
+    vals = torch.tensor([-2.0, -0.5, 0.0, 0.25, 1.0, 3.0])
+    base = vals[torch.randint(0, len(vals), (B, gamma, V), generator=g)]
+    base[:, :, :5] = -1.0                                   # the first ids never positive
+    top = torch.randint(5, V, (B, gamma), generator=g)
+    for b in range(B):
+        for k in range(gamma):
+            base[b, k, top[b, k]] = 8.0                     # one unique maximum per row
+    base = base.to(torch.bfloat16)
+    anchor = torch.randint(0, V, (B,), generator=g).int().numpy()
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    temps = np.array([1e-40, 3e-39, 2.0**-127, 1e-45], np.float32)
+    bf = base.float().numpy()
+    with np.errstate(over="ignore"):
+        q = (bf.astype(np.float64) / temps.astype(np.float64)[:, None, None]).astype(np.float32)
+    assert np.isposinf(q).any(axis=2).all(), "every row needs an overflowing logit"
+    first_pos = np.argmax(np.isposinf(q), axis=2)
+    for seed in (0, 5):
+        t, _, _ = O.walk(bits(W1), bits(W2), bits(base), anchor, temps, seed)
+        assert np.array_equal(t, first_pos), \
+            "overflowing quotient: tokens %r, first +inf ids %r" % (t.tolist(), first_pos.tolist())
+        tg, _, _ = O.walk(bits(W1), bits(W2), bits(base), anchor, temps, seed, sampler=1)
+        assert np.array_equal(tg, top.numpy()), "group sampler at tiny T must take the argmax"
+
+
 def pin_forced(O):
     """Teacher forcing with a walk's own tokens reproduces that walk."""
     import synth
@@ -783,7 +817,7 @@ ALL_PINS = [
     pin_philox_vs_triton, pin_noise_layout, pin_uniform, pin_gumbel,
     pin_hand_walk, pin_fig2_bruteforce, pin_w2_zero, pin_spike,
     pin_batch_independence, pin_permutation, pin_sampling_law, pin_t_to_zero,
-    pin_forced, pin_errors, pin_group_layout, pin_group_sampling_law, pin_group_t_to_zero,
+    pin_overflowing_quotient, pin_forced, pin_errors, pin_group_layout, pin_group_sampling_law, pin_group_t_to_zero,
     pin_group_batch_independence, pin_cell_rnn_zero_matrix, pin_cell_gated_half,
     pin_cell_gated_saturation, pin_cell_rnn_permutation, pin_cell_gru_reduces_to_rnn,
     pin_cell_gru_hold, pin_cell_gru_permutation, pin_cell_batch_and_forcing,
