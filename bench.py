@@ -44,7 +44,7 @@ L2_FLUSH_BYTES = 256 << 20
 # whenever the kernel changes (profiles/walk_resident_qwen3_resident.md,
 # walk_resident_partial_b8.md, walk_batched_sampled_b253.md,
 # walk_resident_rnn_long_block_b1.md)
-TRAFFIC = {("qwen3_resident", 1, "markov"): 81_745_664,
+TRAFFIC = {("qwen3_resident", 1, "markov"): 81_780_992,
            ("partial", 8, "markov"): 273_919_232,
            ("sampled", 253, "markov"): 401_235_968,
            ("long_block", 1, "rnn"): 86_085_632}
