@@ -54,3 +54,14 @@ def test_create_without_a_device_fails_cleanly():
     from serial_draft_head_gb300 import walk
     with pytest.raises(walk.WalkError):
         walk.dspark_walk_create(16, 16, 100, 256, 1, 1)
+
+
+def test_binding_constants_match_the_header():
+    """Every DSPARK_* value the header defines has the same value in the binding."""
+    from serial_draft_head_gb300 import walk
+    text = open(os.path.join(ROOT, "include", "dspark_walk.h")).read()
+    defs = re.findall(r"^#define DSPARK_(\w+)\s+\(?(-?\d+)\)?", text, flags=re.M)
+    assert len(defs) >= 20
+    for name, value in defs:
+        assert hasattr(walk, name), "DSPARK_%s has no binding constant" % name
+        assert getattr(walk, name) == int(value), "DSPARK_%s differs" % name
