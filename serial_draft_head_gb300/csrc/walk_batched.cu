@@ -26,8 +26,10 @@
 // goes through the atomic rendezvous and the next u rows are gathered into U.
 //
 // Requests are laid out in MMA columns greedy-first (a stable partition by
-// temperature), so a 16-column chunk is, but for one, all greedy or all
-// sampled and the lanes of a warp rarely diverge on the noise.
+// temperature), so an 8-column chunk is, but for one, all greedy or all
+// sampled and the lanes of a warp rarely diverge on the noise.  W2 copies
+// carry an L2 evict-last policy and the base loads evict-first: W2 (re-read
+// every step) then stays in L2 beside the base stream (read once).
 #include "tc_ptx.cuh"
 #include "walk_common.cuh"
 #include "walk_kernels.h"
@@ -151,9 +153,10 @@ __device__ __forceinline__ void order_columns(int B, int N, const float* temp_s,
   __syncwarp();
 }
 
-// Base logits of tokens v0 .. v0 + 7 of request b (b < 0: none) at step k,
-// packed two per word; tokens at or past V read as 0.  `vec`: one 16-byte
-// load (V a multiple of 8, 16-byte aligned base).
+// Base logits of tokens v0 .. v0 + 7 from one request's row of this step
+// (row null: none), packed two per word; tokens at or past V read as 0.
+// `vec`: one 16-byte load that skips L1 and carries the L2 `policy` (V a
+// multiple of 8, 16-byte aligned base).
 __device__ __forceinline__ void load_base8(const WalkArgs& a, const uint16_t* row, int64_t v0,
                                            bool vec, uint64_t policy, uint32_t (&w)[4]) {
 #pragma unroll
