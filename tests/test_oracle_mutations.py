@@ -42,6 +42,9 @@ MUTATIONS = {
                            "    const double target = (double)U1 * S;\n    double run = 0.0;\n"),
     "group_counter_word": ("{(uint32_t)(j >> 1), (uint32_t)k, (uint32_t)b, 1u}",
                            "{(uint32_t)(j >> 1), (uint32_t)k, (uint32_t)b, 0u}"),
+    # the group scores from z rounded to fp32: overflows at tiny T
+    "group_z_in_fp32": ("            z[i] = orc_bf16_to_f64(logit[v0 + i]) / (double)T;",
+                        "            z[i] = (double)(float)(orc_bf16_to_f64(logit[v0 + i]) / (double)T);"),
     # recurrent heads
     "cell_gate_swapped": ("val = (1.0 - z) * hp + z * xi;", "val = z * hp + (1.0 - z) * xi;"),
     "cell_gate_sign": ("1.0 / (1.0 + exp(-p));", "1.0 / (1.0 + exp(p));"),
