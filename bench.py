@@ -2,12 +2,18 @@
 
 A step is one round: the whole gamma-step walk of one batch, one launch of
 the persistent kernel, on seeded synthetic inputs already resident in HBM.
-The default workload is the Qwen3-scale fully resident walk (V = 151,936,
-r = 256, gamma = 7, B = 1, greedy, 100 seeded rounds; each step takes the
-next round's base logits and anchor).  Between timed steps L2 is flushed by
-writing a 256 MiB buffer, so every step starts with a cold L2 (as the pages
-time the walk: CUDA-graph replay, cold L2).  Each step's kernel is timed with
-CUDA events on the stream it is launched on.
+The default workload is the long-block fully resident walk (V = 151,936,
+r = 256, gamma = 16, B = 1, greedy), the configuration whose on-chip-read
+roofline fraction is the figure of merit.  Between timed steps L2 is flushed
+by writing a 256 MiB buffer, so every step starts with a cold L2 (as the
+pages time the walk: CUDA-graph replay, cold L2).  Each step's kernel is
+timed with CUDA events on the stream it is launched on.
+
+`roofline` is the on-chip-read roofline of the resident tiers: W2 is read
+from HBM once per process, and every step reads the whole table (gamma V r 2
+bytes per walk) out of tensor memory, registers and shared memory at the
+tier rates `--unit-rates` measures.  `effective_w2` reports the same bytes
+against the HBM copy peak.
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle
 instead, on a bounded sample per step, and prints the same metric.
@@ -36,18 +42,9 @@ import synth  # noqa: E402
 METRIC = ("µs per γ-step draft walk at B=1..128; effective W2 GB/s vs "
           "on-chip/HBM roofline")
 # context only (another GPU, int8 weights): the pages' H100 resident walk at
-# V = 151,936, gamma = 7, bs = 1 took 37 us per call
-PAGES_US = {("qwen3_resident", 1): 37.0}
+# V = 151,936, bs = 1 took 37 us per call at gamma = 7 and 62 us at gamma = 16
+PAGES_US = {("qwen3_resident", 1): 37.0, ("long_block", 1): 62.0}
 L2_FLUSH_BYTES = 256 << 20
-# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the walk
-# kernel (ncu, --clock-control none), per (workload, B, head); refreshed
-# whenever the kernel changes (profiles/walk_resident_qwen3_resident.md,
-# walk_resident_partial_b8.md, walk_batched_sampled_b253.md,
-# walk_resident_rnn_long_block_b1.md)
-TRAFFIC = {("qwen3_resident", 1, "markov"): 81_780_992,
-           ("partial", 8, "markov"): 273_919_232,
-           ("sampled", 253, "markov"): 401_235_968,
-           ("long_block", 1, "rnn"): 86_085_632}
 
 
 def parse():
@@ -56,7 +53,7 @@ def parse():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="qwen3_resident", choices=sorted(synth.CONFIGS))
+    p.add_argument("--workload", default="long_block", choices=sorted(synth.CONFIGS))
     p.add_argument("--batch", type=int, default=None)
     p.add_argument("--sampler", default="gumbel", choices=["gumbel", "group"],
                    help="sampling of T > 0 requests: per-token Gumbel-max (the configs') or the "
@@ -75,6 +72,13 @@ def parse():
                         "us = entry + gamma * per-step into 'gamma_fit'")
     p.add_argument("--trace", action="store_true",
                    help="after timing, run traced rounds and report the per-phase breakdown")
+    p.add_argument("--ncu-csv", default=None,
+                   help="an ncu --csv --page raw export (dram__bytes_read.sum, "
+                        "dram__bytes_write.sum) of the walk kernel of this build and workload: "
+                        "reported as roofline.traffic (DRAM bytes per launch); else null")
+    p.add_argument("--unit-rates", action="store_true",
+                   help="measure the tier rates the on-chip roofline uses (tensor-memory "
+                        "tcgen05.mma and mma.sync cycles per SM) and print them as one JSON line")
     p.add_argument("--only-timed", action="store_true",
                    help="warm-up and timed steps only (for profiler runs): no warm-L2 pass, "
                         "no end-to-end pass, no CPU baseline")
@@ -163,6 +167,17 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def measured_tflops():
+    """Sustained dense bf16 (the walk is a long step): measured, else fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), "measured (sustained)"
+    except (OSError, KeyError, ValueError):
+        return 1700.0, "fallback (sustained)"
+
+
 def load_inputs(cfg, B, n_rounds):
     W1, W2, _ = synth.make_weights(cfg.V, cfg.r, cfg.seed)
     rounds = [synth.make_inputs(cfg, B=B, round_index=i, weights=(W1, W2))
@@ -224,30 +239,77 @@ def kernel_label(walk, plan, B):
     return "batched"
 
 
-# GB300 unit rates measured for the on-chip roofline (probes summarised in
-# profiles/gb300_unit_rates.md and profiles/gb300_streaming.md): a tcgen05.mma
-# M=128 N=16 K=16 with A in tensor memory holds the tensor pipe ~13.4 SM
-# cycles; an mma.sync m16n8k16 ~2.0 cycles per SM; bulk copies from L2 bring
-# ~142 GB/s per SM.
-TC_CYCLES_PER_TMEM_MMA = 13.4
-HMMA_CYCLES = 2.0
+# Tier rates of the on-chip roofline, in SM cycles (dspark_walk_unit_rates
+# re-measures them at the start of every run; these are the values a GB300
+# gave, used only if that probe fails): an mma.sync m16n8k16 from registers
+# holds the tensor pipe 2.0 cycles per SM, one fed by ldmatrix from shared
+# memory 4.0 (the shared-memory port: 128 B per cycle), a tcgen05.mma M=128
+# N=16 K=16 with A in tensor memory 13.5; bulk copies bring ~142 GB/s per SM
+# from L2.
+FALLBACK_RATES = {"hmma_rf_cycles": 2.0, "hmma_smem_cycles": 4.0, "tc_tmem_a_cycles": 13.5}
 STREAM_GBS_PER_SM = 142.0
 
 
-def onchip_roofline_us(plan, gamma, mhz):
-    """Lower bound of the walk from on-chip reads: per step and CTA, the
-    tensor-memory tiles through tcgen05 plus the register, shared and streamed
-    strips through mma.sync (the two share the tensor pipe), or the streamed
-    bytes at the L2 streaming rate if that is longer; W2 read once from HBM per
-    process (the entry load is not counted)."""
-    if plan["kernel"] != 1 or not plan["rows_per_cta"]:      # 1: the resident kernel
+def unit_rates(walk):
+    """The tier rates measured on this device now, or the fallback values."""
+    try:
+        r = walk.dspark_walk_unit_rates()
+        if all(r.get(k, 0) > 0 for k in FALLBACK_RATES):
+            return r, "measured in this run (dspark_walk_unit_rates)"
+    except Exception as e:             # noqa: BLE001 -- reported, not hidden
+        return dict(FALLBACK_RATES), "fallback constants (probe failed: %s)" % e
+    return dict(FALLBACK_RATES), "fallback constants"
+
+
+def onchip_step_us(plan, rates, mhz):
+    """Lower bound of one walk step from on-chip reads, per SM (the slowest
+    CTA's shard): every resident row is read once per step, each tier by its
+    fastest consumer -- tensor-memory rows at the tcgen05.mma rate (4 KB per
+    M=128 K=16 MMA), register and shared rows at the mma.sync rate (512 B per
+    m16n8k16); the tensor pipe is shared, so the times add; the shared-memory
+    port (512 B per ldmatrix-fed MMA) is a parallel bound, and so are streamed
+    rows at the L2 streaming rate.  W2 is read once from HBM per process, so
+    the round's entry load is not counted."""
+    if plan["kernel"] != 1 or not plan["rows_per_cta"]:      # 1: a resident kernel
         return None
-    tmem_mmas = plan["rows_tmem"] // 128 * 16
-    strips = (plan["rows_rf"] + plan["rows_smem"] + plan["rows_stream"]) // 16
-    cycles = tmem_mmas * TC_CYCLES_PER_TMEM_MMA + strips * 16 * HMMA_CYCLES
-    t_tensor = cycles / mhz                                   # us
+    tc = plan["rows_tmem"] / 128 * 16 * rates["tc_tmem_a_cycles"]
+    hmma = (plan["rows_rf"] + plan["rows_smem"] + plan["rows_stream"]) / 16 * 16 * \
+        rates["hmma_rf_cycles"]
+    port = (plan["rows_smem"] + plan["rows_stream"]) / 16 * 16 * rates["hmma_smem_cycles"]
+    t_cyc = max(tc + hmma, port)
     t_stream = plan["rows_stream"] * 512 / (STREAM_GBS_PER_SM * 1e3)
-    return gamma * max(t_tensor, t_stream)
+    return max(t_cyc / mhz, t_stream)
+
+
+def read_ncu_traffic(path, pattern="walk_"):
+    """Mean DRAM bytes (read + write) per launch of the kernels whose name
+    contains `pattern`, from an `ncu --csv --page raw` export; None if absent."""
+    import csv
+    scale = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "b": 1, "kb": 1e3,
+             "mb": 1e6, "gb": 1e9}
+    try:
+        with open(path, newline="") as f:
+            rows = [r for r in csv.reader(f) if r]
+    except OSError:
+        return None
+    hdr = next((i for i, r in enumerate(rows) if "dram__bytes_read.sum" in r), None)
+    if hdr is None:
+        return None
+    names = rows[hdr]
+    ir, iw = names.index("dram__bytes_read.sum"), names.index("dram__bytes_write.sum")
+    ik = next((i for i, n in enumerate(names) if n in ("Kernel Name", "kernel_name")), None)
+    units = rows[hdr + 1] if len(rows) > hdr + 1 else []
+    per = []
+    for r in rows[hdr + 1:]:
+        if ik is None or len(r) <= max(ir, iw) or pattern not in r[ik]:
+            continue
+        try:
+            ur = scale.get(units[ir].strip().lower(), 1) if units else 1
+            uw = scale.get(units[iw].strip().lower(), 1) if units else 1
+            per.append(float(r[ir].replace(",", "")) * ur + float(r[iw].replace(",", "")) * uw)
+        except (ValueError, IndexError):
+            continue
+    return statistics.mean(per) if per else None
 
 
 def gamma_fit(walk, gammas=(1, 4, 7, 16), steps=100, warmup=5):
@@ -306,7 +368,8 @@ def cell_weights(cfg, cell):
     return synth.make_cell_matrix(cfg.seed + 500), None
 
 
-def measure_config(walk, cfg, B, steps=50, warmup=5, sampler="gumbel", cell="markov"):
+def measure_config(walk, cfg, B, steps=50, warmup=5, sampler="gumbel", cell="markov",
+                   rates=None, mhz=2070.0):
     """Cold- and warm-L2 us per walk of one workload at batch B (sweep mode)."""
     dev = torch.device("cuda", torch.cuda.current_device())
     W1, W2, _ = synth.make_weights(cfg.V, cfg.r, cfg.seed)
@@ -347,11 +410,12 @@ def measure_config(walk, cfg, B, steps=50, warmup=5, sampler="gumbel", cell="mar
            "kernel": kernel_label(walk, plan, B),
            "us_cold_l2": cold, "us_warm_l2": warm,
            "eff_w2_GBs_cold": cfg.gamma * cfg.V * cfg.r * 2 * B / (cold * 1e-6) / 1e9}
-    if res["kernel"] != "batched":
-        onchip = onchip_roofline_us(plan, cfg.gamma, 2070.0)
-        if onchip is not None:
-            res["onchip_roofline_us"] = onchip
-            res["onchip_frac_warm_l2"] = onchip / warm
+    if res["kernel"] != "batched" and rates is not None:
+        step = onchip_step_us(plan, rates, mhz)
+        if step is not None:
+            res["onchip_roofline_us"] = cfg.gamma * step
+            res["onchip_frac_cold_l2"] = cfg.gamma * step / cold
+            res["onchip_frac_warm_l2"] = cfg.gamma * step / warm
     w.close()
     del flush, base
     torch.cuda.empty_cache()
@@ -486,6 +550,14 @@ def main():
 
     from serial_draft_head_gb300 import walk
     walk.load(build_if_missing=True)
+    if args.unit_rates:
+        rates, kind = unit_rates(walk)
+        if rank == 0:
+            print(json.dumps({"unit_rates": rates, "kind": kind}), flush=True)
+        if dist:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
     dev = torch.device("cuda", torch.cuda.current_device())
     n_rounds = min(cfg.rounds, 100)
     W1c, W2c, rounds = load_inputs(cfg, B, n_rounds)
@@ -525,6 +597,7 @@ def main():
     st = w.status(stream)
     if st != 0:
         raise RuntimeError("walk status %d during warm-up" % st)
+    rates, rates_kind = unit_rates(walk)         # the roofline's tier rates, this device
 
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
@@ -614,29 +687,57 @@ def main():
     w2_bytes = cfg.gamma * cfg.V * cfg.r * 2 * B           # effective W2 bytes per walk
     eff_gbs = w2_bytes / (mean_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
-    roof = {"bound": "hbm", "achieved": eff_gbs, "peak": peak, "unit": "GB/s",
-            "frac": eff_gbs / peak,
-            "traffic": TRAFFIC.get((cfg.name, B, args.cell)),
-            "peak_kind": peak_kind,
-            "note": "achieved = effective W2 bytes (gamma*V*r*2*B) per launch / mean launch "
-                    "time; >1 means W2 is served from on-chip memory or L2, not HBM"}
     label = kernel_label(walk, plan, B) if args.kernel == "planned" else args.kernel
-    onchip = (onchip_roofline_us(plan, cfg.gamma, clocks.get("sm_mhz") or 2070.0)
-              if label != "batched" else None)
-    if onchip is not None:
-        roof["onchip"] = {
-            "roofline_us": onchip, "unit": "us per walk",
-            "frac_cold_l2": onchip / us,
-            "frac_warm_l2": onchip / (warm_ms * 1000.0) if warm_ms else None,
-            "how": "per step: tensor-memory MMAs x 13.4 cycles + mma.sync strips x 16 x 2.0 "
-                   "cycles (shared tensor pipe), or streamed bytes at 142 GB/s per SM; x gamma"}
+    mhz = clocks.get("sm_mhz") or 2070.0
+    traffic = read_ncu_traffic(args.ncu_csv) if args.ncu_csv else None
+    step = onchip_step_us(plan, rates, mhz) if label != "batched" else None
+    if step is not None:
+        onchip_bytes = cfg.gamma * cfg.V * cfg.r * 2          # every step reads all of W2
+        achieved = onchip_bytes / (mean_ms * 1e-3) / 1e9
+        roof_peak = cfg.V * cfg.r * 2 / (step * 1e-6) / 1e9
+        roof = {"bound": "onchip", "achieved": achieved, "peak": roof_peak, "unit": "GB/s",
+                "frac": achieved / roof_peak, "traffic": traffic,
+                "roofline_us": cfg.gamma * step, "per_step_us": step,
+                "frac_warm_l2": cfg.gamma * step / (warm_ms * 1000.0) if warm_ms else None,
+                "peak_kind": "on-chip tier rates " + rates_kind,
+                "sm_mhz": mhz,
+                "rates": {k: rates[k] for k in rates},
+                "how": "achieved = W2 bytes read from on-chip tiers per walk (gamma*V*r*2, "
+                       "W2 read from HBM once per process) / mean launch time; peak = the "
+                       "same bytes per step / the step's on-chip roofline (per SM: tensor-"
+                       "memory rows at the tcgen05.mma rate plus register and shared rows "
+                       "at the mma.sync rate, or the shared-memory port if slower); frac = "
+                       "roofline time / measured time; traffic = DRAM bytes per launch from "
+                       "an ncu capture of this build (--ncu-csv), else null"}
+    else:
+        hbm_bytes = B * cfg.gamma * cfg.V * 2                  # base logits, read once
+        flops = 2.0 * cfg.V * cfg.r * B * cfg.gamma
+        tflops_peak, tkind = measured_tflops()
+        hbm_frac = hbm_bytes / (mean_ms * 1e-3) / 1e9 / peak
+        tc_frac = flops / (mean_ms * 1e-3) / 1e12 / tflops_peak
+        if tc_frac >= hbm_frac:
+            roof = {"bound": "tensor", "achieved": flops / (mean_ms * 1e-3) / 1e12,
+                    "peak": tflops_peak, "unit": "TFLOP/s", "frac": tc_frac,
+                    "peak_kind": tkind}
+        else:
+            roof = {"bound": "hbm", "achieved": hbm_bytes / (mean_ms * 1e-3) / 1e9,
+                    "peak": peak, "unit": "GB/s", "frac": hbm_frac, "peak_kind": peak_kind}
+        roof.update({"traffic": traffic, "hbm_frac": hbm_frac, "tensor_frac": tc_frac,
+                     "how": "hbm: base logits B*gamma*V*2 bytes per walk against the HBM "
+                            "copy peak; tensor: 2*V*r*B*gamma flops against the sustained "
+                            "bf16 GEMM peak; bound = the larger fraction"})
+    effective = {"achieved": eff_gbs, "unit": "GB/s", "hbm_peak": peak, "ratio": eff_gbs / peak,
+                 "peak_kind": peak_kind,
+                 "how": "gamma*V*r*2*B bytes per walk / mean launch time, against the HBM "
+                        "copy peak (above 1: W2 is served from on-chip memory)"}
     line = {
         "metric": METRIC, "value": us, "unit": "us", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
         "higher_is_better": False, "scaling": "weak",
         "vs_baseline": (us / PAGES_US[(cfg.name, B)]) if (cfg.name, B) in PAGES_US else None,
-        "vs_baseline_note": "value / the pages' 37 us (H100, int8 W2): context on other "
-                            "hardware and precision" if (cfg.name, B) in PAGES_US else None,
+        "vs_baseline_note": "value / the pages' %.0f us (H100, int8 W2): context on other "
+                            "hardware and precision" % PAGES_US[(cfg.name, B)]
+                            if (cfg.name, B) in PAGES_US else None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": cfg.note, "sampler": args.sampler, "cell": args.cell, "V": cfg.V, "r": cfg.r, "gamma": cfg.gamma, "B": B,
                    "rounds": n_rounds, "parallelism": "replicas" if world > 1 else "single",
@@ -649,6 +750,7 @@ def main():
         "warm_l2_us": warm_ms * 1000.0 if warm_ms is not None else None,
         "graph_warm_l2_us": graph_warm_ms * 1000.0 if graph_warm_ms is not None else None,
         "roofline": roof,
+        "effective_w2": effective,
         "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "how": "dspark_walk_run_host on pinned host buffers: base/anchor/temperature "
@@ -660,17 +762,21 @@ def main():
         "clocks": clocks,
         "plan": plan,
     }
+    if args.ncu_csv:
+        line["traffic_source"] = os.path.basename(args.ncu_csv)
     if args.sweep or args.gamma_fit:
         w.close()
     if args.sweep:
-        line["sweep"] = [measure_config(walk, c, b) for c in synth.CONFIGS.values()
-                         for b in c.batches]
+        line["sweep"] = [measure_config(walk, c, b, rates=rates, mhz=mhz)
+                         for c in synth.CONFIGS.values() for b in c.batches]
         # the group inverse-CDF sampler on the sampled workload (not the configs' sampler)
-        line["sweep"] += [measure_config(walk, synth.CONFIGS["sampled"], b, sampler="group")
+        line["sweep"] += [measure_config(walk, synth.CONFIGS["sampled"], b, sampler="group",
+                                         rates=rates, mhz=mhz)
                           for b in synth.CONFIGS["sampled"].batches]
         # the recurrent heads on the fully resident long block (B = 1 as the pages
         # time them, and the largest resident batch)
-        line["sweep"] += [measure_config(walk, synth.CONFIGS["long_block"], b, cell=c)
+        line["sweep"] += [measure_config(walk, synth.CONFIGS["long_block"], b, cell=c,
+                                         rates=rates, mhz=mhz)
                           for c in ("gated", "rnn", "gru") for b in (1, 16)]
     if args.gamma_fit:
         line["gamma_fit"] = gamma_fit(walk)

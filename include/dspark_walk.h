@@ -82,6 +82,7 @@ struct dspark_walk_plan {
     int max_gamma;          /* longest walk a run may pass */
     int kernel;             /* which kernel runs small batches (DSPARK_KERNEL_*) */
     int sm_count;           /* SMs on the device */
+    int64_t weight_bytes;   /* device bytes of the W2 layouts the handle holds now */
 };
 
 #define DSPARK_KERNEL_STREAM 0   /* every row re-read from global memory each step */
@@ -302,6 +303,31 @@ int dspark_walk_gumbel_noise(const uint32_t *bits, float *noise, int64_t n, void
  * Only the resident kernel writes stamps.  NULL turns tracing off.
  */
 int dspark_walk_set_trace(dspark_walk_t h, void *device_buffer, int64_t bytes);
+
+/*
+ * dspark_walk_unit_rates -- measure, on the current device, the rates at
+ * which the resident walk's on-chip tiers feed the tensor cores: the unit
+ * costs of the walk's on-chip-read roofline ("Keeping the Draft Walk on
+ * Chip", section "B200: the bf16 table fits on chip": tcgen05 reads the
+ * tensor-memory part of W2, mma.sync the register and shared-memory parts).
+ * One CTA of 256 threads per SM runs each pattern; the medians over SMs are
+ * written to out (SM clock cycles):
+ *   out[0]  mma.sync m16n8k16 bf16, A in registers: cycles per MMA per SM
+ *   out[1]  mma.sync with A read by ldmatrix from shared memory: per MMA
+ *   out[2]  tcgen05.mma M=128 N=16 K=16, A in tensor memory, six issuing
+ *           warps: cycles per MMA per SM
+ *   out[3]  one step's projection at the resident shapes (48 tensor-memory
+ *           MMAs, 16 k-tiles of 2 register and 3 shared strips per warp)
+ *   out[4]  SM clock during the probe, MHz (clock64 over the global timer)
+ *   out[5]  tcgen05.ld of 32-column blocks: cycles per KB per SM (n_out >= 7)
+ *   out[6]  one step's projection with 4 tensor-memory strips per warp fed to
+ *           mma.sync by tcgen05.ld, 1 register and 3 shared strips (n_out >= 7)
+ * n_out >= 5.  Allocates and frees a few KB of device memory, runs on
+ * `stream` and synchronises it.  DSPARK_EINVAL (out NULL or n_out < 5),
+ * DSPARK_EUNSUPPORTED (not sm_103), DSPARK_ENOMEM, DSPARK_ECUDA, and
+ * DSPARK_ETIMEOUT if a tensor-core completion wait ran out.
+ */
+int dspark_walk_unit_rates(double *out, int n_out, void *stream);
 
 /* dspark_walk_strerror -- a static description of a status code. */
 const char *dspark_walk_strerror(int code);

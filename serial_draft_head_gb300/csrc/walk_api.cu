@@ -21,12 +21,22 @@ struct dspark_walk {
   int max_B = 0;
   int max_gamma = 0;
   const uint16_t* W1 = nullptr;   // caller-owned
-  uint16_t* W2 = nullptr;         // handle-owned copy
+  // W2 is kept only in the layouts the runs need, each built when first
+  // needed (the row-major copy only for the streamed kernel); any missing
+  // layout is rebuilt from one that exists.
+  uint16_t* W2 = nullptr;         // row-major copy (streamed kernel)
   void* sync_mem = nullptr;       // SyncHeader + counts + keys + resident slots
   SyncView sync{};
-  // resident layout (used for runs with B <= res_max_B)
+  // mma.sync resident layout (Markov runs with B <= mr_max_B)
+  uint32_t* W2m = nullptr;
+  bool mr_ok = false;             // the shard fits the layout
+  int mr_max_B = 0, mr_R = 0, mr_S = 0, mr_n_cta = 0;
+  int64_t mr_wpc = 0;
+  size_t mr_smem = 0;
+  // tcgen05 resident layout (runs with B <= res_max_B the layout above does
+  // not take: larger batches, recurrent heads, partial residency)
   uint32_t* W2p = nullptr;        // tiered repack, res_wpc words per CTA
-  int res_max_B = 0;              // 0: no resident layout
+  int res_max_B = 0;              // 0: no resident placement
   bool use_resident = true;       // dspark_walk_set_kernel
   int seed_per_round = 0;         // dspark_walk_set_seed_mode
   int sampler = 0;                // dspark_walk_set_sampler
@@ -132,6 +142,31 @@ bool plan_resident(dspark_walk* h) {
   return true;
 }
 
+// mma.sync resident plan: rows spread over at most one CTA per SM, each CTA
+// holding 512 rows in tensor memory, 128 in registers and 0, 128, 256 or 384
+// in shared memory (the same number of shared strips in every warp), so shards
+// of 640 .. 1,024 rows: V <= 155,648 on 152 SMs.
+bool plan_mma(dspark_walk* h) {
+  if (h->V >= (1 << 18)) return false;          // the 18-bit id field of the slot word
+  const int mb = h->max_B < mma_resident_max_batch() ? h->max_B : mma_resident_max_batch();
+  const int fixed = mma_resident_fixed_rows();
+  int64_t R = (h->V + h->sm_count - 1) / h->sm_count;
+  R = (R + 127) / 128 * 128;        // every warp holds the same number of shared strips
+  if (R < fixed) R = fixed;
+  if (R > mma_resident_max_rows()) return false;
+  const int S = (int)((R - fixed) / 16);
+  const size_t smem = mma_resident_smem_bytes(S, mb, (int)R);
+  if (smem > kSmemBudget) return false;
+  h->mr_ok = true;
+  h->mr_max_B = mb;
+  h->mr_R = (int)R;
+  h->mr_S = S;
+  h->mr_n_cta = (int)((h->V + R - 1) / R);
+  h->mr_wpc = mma_resident_words_per_cta(S);
+  h->mr_smem = smem;
+  return true;
+}
+
 // Shard plan of the streamed kernel: rows split evenly over at most one CTA
 // per SM; tiny vocabularies use fewer CTAs (at least 32 rows each), since
 // the rendezvous costs more with more CTAs.
@@ -158,7 +193,18 @@ void plan_stream(dspark_walk* h) {
   p.max_gamma = h->max_gamma;
   p.kernel = DSPARK_KERNEL_STREAM;
   p.sm_count = h->sm_count;
-  if (h->res_max_B > 0) {
+  if (h->mr_ok) {
+    p.n_cta = h->mr_n_cta;
+    p.threads = resident_threads();
+    p.rows_per_cta = h->mr_R;
+    p.rows_tmem = 512;
+    p.rows_rf = 128;
+    p.rows_smem = 16 * h->mr_S;
+    p.rows_stream = 0;
+    p.streamed_bytes = 0;
+    p.resident_bytes = h->V * (int64_t)h->r * 2;
+    p.kernel = DSPARK_KERNEL_RESIDENT;
+  } else if (h->res_max_B > 0) {
     p.n_cta = h->res_n_cta;
     p.threads = resident_threads();
     p.rows_per_cta = h->res_R;
@@ -171,6 +217,114 @@ void plan_stream(dspark_walk* h) {
     if (p.resident_bytes < 0) p.resident_bytes = 0;
     p.kernel = DSPARK_KERNEL_RESIDENT;
   }
+}
+
+// ------------------------------------------------------- W2 layouts ----
+// Which layout a Markov run of B requests takes, given the kernel choice.
+enum class Path { kMma, kResident, kBatched, kStream };
+
+bool cell_run(const dspark_walk* h) {
+  return h->cell != DSPARK_CELL_MARKOV || h->out_state != nullptr;
+}
+
+Path path_for(const dspark_walk* h, int B) {
+  if (h->use_resident) {
+    if (h->mr_ok && !cell_run(h) && B <= h->mr_max_B) return Path::kMma;
+    if (h->res_max_B > 0 && B <= h->res_max_B) return Path::kResident;
+  }
+  if (h->use_batched) return Path::kBatched;
+  return Path::kStream;
+}
+
+size_t rowmajor_bytes(const dspark_walk* h) { return (size_t)h->V * h->r * 2; }
+
+// Row-major W2 into `dst` from any layout the handle holds.
+cudaError_t unpack_rowmajor(dspark_walk* h, void* dst) {
+  if (h->W2) return cudaMemcpy(dst, h->W2, rowmajor_bytes(h), cudaMemcpyDeviceToDevice);
+  if (h->W2m)
+    return mma_resident_repack(dst, h->W2m, h->V, h->mr_R, h->mr_S, h->mr_n_cta, true, 0);
+  if (h->W2p)
+    return resident_repack(dst, h->W2p, h->V, h->res_R, h->res_RS, h->res_S + h->res_ST,
+                           h->res_n_cta, true, 0);
+  if (h->W2b) return batched_repack(dst, h->W2b, h->V, h->bat_R, h->bat_n_cta, true, 0);
+  return cudaErrorInvalidValue;
+}
+
+// Build the layout `which` from row-major W2 at `src` (device) if it is missing.
+cudaError_t build_layout(dspark_walk* h, Path which, const void* src) {
+  cudaError_t e = cudaSuccess;
+  void* s = const_cast<void*>(src);
+  switch (which) {
+    case Path::kMma:
+      if (h->W2m || !h->mr_ok) return cudaSuccess;
+      e = cudaMalloc(&h->W2m, (size_t)h->mr_wpc * h->mr_n_cta * sizeof(uint32_t));
+      if (e == cudaSuccess)
+        e = mma_resident_repack(s, h->W2m, h->V, h->mr_R, h->mr_S, h->mr_n_cta, false, 0);
+      return e;
+    case Path::kResident:
+      if (h->W2p || h->res_max_B == 0) return cudaSuccess;
+      e = cudaMalloc(&h->W2p, (size_t)h->res_wpc * h->res_n_cta * sizeof(uint32_t));
+      if (e == cudaSuccess)
+        e = resident_repack(s, h->W2p, h->V, h->res_R, h->res_RS, h->res_S + h->res_ST,
+                            h->res_n_cta, false, 0);
+      return e;
+    case Path::kBatched:
+      if (h->W2b) return cudaSuccess;
+      e = cudaMalloc(&h->W2b, (size_t)h->bat_R * h->bat_n_cta * 512);
+      if (e == cudaSuccess) e = batched_repack(s, h->W2b, h->V, h->bat_R, h->bat_n_cta, false, 0);
+      return e;
+    case Path::kStream:
+      if (h->W2) return cudaSuccess;
+      e = cudaMalloc(&h->W2, rowmajor_bytes(h));
+      if (e == cudaSuccess) e = cudaMemcpy(h->W2, src, rowmajor_bytes(h), cudaMemcpyDeviceToDevice);
+      return e;
+  }
+  return cudaErrorInvalidValue;
+}
+
+// Make sure a run of B requests finds its layout (built from the layouts the
+// handle holds, through a temporary row-major copy).  Synchronises the device.
+int ensure_layout(dspark_walk* h, int B) {
+  const Path need = path_for(h, B);
+  const bool have = (need == Path::kMma && h->W2m) || (need == Path::kResident && h->W2p) ||
+                    (need == Path::kBatched && h->W2b) || (need == Path::kStream && h->W2);
+  if (have) return DSPARK_OK;
+  CUDA_TRY(cudaSetDevice(h->device));
+  void* tmp = nullptr;
+  const void* src = h->W2;
+  if (!src) {
+    CUDA_TRY(cudaMalloc(&tmp, rowmajor_bytes(h)));
+    cudaError_t e = unpack_rowmajor(h, tmp);
+    if (e != cudaSuccess) {
+      cudaFree(tmp);
+      return cuda_fail(e);
+    }
+    src = tmp;
+  }
+  cudaError_t e = build_layout(h, need, src);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (tmp) cudaFree(tmp);
+  return e == cudaSuccess ? DSPARK_OK : cuda_fail(e);
+}
+
+// Every batch size a handle may run under its current settings.
+int ensure_layouts(dspark_walk* h) {
+  int rc = ensure_layout(h, 1);
+  if (rc == DSPARK_OK) rc = ensure_layout(h, h->max_B);
+  if (rc == DSPARK_OK && h->mr_max_B > 0 && h->mr_max_B < h->max_B)
+    rc = ensure_layout(h, h->mr_max_B + 1);
+  if (rc == DSPARK_OK && h->res_max_B > 0 && h->res_max_B < h->max_B)
+    rc = ensure_layout(h, h->res_max_B + 1);
+  return rc;
+}
+
+int64_t layout_bytes(const dspark_walk* h) {
+  int64_t n = 0;
+  if (h->W2) n += (int64_t)rowmajor_bytes(h);
+  if (h->W2m) n += h->mr_wpc * h->mr_n_cta * 4;
+  if (h->W2p) n += h->res_wpc * h->res_n_cta * 4;
+  if (h->W2b) n += (int64_t)h->bat_R * h->bat_n_cta * 512;
+  return n;
 }
 
 int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const float* temp,
@@ -195,9 +349,12 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
   a.sampler = h->sampler;
   a.timeout_ns = h->timeout_ns;
   a.skip_cta = h->skip_cta;
+  const Path path = path_for(h, B);
   {
-    const bool res = h->res_max_B > 0 && h->use_resident && B <= h->res_max_B;
-    const int n = res ? h->res_n_cta : (h->W2b && h->use_batched ? h->bat_n_cta : h->st_n_cta);
+    const int n = path == Path::kMma        ? h->mr_n_cta
+                  : path == Path::kResident ? h->res_n_cta
+                  : path == Path::kBatched  ? h->bat_n_cta
+                                            : h->st_n_cta;
     const int64_t need = (int64_t)n * (gamma + 1) * 8 * 8;
     a.trace = (h->trace && h->trace_bytes >= need) ? h->trace : nullptr;
   }
@@ -208,39 +365,44 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
   a.cell_X = h->cell_X;
   a.cell_p = h->cell_p;
   a.cell_q = 1;
-  const bool resident_run = h->res_max_B > 0 && h->use_resident && B <= h->res_max_B;
-  // recurrent heads and the state output run on the resident kernel only
-  if ((h->cell != DSPARK_CELL_MARKOV || h->out_state) && !resident_run)
-    return DSPARK_EUNSUPPORTED;
-  if (resident_run) {
+  // recurrent heads and the state output run on the tcgen05 resident kernel only
+  if (cell_run(h) && path != Path::kResident) return DSPARK_EUNSUPPORTED;
+  if (path == Path::kResident) {
     const int P = h->cell == DSPARK_CELL_GRU ? kCellP : kRank;   // recurrent rows
     a.cell_q = (P + h->res_n_cta - 1) / h->res_n_cta;
   }
+  // the layout this run reads (set_kernel / set_cell build it when they
+  // change the path; a handle always holds the layouts its settings need)
+  const bool have = (path == Path::kMma && h->W2m) || (path == Path::kResident && h->W2p) ||
+                    (path == Path::kBatched && h->W2b) || (path == Path::kStream && h->W2);
+  if (!have) return DSPARK_EINTERNAL;
 
-  if (!(h->res_max_B > 0 && h->use_resident && B <= h->res_max_B) && h->W2b && h->use_batched) {
+  if (path == Path::kBatched) {
     CUDA_TRY(batched_launch(a, h->W2b, h->bat_R, h->bat_n_cta, h->max_B, B,
                             232448 - 1024, stream));
     return DSPARK_OK;
   }
 
-  if (h->res_max_B > 0 && h->use_resident && B <= h->res_max_B) {
+  if (path == Path::kMma || path == Path::kResident) {
+    const bool mma = path == Path::kMma;
     ResidentArgs ra{};
     ra.w = a;
-    ra.w.rows_per_cta = h->res_R;
-    ra.W2p = h->W2p;
-    ra.R = h->res_R;
-    ra.S = h->res_S;
-    ra.ST = h->res_ST;
-    ra.nslot = h->res_nslot;
-    ra.words_per_cta = h->res_wpc;
+    ra.w.rows_per_cta = mma ? h->mr_R : h->res_R;
+    ra.W2p = mma ? h->W2m : h->W2p;
+    ra.R = mma ? h->mr_R : h->res_R;
+    ra.S = mma ? h->mr_S : h->res_S;
+    ra.ST = mma ? 0 : h->res_ST;
+    ra.nslot = mma ? 0 : h->res_nslot;
+    ra.words_per_cta = mma ? h->mr_wpc : h->res_wpc;
     const uintptr_t bp = reinterpret_cast<uintptr_t>(base);
     ra.base_mode = (h->V % 8 == 0 && (bp & 15u) == 0) ? 16
                    : (h->V % 2 == 0 && (bp & 3u) == 0) ? 4 : 2;
-    const void* rfn = resident_kernel_for(h->res_RS, h->res_NT,
-                                          h->cell != DSPARK_CELL_MARKOV || h->out_state);
+    const void* rfn = mma ? mma_resident_kernel(h->mr_S)
+                          : resident_kernel_for(h->res_RS, h->res_NT, cell_run(h));
     void* rargs[] = {&ra};
-    CUDA_TRY(cudaLaunchCooperativeKernel(rfn, dim3(h->res_n_cta), dim3(resident_threads()), rargs,
-                                         h->res_smem, stream));
+    CUDA_TRY(cudaLaunchCooperativeKernel(rfn, dim3(mma ? h->mr_n_cta : h->res_n_cta),
+                                         dim3(resident_threads()), rargs,
+                                         mma ? h->mr_smem : h->res_smem, stream));
     return DSPARK_OK;
   }
 
@@ -305,29 +467,23 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
   h->W1 = static_cast<const uint16_t*>(W1);
 
   int rc = DSPARK_OK;
+  plan_mma(h);
   const bool resident = plan_resident(h);
+  plan_batched(h);
   size_t count_off, key_off, total;
   sync_layout(max_gamma, max_B, &count_off, &key_off, &total);
-  cudaError_t e = cudaMalloc(&h->W2, (size_t)V * r * 2);
-  if (e == cudaSuccess) e = cudaMemcpy(h->W2, W2, (size_t)V * r * 2, cudaMemcpyDeviceToDevice);
-  if (e == cudaSuccess) e = cudaMalloc(&h->sync_mem, total);
+  cudaError_t e = cudaMalloc(&h->sync_mem, total);
   if (e == cudaSuccess) e = cudaMemset(h->sync_mem, 0, total);
-  if (e == cudaSuccess && resident)
-    e = cudaMalloc(&h->W2p, (size_t)h->res_wpc * h->res_n_cta * sizeof(uint32_t));
-  if (e == cudaSuccess && resident)
-    e = resident_repack(W2, h->W2p, V, h->res_R, h->res_RS, h->res_S + h->res_ST, h->res_n_cta, 0);
-  plan_batched(h);
-  if (e == cudaSuccess) e = cudaMalloc(&h->W2b, (size_t)h->bat_R * h->bat_n_cta * 512);
-  if (e == cudaSuccess) e = batched_repack(W2, h->W2b, V, h->bat_R, h->bat_n_cta, 0);
-  if (e == cudaSuccess) e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) rc = cuda_fail(e);
-  if (rc == DSPARK_OK) {
+  if (e == cudaSuccess) {
     uint8_t* base = static_cast<uint8_t*>(h->sync_mem);
     h->sync.hdr = reinterpret_cast<SyncHeader*>(base);
     h->sync.count = reinterpret_cast<uint32_t*>(base + count_off);
     h->sync.key = reinterpret_cast<unsigned long long*>(base + key_off);
     h->sync.max_gamma = max_gamma;
     h->sync.max_B = max_B;
+  }
+  if (e != cudaSuccess) rc = cuda_fail(e);
+  if (rc == DSPARK_OK) {
     plan_stream(h);
     // every instantiation may use the shared memory of max_B, and one CTA
     // per SM must fit.  A kernel's shared-memory limit is one setting for the
@@ -372,9 +528,37 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
         // the resident kernel cannot run here: every run streams instead
         cudaGetLastError();
         h->res_max_B = 0;
-        plan_stream(h);
       }
     }
+    if (rc == DSPARK_OK && h->mr_ok) {
+      int per_sm = 0;
+      for (int s = 0; s <= 24 && e == cudaSuccess; s += 8)
+        e = cudaFuncSetAttribute(mma_resident_kernel(s),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mma_resident_kernel(h->mr_S),
+                                                          resident_threads(), h->mr_smem);
+      if (e != cudaSuccess || per_sm != 1) {
+        cudaGetLastError();
+        h->mr_ok = false;
+        h->mr_max_B = 0;
+      }
+    }
+    plan_stream(h);
+  }
+  // the layouts the runs of this handle can take, each repacked from the
+  // caller's W2 (no row-major copy is kept)
+  if (rc == DSPARK_OK) {
+    const Path paths[] = {path_for(h, 1), path_for(h, max_B),
+                          path_for(h, h->mr_max_B > 0 && h->mr_max_B < max_B ? h->mr_max_B + 1 : 1),
+                          path_for(h, h->res_max_B > 0 && h->res_max_B < max_B ? h->res_max_B + 1
+                                                                                 : 1)};
+    for (const Path pth : paths) {
+      e = build_layout(h, pth, W2);
+      if (e != cudaSuccess) break;
+    }
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) rc = cuda_fail(e);
   }
   if (rc != DSPARK_OK) {
     dspark_walk_destroy(h);
@@ -471,6 +655,7 @@ int dspark_walk_status(dspark_walk_t h, void* stream) {
 int dspark_walk_get_plan(dspark_walk_t h, struct dspark_walk_plan* p) {
   if (!h || !p) return DSPARK_EINVAL;
   *p = h->plan;
+  p->weight_bytes = layout_bytes(h);
   return DSPARK_OK;
 }
 
@@ -490,23 +675,26 @@ int dspark_walk_set_trace(dspark_walk_t h, void* device_buffer, int64_t bytes) {
 
 int dspark_walk_set_kernel(dspark_walk_t h, int kernel) {
   if (!h) return DSPARK_EINVAL;
+  const bool r0 = h->use_resident, b0 = h->use_batched;
   if (kernel == DSPARK_KERNEL_STREAM) {
     h->use_resident = false;
     h->use_batched = false;
-    return DSPARK_OK;
-  }
-  if (kernel == DSPARK_KERNEL_RESIDENT) {
-    if (h->res_max_B == 0) return DSPARK_EUNSUPPORTED;
+  } else if (kernel == DSPARK_KERNEL_RESIDENT) {
+    if (h->res_max_B == 0 && !h->mr_ok) return DSPARK_EUNSUPPORTED;
     h->use_resident = true;
     h->use_batched = true;
-    return DSPARK_OK;
-  }
-  if (kernel == DSPARK_KERNEL_BATCHED) {
+  } else if (kernel == DSPARK_KERNEL_BATCHED) {
     h->use_resident = false;
     h->use_batched = true;
-    return DSPARK_OK;
+  } else {
+    return DSPARK_EINVAL;
   }
-  return DSPARK_EINVAL;
+  const int rc = ensure_layouts(h);
+  if (rc != DSPARK_OK) {
+    h->use_resident = r0;
+    h->use_batched = b0;
+  }
+  return rc;
 }
 
 int dspark_walk_set_seed_mode(dspark_walk_t h, int mode) {
@@ -539,7 +727,13 @@ int dspark_walk_set_cell(dspark_walk_t h, int cell, const void* M, const void* X
     CUDA_TRY(cudaSetDevice(h->device));
     CUDA_TRY(cudaMalloc(&h->cell_p, (size_t)h->max_gamma * 16 * kCellP * sizeof(float)));
   }
+  const int cell0 = h->cell;
   h->cell = cell;
+  const int rc = ensure_layouts(h);
+  if (rc != DSPARK_OK) {
+    h->cell = cell0;
+    return rc;
+  }
   h->cell_M = static_cast<const uint16_t*>(M);
   h->cell_X = cell == DSPARK_CELL_GRU ? static_cast<const uint16_t*>(X) : nullptr;
   return DSPARK_OK;
@@ -547,7 +741,15 @@ int dspark_walk_set_cell(dspark_walk_t h, int cell, const void* M, const void* X
 
 int dspark_walk_set_state_output(dspark_walk_t h, void* out_state) {
   if (!h || (reinterpret_cast<uintptr_t>(out_state) & 1u) != 0) return DSPARK_EINVAL;
+  uint16_t* prev = h->out_state;
   h->out_state = static_cast<uint16_t*>(out_state);
+  if (out_state && h->res_max_B > 0) {
+    const int rc = ensure_layouts(h);
+    if (rc != DSPARK_OK) {
+      h->out_state = prev;
+      return rc;
+    }
+  }
   return DSPARK_OK;
 }
 
@@ -593,6 +795,7 @@ int dspark_walk_destroy(dspark_walk_t h) {
   if (h->W2) cudaFree(h->W2);
   if (h->W2p) cudaFree(h->W2p);
   if (h->W2b) cudaFree(h->W2b);
+  if (h->W2m) cudaFree(h->W2m);
   if (h->sync_mem) cudaFree(h->sync_mem);
   if (h->stage) cudaFree(h->stage);
   if (h->hstage) cudaFreeHost(h->hstage);

@@ -598,8 +598,8 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
 // Row-major W2 -> per CTA, per 128-row tile, per 16-wide K block a 4 KB block
 // of 8x16-byte core matrices: row r = 8 mg + i, k = 8 kc + j at byte
 // ((kc * 16 + mg) * 8 + i) * 16 + 2 j.  Rows past V are zero.
-__global__ void repack_batched_kernel(const uint32_t* __restrict__ W2w, uint32_t* __restrict__ out,
-                                      int64_t V, int R, int64_t total_words) {
+__global__ void repack_batched_kernel(uint32_t* __restrict__ W2w, uint32_t* __restrict__ out,
+                                      int64_t V, int R, int64_t total_words, int inverse) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total_words;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t blk = i >> 10;              // 1024 words per 4 KB block
@@ -611,7 +611,11 @@ __global__ void repack_batched_kernel(const uint32_t* __restrict__ W2w, uint32_t
     const int64_t cta = tile / tiles_per_cta, t = tile - cta * tiles_per_cta;
     const int64_t row = cta * R + t * 128 + 8 * mg + ii;
     const int64_t kp = kt * 8 + kc * 4 + jp;  // word (pair) index along K
-    out[i] = row < V ? W2w[row * (kRank / 2) + kp] : 0u;
+    if (inverse) {
+      if (row < V) W2w[row * (kRank / 2) + kp] = out[i];
+    } else {
+      out[i] = row < V ? W2w[row * (kRank / 2) + kp] : 0u;
+    }
   }
 }
 
@@ -629,13 +633,14 @@ int batched_max_stages() { return kMaxStages; }
 
 const void* batched_kernel() { return reinterpret_cast<const void*>(&walk_batched_kernel); }
 
-cudaError_t batched_repack(const void* W2, void* out, int64_t V, int R, int n_cta,
-                           cudaStream_t stream) {
+cudaError_t batched_repack(void* rowmajor, void* packed, int64_t V, int R, int n_cta,
+                           bool inverse, cudaStream_t stream) {
   const int64_t total = (int64_t)n_cta * (R / 128) * 16 * 1024;
   int blocks = (int)((total + 255) / 256);
   if (blocks > 65535 * 8) blocks = 65535 * 8;
-  repack_batched_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint32_t*>(W2),
-                                                    static_cast<uint32_t*>(out), V, R, total);
+  repack_batched_kernel<<<blocks, 256, 0, stream>>>(static_cast<uint32_t*>(rowmajor),
+                                                    static_cast<uint32_t*>(packed), V, R, total,
+                                                    inverse ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -23,8 +23,20 @@ size_t resident_smem_bytes(int S, int ST, int nslot, int max_B, int R);
 int resident_max_ring_slots();
 const void* resident_kernel_for(int RS, int NT, bool cell);   // cell: recurrent heads / state output
 int resident_max_smem_strips();
-cudaError_t resident_repack(const void* W2, void* out, int64_t V, int R, int RS, int S, int n_cta,
-                            cudaStream_t stream);
+cudaError_t resident_repack(void* rowmajor, void* packed, int64_t V, int R, int RS, int S,
+                            int n_cta, bool inverse, cudaStream_t stream);
+
+// Resident kernel with every tier read by mma.sync (tensor memory through
+// tcgen05.ld): fully resident shards of at most mma_resident_max_rows() rows,
+// batches up to mma_resident_max_batch(), the Markov head.
+int mma_resident_fixed_rows();
+int mma_resident_max_rows();
+int mma_resident_max_batch();
+int64_t mma_resident_words_per_cta(int S);
+size_t mma_resident_smem_bytes(int S, int max_B, int R);
+const void* mma_resident_kernel(int S);   // S: shared strips per CTA, a multiple of 8
+cudaError_t mma_resident_repack(void* rowmajor, void* packed, int64_t V, int R, int S, int n_cta,
+                                bool inverse, cudaStream_t stream);
 
 // Batched kernel: W2 streamed through a TMA ring, tcgen05 with N = B.
 struct WalkArgs;
@@ -32,8 +44,8 @@ int batched_threads();
 size_t batched_smem_bytes(int nst, int N);
 int batched_max_stages();
 const void* batched_kernel();
-cudaError_t batched_repack(const void* W2, void* out, int64_t V, int R, int n_cta,
-                           cudaStream_t stream);
+cudaError_t batched_repack(void* rowmajor, void* packed, int64_t V, int R, int n_cta,
+                           bool inverse, cudaStream_t stream);
 cudaError_t batched_launch(const WalkArgs& w, const void* W2b, int R, int n_cta, int max_B, int B,
                            size_t smem_budget, cudaStream_t stream);
 

@@ -1,0 +1,539 @@
+// walk_mma_resident.cu -- the persistent walk with W2 held on chip for the
+// whole round, every tier read by mma.sync: "Keeping the Draft Walk on Chip:
+// One Launch for DSpark's Markov Head", sections "The idea: make the walk
+// resident" (one CTA per SM, one launch per round, each CTA loads its slice of
+// rows once and runs all gamma steps, only token ids cross between steps) and
+// "B200: the bf16 table fits on chip" (the table split over tensor memory,
+// shared memory and registers; fp32 accumulation, bias rounded to bf16, then
+// the sum rounded to bf16; request n is column n of the MMA's N operand).
+//
+// The pages' B200 kernel reads its tensor-memory rows with tcgen05.mma.  At one
+// request the MMA's N operand is nearly empty, so what bounds a step is how fast
+// each tier hands rows to the tensor cores, plus the fixed costs around the
+// MMAs.  On GB300 a tcgen05.mma costs ~45 cycles to issue from one thread, its
+// accumulators take tensor-memory columns, and its results need an extra
+// completion wait and read-out per step.  Here tensor memory instead holds W2
+// rows already laid out as mma.sync A fragments, in all 512 columns, and each
+// warp streams its 32 KB share into registers with tcgen05.ld (~384 B per
+// cycle per SM) one k-tile pair ahead of the mma.sync that consume them.  All
+// three tiers then run as independent accumulation chains of one k loop.
+//
+// Per CTA (256 threads, 8 warps) the R rows of its shard are placed as
+//   rows [0, 512)            tensor memory: warp w holds strips 4w .. 4w + 3
+//                            (16 rows each) in lanes 32 (w % 4) .. + 31,
+//                            columns 256 (w / 4) .. + 255;
+//   rows [512, 640)          registers: one 16-row strip per warp;
+//   rows [640, R)            shared memory: NS = 0..3 strips per warp (the
+//                            same count in every warp, R = 640 + 128 NS),
+//                            read by ldmatrix.
+// Requests: B <= 8 (one mma.sync n-tile).  Shards larger than 1,024 rows,
+// larger batches and the recurrent heads run the other resident kernel.
+//
+// Epilogue: when every request of the round is greedy and no logits are
+// written, each thread turns its accumulators straight into 32-bit keys {bf16
+// logit order bits : 16, inverted local row : 16} and the maxima go through
+// two warp and one CTA reduction; otherwise the logits are written into the
+// shared base buffer and the common key pass scores them (Gumbel-max, the
+// group sampler, the logits copy).
+#include "resident_pass.cuh"
+#include "tc_ptx.cuh"
+#include "walk_common.cuh"
+#include "walk_kernels.h"
+
+namespace dspark {
+
+namespace {
+
+constexpr int kMrWarps = kResWarps;                   // 8
+constexpr int kTmStrips = 4;                          // tensor-memory strips per warp
+constexpr int kTmRows = kMrWarps * kTmStrips * 16;    // 512
+constexpr int kRfRows = kMrWarps * 16;                // 128
+constexpr int kMrFixedRows = kTmRows + kRfRows;       // 640
+constexpr int kMrSmax = 3;                            // shared strips per warp, at most
+constexpr int kMrMaxRows = kMrFixedRows + kMrSmax * kMrWarps * 16;   // 1024
+constexpr int kMrMaxB = 8;
+constexpr int kTmWordsPerWarp = 32 * 256;             // 32 lanes x 256 columns
+constexpr int kTmWords = kMrWarps * kTmWordsPerWarp;  // 256 KB
+constexpr int kMrRfWords = kMrWarps * 16 * 32 * 4;    // 64 KB
+constexpr int kMbarSmem = 0;
+
+// Local row of the first row of strip st of warp w (st: 0 register, 1..4
+// tensor memory, 5..7 shared, the j-th shared strip of the warp being strip
+// w + 8 j of the shared tier).
+__device__ __forceinline__ int strip_row0(int st, int w) {
+  if (st == 0) return kTmRows + 16 * w;
+  if (st <= kTmStrips) return 16 * (kTmStrips * w + st - 1);
+  return kMrFixedRows + 16 * (w + kMrWarps * (st - 1 - kTmStrips));
+}
+
+// Order bits of two bf16 values packed in a word (-0 folded onto +0): larger
+// value, larger bits, as the resident key pass forms them.
+__device__ __forceinline__ uint32_t bf16_order(uint32_t x) {
+  x = x == 0x8000u ? 0u : x;
+  return (x & 0x8000u) ? (~x & 0xFFFFu) : (x | 0x8000u);
+}
+
+__device__ __forceinline__ uint32_t max_u32(uint32_t a, uint32_t b) { return a > b ? a : b; }
+
+// NS: shared strips per warp (0 .. 3; every warp the same), so the shard has
+// R = 640 + 128 NS rows and each warp NST = 5 + NS accumulation chains.
+template <int NS>
+__global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const ResidentArgs ra) {
+  constexpr int NST = 1 + kTmStrips + NS;
+  const WalkArgs& a = ra.w;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* smem_w2 = smem;
+  uint8_t* U = smem + (size_t)ra.S * kSmemStripBytes;
+  uint16_t* base_s = reinterpret_cast<uint16_t*>(U + 16 * 512);
+  __shared__ __align__(8) uint64_t mbar[1];
+  __shared__ unsigned long long group_best[16][kResWarps];
+  __shared__ uint32_t warp_key[kMrWarps][kMrMaxB];
+  __shared__ float temp_s[16];
+  __shared__ int32_t tok_s[16];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int flag_s;
+  __shared__ int fast_s;
+  __shared__ int abort_s;
+  __shared__ uint32_t round_s;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int cta = blockIdx.x;
+  const int n_cta = gridDim.x;
+  const int64_t row0 = (int64_t)cta * ra.R;
+  const int nv = (int)((a.V - row0) < ra.R ? (a.V - row0) : ra.R);  // valid rows (>= 1)
+  const uint32_t* gw = ra.W2p + (size_t)cta * (size_t)ra.words_per_cta;
+
+  const int bad = check_inputs(a, &flag_s);
+  if (bad != 0) {
+    if (cta == 0) {
+      if (threadIdx.x == 0) set_status(a.sync.hdr, bad);
+      for (int i = threadIdx.x; i < a.B * a.gamma; i += blockDim.x) a.out_tokens[i] = -1;
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------- entry ----
+  trace_stamp(a, a.gamma, 0);
+  if (threadIdx.x == 0) {
+    round_s = *reinterpret_cast<volatile uint32_t*>(&a.sync.hdr->round);
+    abort_s = 0;
+    ptx::mbar_init(&mbar[kMbarSmem], 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(&tmem_base_s, 512);
+    ptx::tmem_relinquish();
+  }
+  if (threadIdx.x < 16) {
+    temp_s[threadIdx.x] = threadIdx.x < a.B ? a.temperature[threadIdx.x] : 0.0f;
+    tok_s[threadIdx.x] = threadIdx.x < a.B ? a.anchor[threadIdx.x] : 0;
+  }
+  for (int i = threadIdx.x; i < 16 * 512 / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(U)[i] = make_uint4(0u, 0u, 0u, 0u);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  if (threadIdx.x == 0) {      // every request greedy and no logits out: fused keys
+    int f = a.out_logits == nullptr ? 1 : 0;
+    for (int b = 0; b < a.B; ++b) f = (temp_s[b] == 0.0f) ? f : 0;
+    fast_s = f;
+  }
+
+  // the other parity's keys and counts start empty for the next round
+  if (cta == 0) clear_other_parity(a.sync, round_s & 1u);
+
+  // shared-memory tier: bulk copies straight to its final place
+  const uint64_t t_entry = globaltimer_ns();
+  if (threadIdx.x == 0 && ra.S > 0) {
+    const uint32_t bytes = (uint32_t)ra.S * kSmemStripBytes;
+    ptx::mbar_expect_tx(&mbar[kMbarSmem], bytes);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(gw + kTmWords + kMrRfWords);
+    for (uint32_t off = 0; off < bytes; off += 32768u) {
+      const uint32_t n = bytes - off < 32768u ? bytes - off : 32768u;
+      ptx::bulk_g2s(smem_w2 + off, src + off, n, &mbar[kMbarSmem]);
+    }
+  }
+
+  // step 0's base rows: asynchronous copies, in flight during the loads below
+  prefetch_base(ra, 0, row0, nv, base_s);
+
+  // register tier and tensor-memory tier: global -> registers (-> tcgen05.st).
+  // Warp w's tensor-memory block is 8 chunks of 32 columns; lane l's 32 words
+  // of chunk p sit at [w][p][m][l][4], m = 0..7 (512 contiguous bytes per load).
+  const uint32_t tq = (uint32_t)(32 * (warp & 3)) << 16;
+  const uint32_t tcol = 256u * (uint32_t)(warp >> 2);
+  const uint32_t tm_addr = tmem + tq + tcol;
+  uint32_t wr[16][4];                  // register tier: this warp's strip as A fragments
+  {
+    const uint4* rsrc = reinterpret_cast<const uint4*>(gw + kTmWords) + (size_t)warp * 16 * 32 + lane;
+    const uint4* tsrc = reinterpret_cast<const uint4*>(gw) + (size_t)warp * (kTmWordsPerWarp / 4) + lane;
+    uint32_t v0[32], v1[32];
+    auto load_chunk = [&](int p, uint32_t (&v)[32]) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const uint4 x = __ldg(tsrc + (p * 8 + m) * 32);
+        v[4 * m + 0] = x.x;
+        v[4 * m + 1] = x.y;
+        v[4 * m + 2] = x.z;
+        v[4 * m + 3] = x.w;
+      }
+    };
+    auto store_chunk = [&](int p, uint32_t (&v)[32]) { ptx::tmem_st32(tm_addr + 32 * p, v); };
+    load_chunk(0, v0);
+    load_chunk(1, v1);
+#pragma unroll
+    for (int kt = 0; kt < 16; ++kt) {
+      const uint4 x = __ldg(rsrc + kt * 32);
+      wr[kt][0] = x.x;
+      wr[kt][1] = x.y;
+      wr[kt][2] = x.z;
+      wr[kt][3] = x.w;
+    }
+#pragma unroll
+    for (int p = 0; p < 8; p += 2) {
+      store_chunk(p, v0);
+      store_chunk(p + 1, v1);
+      ptx::tmem_wait_st();
+      if (p + 2 < 8) {
+        load_chunk(p + 2, v0);
+        load_chunk(p + 3, v1);
+      }
+    }
+  }
+  trace_stamp(a, a.gamma, 1);
+
+  // step 0's u = W1[anchor]
+  for (int b = warp; b < a.B; b += kResWarps) gather_u_row(a, tok_s[b], b, U, lane, 0);
+  if (ra.S > 0 && threadIdx.x == 0) {
+    if (!wait_mbar(&mbar[kMbarSmem], 0, t_entry, a.timeout_ns)) {
+      abort_round(a.sync.hdr, round_s, kStatusTimeout);
+      abort_s = 1;
+    }
+  }
+  ptx::cp_async_wait_all();
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  trace_stamp(a, a.gamma, 2);
+
+  const bool fast = fast_s != 0;
+  const KeyPassMap kpm = key_pass_map(a.B, temp_s);
+  const uint2 eseed = round_seed(a, round_s);             // this round's Philox key
+  const int nslots = kpm.tpr >= 32 ? kpm.tpr / 32 : 1;   // group_best slots per request
+
+  // ----------------------------------------------------------- the walk ---
+  const uint32_t w2_addr = ptx::smem_u32(smem_w2);
+  const uint32_t blk0 =
+      w2_addr + (uint32_t)warp * kSmemStripBytes + (lane >> 3) * 128 + (lane & 7) * 16;
+  const bool bcol = g < a.B;           // this lane's B-fragment column is a request
+  bool ok = abort_s == 0;
+  int k = 0;
+  for (; k < a.gamma && ok; ++k) {
+    const uint64_t t_step = globaltimer_ns();
+    trace_stamp(a, k, 0);
+
+    // (1) projection: 16 k-tiles of up to 8 independent mma.sync chains (the
+    // register strip, the four tensor-memory strips, the shared strips); the
+    // tensor-memory fragments of k-tile pair p + 1 load while pair p computes
+    float acc[NST][4];
+#pragma unroll
+    for (int s = 0; s < NST; ++s)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[s][e] = 0.0f;
+    {
+      uint32_t fr[2][32];
+      ptx::tmem_ld32(tm_addr, fr[0]);
+      ptx::tmem_wait_ld32(fr[0]);
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        if (p + 1 < 8) ptx::tmem_ld32(tm_addr + 32 * (p + 1), fr[(p + 1) & 1]);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int kt = 2 * p + e;
+          uint32_t af[NS > 0 ? NS : 1][4];
+#pragma unroll
+          for (int j = 0; j < NS; ++j)
+              ptx::ldmatrix_x4(blk0 + (uint32_t)(j * kResWarps) * kSmemStripBytes + kt * 512,
+                               af[j][0], af[j][1], af[j][2], af[j][3]);
+          uint32_t b0 = 0u, b1 = 0u;
+          if (bcol) {
+            b0 = *reinterpret_cast<const uint32_t*>(U + (4 * kt) * 128 + lane * 4);
+            b1 = *reinterpret_cast<const uint32_t*>(U + (4 * kt + 2) * 128 + lane * 4);
+          }
+          ptx::mma_16816(acc[0], wr[kt][0], wr[kt][1], wr[kt][2], wr[kt][3], b0, b1);
+#pragma unroll
+          for (int s = 0; s < kTmStrips; ++s) {
+            const uint32_t* f = &fr[p & 1][16 * e + 4 * s];
+            ptx::mma_16816(acc[1 + s], f[0], f[1], f[2], f[3], b0, b1);
+          }
+#pragma unroll
+          for (int j = 0; j < NS; ++j)
+              ptx::mma_16816(acc[1 + kTmStrips + j], af[j][0], af[j][1], af[j][2], af[j][3], b0,
+                             b1);
+        }
+        if (p + 1 < 8) ptx::tmem_wait_ld32(fr[(p + 1) & 1]);
+      }
+    }
+    trace_stamp(a, k, 1);
+
+    // (2) epilogue
+    if (fast) {
+      // greedy, no logits out: this thread's rows are g and g + 8 of each of
+      // its NST strips, its requests 2 t4 and 2 t4 + 1.  Branch-free: every
+      // base value is read first, then the independent roundings and keys
+      // {bf16 order bits : 16, inverted local row : 16}, then a max tree;
+      // rows past the shard's end and requests past B give key 0.
+      constexpr int NR = 2 * NST;
+      int rl[NR];
+#pragma unroll
+      for (int s = 0; s < NST; ++s) {
+        rl[2 * s] = strip_row0(s, warp) + g;
+        rl[2 * s + 1] = rl[2 * s] + 8;
+      }
+      uint32_t kb[2] = {0u, 0u};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        if (e == 1 && a.B < 2) continue;            // uniform: one request per round
+        const int b = 2 * t4 + e < a.B ? 2 * t4 + e : 0;
+        const uint16_t* bs = base_s + (size_t)b * ra.R;
+        uint32_t key[NR];
+#pragma unroll
+        for (int i = 0; i < NR; ++i) key[i] = bs[rl[i]];
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+          const float bias =
+              __bfloat162float(__float2bfloat16_rn(acc[i >> 1][2 * (i & 1) + e]));
+          const uint32_t lb = float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(key[i]), bias));
+          key[i] = rl[i] < nv ? (bf16_order(lb) << 16) | (0xFFFFu - (uint32_t)rl[i]) : 0u;
+        }
+#pragma unroll
+        for (int w = 1; w < NR; w <<= 1)
+#pragma unroll
+          for (int i = 0; i + w < NR; i += 2 * w) key[i] = max_u32(key[i], key[i + w]);
+        kb[e] = 2 * t4 + e < a.B ? key[0] : 0u;
+      }
+      // the eight lanes of one t4 share requests 2 t4, 2 t4 + 1
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) kb[e] = max_u32(kb[e], __shfl_xor_sync(0xFFFFFFFFu, kb[e], o));
+      if (g == 0)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          if (2 * t4 + e < a.B) warp_key[warp][2 * t4 + e] = kb[e];
+      trace_stamp(a, k, 2);
+      trace_stamp(a, k, 3);
+      __syncthreads();
+    } else {
+      // logits into the shared base buffer (in place), then the key pass
+#pragma unroll
+      for (int s = 0; s < NST; ++s) {
+        float a1[1][4] = {{acc[s][0], acc[s][1], acc[s][2], acc[s][3]}};
+        logits_strip<1>(a1, base_s, ra.R, a.B, strip_row0(s, warp), lane);
+      }
+      trace_stamp(a, k, 2);
+      __syncthreads();
+      key_pass<false>(a, base_s, ra.R, nv, row0, k, kpm, eseed, group_best);
+      trace_stamp(a, k, 3);
+      __syncthreads();
+    }
+    trace_stamp(a, k, 4);
+
+    // (3) next step's base rows (the current ones are no longer read), by
+    // warps 1-7: warp 0's release below would otherwise wait for these loads
+    if (warp != 0) prefetch_base(ra, k + 1, row0, nv, base_s, 32, kResThreads - 32);
+
+    // (4) the rendezvous (warp 0): per request an atomic max into the step's
+    // key slot, released by an arrival count; wait until every CTA has
+    // counted every request, read the winners, gather the next u rows
+    if (warp == 0) {
+      const uint32_t parity = round_s & 1u;
+      const uint32_t target = (uint32_t)n_cta;
+      uint32_t* cnt = a.sync.count_at(parity, k);
+      unsigned long long* keyk = a.sync.key_at(parity, k, 0);
+      unsigned long long cand = 0ull;
+      if (lane < a.B) {
+        unsigned long long mine = 0ull;
+        if (fast) {
+          uint32_t m = 0u;
+#pragma unroll
+          for (int w = 0; w < kMrWarps; ++w) m = max_u32(m, warp_key[w][lane]);
+          if (m != 0u) {
+            const uint32_t v = (uint32_t)(row0 + (0xFFFFu - (m & 0xFFFFu)));
+            mine = ((unsigned long long)(m >> 16) << 32) | (unsigned long long)(0xFFFFFFFFu - v);
+          }
+        } else {
+          for (int sl = 0; sl < nslots; ++sl) mine = key_max(mine, group_best[lane][sl]);
+        }
+        if (cta != a.skip_cta) red_relaxed_gpu_max_u64(keyk + lane, mine);
+        cand = mine;
+      }
+      __syncwarp();
+      // one arrival per CTA: lane 0's release is cumulative over the maxes the
+      // warp barrier ordered before it
+      if (lane == 0 && cta != a.skip_cta) red_release_gpu_add(cnt, 1u);
+      if (cand != 0ull) {                          // the candidate's W1 row, into L2
+        const uint16_t* row = a.W1 + (size_t)(0xFFFFFFFFu - (uint32_t)cand) * kRank;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ptx::prefetch_l2(row + 64 * i);
+      }
+      trace_stamp(a, k, 5);
+      int good = 1;
+      if (lane == 0) {
+        uint32_t spins = 0;
+        while (ld_acquire_gpu(cnt) < target) {
+          if ((++spins & 63u) == 0u) {
+            if (round_aborted(a.sync.hdr, round_s)) { good = 0; break; }
+            if ((int64_t)(globaltimer_ns() - t_step) > a.timeout_ns) {
+              abort_round(a.sync.hdr, round_s, kStatusTimeout);
+              good = 0;
+              break;
+            }
+          }
+        }
+        if (!good) abort_s = 1;
+      }
+      good = __shfl_sync(0xFFFFFFFFu, good, 0);
+      if (good) {
+        trace_stamp(a, k, 6);
+        if (lane < a.B) {
+          const int32_t tok = key_token(ld_acquire_gpu_u64(keyk + lane));
+          if (tok < 0 || (int64_t)tok >= a.V) {    // cannot happen: every CTA posts a real row
+            abort_round(a.sync.hdr, round_s, kStatusInternal);
+            abort_s = 1;
+          } else {
+            tok_s[lane] = tok;
+            if (cta == 0) a.out_tokens[(size_t)lane * a.gamma + k] = tok;
+          }
+        }
+        __syncwarp();
+        // up to four next u rows: warp 0 fetches them here (larger batches are
+        // fetched by all warps after the barrier below)
+        if (a.B <= 4 && k + 1 < a.gamma) {
+          uint4 ur[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (j < a.B)
+              ur[j] = __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok_s[j] * kRank) + lane);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (j < a.B)
+              *reinterpret_cast<uint4*>(U + (lane * 2 + (j >> 3)) * 128 + (j & 7) * 16) = ur[j];
+        }
+      }
+    }
+    ptx::cp_async_wait_all();
+    __syncthreads();
+    if (a.B > 4 && abort_s == 0 && k + 1 < a.gamma) {
+      // the next u rows, all in flight at once: warp w fetches row w
+      for (int b = warp; b < a.B; b += kResWarps) {
+        const uint4 x =
+            __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok_s[b] * kRank) + lane);
+        *reinterpret_cast<uint4*>(U + (lane * 2 + (b >> 3)) * 128 + (b & 7) * 16) = x;
+      }
+      __syncthreads();
+    }
+    trace_stamp(a, k, 7);
+    ok = abort_s == 0;
+  }
+
+  // -------------------------------------------------------------- exit ----
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tmem, 512);
+  if (cta == 0) {
+    if (!ok)
+      for (int i = threadIdx.x; i < a.B * a.gamma; i += blockDim.x) a.out_tokens[i] = -1;
+    if (threadIdx.x == 0) atomicAdd(&a.sync.hdr->round, 1u);
+  }
+}
+
+// Position (local row, K word pair) of word i of a CTA's block of the repacked
+// W2 (see the tier layouts above); the repack and its inverse share it.
+__device__ __forceinline__ void mr_word_pos(int64_t i, int* rl, int* kp) {
+  if (i < kTmWords) {           // [warp][p][m][lane][4]
+    const int j4 = (int)(i & 3), l = (int)((i >> 2) & 31), m = (int)((i >> 7) & 7);
+    const int p = (int)((i >> 10) & 7), w = (int)(i >> 13);
+    const int ii = 4 * m + j4;                 // word of lane l's 32-column chunk p
+    const int e = ii >> 4, s = (ii >> 2) & 3, j = ii & 3;
+    const int kt = 2 * p + e;
+    *rl = 16 * (kTmStrips * w + s) + (l >> 2) + 8 * (j & 1);
+    *kp = kt * 8 + (l & 3) + 4 * (j >> 1);
+  } else if (i < kTmWords + kMrRfWords) {    // [warp][kt][lane][4]
+    const int64_t x = i - kTmWords;
+    const int j = (int)(x & 3), l = (int)((x >> 2) & 31), kt = (int)((x >> 7) & 15);
+    const int w = (int)(x >> 11);
+    *rl = kTmRows + 16 * w + (l >> 2) + 8 * (j & 1);
+    *kp = kt * 8 + (l & 3) + 4 * (j >> 1);
+  } else {                                   // [strip][kt][matrix][row][4] (ldmatrix)
+    const int64_t x = i - kTmWords - kMrRfWords;
+    const int p = (int)(x & 3), ii = (int)((x >> 2) & 7), m = (int)((x >> 5) & 3);
+    const int kt = (int)((x >> 7) & 15), s2 = (int)(x >> 11);
+    *rl = kMrFixedRows + 16 * s2 + 8 * (m & 1) + ii;
+    *kp = kt * 8 + 4 * (m >> 1) + p;
+  }
+}
+
+// Repack row-major W2 [V, 256] (32-bit words of two K elements) into the
+// per-CTA tiered layout (rows past V are zero), or, with `inverse`, write the
+// rows held in the layout back to row-major form.
+__global__ void repack_mma_kernel(uint32_t* __restrict__ rowmajor, uint32_t* __restrict__ packed,
+                                  int64_t V, int R, int64_t words_per_cta, int n_cta,
+                                  int inverse) {
+  const int64_t total = words_per_cta * n_cta;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t cta = i / words_per_cta;
+    int rl, kp;
+    mr_word_pos(i - cta * words_per_cta, &rl, &kp);
+    const int64_t row = cta * (int64_t)R + rl;
+    if (inverse) {
+      if (row < V) rowmajor[row * (kRank / 2) + kp] = packed[i];
+    } else {
+      packed[i] = row < V ? rowmajor[row * (kRank / 2) + kp] : 0u;
+    }
+  }
+}
+
+}  // namespace
+
+int mma_resident_fixed_rows() { return kMrFixedRows; }
+
+int mma_resident_max_rows() { return kMrMaxRows; }
+
+int mma_resident_max_batch() { return kMrMaxB; }
+
+int64_t mma_resident_words_per_cta(int S) {
+  return (int64_t)kTmWords + kMrRfWords + (int64_t)S * (kSmemStripBytes / 4);
+}
+
+size_t mma_resident_smem_bytes(int S, int max_B, int R) {
+  return (size_t)S * kSmemStripBytes + 16 * 512 + (((size_t)max_B * R * 2 + 15) & ~(size_t)15);
+}
+
+const void* mma_resident_kernel(int S) {
+  switch (S / kMrWarps) {
+    case 0: return reinterpret_cast<const void*>(&walk_mma_kernel<0>);
+    case 1: return reinterpret_cast<const void*>(&walk_mma_kernel<1>);
+    case 2: return reinterpret_cast<const void*>(&walk_mma_kernel<2>);
+    case 3: return reinterpret_cast<const void*>(&walk_mma_kernel<3>);
+  }
+  return nullptr;
+}
+
+cudaError_t mma_resident_repack(void* rowmajor, void* packed, int64_t V, int R, int S, int n_cta,
+                                bool inverse, cudaStream_t stream) {
+  const int64_t wpc = mma_resident_words_per_cta(S);
+  const int64_t total = wpc * n_cta;
+  int blocks = (int)((total + 255) / 256);
+  if (blocks > 65535 * 8) blocks = 65535 * 8;
+  repack_mma_kernel<<<blocks, 256, 0, stream>>>(static_cast<uint32_t*>(rowmajor),
+                                               static_cast<uint32_t*>(packed), V, R, wpc, n_cta,
+                                               inverse ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

@@ -57,6 +57,7 @@ class dspark_walk_plan(ctypes.Structure):
         ("rows_stream", ctypes.c_int), ("resident_bytes", ctypes.c_int64),
         ("streamed_bytes", ctypes.c_int64), ("max_B", ctypes.c_int),
         ("max_gamma", ctypes.c_int), ("kernel", ctypes.c_int), ("sm_count", ctypes.c_int),
+        ("weight_bytes", ctypes.c_int64),
     ]
 
     def as_dict(self):
@@ -69,7 +70,7 @@ EXPORTS = [
     "dspark_walk_destroy", "dspark_walk_run_noalloc", "dspark_walk_set_kernel",
     "dspark_walk_set_trace", "dspark_walk_set_seed_mode", "dspark_walk_round",
     "dspark_walk_gumbel_noise", "dspark_walk_set_sampler", "dspark_walk_set_cell",
-    "dspark_walk_set_state_output",
+    "dspark_walk_set_state_output", "dspark_walk_unit_rates",
 ]
 
 
@@ -107,6 +108,7 @@ def load(build_if_missing=True):
     L.dspark_walk_set_state_output.argtypes = [vp, vp]
     L.dspark_walk_round.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint64)]
     L.dspark_walk_gumbel_noise.argtypes = [vp, vp, i64, vp]
+    L.dspark_walk_unit_rates.argtypes = [ctypes.POINTER(ctypes.c_double), i32, vp]
     for name in EXPORTS:
         if name != "dspark_walk_strerror":
             getattr(L, name).restype = ctypes.c_int
@@ -225,6 +227,19 @@ def dspark_walk_gumbel_noise(bits, noise, stream=None):
     assert bits.dtype in (torch.int32, torch.uint32) and noise.dtype == torch.float32
     return _check(load().dspark_walk_gumbel_noise(_ptr(bits), _ptr(noise), bits.numel(),
                                                   _stream(stream)), "dspark_walk_gumbel_noise")
+
+
+UNIT_RATE_NAMES = ("hmma_rf_cycles", "hmma_smem_cycles", "tc_tmem_a_cycles",
+                   "resident_step_projection_cycles", "sm_mhz", "tmem_ld_cycles_per_kb",
+                   "tmem_fed_step_projection_cycles")
+
+
+def dspark_walk_unit_rates(stream=None):
+    """The on-chip tier rates of the current device (see the header), as a dict."""
+    out = (ctypes.c_double * len(UNIT_RATE_NAMES))()
+    _check(load().dspark_walk_unit_rates(out, len(UNIT_RATE_NAMES), _stream(stream)),
+           "dspark_walk_unit_rates")
+    return dict(zip(UNIT_RATE_NAMES, list(out)))
 
 
 def dspark_walk_set_trace(h, device_buffer, nbytes):
