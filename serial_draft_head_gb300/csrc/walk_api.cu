@@ -80,11 +80,15 @@ int cuda_fail(cudaError_t e) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Sizes of the parts of the rendezvous memory: header, arrival counts, keys.
-void sync_layout(int max_gamma, int max_B, size_t* count_off, size_t* key_off, size_t* total) {
+// Sizes of the parts of the rendezvous memory: header, arrival counts, keys,
+// tagged slots (slot_B requests, slot_stride words per step and request).
+void sync_layout(int max_gamma, int max_B, int slot_B, int slot_stride, size_t* count_off,
+                 size_t* key_off, size_t* slot_off, size_t* total) {
   *count_off = round_up(sizeof(SyncHeader), 128);
   *key_off = round_up(*count_off + (size_t)2 * max_gamma * kCountStride * sizeof(uint32_t), 128);
-  *total = round_up(*key_off + (size_t)2 * max_gamma * max_B * sizeof(unsigned long long), 128);
+  *slot_off = round_up(*key_off + (size_t)2 * max_gamma * max_B * sizeof(unsigned long long), 128);
+  *total = round_up(*slot_off + (size_t)2 * max_gamma * slot_B * slot_stride *
+                                    sizeof(unsigned long long), 128);
 }
 
 // Shared memory a CTA may use, minus the kernels' static shared variables.
@@ -470,8 +474,10 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
   plan_mma(h);
   const bool resident = plan_resident(h);
   plan_batched(h);
-  size_t count_off, key_off, total;
-  sync_layout(max_gamma, max_B, &count_off, &key_off, &total);
+  size_t count_off, key_off, slot_off, total;
+  const int slot_B = max_B < 16 ? max_B : 16;
+  const int slot_stride = (sms + 15) / 16 * 16;
+  sync_layout(max_gamma, max_B, slot_B, slot_stride, &count_off, &key_off, &slot_off, &total);
   cudaError_t e = cudaMalloc(&h->sync_mem, total);
   if (e == cudaSuccess) e = cudaMemset(h->sync_mem, 0, total);
   if (e == cudaSuccess) {
@@ -481,6 +487,9 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
     h->sync.key = reinterpret_cast<unsigned long long*>(base + key_off);
     h->sync.max_gamma = max_gamma;
     h->sync.max_B = max_B;
+    h->sync.slot = reinterpret_cast<unsigned long long*>(base + slot_off);
+    h->sync.slot_B = slot_B;
+    h->sync.slot_stride = slot_stride;
   }
   if (e != cudaSuccess) rc = cuda_fail(e);
   if (rc == DSPARK_OK) {

@@ -49,6 +49,14 @@ struct SyncView {
   unsigned long long* key;     // [2][max_gamma][max_B]
   int max_gamma;
   int max_B;
+  // tagged slots (the mma.sync resident kernel): [2][max_gamma][slot_B][slot_stride]
+  unsigned long long* slot;
+  int slot_B;                  // requests with slots (min(max_B, 16))
+  int slot_stride;             // words per (parity, step, request): >= CTAs, even
+
+  __device__ __forceinline__ unsigned long long* slot_at(uint32_t parity, int k, int b) const {
+    return slot + (((size_t)parity * max_gamma + k) * slot_B + b) * slot_stride;
+  }
 
   __device__ __forceinline__ uint32_t* count_at(uint32_t parity, int k) const {
     return count + ((size_t)parity * max_gamma + k) * kCountStride;
@@ -456,6 +464,43 @@ __device__ __forceinline__ void clear_other_parity(const SyncView& s, uint32_t p
   for (int i = threadIdx.x; i < s.max_gamma * kCountStride; i += blockDim.x) c[i] = 0u;
   unsigned long long* kk = s.key_at(q, 0, 0);
   for (int i = threadIdx.x; i < s.max_gamma * s.max_B; i += blockDim.x) kk[i] = 0ull;
+}
+
+// Tagged-slot exchange: CTA c's best key of request b at step k of a round is
+// one 64-bit word slot_at(parity, k, b)[c] = {round tag : 14, key : 50}.  The
+// tag makes the word self-validating, so the post is one relaxed store with no
+// fence and no atomic; a reader polls all CTAs' words until each carries this
+// round's tag.  Every CTA clears its own words of the other parity at entry, so
+// the next round never sees a stale word of the same tag.
+__device__ __forceinline__ unsigned long long slot_tag(uint32_t round) {
+  return (unsigned long long)((round & 0x1FFFu) | 0x2000u) << 50;
+}
+
+// The 64-bit key {order bits : 32, 0xFFFFFFFF - v} packed into 50 bits
+// {order bits : 32, 0x3FFFF - v} (same order for token ids v < 2^18).
+__device__ __forceinline__ unsigned long long key50(unsigned long long key64) {
+  return ((key64 >> 32) << 18) | (key64 & 0x3FFFFull);
+}
+
+__device__ __forceinline__ int32_t key50_token(unsigned long long k) {
+  return (int32_t)(0x3FFFFu - (uint32_t)(k & 0x3FFFFull));
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void ld_relaxed_gpu_v2u64(const unsigned long long* p,
+                                                     unsigned long long& a,
+                                                     unsigned long long& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+// This CTA's words of the other parity, zeroed (all threads of the CTA).
+__device__ __forceinline__ void clear_own_slots(const SyncView& s, uint32_t parity) {
+  const uint32_t q = parity ^ 1u;
+  for (int i = threadIdx.x; i < s.max_gamma * s.slot_B; i += blockDim.x)
+    s.slot_at(q, i / s.slot_B, i % s.slot_B)[blockIdx.x] = 0ull;
 }
 
 // One step's cross-CTA selection.  cta_key[b] holds this CTA's best key of

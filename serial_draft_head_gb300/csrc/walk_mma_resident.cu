@@ -56,6 +56,7 @@ constexpr int kTmWordsPerWarp = 32 * 256;             // 32 lanes x 256 columns
 constexpr int kTmWords = kMrWarps * kTmWordsPerWarp;  // 256 KB
 constexpr int kMrRfWords = kMrWarps * 16 * 32 * 4;    // 64 KB
 constexpr int kMbarSmem = 0;
+constexpr unsigned long long kKey50Mask = (1ull << 50) - 1ull;
 
 // Local row of the first row of strip st of warp w (st: 0 register, 1..4
 // tensor memory, 5..7 shared, the j-th shared strip of the warp being strip
@@ -141,8 +142,8 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
     fast_s = f;
   }
 
-  // the other parity's keys and counts start empty for the next round
-  if (cta == 0) clear_other_parity(a.sync, round_s & 1u);
+  // this CTA's slots of the other parity start empty for the next round
+  clear_own_slots(a.sync, round_s & 1u);
 
   // shared-memory tier: bulk copies straight to its final place
   const uint64_t t_entry = globaltimer_ns();
@@ -294,9 +295,44 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
         rl[2 * s + 1] = rl[2 * s] + 8;
       }
       uint32_t kb[2] = {0u, 0u};
+      if (a.B == 1) {
+        // one request: only column 0 (lanes 4 g) holds results.  Spread them
+        // over the warp first -- lane (g, t4) takes strips t4 and t4 + 4, rows
+        // g and g + 8 -- so that every lane scores 4 logits instead of a
+        // quarter of the lanes scoring 16.
+        float v[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
+#pragma unroll
+        for (int s = 0; s < NST; ++s)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float x = __shfl_sync(0xFFFFFFFFu, acc[s][2 * h], lane & ~3);
+            if ((s & 3) == t4) v[s >> 2][h] = x;
+          }
+        uint32_t key[4];
+        int rr[4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int s = t4 + 4 * j;
+          const int r0 = s < NST ? strip_row0(s, warp) + g : 0;
+          rr[2 * j] = r0;
+          rr[2 * j + 1] = r0 + 8;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) key[i] = base_s[rr[i]];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float bias = __bfloat162float(__float2bfloat16_rn(v[i >> 1][i & 1]));
+          const uint32_t lb = float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(key[i]), bias));
+          const bool valid = t4 + 4 * (i >> 1) < NST && rr[i] < nv;
+          key[i] = valid ? (bf16_order(lb) << 16) | (0xFFFFu - (uint32_t)rr[i]) : 0u;
+        }
+        kb[0] = max_u32(max_u32(key[0], key[1]), max_u32(key[2], key[3]));
+        kb[0] = max_u32(kb[0], __shfl_xor_sync(0xFFFFFFFFu, kb[0], 1));
+        kb[0] = max_u32(kb[0], __shfl_xor_sync(0xFFFFFFFFu, kb[0], 2));
+      }
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        if (e == 1 && a.B < 2) continue;            // uniform: one request per round
+        if (a.B == 1 || (e == 1 && a.B < 2)) continue;     // uniform
         const int b = 2 * t4 + e < a.B ? 2 * t4 + e : 0;
         const uint16_t* bs = base_s + (size_t)b * ra.R;
         uint32_t key[NR];
@@ -342,100 +378,99 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
     }
     trace_stamp(a, k, 4);
 
-    // (3) next step's base rows (the current ones are no longer read), by
-    // warps 1-7: warp 0's release below would otherwise wait for these loads
-    if (warp != 0) prefetch_base(ra, k + 1, row0, nv, base_s, 32, kResThreads - 32);
-
-    // (4) the rendezvous (warp 0): per request an atomic max into the step's
-    // key slot, released by an arrival count; wait until every CTA has
-    // counted every request, read the winners, gather the next u rows
-    if (warp == 0) {
-      const uint32_t parity = round_s & 1u;
-      const uint32_t target = (uint32_t)n_cta;
-      uint32_t* cnt = a.sync.count_at(parity, k);
-      unsigned long long* keyk = a.sync.key_at(parity, k, 0);
-      unsigned long long cand = 0ull;
-      if (lane < a.B) {
-        unsigned long long mine = 0ull;
-        if (fast) {
-          uint32_t m = 0u;
+    // (3) the rendezvous.  Post: this CTA's best key of request b goes into
+    // its own tagged slot, one relaxed store (the tag validates the word, so
+    // no fence orders it and no atomic contends for a line).  Then every warp
+    // starts the next step's base rows, and warp b polls request b's slots of
+    // all CTAs until each carries this round's tag, takes the maximum and
+    // fetches the winner's W1 row into U.
+    const uint32_t parity = round_s & 1u;
+    const unsigned long long tag = slot_tag(round_s);
+    if (warp == 0 && lane < a.B) {
+      unsigned long long mine = 0ull;
+      if (fast) {
+        uint32_t m = 0u;
 #pragma unroll
-          for (int w = 0; w < kMrWarps; ++w) m = max_u32(m, warp_key[w][lane]);
-          if (m != 0u) {
-            const uint32_t v = (uint32_t)(row0 + (0xFFFFu - (m & 0xFFFFu)));
-            mine = ((unsigned long long)(m >> 16) << 32) | (unsigned long long)(0xFFFFFFFFu - v);
-          }
-        } else {
-          for (int sl = 0; sl < nslots; ++sl) mine = key_max(mine, group_best[lane][sl]);
+        for (int w = 0; w < kMrWarps; ++w) m = max_u32(m, warp_key[w][lane]);
+        if (m != 0u) {
+          const uint32_t v = (uint32_t)(row0 + (0xFFFFu - (m & 0xFFFFu)));
+          mine = ((unsigned long long)(m >> 16) << 32) | (unsigned long long)(0xFFFFFFFFu - v);
         }
-        if (cta != a.skip_cta) red_relaxed_gpu_max_u64(keyk + lane, mine);
-        cand = mine;
+      } else {
+        for (int sl = 0; sl < nslots; ++sl) mine = key_max(mine, group_best[lane][sl]);
       }
-      __syncwarp();
-      // one arrival per CTA: lane 0's release is cumulative over the maxes the
-      // warp barrier ordered before it
-      if (lane == 0 && cta != a.skip_cta) red_release_gpu_add(cnt, 1u);
-      if (cand != 0ull) {                          // the candidate's W1 row, into L2
-        const uint16_t* row = a.W1 + (size_t)(0xFFFFFFFFu - (uint32_t)cand) * kRank;
+      if (cta != a.skip_cta) st_relaxed_gpu_u64(a.sync.slot_at(parity, k, lane) + cta, tag | key50(mine));
+      if (mine != 0ull) {                          // the candidate's W1 row, into L2
+        const uint16_t* row = a.W1 + (size_t)(0xFFFFFFFFu - (uint32_t)mine) * kRank;
 #pragma unroll
         for (int i = 0; i < 4; ++i) ptx::prefetch_l2(row + 64 * i);
       }
-      trace_stamp(a, k, 5);
+    }
+    trace_stamp(a, k, 5);
+    prefetch_base(ra, k + 1, row0, nv, base_s);
+    if (warp < a.B) {
+      const unsigned long long* s = a.sync.slot_at(parity, k, warp);
+      unsigned long long best = 0ull;
       int good = 1;
-      if (lane == 0) {
-        uint32_t spins = 0;
-        while (ld_acquire_gpu(cnt) < target) {
-          if ((++spins & 63u) == 0u) {
-            if (round_aborted(a.sync.hdr, round_s)) { good = 0; break; }
-            if ((int64_t)(globaltimer_ns() - t_step) > a.timeout_ns) {
+      uint32_t spins = 0;
+      while (true) {
+        bool have = true;
+        best = 0ull;
+        for (int j = 2 * lane; j < n_cta; j += 64) {
+          unsigned long long x0, x1;
+          ld_relaxed_gpu_v2u64(s + j, x0, x1);
+          const bool v1 = j + 1 < n_cta;
+          have = have && (x0 & ~kKey50Mask) == tag && (!v1 || (x1 & ~kKey50Mask) == tag);
+          x0 &= kKey50Mask;
+          x1 = v1 ? (x1 & kKey50Mask) : 0ull;
+          best = x0 > best ? x0 : best;
+          best = x1 > best ? x1 : best;
+        }
+        if (__all_sync(0xFFFFFFFFu, have)) break;
+        if ((++spins & 15u) == 0u) {
+          int stop = 0;
+          if (lane == 0) {
+            if (round_aborted(a.sync.hdr, round_s)) {
+              stop = 1;
+            } else if ((int64_t)(globaltimer_ns() - t_step) > a.timeout_ns) {
               abort_round(a.sync.hdr, round_s, kStatusTimeout);
-              good = 0;
-              break;
+              stop = 1;
             }
           }
-        }
-        if (!good) abort_s = 1;
-      }
-      good = __shfl_sync(0xFFFFFFFFu, good, 0);
-      if (good) {
-        trace_stamp(a, k, 6);
-        if (lane < a.B) {
-          const int32_t tok = key_token(ld_acquire_gpu_u64(keyk + lane));
-          if (tok < 0 || (int64_t)tok >= a.V) {    // cannot happen: every CTA posts a real row
-            abort_round(a.sync.hdr, round_s, kStatusInternal);
-            abort_s = 1;
-          } else {
-            tok_s[lane] = tok;
-            if (cta == 0) a.out_tokens[(size_t)lane * a.gamma + k] = tok;
+          if (__shfl_sync(0xFFFFFFFFu, stop, 0)) {
+            good = 0;
+            break;
           }
         }
-        __syncwarp();
-        // up to four next u rows: warp 0 fetches them here (larger batches are
-        // fetched by all warps after the barrier below)
-        if (a.B <= 4 && k + 1 < a.gamma) {
-          uint4 ur[4];
+      }
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (j < a.B)
-              ur[j] = __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok_s[j] * kRank) + lane);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (j < a.B)
-              *reinterpret_cast<uint4*>(U + (lane * 2 + (j >> 3)) * 128 + (j & 7) * 16) = ur[j];
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        best = y > best ? y : best;
+      }
+      if (good) {
+        if (warp == 0) trace_stamp(a, k, 6);
+        const int32_t tok = key50_token(best);
+        if (tok < 0 || (int64_t)tok >= a.V) {      // cannot happen: every CTA posts a real row
+          if (lane == 0) {
+            abort_round(a.sync.hdr, round_s, kStatusInternal);
+            abort_s = 1;
+          }
+        } else {
+          if (lane == 0) {
+            tok_s[warp] = tok;
+            if (cta == 0) a.out_tokens[(size_t)warp * a.gamma + k] = tok;
+          }
+          if (k + 1 < a.gamma)
+            *reinterpret_cast<uint4*>(U + (lane * 2 + (warp >> 3)) * 128 + (warp & 7) * 16) =
+                __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok * kRank) + lane);
         }
+      } else if (lane == 0) {
+        abort_s = 1;
       }
     }
     ptx::cp_async_wait_all();
     __syncthreads();
-    if (a.B > 4 && abort_s == 0 && k + 1 < a.gamma) {
-      // the next u rows, all in flight at once: warp w fetches row w
-      for (int b = warp; b < a.B; b += kResWarps) {
-        const uint4 x =
-            __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok_s[b] * kRank) + lane);
-        *reinterpret_cast<uint4*>(U + (lane * 2 + (b >> 3)) * 128 + (b & 7) * 16) = x;
-      }
-      __syncthreads();
-    }
     trace_stamp(a, k, 7);
     ok = abort_s == 0;
   }
