@@ -76,6 +76,77 @@ __device__ __forceinline__ uint32_t bf16_order(uint32_t x) {
 
 __device__ __forceinline__ uint32_t max_u32(uint32_t a, uint32_t b) { return a > b ? a : b; }
 
+// The fused epilogue of a greedy round without logits out, for one warp:
+// each request's best key over the warp's NST strips, 32-bit {bf16 logit
+// order bits : 16, inverted local row : 16}, into wkey[b].
+// Lane (g, t4) holds rows g and g + 8 of columns 2 t4 and 2 t4 + 1 (requests)
+// of every strip.  With B <= 8 / G requests only the lanes t4 < 4 / G hold
+// results, so they are first spread over the G lane groups: lane (g, t4)
+// takes strips s = part (mod G), part = t4 / (4 / G), from lane (g, t4 mod
+// (4 / G)).  Every lane then scores NST / G strips x 4 values: base values
+// read first, then independent roundings and keys, then a max over the
+// lanes that hold the same request.
+template <int NST, int G>
+__device__ __forceinline__ void fast_keys(const float (&acc)[NST][4], const uint16_t* base_s,
+                                          int R, int B, int nv, int warp, int lane,
+                                          uint32_t* wkey) {
+  constexpr int NJ = (NST + G - 1) / G;          // strips per lane
+  constexpr int SRC = 4 / G;                     // lanes per row group holding results
+  const int g = lane >> 2, t4 = lane & 3;
+  const int src = t4 % SRC, part = t4 / SRC;
+  float v[NJ][4];
+#pragma unroll
+  for (int s = 0; s < NST; ++s)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x = G > 1 ? __shfl_sync(0xFFFFFFFFu, acc[s][e], (lane & ~3) | src) : acc[s][e];
+      if (G == 1 || s % G == part) v[s / G][e] = x;
+    }
+  int rr[NJ][2];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int s = part + G * j;
+    const int r0 = s < NST ? strip_row0(s, warp) + g : 0;
+    rr[j][0] = r0;
+    rr[j][1] = r0 + 8;
+  }
+  uint32_t kb[2] = {0u, 0u};
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {                  // requests 2 src and 2 src + 1
+    const int b = 2 * src + q;
+    if (q == 1 && B < 2) continue;               // uniform
+    const uint16_t* bs = base_s + (size_t)(b < B ? b : 0) * R;
+    uint32_t key[NJ][2];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) key[j][h] = bs[rr[j][h]];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float bias = __bfloat162float(__float2bfloat16_rn(v[j][2 * h + q]));
+        const uint32_t lb =
+            float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(key[j][h]), bias));
+        const bool valid = part + G * j < NST && rr[j][h] < nv;
+        key[j][h] = valid ? (bf16_order(lb) << 16) | (0xFFFFu - (uint32_t)rr[j][h]) : 0u;
+      }
+    uint32_t m = 0u;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) m = max_u32(m, max_u32(key[j][0], key[j][1]));
+    kb[q] = b < B ? m : 0u;
+  }
+  // lanes with the same src hold the same two requests: reduce over g and part
+#pragma unroll
+  for (int o = SRC; o < 32; o <<= 1)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) kb[q] = max_u32(kb[q], __shfl_xor_sync(0xFFFFFFFFu, kb[q], o));
+  if (g == 0 && part == 0)
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (2 * src + q < B) wkey[2 * src + q] = kb[q];
+}
+
 // NS: shared strips per warp (0 .. 3; every warp the same), so the shard has
 // R = 640 + 128 NS rows and each warp NST = 5 + NS accumulation chains.
 template <int NS>
@@ -142,8 +213,10 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
     fast_s = f;
   }
 
-  // this CTA's slots of the other parity start empty for the next round
+  // this CTA's slots of the other parity start empty for the next round, and
+  // so do that parity's arrival counts
   clear_own_slots(a.sync, round_s & 1u);
+  if (cta == 0) clear_other_parity(a.sync, round_s & 1u);
 
   // shared-memory tier: bulk copies straight to its final place
   const uint64_t t_entry = globaltimer_ns();
@@ -282,84 +355,13 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
 
     // (2) epilogue
     if (fast) {
-      // greedy, no logits out: this thread's rows are g and g + 8 of each of
-      // its NST strips, its requests 2 t4 and 2 t4 + 1.  Branch-free: every
-      // base value is read first, then the independent roundings and keys
-      // {bf16 order bits : 16, inverted local row : 16}, then a max tree;
-      // rows past the shard's end and requests past B give key 0.
-      constexpr int NR = 2 * NST;
-      int rl[NR];
-#pragma unroll
-      for (int s = 0; s < NST; ++s) {
-        rl[2 * s] = strip_row0(s, warp) + g;
-        rl[2 * s + 1] = rl[2 * s] + 8;
-      }
-      uint32_t kb[2] = {0u, 0u};
-      if (a.B == 1) {
-        // one request: only column 0 (lanes 4 g) holds results.  Spread them
-        // over the warp first -- lane (g, t4) takes strips t4 and t4 + 4, rows
-        // g and g + 8 -- so that every lane scores 4 logits instead of a
-        // quarter of the lanes scoring 16.
-        float v[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
-#pragma unroll
-        for (int s = 0; s < NST; ++s)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float x = __shfl_sync(0xFFFFFFFFu, acc[s][2 * h], lane & ~3);
-            if ((s & 3) == t4) v[s >> 2][h] = x;
-          }
-        uint32_t key[4];
-        int rr[4];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int s = t4 + 4 * j;
-          const int r0 = s < NST ? strip_row0(s, warp) + g : 0;
-          rr[2 * j] = r0;
-          rr[2 * j + 1] = r0 + 8;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) key[i] = base_s[rr[i]];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float bias = __bfloat162float(__float2bfloat16_rn(v[i >> 1][i & 1]));
-          const uint32_t lb = float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(key[i]), bias));
-          const bool valid = t4 + 4 * (i >> 1) < NST && rr[i] < nv;
-          key[i] = valid ? (bf16_order(lb) << 16) | (0xFFFFu - (uint32_t)rr[i]) : 0u;
-        }
-        kb[0] = max_u32(max_u32(key[0], key[1]), max_u32(key[2], key[3]));
-        kb[0] = max_u32(kb[0], __shfl_xor_sync(0xFFFFFFFFu, kb[0], 1));
-        kb[0] = max_u32(kb[0], __shfl_xor_sync(0xFFFFFFFFu, kb[0], 2));
-      }
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        if (a.B == 1 || (e == 1 && a.B < 2)) continue;     // uniform
-        const int b = 2 * t4 + e < a.B ? 2 * t4 + e : 0;
-        const uint16_t* bs = base_s + (size_t)b * ra.R;
-        uint32_t key[NR];
-#pragma unroll
-        for (int i = 0; i < NR; ++i) key[i] = bs[rl[i]];
-#pragma unroll
-        for (int i = 0; i < NR; ++i) {
-          const float bias =
-              __bfloat162float(__float2bfloat16_rn(acc[i >> 1][2 * (i & 1) + e]));
-          const uint32_t lb = float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(key[i]), bias));
-          key[i] = rl[i] < nv ? (bf16_order(lb) << 16) | (0xFFFFu - (uint32_t)rl[i]) : 0u;
-        }
-#pragma unroll
-        for (int w = 1; w < NR; w <<= 1)
-#pragma unroll
-          for (int i = 0; i + w < NR; i += 2 * w) key[i] = max_u32(key[i], key[i + w]);
-        kb[e] = 2 * t4 + e < a.B ? key[0] : 0u;
-      }
-      // the eight lanes of one t4 share requests 2 t4, 2 t4 + 1
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) kb[e] = max_u32(kb[e], __shfl_xor_sync(0xFFFFFFFFu, kb[e], o));
-      if (g == 0)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          if (2 * t4 + e < a.B) warp_key[warp][2 * t4 + e] = kb[e];
+      // greedy, no logits out: keys straight from the accumulators
+      if (a.B <= 2)
+        fast_keys<NST, 4>(acc, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
+      else if (a.B <= 4)
+        fast_keys<NST, 2>(acc, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
+      else
+        fast_keys<NST, 1>(acc, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
       trace_stamp(a, k, 2);
       trace_stamp(a, k, 3);
       __syncthreads();
@@ -399,7 +401,10 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
       } else {
         for (int sl = 0; sl < nslots; ++sl) mine = key_max(mine, group_best[lane][sl]);
       }
-      if (cta != a.skip_cta) st_relaxed_gpu_u64(a.sync.slot_at(parity, k, lane) + cta, tag | key50(mine));
+      if (cta != a.skip_cta) {
+        st_relaxed_gpu_u64(a.sync.slot_at(parity, k, lane) + cta, tag | key50(mine));
+        red_relaxed_gpu_add(a.sync.count_at(parity, k) + lane, 1u);   // a hint, see below
+      }
       if (mine != 0ull) {                          // the candidate's W1 row, into L2
         const uint16_t* row = a.W1 + (size_t)(0xFFFFFFFFu - (uint32_t)mine) * kRank;
 #pragma unroll
@@ -413,6 +418,21 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
       unsigned long long best = 0ull;
       int good = 1;
       uint32_t spins = 0;
+      // lane 0 first waits on the request's arrival count (one word: far less
+      // polling traffic than reading every slot); the count carries no
+      // ordering, the slots' tags decide, so the slots are then read (again
+      // if one has not landed yet)
+      if (lane == 0) {
+        const uint32_t* cp = a.sync.count_at(parity, k) + warp;
+        while (ld_relaxed_gpu_u32(cp) < (uint32_t)n_cta) {
+          if ((++spins & 63u) == 0u &&
+              (round_aborted(a.sync.hdr, round_s) ||
+               (int64_t)(globaltimer_ns() - t_step) > a.timeout_ns))
+            break;                     // the slot loop below reports it
+        }
+      }
+      __syncwarp();
+      spins = 0;
       while (true) {
         bool have = true;
         best = 0ull;
