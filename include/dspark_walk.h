@@ -90,7 +90,11 @@ struct dspark_walk_plan {
 #define DSPARK_KERNEL_BATCHED 2  /* rows streamed by TMA, tcgen05 with N = B (large B) */
 
 /*
- * dspark_walk_create -- prepare a walk over fixed weights.
+ * dspark_walk_create -- prepare a walk over fixed weights ("Keeping the Draft
+ * Walk on Chip", section "The idea: make the walk resident": the weights are
+ * laid out once so that each CTA can load its slice of W2 rows at the start
+ * of a round; section "B200: the bf16 table fits on chip" for the split of
+ * those rows over tensor memory, shared memory and registers).
  *
  *   W1        device, bf16 [V, r] row-major: the Markov embedding.  Referenced,
  *             not copied: keep it alive and unchanged until destroy.
@@ -103,6 +107,11 @@ struct dspark_walk_plan {
  *   max_gamma 1 <= max_gamma <= 64: longest walk any run will pass
  *   out       receives the handle (set to NULL on failure)
  *
+ * The handle holds W2 only in the layouts its runs can take under its current
+ * settings (the on-chip layout of the resident kernels, and the batched
+ * kernel's layout when max_B is above the resident batch); another layout is
+ * built from one it holds when set_kernel / set_cell / set_state_output first
+ * need it.  dspark_walk_get_plan reports the bytes held (weight_bytes).
  * Uses the current CUDA device; synchronises it once.  Errors: DSPARK_EINVAL,
  * DSPARK_EUNSUPPORTED, DSPARK_ENOMEM, DSPARK_ECUDA.
  */
@@ -113,6 +122,10 @@ int dspark_walk_create(const void *W1, const void *W2, int64_t V, int r, int max
  * dspark_walk_run -- one round: the whole gamma-step walk for B requests in
  * one launch on `stream` (asynchronous; capturable in a CUDA graph, and needs
  * no memset between replays: the rendezvous state alternates by round parity).
+ * Source: "Keeping the Draft Walk on Chip", section "The serial part of a
+ * parallel drafter" (the recurrence), section "The idea: make the walk
+ * resident" (one launch per round, the cross-CTA selection, per-request
+ * temperatures read on the device, logits written for the verifier).
  *
  *   base_logits  device, bf16 [B, gamma, V]: the parallel pass's logits
  *   anchor       device, int32 [B]: the last accepted token of each request
@@ -159,11 +172,18 @@ int dspark_walk_run_host(dspark_walk_t h, const void *base_logits_host,
 
 /*
  * dspark_walk_status -- wait for `stream`, then return and clear the status
- * word the device wrote during earlier runs (DSPARK_OK if none failed).
+ * word the device wrote during earlier runs (DSPARK_OK if none failed).  The
+ * pages define no error channel; device-detected errors (a bad anchor or
+ * temperature, a rendezvous timeout) set this word instead of trapping.
  */
 int dspark_walk_status(dspark_walk_t h, void *stream);
 
-/* dspark_walk_get_plan -- copy the placement chosen at create into *p. */
+/*
+ * dspark_walk_get_plan -- copy the placement chosen at create into *p (the
+ * per-CTA split of W2 rows over the on-chip tiers: "Keeping the Draft Walk on
+ * Chip", sections "B200: the bf16 table fits on chip" and "V = 248,320: 62% on
+ * chip, the rest streamed"), with the bytes of W2 layouts held now.
+ */
 int dspark_walk_get_plan(dspark_walk_t h, struct dspark_walk_plan *p);
 
 /*
@@ -332,7 +352,12 @@ int dspark_walk_unit_rates(double *out, int n_out, void *stream);
 /* dspark_walk_strerror -- a static description of a status code. */
 const char *dspark_walk_strerror(int code);
 
-/* dspark_walk_destroy -- free everything the handle owns (synchronises the device). */
+/*
+ * dspark_walk_destroy -- free everything the handle owns (the W2 layouts
+ * dspark_walk_create built, the rendezvous memory, the staging buffers);
+ * synchronises the device.  W1 and any M / X passed to set_cell stay the
+ * caller's.
+ */
 int dspark_walk_destroy(dspark_walk_t h);
 
 /*
@@ -351,12 +376,17 @@ int dspark_walk_destroy(dspark_walk_t h);
  *
  * The rendezvous slots live in one fixed ~17.5 KB block of device memory
  * built into the library (every GPU that loads the library keeps it until
- * the process exits).  The first call on a device looks up that block's
- * address, so make it before capturing a stream into a CUDA graph.  Each
- * call clears the block on `stream` before its launch; calls that could
- * overlap on the GPU (unordered streams) race on the block and must not be
- * made.  Device-detected errors (bad anchor or temperature, a rendezvous
- * timeout) are reported only as -1 in out_tokens.
+ * the process exits).  The block's address belongs to a CUDA context: every
+ * call looks it up in the caller's current context (cudaGetSymbolAddress, a
+ * lookup that allocates nothing) and makes sure the kernels it launches are
+ * loaded, so the entry point also works in a context created after
+ * cudaDeviceReset.  The first call in a context is where the driver loads
+ * those kernels (with lazy module loading that may allocate and synchronise):
+ * make it once before capturing a stream into a CUDA graph or entering code
+ * that must not allocate.  Each call clears the block on `stream` before its
+ * launch; calls that could overlap on the GPU (unordered streams) race on the
+ * block and must not be made.  Device-detected errors (bad anchor or
+ * temperature, a rendezvous timeout) are reported only as -1 in out_tokens.
  */
 int dspark_walk_run_noalloc(const void *W1, const void *W2, int64_t V, int r,
                             const void *base_logits, const int32_t *anchor,

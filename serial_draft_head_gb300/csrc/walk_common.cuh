@@ -530,7 +530,8 @@ __device__ __forceinline__ bool exchange(const WalkArgs& a, uint32_t round, int 
   if (threadIdx.x == 0) {
     int ok = 1;
     uint32_t* cnt = a.sync.count_at(parity, k);
-    __threadfence();
+    // the release is cumulative over the maxima the CTA barrier ordered
+    // before it (no separate fence)
     if (post) red_release_gpu_add(cnt, 1u);
     const uint32_t target = gridDim.x;
     const uint64_t t0 = globaltimer_ns();

@@ -12,10 +12,16 @@
 //
 // The block is a file-scope __device__ array, so every GPU that loads this
 // library holds it (kScratchBytes below, about 17.5 KB) until the process exits.
-// Host code cannot use the array's name as a device address; the first call
-// on each device looks the address up with cudaGetSymbolAddress (with that
-// device current) and remembers it.  Make that first call before capturing
-// any stream into a CUDA graph.
+// A __device__ variable's address belongs to a CUDA context, and host code
+// cannot use the array's name as a device address.  So every call looks the
+// address up in the caller's current context with cudaGetSymbolAddress (a
+// lookup, no allocation), and makes sure the streamed kernels it may launch
+// are loaded (cudaFuncGetAttributes): the entry point follows the caller's
+// context, including a context created anew after cudaDeviceReset.  The first
+// call in a context is where the driver loads these kernels (with lazy module
+// loading, the default, that can allocate and synchronise), so make it once
+// before capturing any stream into a CUDA graph or entering code that must
+// not allocate.
 //
 // All calls share the one block: each call clears it on its stream before
 // launching, so calls that overlap on the GPU (different streams without an
@@ -47,18 +53,17 @@ static __device__ __align__(256) unsigned char g_walk_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 
-struct DeviceSetup {
+struct DeviceCheck {
   std::once_flag once;
   int rc = DSPARK_OK;
-  void* scratch = nullptr;
   int sm_count = 0;
 };
 
-DeviceSetup g_setup[kMaxDevices];
+DeviceCheck g_check[kMaxDevices];
 
-// Once per device, with that device current: find the scratch block's device
-// address and check the device.  Allocates nothing.
-void setup_device(DeviceSetup* s, int dev) {
+// Once per device: the device is an sm_103 part that can run cooperative
+// kernels (properties of the device, not of a context).
+void check_device(DeviceCheck* s, int dev) {
   int major = 0, minor = 0, sms = 0, coop = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -71,14 +76,27 @@ void setup_device(DeviceSetup* s, int dev) {
     s->rc = DSPARK_EUNSUPPORTED;
     return;
   }
-  void* ptr = nullptr;
-  if (cudaGetSymbolAddress(&ptr, g_walk_scratch) != cudaSuccess || ptr == nullptr) {
-    s->rc = DSPARK_ECUDA;
-    return;
-  }
-  s->scratch = ptr;
   s->sm_count = sms;
   s->rc = DSPARK_OK;
+}
+
+// In the current context: the scratch block's device address, and the four
+// streamed-kernel instantiations loaded.  Allocates nothing itself.
+int resolve_in_context(void** scratch) {
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_walk_scratch) != cudaSuccess || ptr == nullptr) {
+    cudaGetLastError();
+    return DSPARK_ECUDA;
+  }
+  for (int b = 1; b <= 8; b *= 2) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, stream_kernel_for(b)) != cudaSuccess) {
+      cudaGetLastError();
+      return DSPARK_ECUDA;
+    }
+  }
+  *scratch = ptr;
+  return DSPARK_OK;
 }
 
 }  // namespace
@@ -98,9 +116,12 @@ extern "C" int dspark_walk_run_noalloc(const void* W1, const void* W2, int64_t V
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ECUDA;
   if (dev < 0 || dev >= kMaxDevices) return DSPARK_EUNSUPPORTED;
-  DeviceSetup* s = &g_setup[dev];
-  std::call_once(s->once, setup_device, s, dev);
+  DeviceCheck* s = &g_check[dev];
+  std::call_once(s->once, check_device, s, dev);
   if (s->rc != DSPARK_OK) return s->rc;
+  void* scratch = nullptr;
+  const int rc = resolve_in_context(&scratch);
+  if (rc != DSPARK_OK) return rc;
 
   // shard plan: at least 32 rows per CTA, at most one CTA per SM
   int64_t n = (V + 31) / 32;
@@ -111,9 +132,9 @@ extern "C" int dspark_walk_run_noalloc(const void* W1, const void* W2, int64_t V
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the previous call's state is still in the block: start from zero
-  if (cudaMemsetAsync(s->scratch, 0, kScratchBytes, st) != cudaSuccess) return DSPARK_ECUDA;
+  if (cudaMemsetAsync(scratch, 0, kScratchBytes, st) != cudaSuccess) return DSPARK_ECUDA;
 
-  uint8_t* base = static_cast<uint8_t*>(s->scratch);
+  uint8_t* base = static_cast<uint8_t*>(scratch);
   WalkArgs a{};
   a.W1 = static_cast<const uint16_t*>(W1);
   a.W2 = static_cast<const uint16_t*>(W2);

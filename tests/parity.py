@@ -238,6 +238,34 @@ def check(inputs: "synth.WalkInputs", gpu_tokens, gpu_logits=None, requests=None
     return rep
 
 
+def check_all_tokens(inputs: "synth.WalkInputs", gpu_tokens, nthreads=0, O=None, sampler=0):
+    """Every request's tokens, teacher-forced, at any size: one tokens-only
+    oracle walk of the whole batch (the oracle fed the GPU's previous token at
+    every step), then the full rule of `check` (near-ties from the oracle's
+    logits or scores) for the requests where some step differs.  Returns a
+    Report whose steps_checked is B * gamma."""
+    O = O or oracle.default()
+    rep = Report()
+    B, gamma, V = inputs.base.shape
+    toks = np.asarray(gpu_tokens).astype(np.int32)
+    bad = [b for b in range(B) if np.any(toks[b] < 0) or np.any(toks[b] >= V)]
+    for b in bad:
+        rep.failures.append(("token out of range", b, toks[b].tolist()))
+    if bad:
+        return rep
+    ot = O.walk(synth.bits(inputs.W1), synth.bits(inputs.W2), synth.bits(inputs.base),
+                inputs.anchor.numpy(), inputs.temperature.numpy(), inputs.seed, forced=toks,
+                want_logits=False, nthreads=nthreads, sampler=sampler)[0]
+    differ = [b for b in range(B) if not np.array_equal(ot[b], toks[b])]
+    same = B - len(differ)
+    rep.steps_checked += same * gamma
+    rep.steps_exact += same * gamma
+    if differ:
+        check(inputs, toks, None, requests=differ, nthreads=nthreads, O=O, report=rep,
+              sampler=sampler)
+    return rep
+
+
 def _oracle_request(O, W1, W2, base_all, inputs, b, toks, nthreads, sampler=0):
     """Oracle walk of request b alone (at request index b), teacher-forced."""
     T = float(inputs.temperature[b])

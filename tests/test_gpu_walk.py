@@ -1,8 +1,10 @@
 """Parity of the CUDA walk with the CPU oracle, through the C ABI (GPU only).
 
-Small shapes are compared on every logit and every step; the five full-size
-workloads are compared on sampled requests (the oracle replays one request
-at its own request index), in the launch configuration the benchmark times.
+Small shapes are compared on every logit and every step.  The five full-size
+workloads, in the launch configuration the benchmark times, are compared on
+every logit of sampled requests (the oracle replays one request at its own
+request index) and on every token of every request (one teacher-forced,
+tokens-only oracle walk of the whole batch).
 """
 import dataclasses
 import numpy as np
@@ -188,6 +190,8 @@ def test_long_block(walkmod, B, want_logits):
     assert st == 0
     rep = parity.check(x, toks, lg, requests=_sample_requests(B, (0.0,)))
     assert rep.ok(), rep
+    full = parity.check_all_tokens(x, toks)
+    assert full.ok() and full.steps_checked == B * x.gamma, full
 
 
 @pytest.mark.parametrize("B", [1, 8])
@@ -201,6 +205,8 @@ def test_partial(walkmod, B, want_logits):
     assert st == 0
     rep = parity.check(x, toks, lg, requests=_sample_requests(B, (0.0,)))
     assert rep.ok(), rep
+    full = parity.check_all_tokens(x, toks)
+    assert full.ok() and full.steps_checked == B * x.gamma, full
 
 
 @pytest.mark.parametrize("B", [1, 16, 64, 128, 253])
@@ -211,6 +217,8 @@ def test_sampled(walkmod, B):
     assert st == 0
     rep = parity.check(x, toks, lg, requests=_sample_requests(B, (0.0, 0.6, 1.0)))
     assert rep.ok(), rep
+    full = parity.check_all_tokens(x, toks)
+    assert full.ok() and full.steps_checked == B * x.gamma, full
 
 
 def test_sampled_full_batch_zero_projection_property(walkmod):
@@ -569,6 +577,8 @@ def test_group_sampler_sampled_config(walkmod, B):
     assert st == 0
     rep = parity.check(x, toks, lg, requests=_sample_requests(B, (0.0, 0.6, 1.0)), sampler=1)
     assert rep.ok(), rep
+    full = parity.check_all_tokens(x, toks, sampler=1)
+    assert full.ok() and full.steps_checked == B * x.gamma, full
 
 
 def test_group_sampler_not_on_the_streamed_kernel(walkmod):

@@ -176,3 +176,23 @@ def test_gru_accepts_the_oracle_and_rejects_a_wrong_state():
     st2[1, 2, i] = st2[1, 2, i] + 1
     rep = parity.check(x, t, None, cell=3, M=M, X=X, gpu_states=st2)
     assert not rep.ok() and any(f[0] == "state" for f in rep.failures), rep
+
+
+def test_every_request_check_accepts_the_oracle_and_rejects_planted_tokens():
+    """check_all_tokens (the tokens-only, whole-batch check used at full size)
+    passes the oracle's own walk, counts every step, and catches a wrong token
+    in any request, greedy or sampled."""
+    x = synth.make_custom(V=700, gamma=5, B=9, seed=25, temperatures=(0.0, 0.6, 1.0),
+                          noise_seed=11)
+    t, _, sc = _walk(x, want_logits=False, want_scores=True)
+    rep = parity.check_all_tokens(x, t)
+    assert rep.ok() and rep.steps_checked == 9 * 5 and rep.steps_exact == 9 * 5, rep
+    for b, k in ((0, 3), (4, 1), (8, 4)):          # greedy, sampled at 0.6, sampled at 1.0
+        t2 = t.copy()
+        t2[b, k] = int(np.argmin(sc[b, k])) if x.temperature[b] > 0 else \
+            int(np.argmin(parity.bf16_vals(_walk(x)[1][b, k])))
+        rep = parity.check_all_tokens(x, t2)
+        assert not rep.ok() and rep.failures[0][1] == b and rep.failures[0][2] == k, rep
+    t3 = t.copy()
+    t3[2, 0] = x.base.shape[2]                     # out of range
+    assert parity.check_all_tokens(x, t3).failures[0][0] == "token out of range"
