@@ -58,12 +58,13 @@ constexpr int kMrRfWords = kMrWarps * 16 * 32 * 4;    // 64 KB
 constexpr int kMbarSmem = 0;
 constexpr unsigned long long kKey50Mask = (1ull << 50) - 1ull;
 
-// Local row of the first row of strip st of warp w (st: 0 register, 1..4
-// tensor memory, 5..7 shared, the j-th shared strip of the warp being strip
-// w + 8 j of the shared tier).
+// Local row of the first row of strip st of warp w: st 0..3 tensor memory,
+// 4 the register strip, 5.. shared memory (the j-th shared strip of the warp
+// being strip w + 8 j of the shared tier).  Increasing st, increasing rows:
+// the fused epilogue's running argmax relies on it for its ties.
 __device__ __forceinline__ int strip_row0(int st, int w) {
-  if (st == 0) return kTmRows + 16 * w;
-  if (st <= kTmStrips) return 16 * (kTmStrips * w + st - 1);
+  if (st < kTmStrips) return 16 * (kTmStrips * w + st);
+  if (st == kTmStrips) return kTmRows + 16 * w;
   return kMrFixedRows + 16 * (w + kMrWarps * (st - 1 - kTmStrips));
 }
 
@@ -76,6 +77,32 @@ __device__ __forceinline__ uint32_t bf16_order(uint32_t x) {
 
 __device__ __forceinline__ uint32_t max_u32(uint32_t a, uint32_t b) { return a > b ? a : b; }
 
+// Bits of a bf16 pair (two logits), as __nv_bfloat162.
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t x) {
+  return *reinterpret_cast<const __nv_bfloat162*>(&x);
+}
+__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 x) {
+  return *reinterpret_cast<const uint32_t*>(&x);
+}
+
+// Running argmax of two independent streams of bf16 logits packed in one
+// word (each half its own stream): where a half of `l` is greater than the
+// same half of `best`, it replaces it and its row (a half of `rows`) replaces
+// the kept row.  Rows come in increasing order, so the strict comparison
+// keeps the smallest row among equal logits; -0 and +0 compare equal.
+__device__ __forceinline__ void argmax2(uint32_t l, uint32_t rows, uint32_t& best,
+                                        uint32_t& best_rows) {
+  const uint32_t m = __hgt2_mask(as_bf2(l), as_bf2(best));
+  best = (l & m) | (best & ~m);
+  best_rows = (rows & m) | (best_rows & ~m);
+}
+
+// {bf16 order bits : 16, inverted local row : 16} of a bf16 logit and its
+// row (-0 folded onto +0).
+__device__ __forceinline__ uint32_t key32(uint32_t lb, uint32_t row) {
+  return (bf16_order(lb & 0xFFFFu) << 16) | (0xFFFFu - (row & 0xFFFFu));
+}
+
 // The fused epilogue of a greedy round without logits out, for one warp:
 // each request's best key over the warp's NST strips, 32-bit {bf16 logit
 // order bits : 16, inverted local row : 16}, into wkey[b].
@@ -83,15 +110,20 @@ __device__ __forceinline__ uint32_t max_u32(uint32_t a, uint32_t b) { return a >
 // of every strip.  With B <= 8 / G requests only the lanes t4 < 4 / G hold
 // results, so they are first spread over the G lane groups: lane (g, t4)
 // takes strips s = part (mod G), part = t4 / (4 / G), from lane (g, t4 mod
-// (4 / G)).  Every lane then scores NST / G strips x 4 values: base values
-// read first, then independent roundings and keys, then a max over the
-// lanes that hold the same request.
+// (4 / G)).  Every lane then scores NST / G strips, two logits per
+// instruction: the two bias roundings in one bf16x2 conversion, the base add
+// as one correctly rounded bf16x2 addition (for bf16 operands the same value
+// as bf16(fp32 sum), whose fp32 sum is exact whenever it could matter), and a
+// packed running argmax (argmax2).  The pairs are the two requests of a row,
+// or, with one request, rows g and g + 8.  Rows past the shard's end score
+// -inf.  Then a max over the lanes that hold the same request.
 template <int NST, int G>
 __device__ __forceinline__ void fast_keys(const float (&acc)[NST][4], const uint16_t* base_s,
                                           int R, int B, int nv, int warp, int lane,
                                           uint32_t* wkey) {
   constexpr int NJ = (NST + G - 1) / G;          // strips per lane
   constexpr int SRC = 4 / G;                     // lanes per row group holding results
+  constexpr uint32_t kNegInf2 = 0xFF80FF80u;
   const int g = lane >> 2, t4 = lane & 3;
   const int src = t4 % SRC, part = t4 / SRC;
   float v[NJ][4];
@@ -102,40 +134,58 @@ __device__ __forceinline__ void fast_keys(const float (&acc)[NST][4], const uint
       const float x = G > 1 ? __shfl_sync(0xFFFFFFFFu, acc[s][e], (lane & ~3) | src) : acc[s][e];
       if (G == 1 || s % G == part) v[s / G][e] = x;
     }
-  int rr[NJ][2];
+  int rr[NJ];
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     const int s = part + G * j;
-    const int r0 = s < NST ? strip_row0(s, warp) + g : 0;
-    rr[j][0] = r0;
-    rr[j][1] = r0 + 8;
+    rr[j] = s < NST ? strip_row0(s, warp) + g : 0;
   }
-  uint32_t kb[2] = {0u, 0u};
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {                  // requests 2 src and 2 src + 1
-    const int b = 2 * src + q;
-    if (q == 1 && B < 2) continue;               // uniform
-    const uint16_t* bs = base_s + (size_t)(b < B ? b : 0) * R;
-    uint32_t key[NJ][2];
+  uint32_t best = kNegInf2, brow = 0xFFFFFFFFu;
+  if (B == 1) {
+    // pairs = rows (g, g + 8) of request 0
+    uint32_t bb[NJ];
 #pragma unroll
     for (int j = 0; j < NJ; ++j)
+      bb[j] = (uint32_t)base_s[rr[j]] | ((uint32_t)base_s[rr[j] + 8] << 16);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) key[j][h] = bs[rr[j][h]];
+    for (int j = 0; j < NJ; ++j) {
+      const uint32_t bias = bf2_bits(__floats2bfloat162_rn(v[j][0], v[j][2]));
+      uint32_t l = bf2_bits(__hadd2(as_bf2(bb[j]), as_bf2(bias)));
+      const bool ok = part + G * j < NST;
+      const uint32_t lo_ok = ok && rr[j] < nv ? 0u : 0x0000FFFFu;
+      const uint32_t hi_ok = ok && rr[j] + 8 < nv ? 0u : 0xFFFF0000u;
+      l = (l & ~(lo_ok | hi_ok)) | (kNegInf2 & (lo_ok | hi_ok));
+      argmax2(l, (uint32_t)rr[j] | ((uint32_t)(rr[j] + 8) << 16), best, brow);
+    }
+    const uint32_t k0 = key32(best, brow), k1 = key32(best >> 16, brow >> 16);
+    uint32_t kb = max_u32(k0, k1);
+    if (best == kNegInf2 && k0 == k1) kb = 0u;    // no valid row at all
 #pragma unroll
-    for (int j = 0; j < NJ; ++j)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float bias = __bfloat162float(__float2bfloat16_rn(v[j][2 * h + q]));
-        const uint32_t lb =
-            float_to_bf16_bits_rn(__fadd_rn(bf16_bits_to_float(key[j][h]), bias));
-        const bool valid = part + G * j < NST && rr[j][h] < nv;
-        key[j][h] = valid ? (bf16_order(lb) << 16) | (0xFFFFu - (uint32_t)rr[j][h]) : 0u;
-      }
-    uint32_t m = 0u;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) m = max_u32(m, max_u32(key[j][0], key[j][1]));
-    kb[q] = b < B ? m : 0u;
+    for (int o = 1; o < 32; o <<= 1) kb = max_u32(kb, __shfl_xor_sync(0xFFFFFFFFu, kb, o));
+    if (lane == 0) wkey[0] = kb;
+    return;
   }
+  // pairs = requests (2 src, 2 src + 1) of one row
+  const int b0 = 2 * src < B ? 2 * src : 0, b1 = 2 * src + 1 < B ? 2 * src + 1 : 0;
+  const uint16_t* bs0 = base_s + (size_t)b0 * R;
+  const uint16_t* bs1 = base_s + (size_t)b1 * R;
+  uint32_t bb[NJ][2];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j)
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      bb[j][h] = (uint32_t)bs0[rr[j] + 8 * h] | ((uint32_t)bs1[rr[j] + 8 * h] << 16);
+#pragma unroll
+  for (int j = 0; j < NJ; ++j)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t bias = bf2_bits(__floats2bfloat162_rn(v[j][2 * h], v[j][2 * h + 1]));
+      uint32_t l = bf2_bits(__hadd2(as_bf2(bb[j][h]), as_bf2(bias)));
+      const int row = rr[j] + 8 * h;
+      if (!(part + G * j < NST && row < nv)) l = kNegInf2;
+      argmax2(l, (uint32_t)row * 0x10001u, best, brow);
+    }
+  uint32_t kb[2] = {key32(best, brow), key32(best >> 16, brow >> 16)};
   // lanes with the same src hold the same two requests: reduce over g and part
 #pragma unroll
   for (int o = SRC; o < 32; o <<= 1)
@@ -147,8 +197,6 @@ __device__ __forceinline__ void fast_keys(const float (&acc)[NST][4], const uint
       if (2 * src + q < B) wkey[2 * src + q] = kb[q];
 }
 
-// NS: shared strips per warp (0 .. 3; every warp the same), so the shard has
-// R = 640 + 128 NS rows and each warp NST = 5 + NS accumulation chains.
 template <int NS>
 __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const ResidentArgs ra) {
   constexpr int NST = 1 + kTmStrips + NS;
@@ -310,7 +358,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
     trace_stamp(a, k, 0);
 
     // (1) projection: 16 k-tiles of up to 8 independent mma.sync chains (the
-    // register strip, the four tensor-memory strips, the shared strips); the
+    // four tensor-memory strips, the register strip, the shared strips); the
     // tensor-memory fragments of k-tile pair p + 1 load while pair p computes
     float acc[NST][4];
 #pragma unroll
@@ -337,12 +385,12 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
             b0 = *reinterpret_cast<const uint32_t*>(U + (4 * kt) * 128 + lane * 4);
             b1 = *reinterpret_cast<const uint32_t*>(U + (4 * kt + 2) * 128 + lane * 4);
           }
-          ptx::mma_16816(acc[0], wr[kt][0], wr[kt][1], wr[kt][2], wr[kt][3], b0, b1);
 #pragma unroll
           for (int s = 0; s < kTmStrips; ++s) {
             const uint32_t* f = &fr[p & 1][16 * e + 4 * s];
-            ptx::mma_16816(acc[1 + s], f[0], f[1], f[2], f[3], b0, b1);
+            ptx::mma_16816(acc[s], f[0], f[1], f[2], f[3], b0, b1);
           }
+          ptx::mma_16816(acc[kTmStrips], wr[kt][0], wr[kt][1], wr[kt][2], wr[kt][3], b0, b1);
 #pragma unroll
           for (int j = 0; j < NS; ++j)
               ptx::mma_16816(acc[1 + kTmStrips + j], af[j][0], af[j][1], af[j][2], af[j][3], b0,

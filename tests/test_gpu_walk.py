@@ -446,6 +446,39 @@ def test_host_side_errors(walkmod):
     assert e.value.code == walkmod.EUNSUPPORTED
 
 
+@pytest.mark.parametrize("B", [1, 2, 5, 8, 12])
+def test_exact_ties_go_to_the_smallest_token(walkmod, B):
+    """W2 = 0, so every logit is its base value.  Each step plants the same
+    maximum at rows of one lane in several tiers of one CTA's shard (tensor
+    memory, a later tensor-memory strip's second row half, the register
+    strip, a shared strip) and in a later CTA; the smallest token id must win,
+    exactly (the near-tie rule would accept any of them).  Greedy rounds
+    without logits take the fused epilogue."""
+    V, gamma = 151936, 8
+    x = synth.make_custom(V=V, gamma=gamma, B=B, seed=70 + B)
+    g = torch.Generator().manual_seed(700 + B)
+    base = (torch.rand(B, gamma, V, generator=g) * -7.0 - 1.0).to(torch.bfloat16)
+    w = walkmod.Walk(x.W1.cuda(), torch.zeros_like(x.W2).cuda(), B, gamma)
+    plan = w.plan()
+    R, n = plan["rows_per_cta"], plan["n_cta"]
+    want = np.zeros((B, gamma), dtype=np.int64)
+    for b in range(B):
+        for k in range(gamma):
+            c = (7 * k + 13 * b) % (n - 3)
+            wp, gl = (k + b) % 8, (3 * k + b) % 8
+            local = [640 + 16 * (wp + 8) + gl, 64 * wp + 32 + gl + 8, 512 + 16 * wp + gl,
+                     64 * wp + gl]
+            toks = [c * R + r for r in local if r < R] + [(c + 3) * R + 64 * wp + gl]
+            toks = [v for v in toks if v < V]
+            base[b, k, toks] = 2.0
+            want[b, k] = min(toks)
+    x.base = base
+    st, toks, _ = gpu_run(w, x, want_logits=False)
+    assert st == 0
+    assert np.array_equal(toks, want), (toks, want)
+    w.close()
+
+
 @pytest.mark.parametrize("kernel", ["planned", "stream", "batched"])
 @pytest.mark.parametrize("V", [1, 2, 7])
 def test_degenerate_vocabularies(walkmod, V, kernel):
