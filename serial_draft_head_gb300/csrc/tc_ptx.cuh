@@ -272,6 +272,17 @@ __device__ __forceinline__ void tmem_wait_ld32(uint32_t (&v)[32]) {
       : "memory");
 }
 
+// tcgen05.wait::ld naming the 16 registers a 16-column tcgen05.ld writes.
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+        "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]),
+        "+r"(v[13]), "+r"(v[14]), "+r"(v[15])
+      :
+      : "memory");
+}
+
 // Shared-memory matrix descriptor (sm_100 format): start address, leading
 // (K-direction) and stride (M/N-direction) byte offsets between 8x16-byte
 // core matrices, version 1, no swizzle.

@@ -154,10 +154,17 @@ bool plan_mma(dspark_walk* h) {
   if (h->V >= (1 << 18)) return false;          // the 18-bit id field of the slot word
   const int mb = h->max_B < mma_resident_max_batch() ? h->max_B : mma_resident_max_batch();
   const int fixed = mma_resident_fixed_rows();
-  int64_t R = (h->V + h->sm_count - 1) / h->sm_count;
-  R = (R + 127) / 128 * 128;        // every warp holds the same number of shared strips
-  if (R < fixed) R = fixed;
+  int64_t R0 = (h->V + h->sm_count - 1) / h->sm_count;
+  R0 = (R0 + 15) / 16 * 16;
+  if (R0 < fixed) R0 = fixed;
+  // every warp runs the same number NS of shared strips: R = 640 + 128 NS, or
+  // one strip less when the batch's base rows would not fit otherwise (the
+  // last warp's third strip then only pads, over the U buffer that follows)
+  int64_t R = fixed + (R0 - fixed + 127) / 128 * 128;
   if (R > mma_resident_max_rows()) return false;
+  if (mma_resident_smem_bytes((int)((R - fixed) / 16), mb, (int)R) > kSmemBudget && R > fixed &&
+      R - 16 >= R0)
+    R -= 16;
   const int S = (int)((R - fixed) / 16);
   const size_t smem = mma_resident_smem_bytes(S, mb, (int)R);
   if (smem > kSmemBudget) return false;
@@ -401,7 +408,7 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
     const uintptr_t bp = reinterpret_cast<uintptr_t>(base);
     ra.base_mode = (h->V % 8 == 0 && (bp & 15u) == 0) ? 16
                    : (h->V % 2 == 0 && (bp & 3u) == 0) ? 4 : 2;
-    const void* rfn = mma ? mma_resident_kernel(h->mr_S)
+    const void* rfn = mma ? mma_resident_kernel(h->mr_S, B <= 8 ? 1 : 2)
                           : resident_kernel_for(h->res_RS, h->res_NT, cell_run(h));
     void* rargs[] = {&ra};
     CUDA_TRY(cudaLaunchCooperativeKernel(rfn, dim3(mma ? h->mr_n_cta : h->res_n_cta),
@@ -542,11 +549,13 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
     if (rc == DSPARK_OK && h->mr_ok) {
       int per_sm = 0;
       for (int s = 0; s <= 24 && e == cudaSuccess; s += 8)
-        e = cudaFuncSetAttribute(mma_resident_kernel(s),
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+        for (int nt = 1; nt <= 2 && e == cudaSuccess; ++nt)
+          e = cudaFuncSetAttribute(mma_resident_kernel(s, nt),
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
       if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mma_resident_kernel(h->mr_S),
-                                                          resident_threads(), h->mr_smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, mma_resident_kernel(h->mr_S, h->mr_max_B > 8 ? 2 : 1), resident_threads(),
+            h->mr_smem);
       if (e != cudaSuccess || per_sm != 1) {
         cudaGetLastError();
         h->mr_ok = false;

@@ -41,7 +41,7 @@ struct SyncHeader {
   uint32_t abort_round;  // round + 1 of the last round a CTA gave up on
   uint32_t pad[5];
 };
-constexpr int kCountStride = 8;  // uint32 per count slot (32 bytes)
+constexpr int kCountStride = 16;  // uint32 per count slot (64 bytes: one per request <= 16)
 
 struct SyncView {
   SyncHeader* hdr;

@@ -34,7 +34,7 @@ int mma_resident_max_rows();
 int mma_resident_max_batch();
 int64_t mma_resident_words_per_cta(int S);
 size_t mma_resident_smem_bytes(int S, int max_B, int R);
-const void* mma_resident_kernel(int S);   // S: shared strips per CTA, a multiple of 8
+const void* mma_resident_kernel(int S, int NT);   // S shared strips, NT n-tiles (B <= 8 NT)
 cudaError_t mma_resident_repack(void* rowmajor, void* packed, int64_t V, int R, int S, int n_cta,
                                 bool inverse, cudaStream_t stream);
 

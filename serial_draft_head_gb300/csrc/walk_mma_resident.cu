@@ -51,7 +51,7 @@ constexpr int kRfRows = kMrWarps * 16;                // 128
 constexpr int kMrFixedRows = kTmRows + kRfRows;       // 640
 constexpr int kMrSmax = 3;                            // shared strips per warp, at most
 constexpr int kMrMaxRows = kMrFixedRows + kMrSmax * kMrWarps * 16;   // 1024
-constexpr int kMrMaxB = 8;
+constexpr int kMrMaxB = 16;
 constexpr int kTmWordsPerWarp = 32 * 256;             // 32 lanes x 256 columns
 constexpr int kTmWords = kMrWarps * kTmWordsPerWarp;  // 256 KB
 constexpr int kMrRfWords = kMrWarps * 16 * 32 * 4;    // 64 KB
@@ -117,36 +117,42 @@ __device__ __forceinline__ uint32_t key32(uint32_t lb, uint32_t row) {
 // packed running argmax (argmax2).  The pairs are the two requests of a row,
 // or, with one request, rows g and g + 8.  Rows past the shard's end score
 // -inf.  Then a max over the lanes that hold the same request.
-template <int NST, int G>
-__device__ __forceinline__ void fast_keys(const float (&acc)[NST][4], const uint16_t* base_s,
-                                          int R, int B, int nv, int warp, int lane,
-                                          uint32_t* wkey) {
+template <int NST, int G, int NT>
+__device__ __forceinline__ void fast_keys(const float (&accs)[NST][NT][4], int nt,
+                                          const uint16_t* base_s, int R, int B, int nv, int warp,
+                                          int lane, uint32_t* wkey) {
   constexpr int NJ = (NST + G - 1) / G;          // strips per lane
   constexpr int SRC = 4 / G;                     // lanes per row group holding results
   constexpr uint32_t kNegInf2 = 0xFF80FF80u;
   const int g = lane >> 2, t4 = lane & 3;
   const int src = t4 % SRC, part = t4 / SRC;
+  const int bq = 8 * nt;                         // requests of this n-tile: bq + column
+  B -= bq;
+  wkey += bq;
   float v[NJ][4];
 #pragma unroll
   for (int s = 0; s < NST; ++s)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float x = G > 1 ? __shfl_sync(0xFFFFFFFFu, acc[s][e], (lane & ~3) | src) : acc[s][e];
+      const float a_ = accs[s][nt][e];
+      const float x = G > 1 ? __shfl_sync(0xFFFFFFFFu, a_, (lane & ~3) | src) : a_;
       if (G == 1 || s % G == part) v[s / G][e] = x;
     }
-  int rr[NJ];
+  int rr[NJ], rl[NJ][2];              // rows; the rows the base loads read (kept below R)
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     const int s = part + G * j;
     rr[j] = s < NST ? strip_row0(s, warp) + g : 0;
+    rl[j][0] = rr[j] < R ? rr[j] : R - 1;            // a padding strip's rows lie past R
+    rl[j][1] = rr[j] + 8 < R ? rr[j] + 8 : R - 1;
   }
   uint32_t best = kNegInf2, brow = 0xFFFFFFFFu;
-  if (B == 1) {
+  if (G == 4 && B == 1) {
     // pairs = rows (g, g + 8) of request 0
     uint32_t bb[NJ];
 #pragma unroll
     for (int j = 0; j < NJ; ++j)
-      bb[j] = (uint32_t)base_s[rr[j]] | ((uint32_t)base_s[rr[j] + 8] << 16);
+      bb[j] = (uint32_t)base_s[rl[j][0]] | ((uint32_t)base_s[rl[j][1]] << 16);
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
       const uint32_t bias = bf2_bits(__floats2bfloat162_rn(v[j][0], v[j][2]));
@@ -167,14 +173,14 @@ __device__ __forceinline__ void fast_keys(const float (&acc)[NST][4], const uint
   }
   // pairs = requests (2 src, 2 src + 1) of one row
   const int b0 = 2 * src < B ? 2 * src : 0, b1 = 2 * src + 1 < B ? 2 * src + 1 : 0;
-  const uint16_t* bs0 = base_s + (size_t)b0 * R;
-  const uint16_t* bs1 = base_s + (size_t)b1 * R;
+  const uint16_t* bs0 = base_s + (size_t)(bq + b0) * R;
+  const uint16_t* bs1 = base_s + (size_t)(bq + b1) * R;
   uint32_t bb[NJ][2];
 #pragma unroll
   for (int j = 0; j < NJ; ++j)
 #pragma unroll
     for (int h = 0; h < 2; ++h)
-      bb[j][h] = (uint32_t)bs0[rr[j] + 8 * h] | ((uint32_t)bs1[rr[j] + 8 * h] << 16);
+      bb[j][h] = (uint32_t)bs0[rl[j][h]] | ((uint32_t)bs1[rl[j][h]] << 16);
 #pragma unroll
   for (int j = 0; j < NJ; ++j)
 #pragma unroll
@@ -197,7 +203,7 @@ __device__ __forceinline__ void fast_keys(const float (&acc)[NST][4], const uint
       if (2 * src + q < B) wkey[2 * src + q] = kb[q];
 }
 
-template <int NS>
+template <int NS, int NT>
 __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const ResidentArgs ra) {
   constexpr int NST = 1 + kTmStrips + NS;
   const WalkArgs& a = ra.w;
@@ -350,7 +356,6 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
   const uint32_t w2_addr = ptx::smem_u32(smem_w2);
   const uint32_t blk0 =
       w2_addr + (uint32_t)warp * kSmemStripBytes + (lane >> 3) * 128 + (lane & 7) * 16;
-  const bool bcol = g < a.B;           // this lane's B-fragment column is a request
   bool ok = abort_s == 0;
   int k = 0;
   for (; k < a.gamma && ok; ++k) {
@@ -360,43 +365,65 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
     // (1) projection: 16 k-tiles of up to 8 independent mma.sync chains (the
     // four tensor-memory strips, the register strip, the shared strips); the
     // tensor-memory fragments of k-tile pair p + 1 load while pair p computes
-    float acc[NST][4];
+    float acc[NST][NT][4];
 #pragma unroll
     for (int s = 0; s < NST; ++s)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[s][e] = 0.0f;
-    {
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[s][nt][e] = 0.0f;
+    // the k-tile's A fragments of every strip against both n-tiles' B
+    auto ktile = [&](int kt, const uint32_t* f) {     // f: the 4 strips' tensor-memory words
+      uint32_t af[NS > 0 ? NS : 1][4];
+#pragma unroll
+      for (int j = 0; j < NS; ++j)
+        ptx::ldmatrix_x4(blk0 + (uint32_t)(j * kResWarps) * kSmemStripBytes + kt * 512, af[j][0],
+                         af[j][1], af[j][2], af[j][3]);
+      uint32_t bf[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        bf[nt][0] = bf[nt][1] = 0u;
+        if (8 * nt + g < a.B) {            // this lane's B-fragment column is a request
+          bf[nt][0] = *reinterpret_cast<const uint32_t*>(U + (4 * kt + nt) * 128 + lane * 4);
+          bf[nt][1] = *reinterpret_cast<const uint32_t*>(U + (4 * kt + 2 + nt) * 128 + lane * 4);
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int s = 0; s < kTmStrips; ++s)
+          ptx::mma_16816(acc[s][nt], f[4 * s], f[4 * s + 1], f[4 * s + 2], f[4 * s + 3],
+                         bf[nt][0], bf[nt][1]);
+        ptx::mma_16816(acc[kTmStrips][nt], wr[kt][0], wr[kt][1], wr[kt][2], wr[kt][3],
+                       bf[nt][0], bf[nt][1]);
+#pragma unroll
+        for (int j = 0; j < NS; ++j)
+          ptx::mma_16816(acc[1 + kTmStrips + j][nt], af[j][0], af[j][1], af[j][2], af[j][3],
+                         bf[nt][0], bf[nt][1]);
+      }
+    };
+    if constexpr (NT == 1) {
+      // one 32-column load per k-tile pair, one pair ahead
       uint32_t fr[2][32];
       ptx::tmem_ld32(tm_addr, fr[0]);
       ptx::tmem_wait_ld32(fr[0]);
 #pragma unroll
       for (int p = 0; p < 8; ++p) {
         if (p + 1 < 8) ptx::tmem_ld32(tm_addr + 32 * (p + 1), fr[(p + 1) & 1]);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int kt = 2 * p + e;
-          uint32_t af[NS > 0 ? NS : 1][4];
-#pragma unroll
-          for (int j = 0; j < NS; ++j)
-              ptx::ldmatrix_x4(blk0 + (uint32_t)(j * kResWarps) * kSmemStripBytes + kt * 512,
-                               af[j][0], af[j][1], af[j][2], af[j][3]);
-          uint32_t b0 = 0u, b1 = 0u;
-          if (bcol) {
-            b0 = *reinterpret_cast<const uint32_t*>(U + (4 * kt) * 128 + lane * 4);
-            b1 = *reinterpret_cast<const uint32_t*>(U + (4 * kt + 2) * 128 + lane * 4);
-          }
-#pragma unroll
-          for (int s = 0; s < kTmStrips; ++s) {
-            const uint32_t* f = &fr[p & 1][16 * e + 4 * s];
-            ptx::mma_16816(acc[s], f[0], f[1], f[2], f[3], b0, b1);
-          }
-          ptx::mma_16816(acc[kTmStrips], wr[kt][0], wr[kt][1], wr[kt][2], wr[kt][3], b0, b1);
-#pragma unroll
-          for (int j = 0; j < NS; ++j)
-              ptx::mma_16816(acc[1 + kTmStrips + j], af[j][0], af[j][1], af[j][2], af[j][3], b0,
-                             b1);
-        }
+        ktile(2 * p, &fr[p & 1][0]);
+        ktile(2 * p + 1, &fr[p & 1][16]);
         if (p + 1 < 8) ptx::tmem_wait_ld32(fr[(p + 1) & 1]);
+      }
+    } else {
+      // twice the accumulators: one 16-column load per k-tile, one ahead
+      uint32_t fr[2][16];
+      ptx::tmem_ld<16>(tm_addr, fr[0]);
+      ptx::tmem_wait_ld16(fr[0]);
+#pragma unroll
+      for (int kt = 0; kt < 16; ++kt) {
+        if (kt + 1 < 16) ptx::tmem_ld<16>(tm_addr + 16 * (kt + 1), fr[(kt + 1) & 1]);
+        ktile(kt, fr[kt & 1]);
+        if (kt + 1 < 16) ptx::tmem_wait_ld16(fr[(kt + 1) & 1]);
       }
     }
     trace_stamp(a, k, 1);
@@ -404,25 +431,29 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
     // (2) epilogue
     if (fast) {
       // greedy, no logits out: keys straight from the accumulators
-      if (a.B <= 2)
-        fast_keys<NST, 4>(acc, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
-      else if (a.B <= 4)
-        fast_keys<NST, 2>(acc, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
-      else
-        fast_keys<NST, 1>(acc, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
+      if constexpr (NT == 1) {
+        if (a.B <= 2)
+          fast_keys<NST, 4>(acc, 0, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
+        else if (a.B <= 4)
+          fast_keys<NST, 2>(acc, 0, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
+        else
+          fast_keys<NST, 1>(acc, 0, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
+      } else {
+        fast_keys<NST, 1>(acc, 0, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
+        fast_keys<NST, 1>(acc, 1, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
+      }
       trace_stamp(a, k, 2);
       trace_stamp(a, k, 3);
       __syncthreads();
     } else {
       // logits into the shared base buffer (in place), then the key pass
 #pragma unroll
-      for (int s = 0; s < NST; ++s) {
-        float a1[1][4] = {{acc[s][0], acc[s][1], acc[s][2], acc[s][3]}};
-        logits_strip<1>(a1, base_s, ra.R, a.B, strip_row0(s, warp), lane);
-      }
+      for (int s = 0; s < NST; ++s)           // (a padding strip's rows lie past R)
+        if (strip_row0(s, warp) < ra.R)
+          logits_strip<NT>(acc[s], base_s, ra.R, a.B, strip_row0(s, warp), lane);
       trace_stamp(a, k, 2);
       __syncthreads();
-      key_pass<false>(a, base_s, ra.R, nv, row0, k, kpm, eseed, group_best);
+      key_pass<(NT > 1)>(a, base_s, ra.R, nv, row0, k, kpm, eseed, group_best);
       trace_stamp(a, k, 3);
       __syncthreads();
     }
@@ -461,7 +492,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
     }
     trace_stamp(a, k, 5);
     prefetch_base(ra, k + 1, row0, nv, base_s);
-    if (warp < a.B) {
+    if (NT == 1 && warp < a.B) {     // warp w takes request w
       const unsigned long long* s = a.sync.slot_at(parity, k, warp);
       unsigned long long best = 0ull;
       int good = 1;
@@ -532,6 +563,93 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
           if (k + 1 < a.gamma)
             *reinterpret_cast<uint4*>(U + (lane * 2 + (warp >> 3)) * 128 + (warp & 7) * 16) =
                 __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok * kRank) + lane);
+        }
+      } else if (lane == 0) {
+        abort_s = 1;
+      }
+    }
+    // above 8 requests each half-warp of warp w takes one, requests w and
+    // w + 8 side by side
+    constexpr int halves = 2;                            // B > 8 exactly when NT = 2
+    constexpr int span = 32 / halves;                    // lanes per request
+    const int li = lane % span;                          // lane within the request's lanes
+    const int rq = warp + kResWarps * (lane / span);
+    if (NT == 2 && warp < a.B) {
+      const bool mine = rq < a.B;
+      const unsigned long long* s = a.sync.slot_at(parity, k, mine ? rq : warp);
+      unsigned long long best = 0ull;
+      int good = 1;
+      uint32_t spins = 0;
+      // the first lane of a request first waits on its arrival count (one
+      // word: far less polling traffic than reading every slot); the count
+      // carries no ordering, the slots' tags decide, so the slots are then
+      // read (again if one has not landed yet)
+      if (li == 0 && mine) {
+        const uint32_t* cp = a.sync.count_at(parity, k) + rq;
+        while (ld_relaxed_gpu_u32(cp) < (uint32_t)n_cta) {
+          if ((++spins & 63u) == 0u &&
+              (round_aborted(a.sync.hdr, round_s) ||
+               (int64_t)(globaltimer_ns() - t_step) > a.timeout_ns))
+            break;                     // the slot loop below reports it
+        }
+      }
+      __syncwarp();
+      spins = 0;
+      while (true) {
+        bool have = true;
+        best = 0ull;
+        if (mine)
+#pragma unroll 4
+          for (int j = 2 * li; j < n_cta; j += 2 * span) {
+            unsigned long long x0, x1;
+            ld_relaxed_gpu_v2u64(s + j, x0, x1);
+            const bool v1 = j + 1 < n_cta;
+            have = have && (x0 & ~kKey50Mask) == tag && (!v1 || (x1 & ~kKey50Mask) == tag);
+            x0 &= kKey50Mask;
+            x1 = v1 ? (x1 & kKey50Mask) : 0ull;
+            best = x0 > best ? x0 : best;
+            best = x1 > best ? x1 : best;
+          }
+        if (__all_sync(0xFFFFFFFFu, have)) break;
+        if ((++spins & 15u) == 0u) {
+          int stop = 0;
+          if (lane == 0) {
+            if (round_aborted(a.sync.hdr, round_s)) {
+              stop = 1;
+            } else if ((int64_t)(globaltimer_ns() - t_step) > a.timeout_ns) {
+              abort_round(a.sync.hdr, round_s, kStatusTimeout);
+              stop = 1;
+            }
+          }
+          if (__shfl_sync(0xFFFFFFFFu, stop, 0)) {
+            good = 0;
+            break;
+          }
+        }
+      }
+#pragma unroll
+      for (int o = span / 2; o > 0; o >>= 1) {           // within the request's lanes
+        const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        best = y > best ? y : best;
+      }
+      if (good) {
+        if (rq == 0) trace_stamp(a, k, 6);
+        const int32_t tok = key50_token(best);
+        if (mine && (tok < 0 || (int64_t)tok >= a.V)) {   // cannot happen: real rows only
+          if (li == 0) {
+            abort_round(a.sync.hdr, round_s, kStatusInternal);
+            abort_s = 1;
+          }
+        } else if (mine) {
+          if (li == 0) {
+            tok_s[rq] = tok;
+            if (cta == 0) a.out_tokens[(size_t)rq * a.gamma + k] = tok;
+          }
+          if (k + 1 < a.gamma)                           // the 32 16-byte chunks of W1[tok]
+#pragma unroll
+            for (int c = li; c < 32; c += span)
+              *reinterpret_cast<uint4*>(U + (c * 2 + (rq >> 3)) * 128 + (rq & 7) * 16) =
+                  __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok * kRank) + c);
         }
       } else if (lane == 0) {
         abort_s = 1;
@@ -617,12 +735,22 @@ size_t mma_resident_smem_bytes(int S, int max_B, int R) {
   return (size_t)S * kSmemStripBytes + 16 * 512 + (((size_t)max_B * R * 2 + 15) & ~(size_t)15);
 }
 
-const void* mma_resident_kernel(int S) {
-  switch (S / kMrWarps) {
-    case 0: return reinterpret_cast<const void*>(&walk_mma_kernel<0>);
-    case 1: return reinterpret_cast<const void*>(&walk_mma_kernel<1>);
-    case 2: return reinterpret_cast<const void*>(&walk_mma_kernel<2>);
-    case 3: return reinterpret_cast<const void*>(&walk_mma_kernel<3>);
+const void* mma_resident_kernel(int S, int NT) {
+  const int NS = (S + kMrWarps - 1) / kMrWarps;
+  if (NT == 1) {
+    switch (NS) {
+      case 0: return reinterpret_cast<const void*>(&walk_mma_kernel<0, 1>);
+      case 1: return reinterpret_cast<const void*>(&walk_mma_kernel<1, 1>);
+      case 2: return reinterpret_cast<const void*>(&walk_mma_kernel<2, 1>);
+      case 3: return reinterpret_cast<const void*>(&walk_mma_kernel<3, 1>);
+    }
+  } else if (NT == 2) {
+    switch (NS) {
+      case 0: return reinterpret_cast<const void*>(&walk_mma_kernel<0, 2>);
+      case 1: return reinterpret_cast<const void*>(&walk_mma_kernel<1, 2>);
+      case 2: return reinterpret_cast<const void*>(&walk_mma_kernel<2, 2>);
+      case 3: return reinterpret_cast<const void*>(&walk_mma_kernel<3, 2>);
+    }
   }
   return nullptr;
 }
