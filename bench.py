@@ -79,6 +79,9 @@ def parse():
     p.add_argument("--unit-rates", action="store_true",
                    help="measure the tier rates the on-chip roofline uses (tensor-memory "
                         "tcgen05.mma and mma.sync cycles per SM) and print them as one JSON line")
+    p.add_argument("--trace-skew", action="store_true",
+                   help="after timing, run rounds with global-timer stamps and report how far "
+                        "apart the CTAs post and see each step's keys")
     p.add_argument("--only-timed", action="store_true",
                    help="warm-up and timed steps only (for profiler runs): no warm-L2 pass, "
                         "no end-to-end pass, no CPU baseline")
@@ -185,9 +188,11 @@ def load_inputs(cfg, B, n_rounds):
     return W1, W2, rounds
 
 
-PHASES = ["register strips", "shared strips", "tensor-memory epilogue", "CTA reduction",
+# stamps 1..7 of a step (see dspark_walk_set_trace): the time between stamp
+# i - 1 and stamp i is phase i - 1
+PHASES = ["projection k loop", "epilogue (keys or logits)", "key pass", "CTA barrier",
           "post key", "wait for all keys", "gather next u"]
-ENTRY = ["load tensor-memory tier", "load registers + shared tier, first u"]
+ENTRY = ["load tensor-memory + register tiers", "shared tier, first u"]
 
 
 def phase_breakdown(walk, w, B, cfg, launch, stream, n_rounds, clocks, rounds=20):
@@ -230,6 +235,51 @@ def phase_breakdown(walk, w, B, cfg, launch, stream, n_rounds, clocks, rounds=20
     for j, name in enumerate(ENTRY):
         out["entry: " + name] = float(np.median(en[..., j]))
     return out
+
+
+def skew_report(walk, w, B, cfg, launch, stream, rounds=10):
+    """Cross-CTA timing of the rendezvous from global-timer stamps (warm L2):
+    how far apart the CTAs start a step and post their keys, and how long
+    after the last post the CTAs see the winner.  The global timer ticks in
+    coarse steps (256 ns on GB300), so the figures are medians over steps."""
+    plan = w.plan()
+    if plan["kernel"] != walk.KERNEL_RESIDENT or B > 16:
+        return None
+    n, g = plan["n_cta"], cfg.gamma
+    buf = torch.zeros(n * (g + 1) * 8, dtype=torch.int64, device="cuda")
+    walk.dspark_walk_set_trace(w.h, buf, buf.numel() * 8)
+    walk.dspark_walk_set_trace_clock(w.h, walk.TRACE_GLOBAL_TIMER)
+    steps = []
+    for i in range(rounds):
+        buf.zero_()
+        with torch.cuda.stream(stream):
+            launch(i)
+        torch.cuda.synchronize()
+        t = buf.view(n, g + 1, 8).cpu().numpy().astype(np.float64)
+        if not t[:, :g, 0].all():
+            break
+        steps.append(t[:, 1:g, :])                       # steps 1.. (step 0 follows the entry)
+    walk.dspark_walk_set_trace_clock(w.h, walk.TRACE_SM_CLOCK)
+    walk.dspark_walk_set_trace(w.h, None, 0)
+    if not steps:
+        return None
+    t = np.concatenate(steps, axis=1) / 1000.0          # [n, S, 8] us
+    start, post, seen = t[:, :, 0], t[:, :, 5], t[:, :, 6]
+    med = lambda x: float(np.median(x))                 # noqa: E731
+    last_post = post.max(axis=0)
+    resolution = np.diff(np.unique(t[:, :, 0]))
+    return {
+        "unit": "us, median over %d steps of %d rounds (global timer, warm L2)" % (
+            t.shape[1], len(steps)),
+        "timer_step_ns": float(resolution[resolution > 0].min() * 1000) if resolution.size else None,
+        "step_start_spread": med(start.max(0) - start.min(0)),
+        "post_spread": med(post.max(0) - post.min(0)),
+        "post_p90_to_last": med(last_post - np.percentile(post, 90, axis=0)),
+        "last_post_to_first_seen": med(seen.min(0) - last_post),
+        "last_post_to_median_seen": med(np.median(seen, 0) - last_post),
+        "last_post_to_last_seen": med(seen.max(0) - last_post),
+        "step_start_to_post": med(np.median(post - start, 0)),
+    }
 
 
 def kernel_label(walk, plan, B):
@@ -676,6 +726,7 @@ def main():
     d2h = B * cfg.gamma * 4 + 4                             # tokens + the status word
 
     trace = phase_breakdown(walk, w, B, cfg, launch, stream, n_rounds, clocks) if args.trace else None
+    skew = skew_report(walk, w, B, cfg, launch, stream) if args.trace_skew else None
 
     mean_ms = statistics.mean(per)
     local = torch.tensor([mean_ms, (t1 - t0)], dtype=torch.float64, device=dev)
@@ -759,6 +810,7 @@ def main():
                        "stream sync; wall clock, mean of %d" % e2e_n},
         "gpu_launches": args.steps,
         "phases": trace,
+        "rendezvous_skew": skew,
         "clocks": clocks,
         "plan": plan,
     }

@@ -316,13 +316,29 @@ int dspark_walk_gumbel_noise(const uint32_t *bits, float *noise, int64_t n, void
  * dspark_walk_set_trace -- phase timing of later runs (profiling aid).  When
  * `device_buffer` holds at least n_cta * (gamma + 1) * 8 uint64 values, each
  * run's CTA c writes SM clock64() stamps of its thread 0 at
- * [(c * (gamma + 1) + slot) * 8 + phase]: slot k < gamma is step k (phases:
- * start, register strips done, shared strips done, tensor-memory epilogue
- * done, CTA reduction done, key posted, all keys seen, next u gathered);
- * slot gamma is the round's entry (start, tensor memory loaded, ready).
- * Only the resident kernel writes stamps.  NULL turns tracing off.
+ * [(c * (gamma + 1) + slot) * 8 + phase]: slot k < gamma is step k (stamps:
+ * 0 start, 1 projection k loop issued, 2 epilogue done (keys, or logits),
+ * 3 key pass done, 4 CTA barrier passed, 5 key posted, 6 winner seen,
+ * 7 next u gathered; the tcgen05 resident kernel stamps 1 after its register
+ * strips, 2 after its shared strips, 3 after its tensor-memory epilogue and
+ * key pass); slot gamma is the round's entry (start, tensor-memory and
+ * register tiers loaded, ready).  Only the resident kernels write stamps.
+ * NULL turns tracing off.
  */
 int dspark_walk_set_trace(dspark_walk_t h, void *device_buffer, int64_t bytes);
+
+/*
+ * dspark_walk_set_trace_clock -- what later traced runs stamp:
+ *   DSPARK_TRACE_SM_CLOCK (default): clock64() cycles of the CTA's SM (fine
+ *     grained; not comparable between SMs);
+ *   DSPARK_TRACE_GLOBAL_TIMER: the global timer in nanoseconds (coarser, but
+ *     one clock for every SM, so the CTAs' stamps of one step can be compared:
+ *     how far apart they post their keys and see the winner).
+ * DSPARK_EINVAL for another value.
+ */
+#define DSPARK_TRACE_SM_CLOCK 0
+#define DSPARK_TRACE_GLOBAL_TIMER 1
+int dspark_walk_set_trace_clock(dspark_walk_t h, int clock);
 
 /*
  * dspark_walk_unit_rates -- measure, on the current device, the rates at

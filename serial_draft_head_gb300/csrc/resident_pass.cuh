@@ -52,11 +52,14 @@ __device__ __forceinline__ void prefetch_base(const ResidentArgs& ra, int k, int
   const int tid = (int)threadIdx.x - first;      // this thread's index among `count`
   const int nthr = count > 0 ? count : (int)blockDim.x;
   if (ra.base_mode == 16) {
+    // read once: evict-first, so that the base logits do not push out W2
+    // rows that a streamed tier re-reads every step
+    const uint64_t pol = ptx::policy_evict_first();
     const int per = nv >> 3;
     for (int i = tid; i < a.B * per; i += nthr) {
       const int b = i / per, c = i - b * per;
       const uint16_t* src = a.base + ((size_t)b * a.gamma + k) * (size_t)a.V + row0 + 8 * c;
-      ptx::cp_async16(base_s + (size_t)b * ra.R + 8 * c, src);
+      ptx::cp_async16_hint(base_s + (size_t)b * ra.R + 8 * c, src, pol);
     }
   } else if (ra.base_mode == 4) {
     const int per = nv >> 1;

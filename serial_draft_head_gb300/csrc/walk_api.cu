@@ -57,6 +57,7 @@ struct dspark_walk {
   int64_t timeout_ns = 200000000;
   unsigned long long* trace = nullptr;  // caller-owned, see dspark_walk_set_trace
   int64_t trace_bytes = 0;
+  int trace_global = 0;                 // dspark_walk_set_trace_clock
   int skip_cta = -1;
   // staging for dspark_walk_run_host (allocated on first use): device, and a
   // pinned host block {anchor[max_B], temperature[max_B], status}
@@ -368,6 +369,7 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
                                             : h->st_n_cta;
     const int64_t need = (int64_t)n * (gamma + 1) * 8 * 8;
     a.trace = (h->trace && h->trace_bytes >= need) ? h->trace : nullptr;
+    a.trace_global = h->trace_global;
   }
 
   a.out_state = h->out_state;
@@ -688,6 +690,13 @@ int dspark_walk_set_trace(dspark_walk_t h, void* device_buffer, int64_t bytes) {
   if (!h || bytes < 0 || (device_buffer == nullptr && bytes != 0)) return DSPARK_EINVAL;
   h->trace = static_cast<unsigned long long*>(device_buffer);
   h->trace_bytes = bytes;
+  return DSPARK_OK;
+}
+
+int dspark_walk_set_trace_clock(dspark_walk_t h, int clock) {
+  if (!h || (clock != DSPARK_TRACE_SM_CLOCK && clock != DSPARK_TRACE_GLOBAL_TIMER))
+    return DSPARK_EINVAL;
+  h->trace_global = clock == DSPARK_TRACE_GLOBAL_TIMER ? 1 : 0;
   return DSPARK_OK;
 }
 

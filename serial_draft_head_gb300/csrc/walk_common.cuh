@@ -101,7 +101,8 @@ struct WalkArgs {
   int sampler;                 // 0: per-token Gumbel-max; 1: group inverse-CDF
   int64_t timeout_ns;          // rendezvous wait limit
   int skip_cta;                // fault injection: this CTA never posts (-1: off)
-  unsigned long long* trace;   // optional [n_cta][gamma + 1][8] SM-clock stamps
+  unsigned long long* trace;   // optional [n_cta][gamma + 1][8] stamps
+  int trace_global;            // stamps in global-timer ns (comparable across SMs), not SM clocks
   // recurrent heads (resident kernel only)
   int cell;                    // 0: Markov (u = W1[prev]); 1: gated; 2: RNN; 3: GRU
   const uint16_t* cell_M;      // [P, 256] bf16 recurrent rows (P = 256; GRU: 768)
@@ -112,11 +113,15 @@ struct WalkArgs {
 };
 
 
-// Phase stamp of thread 0 (SM clock cycles) into the optional trace buffer:
-// slot k < gamma is step k, slot gamma is the round's entry.
+__device__ __forceinline__ uint64_t globaltimer_ns();
+
+// Phase stamp of thread 0 into the optional trace buffer (SM clock cycles, or
+// global-timer nanoseconds, which compare across SMs): slot k < gamma is step
+// k, slot gamma is the round's entry.
 __device__ __forceinline__ void trace_stamp(const WalkArgs& a, int slot, int phase) {
   if (a.trace != nullptr && threadIdx.x == 0)
-    a.trace[((size_t)blockIdx.x * (a.gamma + 1) + slot) * 8 + phase] = clock64();
+    a.trace[((size_t)blockIdx.x * (a.gamma + 1) + slot) * 8 + phase] =
+        a.trace_global ? globaltimer_ns() : (unsigned long long)clock64();
 }
 
 // The Philox key of this round: the seed, plus the round counter when the

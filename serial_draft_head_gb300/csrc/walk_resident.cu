@@ -213,8 +213,9 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_resident_kernel(const Res
     const uint32_t bytes = (uint32_t)ns * kSmemStripBytes;
     uint64_t* bar = &mbar[kMbarRing + gi % nslot];
     ptx::mbar_expect_tx(bar, bytes);
-    ptx::bulk_g2s(ring + (size_t)(gi % nslot) * kChunkBytes, gstream + (size_t)c * kChunkBytes,
-                  bytes, bar);
+    // re-read every step: evict-last, so that it stays in L2 across the steps
+    ptx::bulk_g2s_hint(ring + (size_t)(gi % nslot) * kChunkBytes,
+                       gstream + (size_t)c * kChunkBytes, bytes, bar, ptx::policy_evict_last());
   };
   if (threadIdx.x == 0 && ra.ST > 0) {
     const int pre = a.gamma * n_chunks < nslot ? a.gamma * n_chunks : nslot;

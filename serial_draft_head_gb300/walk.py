@@ -23,6 +23,9 @@ ETEMP = -7
 ELIMIT = -8
 EINTERNAL = -9
 
+TRACE_SM_CLOCK = 0
+TRACE_GLOBAL_TIMER = 1
+
 KERNEL_STREAM = 0
 KERNEL_RESIDENT = 1
 KERNEL_BATCHED = 2
@@ -70,7 +73,7 @@ EXPORTS = [
     "dspark_walk_destroy", "dspark_walk_run_noalloc", "dspark_walk_set_kernel",
     "dspark_walk_set_trace", "dspark_walk_set_seed_mode", "dspark_walk_round",
     "dspark_walk_gumbel_noise", "dspark_walk_set_sampler", "dspark_walk_set_cell",
-    "dspark_walk_set_state_output", "dspark_walk_unit_rates",
+    "dspark_walk_set_state_output", "dspark_walk_unit_rates", "dspark_walk_set_trace_clock",
 ]
 
 
@@ -101,6 +104,7 @@ def load(build_if_missing=True):
     L.dspark_walk_destroy.argtypes = [vp]
     L.dspark_walk_set_kernel.argtypes = [vp, i32]
     L.dspark_walk_set_trace.argtypes = [vp, vp, i64]
+    L.dspark_walk_set_trace_clock.argtypes = [vp, i32]
     L.dspark_walk_run_noalloc.argtypes = [vp, vp, i64, i32, vp, vp, vp, u64, vp, i32, i32, vp, vp]
     L.dspark_walk_set_seed_mode.argtypes = [vp, i32]
     L.dspark_walk_set_sampler.argtypes = [vp, i32]
@@ -245,6 +249,10 @@ def dspark_walk_unit_rates(stream=None):
 def dspark_walk_set_trace(h, device_buffer, nbytes):
     return _check(load().dspark_walk_set_trace(h, _ptr(device_buffer), int(nbytes)),
                   "dspark_walk_set_trace")
+
+
+def dspark_walk_set_trace_clock(h, clock):
+    return _check(load().dspark_walk_set_trace_clock(h, int(clock)), "dspark_walk_set_trace_clock")
 
 
 def dspark_walk_destroy(h):
