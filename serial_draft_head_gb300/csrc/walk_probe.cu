@@ -372,7 +372,7 @@ extern "C" int dspark_walk_unit_rates(double* out, int n_out, void* stream) {
   out[3] = med[3];
   out[4] = med[kPhases] > 0 ? med[0] / med[kPhases] * 1000.0 : 0.0;   // cycles per us = MHz
   if (n_out >= 7) {
-    out[5] = med[4] / (8.0 * 32768.0);       // cycles per KB of tcgen05.ld per SM
+    out[5] = med[4] / 256.0;                 // 8 warps x 32 KB per rep: cycles per KB per SM
     out[6] = med[5];
   }
   return DSPARK_OK;
