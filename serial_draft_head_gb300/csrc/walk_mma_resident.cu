@@ -116,11 +116,13 @@ __device__ __forceinline__ uint32_t key32(uint32_t lb, uint32_t row) {
 // as bf16(fp32 sum), whose fp32 sum is exact whenever it could matter), and a
 // packed running argmax (argmax2).  The pairs are the two requests of a row,
 // or, with one request, rows g and g + 8.  Rows past the shard's end score
-// -inf.  Then a max over the lanes that hold the same request.
-template <int NST, int G, int NT>
+// -inf.  Then a max over the lanes that hold the same request.  accs[s] is
+// strip st0 + s of the warp; only the first nst of them are real; MERGE keeps
+// the larger of wkey[b] and the new key (strips scored in several calls).
+template <int NST, int G, int NT, bool MERGE = false>
 __device__ __forceinline__ void fast_keys(const float (&accs)[NST][NT][4], int nt,
                                           const uint16_t* base_s, int R, int B, int nv, int warp,
-                                          int lane, uint32_t* wkey) {
+                                          int lane, uint32_t* wkey, int st0 = 0, int nst = NST) {
   constexpr int NJ = (NST + G - 1) / G;          // strips per lane
   constexpr int SRC = 4 / G;                     // lanes per row group holding results
   constexpr uint32_t kNegInf2 = 0xFF80FF80u;
@@ -142,7 +144,7 @@ __device__ __forceinline__ void fast_keys(const float (&accs)[NST][NT][4], int n
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     const int s = part + G * j;
-    rr[j] = s < NST ? strip_row0(s, warp) + g : 0;
+    rr[j] = s < nst ? strip_row0(st0 + s, warp) + g : 0;
     rl[j][0] = rr[j] < R ? rr[j] : R - 1;            // a padding strip's rows lie past R
     rl[j][1] = rr[j] + 8 < R ? rr[j] + 8 : R - 1;
   }
@@ -157,7 +159,7 @@ __device__ __forceinline__ void fast_keys(const float (&accs)[NST][NT][4], int n
     for (int j = 0; j < NJ; ++j) {
       const uint32_t bias = bf2_bits(__floats2bfloat162_rn(v[j][0], v[j][2]));
       uint32_t l = bf2_bits(__hadd2(as_bf2(bb[j]), as_bf2(bias)));
-      const bool ok = part + G * j < NST;
+      const bool ok = part + G * j < nst;
       const uint32_t lo_ok = ok && rr[j] < nv ? 0u : 0x0000FFFFu;
       const uint32_t hi_ok = ok && rr[j] + 8 < nv ? 0u : 0xFFFF0000u;
       l = (l & ~(lo_ok | hi_ok)) | (kNegInf2 & (lo_ok | hi_ok));
@@ -168,7 +170,7 @@ __device__ __forceinline__ void fast_keys(const float (&accs)[NST][NT][4], int n
     if (best == kNegInf2 && k0 == k1) kb = 0u;    // no valid row at all
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) kb = max_u32(kb, __shfl_xor_sync(0xFFFFFFFFu, kb, o));
-    if (lane == 0) wkey[0] = kb;
+    if (lane == 0) wkey[0] = MERGE ? max_u32(wkey[0], kb) : kb;
     return;
   }
   // pairs = requests (2 src, 2 src + 1) of one row
@@ -188,7 +190,7 @@ __device__ __forceinline__ void fast_keys(const float (&accs)[NST][NT][4], int n
       const uint32_t bias = bf2_bits(__floats2bfloat162_rn(v[j][2 * h], v[j][2 * h + 1]));
       uint32_t l = bf2_bits(__hadd2(as_bf2(bb[j][h]), as_bf2(bias)));
       const int row = rr[j] + 8 * h;
-      if (!(part + G * j < NST && row < nv)) l = kNegInf2;
+      if (!(part + G * j < nst && row < nv)) l = kNegInf2;
       argmax2(l, (uint32_t)row * 0x10001u, best, brow);
     }
   uint32_t kb[2] = {key32(best, brow), key32(best >> 16, brow >> 16)};
@@ -200,7 +202,7 @@ __device__ __forceinline__ void fast_keys(const float (&accs)[NST][NT][4], int n
   if (g == 0 && part == 0)
 #pragma unroll
     for (int q = 0; q < 2; ++q)
-      if (2 * src + q < B) wkey[2 * src + q] = kb[q];
+      if (2 * src + q < B) wkey[2 * src + q] = MERGE ? max_u32(wkey[2 * src + q], kb[q]) : kb[q];
 }
 
 template <int NS, int NT>
@@ -464,7 +466,9 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
     // no fence orders it and no atomic contends for a line).  Then every warp
     // starts the next step's base rows, and warp b polls request b's slots of
     // all CTAs until each carries this round's tag, takes the maximum and
-    // fetches the winner's W1 row into U.
+    // puts the winner's W1 row into U.  Up to 8 requests, the row of the best
+    // key seen so far is loaded while the last keys arrive, so that when the
+    // winner posted early its row is already on the way.
     const uint32_t parity = round_s & 1u;
     const unsigned long long tag = slot_tag(round_s);
     if (warp == 0 && lane < a.B) {
@@ -497,13 +501,17 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
       unsigned long long best = 0ull;
       int good = 1;
       uint32_t spins = 0;
-      // lane 0 first waits on the request's arrival count (one word: far less
-      // polling traffic than reading every slot); the count carries no
-      // ordering, the slots' tags decide, so the slots are then read (again
-      // if one has not landed yet)
+      // lane 0 first waits until three quarters of the CTAs have counted in
+      // (one word: far less polling traffic than every warp reading every
+      // slot); the count carries no ordering, the slots' tags decide.  Then
+      // the warp reads all slots until every tag is this round's: a slot not
+      // yet written of this parity holds 0, so the maximum so far is a lower
+      // bound of the winner, and its W1 row is loaded into rowv whenever it
+      // changes (the last load is the winner's)
       if (lane == 0) {
         const uint32_t* cp = a.sync.count_at(parity, k) + warp;
-        while (ld_relaxed_gpu_u32(cp) < (uint32_t)n_cta) {
+        const uint32_t early = (uint32_t)(n_cta - (n_cta >> 2));
+        while (ld_relaxed_gpu_u32(cp) < early) {
           if ((++spins & 63u) == 0u &&
               (round_aborted(a.sync.hdr, round_s) ||
                (int64_t)(globaltimer_ns() - t_step) > a.timeout_ns))
@@ -512,6 +520,8 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
       }
       __syncwarp();
       spins = 0;
+      unsigned long long cand = 0ull;                  // the key whose row rowv holds
+      uint4 rowv = make_uint4(0u, 0u, 0u, 0u);
       while (true) {
         bool have = true;
         best = 0ull;
@@ -525,7 +535,20 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
           best = x0 > best ? x0 : best;
           best = x1 > best ? x1 : best;
         }
-        if (__all_sync(0xFFFFFFFFu, have)) break;
+        const bool all = __all_sync(0xFFFFFFFFu, have);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+          best = y > best ? y : best;
+        }
+        if (best != cand && best != 0ull && k + 1 < a.gamma) {
+          const int32_t t = key50_token(best);
+          if (t >= 0 && (int64_t)t < a.V) {
+            cand = best;
+            rowv = __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)t * kRank) + lane);
+          }
+        }
+        if (all) break;
         if ((++spins & 15u) == 0u) {
           int stop = 0;
           if (lane == 0) {
@@ -542,11 +565,6 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
           }
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-        best = y > best ? y : best;
-      }
       if (good) {
         if (warp == 0) trace_stamp(a, k, 6);
         const int32_t tok = key50_token(best);
@@ -560,9 +578,8 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
             tok_s[warp] = tok;
             if (cta == 0) a.out_tokens[(size_t)warp * a.gamma + k] = tok;
           }
-          if (k + 1 < a.gamma)
-            *reinterpret_cast<uint4*>(U + (lane * 2 + (warp >> 3)) * 128 + (warp & 7) * 16) =
-                __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok * kRank) + lane);
+          if (k + 1 < a.gamma)       // rowv holds W1[tok]: cand == best here
+            *reinterpret_cast<uint4*>(U + (lane * 2 + (warp >> 3)) * 128 + (warp & 7) * 16) = rowv;
         }
       } else if (lane == 0) {
         abort_s = 1;
@@ -580,13 +597,14 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
       unsigned long long best = 0ull;
       int good = 1;
       uint32_t spins = 0;
-      // the first lane of a request first waits on its arrival count (one
-      // word: far less polling traffic than reading every slot); the count
-      // carries no ordering, the slots' tags decide, so the slots are then
-      // read (again if one has not landed yet)
+      // as above: the first lane of a request waits until three quarters of
+      // the CTAs have counted in, then the request's lanes read the slots
+      // until every tag is this round's, loading the row of the best key so
+      // far whenever it changes
       if (li == 0 && mine) {
         const uint32_t* cp = a.sync.count_at(parity, k) + rq;
-        while (ld_relaxed_gpu_u32(cp) < (uint32_t)n_cta) {
+        const uint32_t early = (uint32_t)(n_cta - (n_cta >> 2));
+        while (ld_relaxed_gpu_u32(cp) < early) {
           if ((++spins & 63u) == 0u &&
               (round_aborted(a.sync.hdr, round_s) ||
                (int64_t)(globaltimer_ns() - t_step) > a.timeout_ns))
@@ -595,6 +613,11 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
       }
       __syncwarp();
       spins = 0;
+      constexpr int nchunk = 32 / span;                  // 16-byte chunks of the row per lane
+      unsigned long long cand = 0ull;
+      uint4 rowv[nchunk];
+#pragma unroll
+      for (int i = 0; i < nchunk; ++i) rowv[i] = make_uint4(0u, 0u, 0u, 0u);
       while (true) {
         bool have = true;
         best = 0ull;
@@ -610,7 +633,22 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
             best = x0 > best ? x0 : best;
             best = x1 > best ? x1 : best;
           }
-        if (__all_sync(0xFFFFFFFFu, have)) break;
+        const bool all = __all_sync(0xFFFFFFFFu, have);
+#pragma unroll
+        for (int o = span / 2; o > 0; o >>= 1) {         // within the request's lanes
+          const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+          best = y > best ? y : best;
+        }
+        if (mine && best != cand && best != 0ull && k + 1 < a.gamma) {
+          const int32_t t = key50_token(best);
+          if (t >= 0 && (int64_t)t < a.V) {
+            cand = best;
+#pragma unroll
+            for (int i = 0; i < nchunk; ++i)
+              rowv[i] = __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)t * kRank) + li + span * i);
+          }
+        }
+        if (all) break;
         if ((++spins & 15u) == 0u) {
           int stop = 0;
           if (lane == 0) {
@@ -627,11 +665,6 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
           }
         }
       }
-#pragma unroll
-      for (int o = span / 2; o > 0; o >>= 1) {           // within the request's lanes
-        const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-        best = y > best ? y : best;
-      }
       if (good) {
         if (rq == 0) trace_stamp(a, k, 6);
         const int32_t tok = key50_token(best);
@@ -645,11 +678,12 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
             tok_s[rq] = tok;
             if (cta == 0) a.out_tokens[(size_t)rq * a.gamma + k] = tok;
           }
-          if (k + 1 < a.gamma)                           // the 32 16-byte chunks of W1[tok]
+          if (k + 1 < a.gamma)                 // rowv holds W1[tok]'s chunks li + span i
 #pragma unroll
-            for (int c = li; c < 32; c += span)
-              *reinterpret_cast<uint4*>(U + (c * 2 + (rq >> 3)) * 128 + (rq & 7) * 16) =
-                  __ldg(reinterpret_cast<const uint4*>(a.W1 + (size_t)tok * kRank) + c);
+            for (int i = 0; i < nchunk; ++i) {
+              const int c = li + span * i;
+              *reinterpret_cast<uint4*>(U + (c * 2 + (rq >> 3)) * 128 + (rq & 7) * 16) = rowv[i];
+            }
         }
       } else if (lane == 0) {
         abort_s = 1;
