@@ -29,12 +29,13 @@ struct dspark_walk {
   SyncView sync{};
   // mma.sync resident layout (Markov runs with B <= mr_max_B)
   uint32_t* W2m = nullptr;
-  bool mr_ok = false;             // the shard fits the layout
+  bool mr_ok = false;             // the layout can hold the shard
   int mr_max_B = 0, mr_R = 0, mr_S = 0, mr_n_cta = 0;
+  int mr_ST = 0, mr_nslot = 0;    // streamed strips per CTA, ring slots per warp
   int64_t mr_wpc = 0;
   size_t mr_smem = 0;
   // tcgen05 resident layout (runs with B <= res_max_B the layout above does
-  // not take: larger batches, recurrent heads, partial residency)
+  // not take: the recurrent heads and the state output)
   uint32_t* W2p = nullptr;        // tiered repack, res_wpc words per CTA
   int res_max_B = 0;              // 0: no resident placement
   bool use_resident = true;       // dspark_walk_set_kernel
@@ -150,7 +151,11 @@ bool plan_resident(dspark_walk* h) {
 // mma.sync resident plan: rows spread over at most one CTA per SM, each CTA
 // holding 512 rows in tensor memory, 128 in registers and 0, 128, 256 or 384
 // in shared memory (the same number of shared strips in every warp), so shards
-// of 640 .. 1,024 rows: V <= 155,648 on 152 SMs.
+// of 640 .. 1,024 rows: V <= 155,648 on 152 SMs.  Larger shards keep tensor
+// memory, registers and NS = 0..2 shared strips per warp, and stream the rest
+// (ST strips per CTA, one of every warp per item) every step through a ring of
+// nslot = 2 or 3 slots of 64 KB, as in "V = 248,320: 62% on chip, the rest
+// streamed": the most shared strips that fit first, then the most slots.
 bool plan_mma(dspark_walk* h) {
   if (h->V >= (1 << 18)) return false;          // the 18-bit id field of the slot word
   const int mb = h->max_B < mma_resident_max_batch() ? h->max_B : mma_resident_max_batch();
@@ -158,23 +163,42 @@ bool plan_mma(dspark_walk* h) {
   int64_t R0 = (h->V + h->sm_count - 1) / h->sm_count;
   R0 = (R0 + 15) / 16 * 16;
   if (R0 < fixed) R0 = fixed;
-  // every warp runs the same number NS of shared strips: R = 640 + 128 NS, or
-  // one strip less when the batch's base rows would not fit otherwise (the
-  // last warp's third strip then only pads, over the U buffer that follows)
-  int64_t R = fixed + (R0 - fixed + 127) / 128 * 128;
-  if (R > mma_resident_max_rows()) return false;
-  if (mma_resident_smem_bytes((int)((R - fixed) / 16), mb, (int)R) > kSmemBudget && R > fixed &&
-      R - 16 >= R0)
-    R -= 16;
-  const int S = (int)((R - fixed) / 16);
-  const size_t smem = mma_resident_smem_bytes(S, mb, (int)R);
+  int64_t R = 0;
+  int S = 0, ST = 0, nslot = 0;
+  if (R0 <= mma_resident_max_rows()) {
+    // every warp runs the same number NS of shared strips: R = 640 + 128 NS, or
+    // one strip less when the batch's base rows would not fit otherwise (the
+    // last warp's third strip then only pads, over the U buffer that follows)
+    R = fixed + (R0 - fixed + 127) / 128 * 128;
+    if (mma_resident_smem_bytes((int)((R - fixed) / 16), mb, (int)R, 0) > kSmemBudget &&
+        R > fixed && R - 16 >= R0)
+      R -= 16;
+    S = (int)((R - fixed) / 16);
+  } else {
+    for (int ns = 2; ns >= 0 && nslot == 0; --ns)
+      for (int sl = 3; sl >= 2; --sl) {
+        const int64_t kept = fixed + 128 * ns;
+        R = kept + (R0 - kept + 127) / 128 * 128;
+        if (R >= 65536) return false;           // the 16-bit local row of the CTA's keys
+        if (mma_resident_smem_bytes(8 * ns, mb, (int)R, sl) <= kSmemBudget) {
+          S = 8 * ns;
+          ST = (int)((R - kept) / 16);
+          nslot = sl;
+          break;
+        }
+      }
+    if (nslot == 0) return false;
+  }
+  const size_t smem = mma_resident_smem_bytes(S, mb, (int)R, nslot);
   if (smem > kSmemBudget) return false;
   h->mr_ok = true;
   h->mr_max_B = mb;
   h->mr_R = (int)R;
   h->mr_S = S;
+  h->mr_ST = ST;
+  h->mr_nslot = nslot;
   h->mr_n_cta = (int)((h->V + R - 1) / R);
-  h->mr_wpc = mma_resident_words_per_cta(S);
+  h->mr_wpc = mma_resident_words_per_cta(S + ST);
   h->mr_smem = smem;
   return true;
 }
@@ -212,9 +236,10 @@ void plan_stream(dspark_walk* h) {
     p.rows_tmem = 512;
     p.rows_rf = 128;
     p.rows_smem = 16 * h->mr_S;
-    p.rows_stream = 0;
-    p.streamed_bytes = 0;
-    p.resident_bytes = h->V * (int64_t)h->r * 2;
+    p.rows_stream = 16 * h->mr_ST;
+    p.streamed_bytes = (int64_t)16 * h->mr_ST * h->mr_n_cta * h->r * 2;
+    p.resident_bytes = h->V * (int64_t)h->r * 2 - p.streamed_bytes;
+    if (p.resident_bytes < 0) p.resident_bytes = 0;
     p.kernel = DSPARK_KERNEL_RESIDENT;
   } else if (h->res_max_B > 0) {
     p.n_cta = h->res_n_cta;
@@ -254,7 +279,8 @@ size_t rowmajor_bytes(const dspark_walk* h) { return (size_t)h->V * h->r * 2; }
 cudaError_t unpack_rowmajor(dspark_walk* h, void* dst) {
   if (h->W2) return cudaMemcpy(dst, h->W2, rowmajor_bytes(h), cudaMemcpyDeviceToDevice);
   if (h->W2m)
-    return mma_resident_repack(dst, h->W2m, h->V, h->mr_R, h->mr_S, h->mr_n_cta, true, 0);
+    return mma_resident_repack(dst, h->W2m, h->V, h->mr_R, h->mr_S + h->mr_ST, h->mr_n_cta, true,
+                               0);
   if (h->W2p)
     return resident_repack(dst, h->W2p, h->V, h->res_R, h->res_RS, h->res_S + h->res_ST,
                            h->res_n_cta, true, 0);
@@ -271,7 +297,8 @@ cudaError_t build_layout(dspark_walk* h, Path which, const void* src) {
       if (h->W2m || !h->mr_ok) return cudaSuccess;
       e = cudaMalloc(&h->W2m, (size_t)h->mr_wpc * h->mr_n_cta * sizeof(uint32_t));
       if (e == cudaSuccess)
-        e = mma_resident_repack(s, h->W2m, h->V, h->mr_R, h->mr_S, h->mr_n_cta, false, 0);
+        e = mma_resident_repack(s, h->W2m, h->V, h->mr_R, h->mr_S + h->mr_ST, h->mr_n_cta, false,
+                                0);
       return e;
     case Path::kResident:
       if (h->W2p || h->res_max_B == 0) return cudaSuccess;
@@ -404,13 +431,13 @@ int launch_round(dspark_walk* h, const void* base, const int32_t* anchor, const 
     ra.W2p = mma ? h->W2m : h->W2p;
     ra.R = mma ? h->mr_R : h->res_R;
     ra.S = mma ? h->mr_S : h->res_S;
-    ra.ST = mma ? 0 : h->res_ST;
-    ra.nslot = mma ? 0 : h->res_nslot;
+    ra.ST = mma ? h->mr_ST : h->res_ST;
+    ra.nslot = mma ? h->mr_nslot : h->res_nslot;
     ra.words_per_cta = mma ? h->mr_wpc : h->res_wpc;
     const uintptr_t bp = reinterpret_cast<uintptr_t>(base);
     ra.base_mode = (h->V % 8 == 0 && (bp & 15u) == 0) ? 16
                    : (h->V % 2 == 0 && (bp & 3u) == 0) ? 4 : 2;
-    const void* rfn = mma ? mma_resident_kernel(h->mr_S, B <= 8 ? 1 : 2)
+    const void* rfn = mma ? mma_resident_kernel(h->mr_S, B <= 8 ? 1 : 2, h->mr_ST > 0)
                           : resident_kernel_for(h->res_RS, h->res_NT, cell_run(h));
     void* rargs[] = {&ra};
     CUDA_TRY(cudaLaunchCooperativeKernel(rfn, dim3(mma ? h->mr_n_cta : h->res_n_cta),
@@ -552,12 +579,14 @@ int dspark_walk_create(const void* W1, const void* W2, int64_t V, int r, int max
       int per_sm = 0;
       for (int s = 0; s <= 24 && e == cudaSuccess; s += 8)
         for (int nt = 1; nt <= 2 && e == cudaSuccess; ++nt)
-          e = cudaFuncSetAttribute(mma_resident_kernel(s, nt),
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+          for (int str = 0; str <= (s <= 16 ? 1 : 0) && e == cudaSuccess; ++str)
+            e = cudaFuncSetAttribute(mma_resident_kernel(s, nt, str != 0),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBudget);
       if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, mma_resident_kernel(h->mr_S, h->mr_max_B > 8 ? 2 : 1), resident_threads(),
-            h->mr_smem);
+            &per_sm, mma_resident_kernel(h->mr_S, h->mr_max_B > 8 ? 2 : 1, h->mr_ST > 0),
+            resident_threads(), h->mr_smem);
       if (e != cudaSuccess || per_sm != 1) {
         cudaGetLastError();
         h->mr_ok = false;

@@ -27,14 +27,17 @@ cudaError_t resident_repack(void* rowmajor, void* packed, int64_t V, int R, int 
                             int n_cta, bool inverse, cudaStream_t stream);
 
 // Resident kernel with every tier read by mma.sync (tensor memory through
-// tcgen05.ld): fully resident shards of at most mma_resident_max_rows() rows,
-// batches up to mma_resident_max_batch(), the Markov head.
+// tcgen05.ld): batches up to mma_resident_max_batch(), the Markov head.
+// Shards of at most mma_resident_max_rows() rows stay on chip; larger ones
+// keep S shared strips per CTA and stream ST more every step through a ring
+// of nslot half-strip slots per warp (S and ST multiples of 8).
 int mma_resident_fixed_rows();
 int mma_resident_max_rows();
 int mma_resident_max_batch();
-int64_t mma_resident_words_per_cta(int S);
-size_t mma_resident_smem_bytes(int S, int max_B, int R);
-const void* mma_resident_kernel(int S, int NT);   // S shared strips, NT n-tiles (B <= 8 NT)
+int64_t mma_resident_words_per_cta(int S);    // S: every strip in the shared-tier format
+size_t mma_resident_smem_bytes(int S, int max_B, int R, int nslot);
+// S shared strips, NT n-tiles (B <= 8 NT), a streamed tier or not
+const void* mma_resident_kernel(int S, int NT, bool streamed);
 cudaError_t mma_resident_repack(void* rowmajor, void* packed, int64_t V, int R, int S, int n_cta,
                                 bool inverse, cudaStream_t stream);
 

@@ -23,11 +23,18 @@
 //                            (16 rows each) in lanes 32 (w % 4) .. + 31,
 //                            columns 256 (w / 4) .. + 255;
 //   rows [512, 640)          registers: one 16-row strip per warp;
-//   rows [640, R)            shared memory: NS = 0..3 strips per warp (the
-//                            same count in every warp, R = 640 + 128 NS),
-//                            read by ldmatrix.
-// Requests: B <= 8 (one mma.sync n-tile).  Shards larger than 1,024 rows,
-// larger batches and the recurrent heads run the other resident kernel.
+//   rows [640, 640 + 128 NS) shared memory: NS = 0..3 strips per warp (the
+//                            same count in every warp), read by ldmatrix;
+//   rows [640 + 128 NS, R)   (shards past 1,024 rows, "V = 248,320: 62% on
+//                            chip, the rest streamed") streamed every step:
+//                            NS <= 2, and the remaining strips come from L2
+//                            through a ring of 2 or 3 shared-memory slots of
+//                            64 KB, one strip of every warp per slot (one
+//                            bulk copy, one mbarrier); the last warp done
+//                            with a slot refills it, so the next step's
+//                            first slots load during the rendezvous.
+// Requests: B <= 16 (one or two mma.sync n-tiles).  Larger batches and the
+// recurrent heads run the other kernels.
 //
 // Epilogue: when every request of the round is greedy and no logits are
 // written, each thread turns its accumulators straight into 32-bit keys {bf16
@@ -57,6 +64,12 @@ constexpr int kTmWords = kMrWarps * kTmWordsPerWarp;  // 256 KB
 constexpr int kMrRfWords = kMrWarps * 16 * 32 * 4;    // 64 KB
 constexpr int kMbarSmem = 0;
 constexpr unsigned long long kKey50Mask = (1ull << 50) - 1ull;
+constexpr int kRingSlotBytes = kMrWarps * kSmemStripBytes;   // 64 KB: a strip of every warp
+constexpr int kMrMaxSlots = 4;                        // ring slots, at most
+constexpr int kStreamGroup = 4;                       // streamed strips scored together
+// the ring's control block after the slots: full mbarriers [kMrMaxSlots],
+// warps still reading each slot [kMrMaxSlots], items issued, items freed
+constexpr int kRingCtlBytes = 128;                    // keeps U 16-byte aligned
 
 // Local row of the first row of strip st of warp w: st 0..3 tensor memory,
 // 4 the register strip, 5.. shared memory (the j-th shared strip of the warp
@@ -205,13 +218,20 @@ __device__ __forceinline__ void fast_keys(const float (&accs)[NST][NT][4], int n
       if (2 * src + q < B) wkey[2 * src + q] = MERGE ? max_u32(wkey[2 * src + q], kb[q]) : kb[q];
 }
 
-template <int NS, int NT>
+template <int NS, int NT, bool STR>
 __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const ResidentArgs ra) {
   constexpr int NST = 1 + kTmStrips + NS;
   const WalkArgs& a = ra.w;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* smem_w2 = smem;
-  uint8_t* U = smem + (size_t)ra.S * kSmemStripBytes;
+  uint8_t* ring = smem + (size_t)ra.S * kSmemStripBytes;   // STR: nslot slots of 64 KB
+  const int nslot = STR ? ra.nslot : 0;
+  uint8_t* ring_ctl = ring + (size_t)nslot * kRingSlotBytes;
+  uint64_t* ring_bar = reinterpret_cast<uint64_t*>(ring_ctl);
+  int* ring_left = reinterpret_cast<int*>(ring_ctl + 8 * kMrMaxSlots);
+  int* ring_sent = ring_left + kMrMaxSlots;            // items issued so far
+  int* ring_freed = ring_sent + 1;                     // items every warp has read
+  uint8_t* U = ring_ctl + (STR ? kRingCtlBytes : 0);
   uint16_t* base_s = reinterpret_cast<uint16_t*>(U + 16 * 512);
   __shared__ __align__(8) uint64_t mbar[1];
   __shared__ unsigned long long group_best[16][kResWarps];
@@ -247,6 +267,14 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
     round_s = *reinterpret_cast<volatile uint32_t*>(&a.sync.hdr->round);
     abort_s = 0;
     ptx::mbar_init(&mbar[kMbarSmem], 1);
+    if constexpr (STR) {
+      for (int i = 0; i < nslot; ++i) {
+        ptx::mbar_init(&ring_bar[i], 1);
+        ring_left[i] = kMrWarps;
+      }
+      *ring_sent = 0;
+      *ring_freed = 0;
+    }
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
@@ -284,6 +312,31 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
       const uint32_t n = bytes - off < 32768u ? bytes - off : 32768u;
       ptx::bulk_g2s(smem_w2 + off, src + off, n, &mbar[kMbarSmem]);
     }
+  }
+
+  // streamed tier: the CTA's ST strips past the shared tier, ST / 8 per warp
+  // (warp w's i-th is shared-tier strip S + 8 i + w, rows 640 + 16 (S + 8 i +
+  // w)), go through a ring of nslot 64 KB slots every step: item n of the
+  // round (step n / nt2, i = n % nt2) is the i-th streamed strip of every
+  // warp, one contiguous bulk copy, warp w's strip at w * 8 KB.  The last
+  // warp done with a slot refills it with item n + nslot, so the next step's
+  // first items load while this step finishes.  L2 keeps these rows
+  // (evict-last): they are read every step.
+  const int nt2 = STR ? ra.ST / kMrWarps : 0;        // streamed strips per warp
+  const int ring_total = a.gamma * nt2;              // items per round
+  const uint64_t pol_stream = ptx::policy_evict_last();
+  auto ring_issue = [&](int n) {                     // one thread
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(gw + kTmWords + kMrRfWords) +
+                         (size_t)(ra.S + kMrWarps * (n % nt2)) * kSmemStripBytes;
+    uint64_t* bar = &ring_bar[n % nslot];
+    ptx::mbar_expect_tx(bar, kRingSlotBytes);
+    ptx::bulk_g2s_hint(ring + (size_t)(n % nslot) * kRingSlotBytes, src, kRingSlotBytes, bar,
+                       pol_stream);
+  };
+  if (STR && threadIdx.x == 0) {
+    const int pre = ring_total < nslot ? ring_total : nslot;
+    for (int n = 0; n < pre; ++n) ring_issue(n);
+    *ring_sent = pre;
   }
 
   // step 0's base rows: asynchronous copies, in flight during the loads below
@@ -356,6 +409,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
 
   // ----------------------------------------------------------- the walk ---
   const uint32_t w2_addr = ptx::smem_u32(smem_w2);
+  const uint32_t ring_addr = ptx::smem_u32(ring);
   const uint32_t blk0 =
       w2_addr + (uint32_t)warp * kSmemStripBytes + (lane >> 3) * 128 + (lane & 7) * 16;
   bool ok = abort_s == 0;
@@ -363,6 +417,87 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
   for (; k < a.gamma && ok; ++k) {
     const uint64_t t_step = globaltimer_ns();
     trace_stamp(a, k, 0);
+
+    // (0) streamed strips, groups of up to four: each strip's 16 k-tiles from
+    // the ring, then the group's keys (greedy, no logits out) or logits
+    if constexpr (STR) {
+      if (fast && lane < a.B) warp_key[warp][lane] = 0u;
+      __syncwarp();
+      const uint32_t rw =
+          ring_addr + (uint32_t)warp * kSmemStripBytes + (lane >> 3) * 128 + (lane & 7) * 16;
+      for (int i0 = 0; i0 < nt2; i0 += kStreamGroup) {
+        float accg[kStreamGroup][NT][4];
+#pragma unroll
+        for (int s = 0; s < kStreamGroup; ++s)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accg[s][nt][e] = 0.0f;
+#pragma unroll
+        for (int ii = 0; ii < kStreamGroup; ++ii) {
+          if (i0 + ii >= nt2) break;
+          const int n = k * nt2 + i0 + ii;
+          const int slot = n % nslot;
+          if (!wait_mbar(&ring_bar[slot], (uint32_t)((n / nslot) & 1), t_step, a.timeout_ns) &&
+              lane == 0) {
+            abort_round(a.sync.hdr, round_s, kStatusTimeout);
+            abort_s = 1;
+          }
+#pragma unroll
+          for (int kt = 0; kt < 16; ++kt) {
+            uint32_t f0, f1, f2, f3;
+            ptx::ldmatrix_x4(rw + (uint32_t)slot * kRingSlotBytes + kt * 512, f0, f1, f2, f3);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              uint32_t b0 = 0u, b1 = 0u;
+              if (8 * nt + g < a.B) {
+                b0 = *reinterpret_cast<const uint32_t*>(U + (4 * kt + nt) * 128 + lane * 4);
+                b1 = *reinterpret_cast<const uint32_t*>(U + (4 * kt + 2 + nt) * 128 + lane * 4);
+              }
+              ptx::mma_16816(accg[ii][nt], f0, f1, f2, f3, b0, b1);
+            }
+          }
+          __syncwarp();                    // every lane's reads of the slot are done
+          if (lane == 0) {
+            __threadfence_block();
+            if (atomicSub(&ring_left[slot], 1) == 1) {   // the last warp: refill the slot
+              ring_left[slot] = kMrWarps;
+              __threadfence_block();
+              if (n + nslot < ring_total) {
+                ptx::fence_proxy_async_smem();
+                ring_issue(n + nslot);
+                atomicMax(ring_sent, n + nslot + 1);
+              }
+              atomicMax(ring_freed, n + 1);
+            }
+          }
+        }
+        const int st0 = 1 + kTmStrips + NS + i0;
+        const int ng = nt2 - i0 < kStreamGroup ? nt2 - i0 : kStreamGroup;
+        if (fast) {
+          if constexpr (NT == 1) {
+            if (a.B <= 2)
+              fast_keys<kStreamGroup, 4, NT, true>(accg, 0, base_s, ra.R, a.B, nv, warp, lane,
+                                                   &warp_key[warp][0], st0, ng);
+            else if (a.B <= 4)
+              fast_keys<kStreamGroup, 2, NT, true>(accg, 0, base_s, ra.R, a.B, nv, warp, lane,
+                                                   &warp_key[warp][0], st0, ng);
+            else
+              fast_keys<kStreamGroup, 1, NT, true>(accg, 0, base_s, ra.R, a.B, nv, warp, lane,
+                                                   &warp_key[warp][0], st0, ng);
+          } else {
+            fast_keys<kStreamGroup, 1, NT, true>(accg, 0, base_s, ra.R, a.B, nv, warp, lane,
+                                                 &warp_key[warp][0], st0, ng);
+            fast_keys<kStreamGroup, 1, NT, true>(accg, 1, base_s, ra.R, a.B, nv, warp, lane,
+                                                 &warp_key[warp][0], st0, ng);
+          }
+        } else {
+#pragma unroll
+          for (int ii = 0; ii < kStreamGroup; ++ii)
+            if (ii < ng) logits_strip<NT>(accg[ii], base_s, ra.R, a.B, strip_row0(st0 + ii, warp), lane);
+        }
+      }
+    }
 
     // (1) projection: 16 k-tiles of up to 8 independent mma.sync chains (the
     // four tensor-memory strips, the register strip, the shared strips); the
@@ -435,14 +570,14 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
       // greedy, no logits out: keys straight from the accumulators
       if constexpr (NT == 1) {
         if (a.B <= 2)
-          fast_keys<NST, 4>(acc, 0, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
+          fast_keys<NST, 4, NT, STR>(acc, 0, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
         else if (a.B <= 4)
-          fast_keys<NST, 2>(acc, 0, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
+          fast_keys<NST, 2, NT, STR>(acc, 0, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
         else
-          fast_keys<NST, 1>(acc, 0, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
+          fast_keys<NST, 1, NT, STR>(acc, 0, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
       } else {
-        fast_keys<NST, 1>(acc, 0, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
-        fast_keys<NST, 1>(acc, 1, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
+        fast_keys<NST, 1, NT, STR>(acc, 0, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
+        fast_keys<NST, 1, NT, STR>(acc, 1, base_s, ra.R, a.B, nv, warp, lane, &warp_key[warp][0]);
       }
       trace_stamp(a, k, 2);
       trace_stamp(a, k, 3);
@@ -698,6 +833,13 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
   // -------------------------------------------------------------- exit ----
   ptx::tc_fence_before();
   __syncthreads();
+  // a walk that stopped early may leave ring copies in flight: let them land
+  // before the CTA's shared memory goes away
+  if (STR && threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    for (int n = *ring_freed; n < *ring_sent; ++n)
+      (void)wait_mbar(&ring_bar[n % nslot], (uint32_t)((n / nslot) & 1), t0, a.timeout_ns);
+  }
   if (warp == 0) ptx::tmem_dealloc(tmem, 512);
   if (cta == 0) {
     if (!ok)
@@ -765,25 +907,43 @@ int64_t mma_resident_words_per_cta(int S) {
   return (int64_t)kTmWords + kMrRfWords + (int64_t)S * (kSmemStripBytes / 4);
 }
 
-size_t mma_resident_smem_bytes(int S, int max_B, int R) {
-  return (size_t)S * kSmemStripBytes + 16 * 512 + (((size_t)max_B * R * 2 + 15) & ~(size_t)15);
+size_t mma_resident_smem_bytes(int S, int max_B, int R, int nslot) {
+  return (size_t)S * kSmemStripBytes +
+         (nslot > 0 ? (size_t)nslot * kRingSlotBytes + kRingCtlBytes : 0) + 16 * 512 +
+         (((size_t)max_B * R * 2 + 15) & ~(size_t)15);
 }
 
-const void* mma_resident_kernel(int S, int NT) {
+const void* mma_resident_kernel(int S, int NT, bool streamed) {
   const int NS = (S + kMrWarps - 1) / kMrWarps;
+  if (streamed) {
+    if (NT == 1) {
+      switch (NS) {
+        case 0: return reinterpret_cast<const void*>(&walk_mma_kernel<0, 1, true>);
+        case 1: return reinterpret_cast<const void*>(&walk_mma_kernel<1, 1, true>);
+        case 2: return reinterpret_cast<const void*>(&walk_mma_kernel<2, 1, true>);
+      }
+    } else if (NT == 2) {
+      switch (NS) {
+        case 0: return reinterpret_cast<const void*>(&walk_mma_kernel<0, 2, true>);
+        case 1: return reinterpret_cast<const void*>(&walk_mma_kernel<1, 2, true>);
+        case 2: return reinterpret_cast<const void*>(&walk_mma_kernel<2, 2, true>);
+      }
+    }
+    return nullptr;
+  }
   if (NT == 1) {
     switch (NS) {
-      case 0: return reinterpret_cast<const void*>(&walk_mma_kernel<0, 1>);
-      case 1: return reinterpret_cast<const void*>(&walk_mma_kernel<1, 1>);
-      case 2: return reinterpret_cast<const void*>(&walk_mma_kernel<2, 1>);
-      case 3: return reinterpret_cast<const void*>(&walk_mma_kernel<3, 1>);
+      case 0: return reinterpret_cast<const void*>(&walk_mma_kernel<0, 1, false>);
+      case 1: return reinterpret_cast<const void*>(&walk_mma_kernel<1, 1, false>);
+      case 2: return reinterpret_cast<const void*>(&walk_mma_kernel<2, 1, false>);
+      case 3: return reinterpret_cast<const void*>(&walk_mma_kernel<3, 1, false>);
     }
   } else if (NT == 2) {
     switch (NS) {
-      case 0: return reinterpret_cast<const void*>(&walk_mma_kernel<0, 2>);
-      case 1: return reinterpret_cast<const void*>(&walk_mma_kernel<1, 2>);
-      case 2: return reinterpret_cast<const void*>(&walk_mma_kernel<2, 2>);
-      case 3: return reinterpret_cast<const void*>(&walk_mma_kernel<3, 2>);
+      case 0: return reinterpret_cast<const void*>(&walk_mma_kernel<0, 2, false>);
+      case 1: return reinterpret_cast<const void*>(&walk_mma_kernel<1, 2, false>);
+      case 2: return reinterpret_cast<const void*>(&walk_mma_kernel<2, 2, false>);
+      case 3: return reinterpret_cast<const void*>(&walk_mma_kernel<3, 2, false>);
     }
   }
   return nullptr;

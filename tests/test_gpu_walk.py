@@ -79,18 +79,20 @@ def test_small_every_logit(walkmod, V, gamma, B, temps, seed, kernel):
 
 
 @pytest.mark.parametrize("V,max_B,B,temps", [
-    (160000, 16, 16, (0.0, 1.0, 0.6)),   # 2 ring slots; chunks of 8, 8 and 3 strips
+    (160000, 16, 16, (0.0, 1.0, 0.6)),   # no shared strips, 4 streamed strips per warp
     (160000, 16, 3, (0.6, 0.0)),
-    (200000, 1, 1, (0.6,)),              # 3 ring slots; 6 chunks, the last of 1 strip
+    (200000, 1, 1, (0.6,)),              # 1 shared, 5 streamed strips per warp (4 + 1)
+    (230000, 2, 2, (0.0, 0.6)),          # 1 shared, 6 streamed strips per warp (4 + 2)
 ])
 def test_streamed_tier_every_logit(walkmod, V, max_B, B, temps):
     """Shards larger than the chip: the rows the chip cannot hold are streamed
-    through the ring every step; every logit and token of every request
-    checked."""
+    through each warp's ring every step; every logit and token of every
+    request checked."""
     x = synth.make_custom(V=V, gamma=3, B=B, seed=21, temperatures=temps, noise_seed=1021)
     w = walkmod.Walk(x.W1.cuda(), x.W2.cuda(), max_B, x.gamma)
     plan = w.plan()
     assert plan["kernel"] == walkmod.KERNEL_RESIDENT and plan["rows_stream"] > 0, plan
+    assert plan["rows_tmem"] == 512, plan          # the mma.sync kernel's streamed tier
     st, toks, lg = gpu_run(w, x)
     assert st == 0, walkmod.dspark_walk_strerror(st)
     rep = parity.check(x, toks, lg)
@@ -107,7 +109,10 @@ GREEDY_TOKENS_ONLY = [
     (3000, 64, 1, 34),
     (130000, 3, 1, 35),
     (90001, 2, 5, 36),
-    (200000, 3, 1, 37),           # streamed tier
+    (200000, 3, 1, 37),           # streamed tier: a group of 4 strips and one of 1
+    (230000, 3, 2, 38),           # streamed tier, two requests: groups of 4 and 2
+    (180000, 3, 4, 39),           # streamed tier, four requests
+    (160000, 3, 12, 40),          # streamed tier, two n-tiles, no shared strips
 ]
 
 
@@ -175,6 +180,7 @@ def test_qwen3_resident(walkmod, round_index, want_logits):
     w = full_walk(walkmod, "qwen3_resident", x)
     plan = w.plan()
     assert plan["kernel"] == walkmod.KERNEL_RESIDENT and plan["rows_stream"] == 0
+    assert plan["rows_tmem"] == 512, plan          # the mma.sync resident kernel
     st, toks, lg = gpu_run(w, x, want_logits=want_logits)
     assert st == 0
     rep = parity.check(x, toks, lg)
@@ -186,6 +192,7 @@ def test_qwen3_resident(walkmod, round_index, want_logits):
 def test_long_block(walkmod, B, want_logits):
     x = full_inputs("long_block", B)
     w = full_walk(walkmod, "long_block", x)
+    assert w.plan()["rows_tmem"] == 512               # the mma.sync resident kernel
     st, toks, lg = gpu_run(w, x, want_logits=want_logits)
     assert st == 0
     rep = parity.check(x, toks, lg, requests=_sample_requests(B, (0.0,)))
@@ -201,6 +208,7 @@ def test_partial(walkmod, B, want_logits):
     w = full_walk(walkmod, "partial", x)
     plan = w.plan()
     assert plan["kernel"] == walkmod.KERNEL_RESIDENT and plan["rows_stream"] > 0
+    assert plan["rows_tmem"] == 512, plan          # the mma.sync kernel's streamed tier
     st, toks, lg = gpu_run(w, x, want_logits=want_logits)
     assert st == 0
     rep = parity.check(x, toks, lg, requests=_sample_requests(B, (0.0,)))
@@ -634,6 +642,7 @@ CELL_SHAPES = [
     (152 * 33 + 17, 4, 16, (0.0, 1.0), 64),       # two n-tiles, the largest resident batch
     (130000, 6, 2, (0.0, 0.6), 65),               # 128 of the CTAs own two rows of M
     (200000, 3, 1, (0.6,), 66),                   # the streamed tier
+    (160000, 3, 5, (0.0, 0.6), 67),               # the streamed tier, five requests
 ]
 
 

@@ -196,3 +196,23 @@ def test_every_request_check_accepts_the_oracle_and_rejects_planted_tokens():
     t3 = t.copy()
     t3[2, 0] = x.base.shape[2]                     # out of range
     assert parity.check_all_tokens(x, t3).failures[0][0] == "token out of range"
+
+
+def test_state_rule_near_zero_takes_any_rounding_within_the_bound():
+    # a state element near zero, where the fp32 error bound 2^-20 spans many
+    # bf16 spacings: a rounding of any value within the bound passes, one
+    # beyond it fails (no previous state, zero inputs: the bound is 2^-20)
+    O = oracle.default()
+    r = 256
+    M = np.zeros((r, r), np.uint16)
+    x_tok = np.zeros(r, np.uint16)
+    ex = np.full(r, 3.0e-7)
+    oh = O.bf16_rne(ex)
+    for shift, ok in ((0.9 * parity.CELL_TOL, True), (-0.9 * parity.CELL_TOL, True),
+                      (3.0 * parity.CELL_TOL, False)):
+        gh = oh.copy()
+        gh[7] = O.bf16_rne(np.array([3.0e-7 + shift]))[0]
+        assert gh[7] != oh[7]
+        rep = parity.Report()
+        parity._check_states(O, rep, 1, M, None, None, x_tok, gh, oh, ex, 0, 0)
+        assert rep.ok() == ok, (shift, rep)
