@@ -302,6 +302,15 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
   clear_own_slots(a.sync, round_s & 1u);
   if (cta == 0) clear_other_parity(a.sync, round_s & 1u);
 
+  // The shard is read from memory once per round, so its loads carry an L2
+  // evict-first policy: when the round starts on an L2 full of other data
+  // (a drafter's forward pass runs between two walks, so it usually does),
+  // the shard's own lines are replaced before that data, and lines that
+  // would have to be written back first stay.  (Back-to-back rounds then
+  // find less of the shard in L2.)  The streamed tier is the other way round:
+  // evict-last, read every step.
+  const uint64_t pol_first = ptx::policy_evict_first();
+
   // shared-memory tier: bulk copies straight to its final place
   const uint64_t t_entry = globaltimer_ns();
   if (threadIdx.x == 0 && ra.S > 0) {
@@ -310,7 +319,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
     const uint8_t* src = reinterpret_cast<const uint8_t*>(gw + kTmWords + kMrRfWords);
     for (uint32_t off = 0; off < bytes; off += 32768u) {
       const uint32_t n = bytes - off < 32768u ? bytes - off : 32768u;
-      ptx::bulk_g2s(smem_w2 + off, src + off, n, &mbar[kMbarSmem]);
+      ptx::bulk_g2s_hint(smem_w2 + off, src + off, n, &mbar[kMbarSmem], pol_first);
     }
   }
 
@@ -356,7 +365,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
     auto load_chunk = [&](int p, uint32_t (&v)[32]) {
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
-        const uint4 x = __ldg(tsrc + (p * 8 + m) * 32);
+        const uint4 x = ptx::ldg_nc_na_hint(tsrc + (p * 8 + m) * 32, pol_first);
         v[4 * m + 0] = x.x;
         v[4 * m + 1] = x.y;
         v[4 * m + 2] = x.z;
@@ -368,7 +377,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
     load_chunk(1, v1);
 #pragma unroll
     for (int kt = 0; kt < 16; ++kt) {
-      const uint4 x = __ldg(rsrc + kt * 32);
+      const uint4 x = ptx::ldg_nc_na_hint(rsrc + kt * 32, pol_first);
       wr[kt][0] = x.x;
       wr[kt][1] = x.y;
       wr[kt][2] = x.z;
