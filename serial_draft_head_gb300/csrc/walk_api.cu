@@ -191,6 +191,7 @@ bool plan_mma(dspark_walk* h) {
   }
   const size_t smem = mma_resident_smem_bytes(S, mb, (int)R, nslot);
   if (smem > kSmemBudget) return false;
+  if ((h->V + R - 1) / R > mma_resident_max_ctas()) return false;
   h->mr_ok = true;
   h->mr_max_B = mb;
   h->mr_R = (int)R;

@@ -34,6 +34,7 @@ cudaError_t resident_repack(void* rowmajor, void* packed, int64_t V, int R, int 
 int mma_resident_fixed_rows();
 int mma_resident_max_rows();
 int mma_resident_max_batch();
+int mma_resident_max_ctas();                  // the grid's largest size
 int64_t mma_resident_words_per_cta(int S);    // S: every strip in the shared-tier format
 size_t mma_resident_smem_bytes(int S, int max_B, int R, int nslot);
 // S shared strips, NT n-tiles (B <= 8 NT), a streamed tier or not

@@ -59,6 +59,7 @@ constexpr int kMrFixedRows = kTmRows + kRfRows;       // 640
 constexpr int kMrSmax = 3;                            // shared strips per warp, at most
 constexpr int kMrMaxRows = kMrFixedRows + kMrSmax * kMrWarps * 16;   // 1024
 constexpr int kMrMaxB = 16;
+constexpr int kMrMaxCtas = 192;                     // CTAs whose slots one poll reads
 constexpr int kTmWordsPerWarp = 32 * 256;             // 32 lanes x 256 columns
 constexpr int kTmWords = kMrWarps * kTmWordsPerWarp;  // 256 KB
 constexpr int kMrRfWords = kMrWarps * 16 * 32 * 4;    // 64 KB
@@ -613,6 +614,12 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
     // puts the winner's W1 row into U.  Up to 8 requests, the row of the best
     // key seen so far is loaded while the last keys arrive, so that when the
     // winner posted early its row is already on the way.
+    //
+    // On GB300 another SM's poll sees a store ~440 ns after it issues (for
+    // every store and load form tried), against ~140 ns for a load's round
+    // trip; so each poll keeps all of its slot loads in flight at once (a
+    // fixed trip count over at most kMrMaxCtas slots), and the maximum of a
+    // poll is two redux.sync.
     const uint32_t parity = round_s & 1u;
     const unsigned long long tag = slot_tag(round_s);
     if (warp == 0 && lane < a.B) {
@@ -669,21 +676,36 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
       while (true) {
         bool have = true;
         best = 0ull;
-        for (int j = 2 * lane; j < n_cta; j += 64) {
-          unsigned long long x0, x1;
-          ld_relaxed_gpu_v2u64(s + j, x0, x1);
-          const bool v1 = j + 1 < n_cta;
-          have = have && (x0 & ~kKey50Mask) == tag && (!v1 || (x1 & ~kKey50Mask) == tag);
-          x0 &= kKey50Mask;
-          x1 = v1 ? (x1 & kKey50Mask) : 0ull;
-          best = x0 > best ? x0 : best;
-          best = x1 > best ? x1 : best;
+        {
+          // every slot load of a poll in flight together (a fixed trip count;
+          // a loop bounded by the CTA count issued them one round trip apart)
+          constexpr int nld = kMrMaxCtas / 64;
+          unsigned long long xx[nld][2];
+#pragma unroll
+          for (int it = 0; it < nld; ++it) {
+            const int j = 2 * lane + 64 * it;
+            if (j < n_cta) {
+              ld_relaxed_gpu_v2u64(s + j, xx[it][0], xx[it][1]);
+            } else {
+              xx[it][0] = tag;
+              xx[it][1] = tag;
+            }
+          }
+#pragma unroll
+          for (int it = 0; it < nld; ++it) {
+            const int j = 2 * lane + 64 * it;
+            if (j + 1 >= n_cta) xx[it][1] = tag;       // the padding word after an odd count
+            have = have && (xx[it][0] & ~kKey50Mask) == tag && (xx[it][1] & ~kKey50Mask) == tag;
+            const unsigned long long x0 = xx[it][0] & kKey50Mask, x1 = xx[it][1] & kKey50Mask;
+            best = x0 > best ? x0 : best;
+            best = x1 > best ? x1 : best;
+          }
         }
         const bool all = __all_sync(0xFFFFFFFFu, have);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-          best = y > best ? y : best;
+        {                                            // the 50-bit maximum as two 32-bit ones
+          const uint32_t hi = (uint32_t)(best >> 32), mh = ptx::redux_max_u32(hi);
+          const uint32_t ml = ptx::redux_max_u32(hi == mh ? (uint32_t)best : 0u);
+          best = ((unsigned long long)mh << 32) | ml;
         }
         if (best != cand && best != 0ull && k + 1 < a.gamma) {
           const int32_t t = key50_token(best);
@@ -765,18 +787,29 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
       while (true) {
         bool have = true;
         best = 0ull;
-        if (mine)
-#pragma unroll 4
-          for (int j = 2 * li; j < n_cta; j += 2 * span) {
-            unsigned long long x0, x1;
-            ld_relaxed_gpu_v2u64(s + j, x0, x1);
-            const bool v1 = j + 1 < n_cta;
-            have = have && (x0 & ~kKey50Mask) == tag && (!v1 || (x1 & ~kKey50Mask) == tag);
-            x0 &= kKey50Mask;
-            x1 = v1 ? (x1 & kKey50Mask) : 0ull;
+        if (mine) {
+          constexpr int nld = kMrMaxCtas / (2 * span);
+          unsigned long long xx[nld][2];
+#pragma unroll
+          for (int it = 0; it < nld; ++it) {
+            const int j = 2 * li + 2 * span * it;
+            if (j < n_cta) {
+              ld_relaxed_gpu_v2u64(s + j, xx[it][0], xx[it][1]);
+            } else {
+              xx[it][0] = tag;
+              xx[it][1] = tag;
+            }
+          }
+#pragma unroll
+          for (int it = 0; it < nld; ++it) {
+            const int j = 2 * li + 2 * span * it;
+            if (j + 1 >= n_cta) xx[it][1] = tag;
+            have = have && (xx[it][0] & ~kKey50Mask) == tag && (xx[it][1] & ~kKey50Mask) == tag;
+            const unsigned long long x0 = xx[it][0] & kKey50Mask, x1 = xx[it][1] & kKey50Mask;
             best = x0 > best ? x0 : best;
             best = x1 > best ? x1 : best;
           }
+        }
         const bool all = __all_sync(0xFFFFFFFFu, have);
 #pragma unroll
         for (int o = span / 2; o > 0; o >>= 1) {         // within the request's lanes
@@ -911,6 +944,8 @@ int mma_resident_fixed_rows() { return kMrFixedRows; }
 int mma_resident_max_rows() { return kMrMaxRows; }
 
 int mma_resident_max_batch() { return kMrMaxB; }
+
+int mma_resident_max_ctas() { return kMrMaxCtas; }
 
 int64_t mma_resident_words_per_cta(int S) {
   return (int64_t)kTmWords + kMrRfWords + (int64_t)S * (kSmemStripBytes / 4);
