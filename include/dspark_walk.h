@@ -321,8 +321,10 @@ int dspark_walk_gumbel_noise(const uint32_t *bits, float *noise, int64_t n, void
  * 3 key pass done, 4 CTA barrier passed, 5 key posted, 6 winner seen,
  * 7 next u gathered; the tcgen05 resident kernel stamps 1 after its register
  * strips, 2 after its shared strips, 3 after its tensor-memory epilogue and
- * key pass); slot gamma is the round's entry (start, tensor-memory and
- * register tiers loaded, ready).  Only the resident kernels write stamps.
+ * key pass); slot gamma is the round's entry (0 start, 1 tensor-memory and
+ * register tiers loaded, 2 ready; the mma.sync kernel also stamps 3 at the
+ * CTA's first instruction and 4 at its last).  Only the resident kernels
+ * write stamps.
  * NULL turns tracing off.
  */
 int dspark_walk_set_trace(dspark_walk_t h, void *device_buffer, int64_t bytes);

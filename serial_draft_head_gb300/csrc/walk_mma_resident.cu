@@ -253,6 +253,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
   const int nv = (int)((a.V - row0) < ra.R ? (a.V - row0) : ra.R);  // valid rows (>= 1)
   const uint32_t* gw = ra.W2p + (size_t)cta * (size_t)ra.words_per_cta;
 
+  trace_stamp(a, a.gamma, 3);          // the CTA's first instruction
   const int bad = check_inputs(a, &flag_s);
   if (bad != 0) {
     if (cta == 0) {
@@ -888,6 +889,7 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
       for (int i = threadIdx.x; i < a.B * a.gamma; i += blockDim.x) a.out_tokens[i] = -1;
     if (threadIdx.x == 0) atomicAdd(&a.sync.hdr->round, 1u);
   }
+  trace_stamp(a, a.gamma, 4);          // the CTA's last
 }
 
 // Position (local row, K word pair) of word i of a CTA's block of the repacked

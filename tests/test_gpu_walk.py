@@ -560,6 +560,24 @@ def test_lost_arrival_times_out_and_recovers(walkmod):
         assert parity.check(x, toks, lg).ok()
 
 
+def test_lost_arrival_one_greedy_request(walkmod):
+    """One greedy request without logits (the next step's projection runs
+    while warp 0 waits): a CTA that never posts still ends the round with
+    ETIMEOUT, and the next rounds run clean."""
+    x = synth.make_custom(V=151936, gamma=5, B=1, seed=48, temperatures=(0.0,))
+    w = make_walk(walkmod, x)
+    walkmod.dspark_walk_set_limits(w.h, 50_000_000, 3)      # 50 ms; CTA 3 skips
+    st, toks, _ = gpu_run(w, x, want_logits=False)
+    assert st == walkmod.ETIMEOUT
+    assert np.all(toks == -1)
+    walkmod.dspark_walk_set_limits(w.h, 200_000_000, -1)
+    for _ in range(2):
+        st, toks, _ = gpu_run(w, x, want_logits=False)
+        assert st == 0
+        assert parity.check(x, toks).ok()
+    w.close()
+
+
 def test_lost_arrival_with_streamed_tier(walkmod):
     """A round aborted while streamed chunks are in flight ends with ETIMEOUT
     (the ring's copies are waited for before the CTAs exit), and the next
