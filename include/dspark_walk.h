@@ -360,6 +360,10 @@ int dspark_walk_set_trace_clock(dspark_walk_t h, int clock);
  *   out[5]  tcgen05.ld of 32-column blocks: cycles per KB per SM (n_out >= 7)
  *   out[6]  one step's projection with 4 tensor-memory strips per warp fed to
  *           mma.sync by tcgen05.ld, 1 register and 3 shared strips (n_out >= 7)
+ *   out[7]  (input, n_out >= 8) nonzero: random MMA operands, else constant
+ *   out[8]  one cross-SM hop: ns from one SM's relaxed store until another
+ *           SM's poll sees it, median over five SM pairs (n_out >= 10)
+ *   out[9]  one dependent load that hits in L2: cycles (n_out >= 10)
  * n_out >= 5.  Allocates and frees a few KB of device memory, runs on
  * `stream` and synchronises it.  DSPARK_EINVAL (out NULL or n_out < 5),
  * DSPARK_EUNSUPPORTED (not sm_103), DSPARK_ENOMEM, DSPARK_ECUDA, and

@@ -24,6 +24,12 @@
 //      strips: 8 chains per warp over 16 k-tiles).
 // Operand values are arbitrary (the rates do not depend on them); nothing of
 // the walk is computed here.  Every wait is bounded by the global timer.
+//
+// A second kernel measures the two latencies that bound the walk's cross-SM
+// rendezvous: how long after one SM's store another SM's poll sees it (CTA 0
+// and one peer CTA bounce a counter through two words in separate lines;
+// one-way time = round trip / 2, median over five peers), and the round trip
+// of one dependent load that hits in L2.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -309,6 +315,50 @@ __global__ void __launch_bounds__(kThreads, 1) unit_rates_kernel(ProbeOut* out, 
   if (warp == 0) ptx::tmem_dealloc(tmem, 512);
 }
 
+constexpr int kHopIters = 200;
+
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// CTA 0 and CTA `peer` (one CTA per SM, co-resident: a cooperative launch)
+// bounce a counter; CTA 0 then times a chain of dependent loads of a word
+// that holds 0 (its own index).  words: [0] 0 -> peer, [32] peer -> 0, [64]
+// the chained word.  out: [0] ns per one-way hop, [1] cycles per load.
+__global__ void hop_kernel(uint32_t* words, int peer, long long* out, int* err) {
+  if (threadIdx.x != 0) return;
+  const int c = blockIdx.x;
+  if (c != 0 && c != peer) return;
+  uint32_t* a = words;
+  uint32_t* b = words + 32;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1; i <= (uint32_t)kHopIters; ++i) {
+    uint32_t spins = 0;
+    if (c == 0) {
+      st_relaxed_u32(a, i);
+      while (ld_relaxed_gpu_u32(b) != i)
+        if ((++spins & 1023u) == 0u && (int64_t)(globaltimer_ns() - t0) > kWaitLimitNs) {
+          *err = 1;
+          return;
+        }
+    } else {
+      while (ld_relaxed_gpu_u32(a) != i)
+        if ((++spins & 1023u) == 0u && (int64_t)(globaltimer_ns() - t0) > kWaitLimitNs) {
+          *err = 1;
+          return;
+        }
+      st_relaxed_u32(b, i);
+    }
+  }
+  if (c != 0) return;
+  out[0] = (long long)((globaltimer_ns() - t0) / (2ull * kHopIters));
+  const uint32_t* w = words + 64;
+  uint32_t idx = 0;
+  const long long c0 = clock64();
+  for (int i = 0; i < 1024; ++i) idx = ld_relaxed_gpu_u32(w + idx);
+  out[1] = (clock64() - c0) / 1024 + (long long)(idx & 0x80000000u);
+}
+
 double median(std::vector<long long> v) {
   std::sort(v.begin(), v.end());
   const size_t n = v.size();
@@ -374,6 +424,50 @@ extern "C" int dspark_walk_unit_rates(double* out, int n_out, void* stream) {
   if (n_out >= 7) {
     out[5] = med[4] / 256.0;                 // 8 warps x 32 KB per rep: cycles per KB per SM
     out[6] = med[5];
+  }
+  if (n_out >= 10) {
+    // cross-SM hop and L2 round trip: CTA 0 against five peers
+    uint32_t* d_words = nullptr;
+    long long* d_hop = nullptr;
+    int* d_err = nullptr;
+    if (cudaMalloc(&d_words, 512) != cudaSuccess) return DSPARK_ENOMEM;
+    if (cudaMalloc(&d_hop, 2 * sizeof(long long)) != cudaSuccess ||
+        cudaMalloc(&d_err, sizeof(int)) != cudaSuccess) {
+      cudaFree(d_words);
+      cudaFree(d_hop);
+      return DSPARK_ENOMEM;
+    }
+    std::vector<long long> hop, rtt;
+    const int peers[5] = {1, sms / 4, sms / 2, (3 * sms) / 4, sms - 1};
+    if (cudaFuncSetAttribute(hop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      rc = DSPARK_ECUDA;
+    for (int pi = 0; pi < 5 && rc == DSPARK_OK && sms > 1; ++pi) {
+      int peer = peers[pi] < 1 ? 1 : peers[pi];
+      long long h[2] = {0, 0};
+      int herr = 0;
+      void* args[] = {&d_words, &peer, &d_hop, &d_err};
+      if (cudaMemsetAsync(d_words, 0, 512, st) != cudaSuccess ||
+          cudaMemsetAsync(d_err, 0, sizeof(int), st) != cudaSuccess ||
+          cudaLaunchCooperativeKernel((const void*)hop_kernel, dim3(sms), dim3(32), args,
+                                      kSmemBytes, st) != cudaSuccess ||
+          cudaMemcpyAsync(h, d_hop, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+          cudaMemcpyAsync(&herr, d_err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+          cudaStreamSynchronize(st) != cudaSuccess) {
+        rc = DSPARK_ECUDA;
+      } else if (herr) {
+        rc = DSPARK_ETIMEOUT;
+      } else {
+        hop.push_back(h[0]);
+        rtt.push_back(h[1]);
+      }
+    }
+    cudaFree(d_words);
+    cudaFree(d_hop);
+    cudaFree(d_err);
+    if (rc != DSPARK_OK) return rc;
+    out[8] = hop.empty() ? 0.0 : median(hop);
+    out[9] = rtt.empty() ? 0.0 : median(rtt);
   }
   return DSPARK_OK;
 }

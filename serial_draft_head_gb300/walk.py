@@ -235,15 +235,17 @@ def dspark_walk_gumbel_noise(bits, noise, stream=None):
 
 UNIT_RATE_NAMES = ("hmma_rf_cycles", "hmma_smem_cycles", "tc_tmem_a_cycles",
                    "resident_step_projection_cycles", "sm_mhz", "tmem_ld_cycles_per_kb",
-                   "tmem_fed_step_projection_cycles")
+                   "tmem_fed_step_projection_cycles", None, "cross_sm_hop_ns",
+                   "l2_load_round_trip_cycles")
 
 
 def dspark_walk_unit_rates(stream=None):
-    """The on-chip tier rates of the current device (see the header), as a dict."""
-    out = (ctypes.c_double * len(UNIT_RATE_NAMES))()
+    """The on-chip tier rates and the cross-SM latencies of the current device
+    (see the header), as a dict."""
+    out = (ctypes.c_double * len(UNIT_RATE_NAMES))()     # out[7] = 0: constant operands
     _check(load().dspark_walk_unit_rates(out, len(UNIT_RATE_NAMES), _stream(stream)),
            "dspark_walk_unit_rates")
-    return dict(zip(UNIT_RATE_NAMES, list(out)))
+    return {k: v for k, v in zip(UNIT_RATE_NAMES, list(out)) if k is not None}
 
 
 def dspark_walk_set_trace(h, device_buffer, nbytes):
