@@ -182,8 +182,7 @@ __device__ __forceinline__ void fast_keys(const float (&accs)[NST][NT][4], int n
     const uint32_t k0 = key32(best, brow), k1 = key32(best >> 16, brow >> 16);
     uint32_t kb = max_u32(k0, k1);
     if (best == kNegInf2 && k0 == k1) kb = 0u;    // no valid row at all
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) kb = max_u32(kb, __shfl_xor_sync(0xFFFFFFFFu, kb, o));
+    kb = ptx::redux_max_u32(kb);
     if (lane == 0) wkey[0] = MERGE ? max_u32(wkey[0], kb) : kb;
     return;
   }
@@ -209,10 +208,15 @@ __device__ __forceinline__ void fast_keys(const float (&accs)[NST][NT][4], int n
     }
   uint32_t kb[2] = {key32(best, brow), key32(best >> 16, brow >> 16)};
   // lanes with the same src hold the same two requests: reduce over g and part
+  if constexpr (SRC == 1) {
 #pragma unroll
-  for (int o = SRC; o < 32; o <<= 1)
+    for (int q = 0; q < 2; ++q) kb[q] = ptx::redux_max_u32(kb[q]);
+  } else {
 #pragma unroll
-    for (int q = 0; q < 2; ++q) kb[q] = max_u32(kb[q], __shfl_xor_sync(0xFFFFFFFFu, kb[q], o));
+    for (int o = SRC; o < 32; o <<= 1)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) kb[q] = max_u32(kb[q], __shfl_xor_sync(0xFFFFFFFFu, kb[q], o));
+  }
   if (g == 0 && part == 0)
 #pragma unroll
     for (int q = 0; q < 2; ++q)
