@@ -211,6 +211,17 @@ __device__ __forceinline__ void fast_keys(const float (&accs)[NST][NT][4], int n
   if constexpr (SRC == 1) {
 #pragma unroll
     for (int q = 0; q < 2; ++q) kb[q] = ptx::redux_max_u32(kb[q]);
+  } else if constexpr (SRC <= 4) {        // one masked maximum per src
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t r = 0u;
+#pragma unroll
+      for (int sv = 0; sv < SRC; ++sv) {
+        const uint32_t m = ptx::redux_max_u32(src == sv ? kb[q] : 0u);
+        r = src == sv ? m : r;
+      }
+      kb[q] = r;
+    }
   } else {
 #pragma unroll
     for (int o = SRC; o < 32; o <<= 1)
@@ -816,10 +827,16 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
           }
         }
         const bool all = __all_sync(0xFFFFFFFFu, have);
-#pragma unroll
-        for (int o = span / 2; o > 0; o >>= 1) {         // within the request's lanes
-          const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-          best = y > best ? y : best;
+        {                                                // each half-warp's 50-bit maximum
+          const bool upper = lane >= 16;
+          const uint32_t h = (uint32_t)(best >> 32);
+          const uint32_t h0 = ptx::redux_max_u32(upper ? 0u : h);
+          const uint32_t h1 = ptx::redux_max_u32(upper ? h : 0u);
+          const uint32_t mh = upper ? h1 : h0;
+          const uint32_t l = h == mh ? (uint32_t)best : 0u;
+          const uint32_t l0 = ptx::redux_max_u32(upper ? 0u : l);
+          const uint32_t l1 = ptx::redux_max_u32(upper ? l : 0u);
+          best = ((unsigned long long)mh << 32) | (upper ? l1 : l0);
         }
         if (mine && best != cand && best != 0ull && k + 1 < a.gamma) {
           const int32_t t = key50_token(best);
