@@ -319,6 +319,24 @@ def test_gumbel_noise_every_uniform(walkmod):
     assert err.max() <= 0.25, (err.max(), int(np.argmax(err)))
 
 
+def test_unit_rates_are_plausible(walkmod):
+    """The roofline's tier rates and the rendezvous latencies come out of the
+    probe finite and in the range one GPU of this class can give: an mma.sync
+    needs at least one cycle of an SM's tensor pipe, the ldmatrix-fed one no
+    less, a cross-SM hop is slower than an L2 round trip, and neither takes
+    microseconds."""
+    r = walkmod.dspark_walk_unit_rates()
+    for k, v in r.items():
+        assert np.isfinite(v) and v > 0, (k, v)
+    assert 1.0 <= r["hmma_rf_cycles"] <= 16.0, r
+    assert r["hmma_smem_cycles"] >= r["hmma_rf_cycles"] * 0.9, r
+    assert 2.0 <= r["tc_tmem_a_cycles"] <= 200.0, r
+    assert 200.0 <= r["sm_mhz"] <= 4000.0, r
+    rtt_ns = r["l2_load_round_trip_cycles"] / r["sm_mhz"] * 1000.0
+    assert 20.0 <= rtt_ns <= 2000.0, r
+    assert rtt_ns < r["cross_sm_hop_ns"] <= 10000.0, r
+
+
 def test_handles_with_different_shared_memory_needs(walkmod):
     """A kernel's shared-memory limit is process-wide: creating a handle that
     needs less must not break a handle (or the allocation-free entry) that
