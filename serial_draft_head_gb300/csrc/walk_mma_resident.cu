@@ -631,11 +631,11 @@ __global__ void __launch_bounds__(kResThreads, 1) walk_mma_kernel(const Resident
     // key seen so far is loaded while the last keys arrive, so that when the
     // winner posted early its row is already on the way.
     //
-    // On GB300 another SM's poll sees a store ~440 ns after it issues (for
-    // every store and load form tried), against ~140 ns for a load's round
+    // On GB300 another SM's poll sees a store 420-440 ns after it issues (for
+    // every store and load form tried), against ~150 ns for a load's round
     // trip; so each poll keeps all of its slot loads in flight at once (a
     // fixed trip count over at most kMrMaxCtas slots), and the maximum of a
-    // poll is two redux.sync.
+    // poll is two redux.sync (two per half-warp above 8 requests).
     const uint32_t parity = round_s & 1u;
     const unsigned long long tag = slot_tag(round_s);
     if (warp == 0 && lane < a.B) {
