@@ -825,6 +825,10 @@ def main():
         line["sweep"] += [measure_config(walk, synth.CONFIGS["sampled"], b, sampler="group",
                                          rates=rates, mhz=mhz)
                           for b in synth.CONFIGS["sampled"].batches]
+        # the metric's batch range up to 128 on the long block: above 16 requests
+        # the batched kernel
+        line["sweep"] += [measure_config(walk, synth.CONFIGS["long_block"], b, rates=rates, mhz=mhz)
+                          for b in (32, 64, 128)]
         # the recurrent heads on the fully resident long block (B = 1 as the pages
         # time them, and the largest resident batch)
         line["sweep"] += [measure_config(walk, synth.CONFIGS["long_block"], b, cell=c,
