@@ -413,19 +413,23 @@ __global__ void __launch_bounds__(kBatThreads, 1) walk_batched_kernel(const Batc
               ok = false;
               break;
             }
-#pragma unroll 1
+            // one descriptor pair per half-tile: the start-address field (bits
+            // 0..13, in 16-byte units) then advances by one 4 KB K block of A and
+            // one 16-deep slice of U per MMA; shared addresses stay below 256 KB,
+            // so the field never carries into the next one
+            const uint64_t adesc0 =
+                ptx::smem_desc_noswizzle(ring_addr + (uint32_t)s * kStageBytes, 2048, 128);
+            const uint64_t bdesc0 = ptx::smem_desc_noswizzle(
+                u_addr + (uint32_t)(8 * h) * 32u * (uint32_t)N, 16u * (uint32_t)N, 128);
+            const uint32_t dcol = tmem + (uint32_t)(d * 256);
+#pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const int kt = 8 * h + j;
-              const uint64_t adesc = ptx::smem_desc_noswizzle(
-                  ring_addr + (uint32_t)s * kStageBytes + (uint32_t)j * kBlockBytes, 2048, 128);
-              const uint64_t bdesc =
-                  ptx::smem_desc_noswizzle(u_addr + (uint32_t)kt * 32u * (uint32_t)N,
-                                           16u * (uint32_t)N, 128);
+              const uint64_t adesc = adesc0 + (uint64_t)(j * (kBlockBytes >> 4));
+              const uint64_t bdesc = bdesc0 + (uint64_t)(j * 2 * N);
               asm volatile(
                   "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
-                      tmem + (uint32_t)(d * 256)),
-                  "l"(adesc), "l"(bdesc), "r"(idesc), "r"(kt > 0 ? 1u : 0u)
+                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dcol),
+                  "l"(adesc), "l"(bdesc), "r"(idesc), "r"((h | j) != 0 ? 1u : 0u)
                   : "memory");
             }
             ptx::tc_commit(&empty_bar[s]);
